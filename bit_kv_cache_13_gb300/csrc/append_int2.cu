@@ -1,0 +1,138 @@
+// Quantise-on-append for the rotated INT2 KV cache.
+//
+// "Output-Aware Rotation for INT2 KV-Cache Quantization": the key is centred
+// (§1, attention-equivalent reparameterisation) and rotated, z = (k - mu) R_k;
+// the value is rotated, w = v R_v (§3.1 Eq. 4); each group of 32 rotated
+// channels is INT2-quantised with one fp16 scale and min (§1).
+//
+// One CTA = 256 threads works on one KV head and a run of tokens.  Thread j
+// (0..127) produces rotated key channel j, thread 128 + j value channel j;
+// each keeps its column of the rotation in registers, so R is read once per
+// CTA.  A rotated coordinate is a fixed-order fp32 fma chain over the 128
+// inputs (the order the format's documentation promises).  Warp w owns one
+// 32-channel group: min/max by shuffles, exact threshold comparisons, and
+// the four 2-bit codes of a byte gathered from four neighbouring lanes.
+#include "kvq_common.cuh"
+
+namespace kvq {
+
+__global__ void __launch_bounds__(256, 1)
+append_int2_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v, int n_tok,
+                   int H_kv, const int32_t* __restrict__ slot_mapping, const float* __restrict__ mu,
+                   const float* __restrict__ Rk, const float* __restrict__ Rv, uint8_t* __restrict__ cache,
+                   int64_t num_pages, float* __restrict__ dbg_k, float* __restrict__ dbg_v,
+                   int32_t* __restrict__ err_count, int tok_per_cta) {
+    const int h = blockIdx.y;
+    const int tid = threadIdx.x;
+    const int is_v = tid >> 7;
+    const int j = tid & (D - 1);
+    const int lane = tid & 31;
+    const int grp = j >> 5;
+
+    const float* R = (is_v ? Rv : Rk) + (size_t)h * D * D;
+    float rcol[D];
+#pragma unroll
+    for (int i = 0; i < D; ++i) rcol[i] = __ldg(R + i * D + j);
+    const float muj = is_v ? 0.f : __ldg(mu + h * D + j);
+
+    __shared__ float xs[2][2][D];
+    const int t0 = blockIdx.x * tok_per_cta;
+    const int t1 = min(n_tok, t0 + tok_per_cta);
+    const int64_t n_slots = num_pages * PAGE;
+    int buf = 0;
+
+    for (int t = t0; t < t1; ++t) {
+        const int slot = __ldg(slot_mapping + t);
+        if (slot < 0 && slot != -1) {
+            if (tid == 0 && err_count) atomicAdd(err_count, 1);
+            continue;
+        }
+        if (slot == -1) continue;
+        if ((int64_t)slot >= n_slots) {
+            if (tid == 0 && err_count) atomicAdd(err_count, 1);
+            continue;
+        }
+        const __nv_bfloat16* src = (is_v ? v : k) + ((size_t)t * H_kv + h) * D;
+        float x = __bfloat162float(src[j]);
+        if (!is_v) x = __fsub_rn(x, muj);
+        xs[buf][is_v][j] = x;
+        __syncthreads();
+
+        const float* xv = xs[buf][is_v];
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < D; ++i) acc = __fmaf_rn(xv[i], rcol[i], acc);
+        buf ^= 1;
+
+        float* dbg = is_v ? dbg_v : dbg_k;
+        if (dbg) dbg[((size_t)t * H_kv + h) * D + j] = acc;
+
+        // group parameters (exact min / max over the 32 lanes)
+        float mn = acc, mx = acc;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        }
+        const __half sh = f16_sat(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+        const __half mh = f16_sat(mn);
+        const float scf = __half2float(sh), mnf = __half2float(mh);
+
+        // code = #{c : mn + (c + 1/2) scale < x}, decided exactly
+        int code = 0;
+        if (scf > 0.f) {
+            float hi, lo;
+            two_sum(acc, -mnf, hi, lo);
+            code = (int)diff_gt(hi, lo, __fmul_rn(scf, 0.5f)) + (int)diff_gt(hi, lo, __fmul_rn(scf, 1.5f)) +
+                   (int)diff_gt(hi, lo, __fmul_rn(scf, 2.5f));
+        }
+
+        // byte 4*b + g holds channels 32g + 4b + c at bits 2c
+        uint32_t bits = (uint32_t)code << (2 * (lane & 3));
+        bits |= __shfl_xor_sync(0xffffffffu, bits, 1);
+        bits |= __shfl_xor_sync(0xffffffffu, bits, 2);
+        const int page = slot / PAGE, s = slot % PAGE;
+        uint8_t* tile = cache + ((size_t)page * H_kv + h) * INT2_TILE;
+        uint8_t* rec = tile + (is_v ? OFF_VC : OFF_KC) + 32 * s;
+        if ((lane & 3) == 0) rec[4 * (lane >> 2) + grp] = (uint8_t)bits;
+        if (lane == 0) {
+            const uint32_t meta = (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(mh) << 16);
+            *reinterpret_cast<uint32_t*>(tile + (is_v ? OFF_VM : OFF_KM) + 16 * s + 4 * grp) = meta;
+        }
+    }
+}
+
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" size_t kvq_int2_tile_bytes(int d) { return d == D ? (size_t)INT2_TILE : 0; }
+
+extern "C" kvq_status kvq_append_int2(const void* k, const void* v, int n_tok, int H_kv, int d,
+                                      const int32_t* slot_mapping, const float* mu_k, const float* R_k,
+                                      const float* R_v, void* cache, int64_t num_pages, float* dbg_rot_k,
+                                      float* dbg_rot_v, int32_t* err_count, void* stream) {
+    if (d != D) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "kvq_append_int2: d=%d (only 128)", d);
+    if (n_tok < 0 || H_kv <= 0 || num_pages <= 0)
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_append_int2: n_tok=%d H_kv=%d num_pages=%lld", n_tok,
+                             H_kv, (long long)num_pages);
+    if (H_kv > 65535) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "kvq_append_int2: H_kv=%d too large", H_kv);
+    if (n_tok == 0) return KVQ_OK;
+    if (!k || !v || !slot_mapping || !mu_k || !R_k || !R_v || !cache)
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_append_int2: null pointer");
+    if (reinterpret_cast<uintptr_t>(cache) % 16)
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_append_int2: cache not 16-byte aligned");
+
+    // enough CTAs for about four waves of the 152 SMs; at most 64 tokens each
+    const int want_ctas = 152 * 4;
+    int chunks = (want_ctas + H_kv - 1) / H_kv;
+    chunks = chunks < 1 ? 1 : chunks;
+    int per = (n_tok + chunks - 1) / chunks;
+    per = per < 1 ? 1 : (per > 64 ? 64 : per);
+    const int grid_x = (n_tok + per - 1) / per;
+    dim3 grid(grid_x, H_kv);
+    append_int2_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), n_tok, H_kv, slot_mapping,
+        mu_k, R_k, R_v, static_cast<uint8_t*>(cache), num_pages, dbg_rot_k, dbg_rot_v, err_count, per);
+    return kvq_check_cuda(cudaGetLastError(), "kvq_append_int2 launch");
+}

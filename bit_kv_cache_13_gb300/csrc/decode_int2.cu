@@ -1,0 +1,572 @@
+// Fused packed-cache decode attention over the rotated INT2 cache.
+//
+// "Output-Aware Rotation for INT2 KV-Cache Quantization" §3 Eqs. (1)-(2)
+// with Eq. (4) folded in: <q, Q2(zR)R^T> = <qR, Q2(zR)>, so the query is
+// rotated once (q' = q R_k), the cache is consumed in the rotated basis and
+// the output is rotated back once (o = o' R_v^T).  The kernel reads only the
+// packed codes and fp16 (scale, min) pairs.
+//
+// Grid (split, kv_head, seq); 4 warps per CTA, each warp streaming its own
+// pages of the split through a 4-stage ring of 1536-byte tiles filled by
+// bulk async copies (cp.async.bulk + mbarrier).  Per page (16 tokens):
+//
+//   QK  logit(s, j) = sum_g [ scale_{s,g} <q'_{j,g}, c_{s,g}> + min_{s,g} S_{j,g} ]
+//       The 2-bit codes c are fed to mma.sync m16n8k16 as exact fp16
+//       subnormals (code << 2k reinterpreted is code * 4^k * 2^-24), one MMA
+//       pair per 32-channel group so the group scale applies afterwards; q'
+//       enters as an fp16 hi/lo pair (fp16 + fp16 ~ 22 bits) in the eight N
+//       columns, pre-scaled by 4^-k and a per-head power of two.
+//   softmax  online, base 2, exact running maximum per head.
+//   PV  o'(j, i) = sum_s p_{s,j} scale_{s,g} c_{s,i} + sum_s p_{s,j} min_{s,g}
+//       rows = channels (codes again as fp16 subnormals), K = the 16 tokens,
+//       B = p * scale (fp16); the min term is one more MMA with A = the fp16
+//       mins of the four groups.
+//
+// Split partials (m, l, o') go to the workspace; the last CTA of a
+// (sequence, KV head) to finish (atomic ticket, no waiting) merges them,
+// applies R_v^T and writes the output.
+#include <math_constants.h>
+
+#include "kvq_common.cuh"
+
+namespace kvq {
+
+constexpr int DEC_WARPS = 4;
+constexpr int DEC_STAGES = 4;
+
+struct __align__(16) DecodeSmem {
+    union {
+        uint8_t ring[DEC_WARPS][DEC_STAGES][INT2_TILE];  // page tiles in flight
+        float o_part[DEC_WARPS][8][D];                   // per-warp o' after the loop
+    } u;
+    uint64_t bar[DEC_WARPS][DEC_STAGES];
+    float q[8][D];        // scaled rotated queries q~ = q R_k * scale * log2(e)
+    float gsum[8][NGROUP];
+    float sigma[8];       // power-of-two pre-scale per head
+    float m_part[DEC_WARPS][8];
+    float l_part[DEC_WARPS][8];
+    float o_final[8][D];
+    int is_last;
+};
+
+template <int NT>
+__global__ void __launch_bounds__(128)
+decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G, const uint8_t* __restrict__ cache,
+                   int64_t num_pages, const int32_t* __restrict__ block_table, int max_pages,
+                   const int32_t* __restrict__ context_lens, const float* __restrict__ Rk,
+                   const float* __restrict__ Rv, float scale_log2, float* __restrict__ out,
+                   uint8_t* __restrict__ ws) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
+
+    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int S = gridDim.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = lane >> 2, t = lane & 3;
+
+    uint32_t* err_word = reinterpret_cast<uint32_t*>(ws);
+    int32_t* tickets = reinterpret_cast<int32_t*>(ws + WS_HEADER);
+    float* partials = reinterpret_cast<float*>(ws + WS_HEADER + tickets_bytes(gridDim.z, H_kv));
+
+    int ctx = __ldg(context_lens + b);
+    ctx = max(0, min(ctx, max_pages * PAGE));
+    const int n_pages = (ctx + PAGE - 1) / PAGE;
+    const int pps = (n_pages + S - 1) / S;
+    const int p_begin = min(split * pps, n_pages);
+    const int p_end = min(p_begin + pps, n_pages);
+    const int my_count = p_end - p_begin > warp ? (p_end - p_begin - warp + DEC_WARPS - 1) / DEC_WARPS : 0;
+    const int32_t* bt = block_table + (size_t)b * max_pages;
+
+    // ---- start streaming before the query set-up
+    if (lane == 0) {
+        for (int s = 0; s < DEC_STAGES; ++s) mbar_init(&sm.bar[warp][s], 1);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    __syncwarp();
+    auto issue = [&](int i) {  // lane 0 only
+        const int p = p_begin + warp + DEC_WARPS * i;
+        const int pid = __ldg(bt + p);
+        uint64_t* bar = &sm.bar[warp][i % DEC_STAGES];
+        if (pid < 0 || (int64_t)pid >= num_pages) {
+            atomicOr(err_word, ERR_BAD_PAGE);
+            mbar_arrive(bar);  // complete the phase without data
+        } else {
+            mbar_arrive_expect_tx(bar, INT2_TILE);
+            bulk_g2s(sm.u.ring[warp][i % DEC_STAGES], cache + ((size_t)pid * H_kv + h) * INT2_TILE, INT2_TILE,
+                     bar);
+        }
+    };
+    if (lane == 0)
+        for (int i = 0; i < min(DEC_STAGES, my_count); ++i) issue(i);
+
+    // ---- q~ = (q R_k) * scale * log2(e) for the G heads of this KV head
+    {
+        const __nv_bfloat16* qb = q + ((size_t)b * H_q + (size_t)h * G) * D;
+        for (int idx = tid; idx < G * D; idx += 128) sm.o_final[idx / D][idx % D] = __bfloat162float(qb[idx]);
+        __syncthreads();
+        const float* R = Rk + (size_t)h * D * D;
+        float acc[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) acc[jj] = 0.f;
+        for (int i = 0; i < D; ++i) {
+            const float rv = __ldg(R + i * D + tid);
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj)
+                if (jj < G) acc[jj] = fmaf(sm.o_final[jj][i], rv, acc[jj]);
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj)
+            if (jj < G) sm.q[jj][tid] = acc[jj] * scale_log2;
+        __syncthreads();
+        // per head: power-of-two pre-scale (max |q~| * sigma in [2^14, 2^15)) and group sums
+        for (int jj = warp; jj < G; jj += DEC_WARPS) {
+            float mx = 0.f;
+            float gs[NGROUP];
+#pragma unroll
+            for (int g = 0; g < NGROUP; ++g) {
+                const float x = sm.q[jj][32 * g + lane];
+                mx = fmaxf(mx, fabsf(x));
+                gs[g] = x;
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+#pragma unroll
+                for (int g = 0; g < NGROUP; ++g) gs[g] += __shfl_xor_sync(0xffffffffu, gs[g], o);
+            }
+            if (lane == 0) {
+                sm.sigma[jj] = mx > 0.f ? ldexpf(1.f, 14 - ilogbf(mx)) : 1.f;
+#pragma unroll
+                for (int g = 0; g < NGROUP; ++g) sm.gsum[jj][g] = gs[g];
+            }
+        }
+        __syncthreads();
+    }
+
+    // ---- QK B fragments: column n = r -> head 4*nt + (r >> 1), part r & 1 (hi / lo)
+    uint32_t bq[NT][8][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int hq = 4 * nt + (r >> 1);
+        const bool lo_part = r & 1;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const int g = s >> 1, hs = s & 1;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {  // b0 (k = 2hs), b1 (k = 2hs + 1)
+                const int k = 2 * hs + e;
+                const int c0 = 32 * g + 8 * t + k, c1 = c0 + 4;
+                float v0 = 0.f, v1 = 0.f;
+                if (hq < G) {
+                    const float f = ldexpf(sm.sigma[hq], -2 * k);
+                    v0 = sm.q[hq][c0] * f;
+                    v1 = sm.q[hq][c1] * f;
+                }
+                const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
+                if (lo_part) {
+                    bq[nt][s][e] = pack_half2(v0 - __half2float(h0), v1 - __half2float(h1));
+                } else {
+                    bq[nt][s][e] = h2_as_u32(__halves2half2(h0, h1));
+                }
+            }
+        }
+    }
+    float inv_sig[NT], gsum[NT][NGROUP];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int hq = 4 * nt + t;
+        inv_sig[nt] = hq < G ? 16777216.f / sm.sigma[hq] : 0.f;
+#pragma unroll
+        for (int g = 0; g < NGROUP; ++g) gsum[nt][g] = hq < G ? sm.gsum[hq][g] : 0.f;
+    }
+
+    float oacc[8][4];
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) oacc[m][e] = 0.f;
+    float cmin[4] = {0.f, 0.f, 0.f, 0.f};
+    float mrun[NT], lsum[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        mrun[nt] = -CUDART_INF_F;
+        lsum[nt] = 0.f;
+    }
+    bool timed_out = false;
+
+    for (int i = 0; i < my_count; ++i) {
+        const int stage = i % DEC_STAGES;
+        const uint32_t parity = (i / DEC_STAGES) & 1;
+        if (!timed_out) {
+            const bool ok = mbar_wait_bounded(&sm.bar[warp][stage], parity, WAIT_LIMIT_CYCLES);
+            if (__any_sync(0xffffffffu, !ok)) {
+                timed_out = true;
+                if (lane == 0) atomicOr(err_word, ERR_TIMEOUT);
+            }
+        }
+        if (timed_out) break;
+        const uint8_t* tile = sm.u.ring[warp][stage];
+        const int p = p_begin + warp + DEC_WARPS * i;
+        const int pid = __ldg(bt + p);
+        const bool valid = pid >= 0 && (int64_t)pid < num_pages;
+        const int n_tok = valid ? min(PAGE, ctx - p * PAGE) : 0;
+
+        // ---------------- QK
+        float lg[NT][2];
+        {
+            const uint2 kr = lds64(tile + OFF_KC + 32 * r + 8 * t);
+            const uint2 kr8 = lds64(tile + OFF_KC + 32 * (r + 8) + 8 * t);
+            const uint32_t P01 = prmt(kr.x, kr.y, 0x5410), P23 = prmt(kr.x, kr.y, 0x7632);
+            const uint32_t Q01 = prmt(kr8.x, kr8.y, 0x5410), Q23 = prmt(kr8.x, kr8.y, 0x7632);
+            const uint4 mr = lds128(tile + OFF_KM + 16 * r);
+            const uint4 mr8 = lds128(tile + OFF_KM + 16 * (r + 8));
+            const uint32_t mrw[4] = {mr.x, mr.y, mr.z, mr.w}, mr8w[4] = {mr8.x, mr8.y, mr8.z, mr8.w};
+            float acc_r[NT], acc_r8[NT], mn_r[NT], mn_r8[NT];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) acc_r[nt] = acc_r8[nt] = mn_r[nt] = mn_r8[nt] = 0.f;
+#pragma unroll
+            for (int g = 0; g < NGROUP; ++g) {
+                const uint32_t xr = g == 0 ? P01 : g == 1 ? (P01 >> 8) : g == 2 ? P23 : (P23 >> 8);
+                const uint32_t xr8 = g == 0 ? Q01 : g == 1 ? (Q01 >> 8) : g == 2 ? Q23 : (Q23 >> 8);
+                const float2 smr = __half22float2(u32_as_h2(mrw[g]));    // (scale, min) token r
+                const float2 smr8 = __half22float2(u32_as_h2(mr8w[g]));  // token r + 8
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int hs = 0; hs < 2; ++hs) {
+                        const uint32_t m0 = 0x00030003u << (4 * hs), m1 = 0x00030003u << (4 * hs + 2);
+                        const uint32_t a[4] = {xr & m0, xr8 & m0, xr & m1, xr8 & m1};
+                        mma_f16_16816(c, a, bq[nt][2 * g + hs][0], bq[nt][2 * g + hs][1]);
+                    }
+                    acc_r[nt] = fmaf(smr.x, c[0] + c[1], acc_r[nt]);
+                    acc_r8[nt] = fmaf(smr8.x, c[2] + c[3], acc_r8[nt]);
+                    mn_r[nt] = fmaf(smr.y, gsum[nt][g], mn_r[nt]);
+                    mn_r8[nt] = fmaf(smr8.y, gsum[nt][g], mn_r8[nt]);
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                lg[nt][0] = r < n_tok ? fmaf(acc_r[nt], inv_sig[nt], mn_r[nt]) : -CUDART_INF_F;
+                lg[nt][1] = r + 8 < n_tok ? fmaf(acc_r8[nt], inv_sig[nt], mn_r8[nt]) : -CUDART_INF_F;
+            }
+        }
+
+        // ---------------- online softmax (base 2), head 4*nt + t
+        float corr[NT];
+        bool need = false;
+        float pr[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            float pm = fmaxf(lg[nt][0], lg[nt][1]);
+            pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+            pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+            pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+            corr[nt] = 1.f;
+            if (pm > mrun[nt]) {
+                corr[nt] = exp2f(mrun[nt] - pm);  // 0 when mrun = -inf
+                mrun[nt] = pm;
+                need = true;
+            }
+            const float mref = mrun[nt] == -CUDART_INF_F ? 0.f : mrun[nt];
+            pr[nt][0] = exp2f(lg[nt][0] - mref);
+            pr[nt][1] = exp2f(lg[nt][1] - mref);
+            lsum[nt] = fmaf(lsum[nt], corr[nt], pr[nt][0] + pr[nt][1]);
+        }
+        if (__any_sync(0xffffffffu, need)) {
+            // PV columns 2t, 2t+1 hold heads 2t, 2t+1, whose maxima live in lanes (2t)&3, (2t+1)&3
+            const int hA = 2 * t, hB = 2 * t + 1;
+            float cA = __shfl_sync(0xffffffffu, corr[0], hA & 3), cB = __shfl_sync(0xffffffffu, corr[0], hB & 3);
+            if constexpr (NT == 2) {
+                const float cA1 = __shfl_sync(0xffffffffu, corr[1], hA & 3);
+                const float cB1 = __shfl_sync(0xffffffffu, corr[1], hB & 3);
+                if (hA >= 4) cA = cA1;
+                if (hB >= 4) cB = cB1;
+            }
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                oacc[m][0] *= cA;
+                oacc[m][2] *= cA;
+                oacc[m][1] *= cB;
+                oacc[m][3] *= cB;
+            }
+            cmin[0] *= cA;
+            cmin[2] *= cA;
+            cmin[1] *= cB;
+            cmin[3] *= cB;
+        }
+
+        // ---------------- P in the PV B layout: column n = r (head n), rows = tokens 2t, 2t+1 | 2t+8, 2t+9
+        uint32_t pb0, pb1;
+        {
+            const uint32_t X0 = pack_half2(pr[0][0], pr[0][1]);  // (token r, token r+8) of head t
+            const int srcA = 8 * t + (r & 3), srcB = 8 * t + 4 + (r & 3);
+            uint32_t Y0 = __shfl_sync(0xffffffffu, X0, srcA), Y1 = __shfl_sync(0xffffffffu, X0, srcB);
+            if constexpr (NT == 2) {
+                const uint32_t X1 = pack_half2(pr[1][0], pr[1][1]);
+                const uint32_t Z0 = __shfl_sync(0xffffffffu, X1, srcA), Z1 = __shfl_sync(0xffffffffu, X1, srcB);
+                if (r >= 4) {
+                    Y0 = Z0;
+                    Y1 = Z1;
+                }
+            }
+            if (r >= G) Y0 = Y1 = 0u;
+            pb0 = prmt(Y0, Y1, 0x5410);  // p(2t), p(2t+1)
+            pb1 = prmt(Y0, Y1, 0x7632);  // p(2t+8), p(2t+9)
+        }
+
+        // ---------------- PV
+        {
+            const uint4 m0 = lds128(tile + OFF_VM + 16 * (2 * t));
+            const uint4 m1 = lds128(tile + OFF_VM + 16 * (2 * t + 1));
+            const uint4 m8 = lds128(tile + OFF_VM + 16 * (2 * t + 8));
+            const uint4 m9 = lds128(tile + OFF_VM + 16 * (2 * t + 9));
+            const uint32_t w0[4] = {m0.x, m0.y, m0.z, m0.w}, w1[4] = {m1.x, m1.y, m1.z, m1.w};
+            const uint32_t w8[4] = {m8.x, m8.y, m8.z, m8.w}, w9[4] = {m9.x, m9.y, m9.z, m9.w};
+            // slots past the context may hold stale bytes (even NaN scales): zero their fp16 words
+            const uint32_t vm01 = (2 * t < n_tok ? 0x0000ffffu : 0u) | (2 * t + 1 < n_tok ? 0xffff0000u : 0u);
+            const uint32_t vm89 = (2 * t + 8 < n_tok ? 0x0000ffffu : 0u) | (2 * t + 9 < n_tok ? 0xffff0000u : 0u);
+
+            // min term: rows = groups (r < 4), K = tokens
+            {
+                uint32_t a[4] = {0u, 0u, 0u, 0u};
+                if (r < NGROUP) {
+                    a[0] = prmt(lds32(tile + OFF_VM + 16 * (2 * t) + 4 * r),
+                                lds32(tile + OFF_VM + 16 * (2 * t + 1) + 4 * r), 0x7632) & vm01;
+                    a[2] = prmt(lds32(tile + OFF_VM + 16 * (2 * t + 8) + 4 * r),
+                                lds32(tile + OFF_VM + 16 * (2 * t + 9) + 4 * r), 0x7632) & vm89;
+                }
+                mma_f16_16816(cmin, a, pb0, pb1);
+            }
+
+            const uint32_t v0 = lds32(tile + OFF_VC + 32 * (2 * t) + 4 * r);
+            const uint32_t v1 = lds32(tile + OFF_VC + 32 * (2 * t + 1) + 4 * r);
+            const uint32_t v8 = lds32(tile + OFF_VC + 32 * (2 * t + 8) + 4 * r);
+            const uint32_t v9 = lds32(tile + OFF_VC + 32 * (2 * t + 9) + 4 * r);
+            const uint32_t A01 = prmt(v0, v1, 0x5410), A23 = prmt(v0, v1, 0x7632);
+            const uint32_t B01 = prmt(v8, v9, 0x5410), B23 = prmt(v8, v9, 0x7632);
+#pragma unroll
+            for (int g = 0; g < NGROUP; ++g) {
+                const uint32_t xa = g == 0 ? A01 : g == 1 ? (A01 >> 8) : g == 2 ? A23 : (A23 >> 8);
+                const uint32_t xb = g == 0 ? B01 : g == 1 ? (B01 >> 8) : g == 2 ? B23 : (B23 >> 8);
+                const uint32_t sc01 = prmt(w0[g], w1[g], 0x5410) & vm01, sc89 = prmt(w8[g], w9[g], 0x5410) & vm89;
+                const uint32_t W0 = h2_as_u32(__hmul2(u32_as_h2(pb0), u32_as_h2(sc01)));
+                const uint32_t W1 = h2_as_u32(__hmul2(u32_as_h2(pb1), u32_as_h2(sc89)));
+#pragma unroll
+                for (int hs = 0; hs < 2; ++hs) {
+                    const uint32_t k0 = 0x00030003u << (4 * hs), k1 = 0x00030003u << (4 * hs + 2);
+                    const uint32_t a[4] = {xa & k0, xa & k1, xb & k0, xb & k1};
+                    mma_f16_16816(oacc[2 * g + hs], a, W0, W1);
+                }
+            }
+        }
+
+        __syncwarp();
+        if (lane == 0 && i + DEC_STAGES < my_count) {
+            fence_proxy_async_smem();
+            issue(i + DEC_STAGES);
+        }
+    }
+    if (timed_out && lane == 0) {
+        // let copies still in flight land before the shared memory is reused
+        for (int s = 0; s < DEC_STAGES; ++s) (void)mbar_wait_bounded(&sm.bar[warp][s], 0, 1000000LL);
+    }
+
+    // ---------------- warp partial -> shared memory
+    __syncthreads();  // all warps are done with the ring (o_part aliases it)
+    {
+        // min term of (group g, head 2t / 2t+1) lives in lane 4g + t
+        float cm[NGROUP][2];
+#pragma unroll
+        for (int g = 0; g < NGROUP; ++g) {
+            cm[g][0] = __shfl_sync(0xffffffffu, cmin[0], 4 * g + t);
+            cm[g][1] = __shfl_sync(0xffffffffu, cmin[1], 4 * g + t);
+        }
+#pragma unroll
+        for (int g = 0; g < NGROUP; ++g)
+#pragma unroll
+            for (int hs = 0; hs < 2; ++hs) {
+                const int m = 2 * g + hs;
+                const int ch0 = 32 * g + 4 * r + 2 * hs;     // row r, k = 2hs
+                const float f0 = ldexpf(1.f, 24 - 4 * hs);  // 2^24 / 4^(2hs)
+                const float f1 = f0 * 0.25f;                     // row r + 8, k = 2hs + 1
+                if (2 * t < G) {
+                    sm.u.o_part[warp][2 * t][ch0] = fmaf(oacc[m][0], f0, cm[g][0]);
+                    sm.u.o_part[warp][2 * t][ch0 + 1] = fmaf(oacc[m][2], f1, cm[g][0]);
+                }
+                if (2 * t + 1 < G) {
+                    sm.u.o_part[warp][2 * t + 1][ch0] = fmaf(oacc[m][1], f0, cm[g][1]);
+                    sm.u.o_part[warp][2 * t + 1][ch0 + 1] = fmaf(oacc[m][3], f1, cm[g][1]);
+                }
+            }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            float l = lsum[nt];
+            l += __shfl_xor_sync(0xffffffffu, l, 4);
+            l += __shfl_xor_sync(0xffffffffu, l, 8);
+            l += __shfl_xor_sync(0xffffffffu, l, 16);
+            const int hq = 4 * nt + t;
+            if (r == 0 && hq < G) {
+                sm.m_part[warp][hq] = mrun[nt];
+                sm.l_part[warp][hq] = l;
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---------------- CTA merge -> split partial in the workspace
+    const int c = tid;
+    for (int jj = 0; jj < G; ++jj) {
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int w = 0; w < DEC_WARPS; ++w) M = fmaxf(M, sm.m_part[w][jj]);
+        float L = 0.f, O = 0.f;
+        if (M != -CUDART_INF_F) {
+#pragma unroll
+            for (int w = 0; w < DEC_WARPS; ++w) {
+                const float f = exp2f(sm.m_part[w][jj] - M);
+                L = fmaf(sm.l_part[w][jj], f, L);
+                O = fmaf(sm.u.o_part[w][jj][c], f, O);
+            }
+        }
+        float* part = partials + (((size_t)b * H_q + (size_t)h * G + jj) * S + split) * PART_STRIDE;
+        part[4 + c] = O;
+        if (c == 0) {
+            part[0] = M;
+            part[1] = L;
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const int prev = atomicAdd(tickets + (size_t)b * H_kv + h, 1);
+        sm.is_last = prev == S - 1;
+    }
+    __syncthreads();
+    if (!sm.is_last) return;
+    __threadfence();
+
+    // ---------------- last CTA: merge the S splits, rotate back, write out
+    for (int jj = 0; jj < G; ++jj) {
+        const float* base = partials + (((size_t)b * H_q + (size_t)h * G + jj) * S) * PART_STRIDE;
+        float M = -CUDART_INF_F;
+        for (int s = 0; s < S; ++s) M = fmaxf(M, __ldcg(base + (size_t)s * PART_STRIDE));
+        float L = 0.f, O = 0.f;
+        if (M != -CUDART_INF_F) {
+            for (int s = 0; s < S; ++s) {
+                const float* ps = base + (size_t)s * PART_STRIDE;
+                const float f = exp2f(__ldcg(ps) - M);
+                L = fmaf(__ldcg(ps + 1), f, L);
+                O = fmaf(__ldcg(ps + 4 + c), f, O);
+            }
+        }
+        sm.o_final[jj][c] = L > 0.f ? O / L : 0.f;
+    }
+    __syncthreads();
+    {
+        // o_i = sum_j o'_j R_v[i][j]
+        const float4* Rrow = reinterpret_cast<const float4*>(Rv + ((size_t)h * D + c) * D);
+        float acc[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) acc[jj] = 0.f;
+        for (int j4 = 0; j4 < D / 4; ++j4) {
+            const float4 rv = __ldg(Rrow + j4);
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj)
+                if (jj < G) {
+                    const float* o = &sm.o_final[jj][4 * j4];
+                    acc[jj] = fmaf(o[0], rv.x, fmaf(o[1], rv.y, fmaf(o[2], rv.z, fmaf(o[3], rv.w, acc[jj]))));
+                }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj)
+            if (jj < G) out[((size_t)b * H_q + (size_t)h * G + jj) * D + c] = acc[jj];
+    }
+    if (tid == 0) tickets[(size_t)b * H_kv + h] = 0;
+}
+
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" int kvq_decode_auto_splits(int B, int H_kv, int max_pages_per_seq) {
+    if (B <= 0 || H_kv <= 0 || max_pages_per_seq <= 0) return 1;
+    // about three resident CTAs per SM of the 152; at least 16 pages per split
+    const long units = (long)B * H_kv;
+    const long target = 152L * 3;
+    long s = (target + units - 1) / units;
+    const long max_s = (max_pages_per_seq + 15) / 16;
+    if (s > max_s) s = max_s;
+    if (s < 1) s = 1;
+    return (int)s;
+}
+
+extern "C" size_t kvq_decode_workspace_bytes(int B, int H_q, int H_kv, int max_pages_per_seq, int num_splits) {
+    if (B <= 0 || H_q <= 0 || H_kv <= 0) return 0;
+    const int S = num_splits > 0 ? num_splits : kvq_decode_auto_splits(B, H_kv, max_pages_per_seq);
+    return WS_HEADER + tickets_bytes(B, H_kv) + (size_t)B * H_q * S * PART_STRIDE * sizeof(float);
+}
+
+extern "C" kvq_status kvq_decode_attn_int2(const void* q, int B, int H_q, int H_kv, int d, const void* cache,
+                                           int64_t num_pages, const int32_t* block_table, int max_pages_per_seq,
+                                           const int32_t* context_lens, const float* R_k, const float* R_v,
+                                           float scale, float* out, void* workspace, size_t workspace_bytes,
+                                           int num_splits, void* stream) {
+    if (d != D) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "kvq_decode_attn_int2: d=%d (only 128)", d);
+    if (B <= 0 || H_kv <= 0 || H_q <= 0 || H_q % H_kv || max_pages_per_seq <= 0 || num_pages <= 0 ||
+        num_splits < 0)
+        return kvq_set_error(KVQ_ERR_INVALID_ARG,
+                             "kvq_decode_attn_int2: B=%d H_q=%d H_kv=%d max_pages=%d num_pages=%lld splits=%d", B,
+                             H_q, H_kv, max_pages_per_seq, (long long)num_pages, num_splits);
+    const int G = H_q / H_kv;
+    if (G > 8) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "kvq_decode_attn_int2: GQA group %d > 8", G);
+    if (B > 65535 || H_kv > 65535)
+        return kvq_set_error(KVQ_ERR_UNSUPPORTED, "kvq_decode_attn_int2: B or H_kv above 65535");
+    if (!q || !cache || !block_table || !context_lens || !R_k || !R_v || !out || !workspace)
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_decode_attn_int2: null pointer");
+    if (reinterpret_cast<uintptr_t>(cache) % 16 || reinterpret_cast<uintptr_t>(workspace) % 16 ||
+        reinterpret_cast<uintptr_t>(R_v) % 16)
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_decode_attn_int2: cache, R_v and workspace need 16-byte alignment");
+    const int S = num_splits > 0 ? num_splits : kvq_decode_auto_splits(B, H_kv, max_pages_per_seq);
+    const size_t need = kvq_decode_workspace_bytes(B, H_q, H_kv, max_pages_per_seq, S);
+    if (workspace_bytes < need)
+        return kvq_set_error(KVQ_ERR_WORKSPACE, "kvq_decode_attn_int2: workspace %zu < %zu bytes", workspace_bytes,
+                             need);
+    const float scale_log2 = scale * 1.4426950408889634f;
+    const size_t smem = sizeof(DecodeSmem);
+    dim3 grid(S, H_kv, B);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (G <= 4) {
+        static_assert(sizeof(DecodeSmem) < 48 * 1024, "decode smem above the default limit");
+        decode_int2_kernel<1><<<grid, 128, smem, st>>>(
+            static_cast<const __nv_bfloat16*>(q), H_q, H_kv, G, static_cast<const uint8_t*>(cache), num_pages,
+            block_table, max_pages_per_seq, context_lens, R_k, R_v, scale_log2, out, static_cast<uint8_t*>(workspace));
+    } else {
+        decode_int2_kernel<2><<<grid, 128, smem, st>>>(
+            static_cast<const __nv_bfloat16*>(q), H_q, H_kv, G, static_cast<const uint8_t*>(cache), num_pages,
+            block_table, max_pages_per_seq, context_lens, R_k, R_v, scale_log2, out, static_cast<uint8_t*>(workspace));
+    }
+    e = cudaGetLastError();
+    return kvq_check_cuda(e, "kvq_decode_attn_int2 launch");
+}
+
+extern "C" kvq_status kvq_workspace_status(void* workspace, void* stream) {
+    if (!workspace) return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_workspace_status: null workspace");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    kvq_status s = kvq_check_cuda(cudaMemcpyAsync(&word, workspace, 4, cudaMemcpyDeviceToHost, st), "status read");
+    if (s != KVQ_OK) return s;
+    s = kvq_check_cuda(cudaStreamSynchronize(st), "status sync");
+    if (s != KVQ_OK) return s;
+    if (word) {
+        s = kvq_check_cuda(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+        if (s != KVQ_OK) return s;
+        s = kvq_check_cuda(cudaStreamSynchronize(st), "status clear sync");
+        if (s != KVQ_OK) return s;
+    }
+    if (word & ERR_TIMEOUT) return kvq_set_error(KVQ_ERR_CUDA, "decode: an in-kernel wait timed out");
+    if (word & ERR_BAD_PAGE) return kvq_set_error(KVQ_ERR_BAD_BLOCK_TABLE, "decode: block table entry out of range");
+    return KVQ_OK;
+}

@@ -1,0 +1,196 @@
+/*
+ * kvq.h - C ABI of the rotated low-bit KV-cache library (libkvq.so).
+ *
+ * Two cache formats, each with a quantise-on-append call and a fused
+ * packed-cache decode-attention call, plus two host-only helpers:
+ *
+ *   INT2     "Output-Aware Rotation for INT2 KV-Cache Quantization":
+ *            keys centred per head (§1, attention-equivalent
+ *            reparameterisation), rotated z = (k - mu) R_k and values
+ *            w = v R_v (§3.1 Eq. 4, row-vector convention), then INT2 group
+ *            quantisation Q2 with groups of 32 rotated channels and fp16
+ *            (scale, min) per group (§1: all values of a group share one
+ *            scale; clip ratio c = 1).  Decode attends in the rotated basis
+ *            (§3 Eqs. 1-2 with Eq. 4 folded in): q' = q R_k once per query
+ *            head, o' = sum_s p_s Q2(w_s), o = o' R_v^T once.
+ *   Block-GTQ "RoPE-Aware Bit Allocation for KV-Cache Quantization":
+ *            greedy per-RoPE-block widths (prerequisites, Theorem 1; method
+ *            step 2), grouped TQ-MSE key encoding (step 3), uniform TQ-MSE
+ *            values (step 4), packed-cache decode (Figure 2).
+ *
+ * Conventions (all calls):
+ *  - d (head dimension) must be 128; the page size is 16 tokens.
+ *  - Device pointers are owned by the caller; the library allocates no
+ *    memory and keeps no global state besides the thread-local error text.
+ *  - Device work is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and is asynchronous: faults surface at the caller's
+ *    next synchronisation.  Argument errors are detected on the host before
+ *    any launch and returned as a kvq_status; nothing is launched then.
+ *  - Tensors are dense row-major: k, v [n_tok][H_kv][d] bf16;
+ *    q [B][H_q][d] bf16; out [B][H_q][d] fp32; block_table [B][max_pages]
+ *    int32 physical page ids; context_lens [B] int32 tokens to attend.
+ *  - Query head j reads KV head j / (H_q / H_kv) (contiguous GQA groups).
+ *  - slot_mapping[t] = page * 16 + slot; -1 skips token t.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KVQ_OK = 0,
+    KVQ_ERR_INVALID_ARG = -1,     /* bad size, null pointer, misalignment */
+    KVQ_ERR_UNSUPPORTED = -2,     /* d != 128, GQA group > 8, widths > 8 ... */
+    KVQ_ERR_WORKSPACE = -3,       /* workspace too small */
+    KVQ_ERR_CUDA = -4,            /* a CUDA runtime call failed */
+    KVQ_ERR_BAD_BLOCK_TABLE = -5  /* reported by kvq_workspace_status */
+} kvq_status;
+
+/* Text of the last error on this thread ("" if none). */
+const char* kvq_last_error(void);
+
+/* ------------------------------------------------------------------ INT2 */
+
+/* Bytes of one (page, KV head) tile of the INT2 cache (1536 at d = 128):
+ *   [   0,  512) K codes, 16 slots x 32 B
+ *   [ 512,  768) K meta, 16 slots x 4 groups x (fp16 scale, fp16 min)
+ *   [ 768, 1280) V codes
+ *   [1280, 1536) V meta
+ * The cache is tiles[num_pages][H_kv].  A 32-byte code record stores
+ * channel 32*g + 4*b + c (g = 0..3 group, b = 0..7, c = 0..3) in bits
+ * 2c..2c+1 of byte 4*b + g.  Returns 0 for unsupported d. */
+size_t kvq_int2_tile_bytes(int d);
+
+/* Quantise-on-append of n_tok tokens into the INT2 cache.
+ *   k, v      device bf16 [n_tok][H_kv][d]
+ *   mu_k      device fp32 [H_kv][d] key centre (fixed offline)
+ *   R_k, R_v  device fp32 [H_kv][d][d] orthogonal rotations, row-major,
+ *             applied as z = (k - mu_k) R_k, w = v R_v
+ *   cache     device, num_pages * H_kv * kvq_int2_tile_bytes(d) bytes
+ *   dbg_rot_k, dbg_rot_v  nullable device fp32 [n_tok][H_kv][d]: the
+ *             rotated vectors the codes were decided from
+ *   err_count nullable device int32: incremented once per token whose
+ *             slot lies outside [0, num_pages*16) (other than -1); such
+ *             tokens are skipped.
+ * Each rotated coordinate is an fp32 fused-multiply-add chain over the
+ * input coordinates in ascending order; per 32-channel group
+ * scale = fp16(fp32(fp32(max - min) / 3)), min = fp16(min) (saturating at
+ * +-65504); code = number of thresholds min + (c + 1/2) scale (c = 0..2)
+ * strictly below the value (ties to the lower level), 0 when scale == 0.
+ * Tokens with equal slots race (last writer unspecified). */
+kvq_status kvq_append_int2(const void* k, const void* v, int n_tok, int H_kv, int d,
+                           const int32_t* slot_mapping, const float* mu_k,
+                           const float* R_k, const float* R_v,
+                           void* cache, int64_t num_pages,
+                           float* dbg_rot_k, float* dbg_rot_v, int32_t* err_count,
+                           void* stream);
+
+/* Bytes of decode workspace for B sequences, H_q query heads, H_kv KV heads
+ * and num_splits split-K partitions (num_splits = 0: the number the
+ * automatic choice would take for max_pages_per_seq pages).  The workspace
+ * must be zero-filled once before its first use; every call leaves its
+ * counters at zero again. */
+size_t kvq_decode_workspace_bytes(int B, int H_q, int H_kv, int max_pages_per_seq, int num_splits);
+
+/* The split count the automatic choice (num_splits = 0) uses. */
+int kvq_decode_auto_splits(int B, int H_kv, int max_pages_per_seq);
+
+/* Fused packed-cache decode attention over the INT2 cache.
+ *   q            device bf16 [B][H_q][d]
+ *   cache        as written by kvq_append_int2 (num_pages pages)
+ *   block_table  device int32 [B][max_pages_per_seq]
+ *   context_lens device int32 [B], 0 <= len <= 16 * max_pages_per_seq
+ *   R_k, R_v     as for append
+ *   scale        logit scale (1/sqrt(d) for Eq. 1)
+ *   out          device fp32 [B][H_q][d]: o = softmax(q'.Q2(z)*scale) Q2(w) R_v^T
+ *                (zeros for an empty context)
+ *   workspace    device, >= kvq_decode_workspace_bytes(...), zeroed once
+ *   num_splits   split-K partitions per sequence (0 = automatic)
+ * Block-table entries outside [0, num_pages) are not read: their tokens are
+ * dropped and kvq_workspace_status reports KVQ_ERR_BAD_BLOCK_TABLE. */
+kvq_status kvq_decode_attn_int2(const void* q, int B, int H_q, int H_kv, int d,
+                                const void* cache, int64_t num_pages,
+                                const int32_t* block_table, int max_pages_per_seq,
+                                const int32_t* context_lens,
+                                const float* R_k, const float* R_v, float scale,
+                                float* out, void* workspace, size_t workspace_bytes,
+                                int num_splits, void* stream);
+
+/* Reads (synchronously, on `stream`) and clears the error word a decode call
+ * left in its workspace: KVQ_OK, KVQ_ERR_BAD_BLOCK_TABLE, or KVQ_ERR_CUDA
+ * when an in-kernel wait gave up. */
+kvq_status kvq_workspace_status(void* workspace, void* stream);
+
+/* ------------------------------------------------------------- Block-GTQ */
+
+/* Host only.  Centroids (ascending, fp64) of the 2^b-level Lloyd-Max
+ * quantiser of a standard Gaussian, 1 <= b <= 8, written to
+ * centroids_out[0 .. 2^b).  The TQ-MSE scalar quantiser of an n-dimensional
+ * sub-vector at width b uses fp32(c / sqrt(n)). */
+kvq_status bgtq_lloyd_max_codebook(int b, double* centroids_out);
+
+/* Host only.  Greedy RoPE-block width allocation (Theorem 1): every block
+ * starts at b_min; one bit at a time goes to the block with the largest
+ * marginal gain (3/4) s_i 4^-b_i among blocks below b_max (ties: lowest
+ * index), until sum(widths) == total_bits or every block is at b_max.
+ *   scores      host fp64 [n_blocks], finite and >= 0
+ *   widths_out  host int8 [n_blocks]
+ * Requires 1 <= b_min <= b_max <= 8 and total_bits >= n_blocks * b_min. */
+kvq_status bgtq_allocate(const double* scores, int n_blocks, int b_min, int b_max,
+                         int64_t total_bits, int8_t* widths_out);
+
+/* Bytes of one (page, KV head) Block-GTQ tile for a per-head key width
+ * budget total_bits (sum over the 64 blocks) and value width v_bits:
+ *   [0, 16*KB)          K codes, KB = 4*ceil(2*total_bits/32) bytes per slot:
+ *                       LSB-first bit stream, groups by ascending width
+ *                       1..8, each group's coordinates in order
+ *   [16*KB, +256)       K norms, 8 fp16 per slot (entry b-1 = width-b group,
+ *                       0 if that group is empty)
+ *   [.., +16*VB)        V codes, VB = 16*v_bits bytes per slot
+ *   [.., +32)           V norm, fp16 per slot
+ * Returns 0 for unsupported arguments. */
+size_t bgtq_tile_bytes(int total_bits, int v_bits);
+
+/* Quantise-on-append into the Block-GTQ cache.
+ *   k, v        device bf16 [n_tok][H_kv][d] (k post-RoPE)
+ *   widths      device int8 [H_kv][d/2] per-block widths in 1..8 whose sum
+ *               is at most total_bits (as bgtq_allocate returns them)
+ *   pi_table    device fp32: shared orthogonal Pi_n (row-major n x n) for
+ *               every even n <= d, Pi_n at pi_table + pi_offsets[n]
+ *   pi_offsets  device int64 [d + 1] (-1 for odd n)
+ *   codebooks   device fp64 [8][256]: row b-1 = bgtq_lloyd_max_codebook(b)
+ * Key: RoPE block i = dims (i, i + d/2); blocks of equal width b form a
+ * sub-vector (ascending block index, each block as its two dims) of length
+ * n; r = ||x|| (fp32 fma chain of squares, correctly rounded sqrt),
+ * u = x / r, y = u Pi_n (fp32 fma chain), code = nearest of
+ * fp32(c_b / sqrt(n)) (ties to the lower index), norm = fp16(r).
+ * Value: the same with n = d and width v_bits. */
+kvq_status bgtq_append(const void* k, const void* v, int n_tok, int H_kv, int d,
+                       const int32_t* slot_mapping, const int8_t* widths, int total_bits,
+                       int v_bits, const float* pi_table, const int64_t* pi_offsets,
+                       const double* codebooks, void* cache, int64_t num_pages,
+                       int32_t* err_count, void* stream);
+
+/* Fused packed-cache decode attention over the Block-GTQ cache; arguments as
+ * kvq_decode_attn_int2 plus the format parameters of bgtq_append.  Logits
+ * are <q, k^>*scale with k^ the decoded post-RoPE key; out = softmax . V^. */
+kvq_status bgtq_decode_attn(const void* q, int B, int H_q, int H_kv, int d,
+                            const void* cache, int64_t num_pages,
+                            const int32_t* block_table, int max_pages_per_seq,
+                            const int32_t* context_lens,
+                            const int8_t* widths, int total_bits, int v_bits,
+                            const float* pi_table, const int64_t* pi_offsets,
+                            const double* codebooks, float scale,
+                            float* out, void* workspace, size_t workspace_bytes,
+                            int num_splits, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -21,3 +21,13 @@ def lib():
         pytest.skip("no CUDA device")
     from bit_kv_cache_13_gb300 import _lib
     return _lib.load()
+
+
+def pytest_collection_modifyitems(config, items):
+    import torch
+    if torch.cuda.is_available():
+        return
+    skip = pytest.mark.skip(reason="no CUDA device")
+    for item in items:
+        if "gpu" in item.keywords:
+            item.add_marker(skip)

@@ -1,0 +1,77 @@
+"""The C-ABI library builds, loads and exports every entry point that
+include/kvq.h declares; host-only entry points work without a GPU."""
+import os
+
+import numpy as np
+import pytest
+
+from bit_kv_cache_13_gb300 import _lib, build
+from oracle import bgtq
+
+
+@pytest.fixture(scope="module")
+def cpu_lib():
+    if not os.path.exists(_lib.LIB_PATH):
+        build.build()
+    return _lib.load()
+
+
+def test_exports_every_declared_symbol(cpu_lib):
+    names = _lib.header_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(cpu_lib, n), n
+    assert set(names) == set(_lib._SIGS), set(names) ^ set(_lib._SIGS)
+
+
+def test_sizes(cpu_lib):
+    assert _lib.kvq_int2_tile_bytes(128) == 1536
+    assert _lib.kvq_int2_tile_bytes(64) == 0
+    assert _lib.bgtq_tile_bytes(192, 3) == 16 * (48 + 16 + 48 + 2)
+    assert _lib.bgtq_tile_bytes(192, 3) == bgtq.tile_layout(192, 3)["tile"]
+    ws = _lib.kvq_decode_workspace_bytes(2, 8, 2, 100, 3)
+    assert ws >= 2 * 8 * 3 * 132 * 4
+
+
+def test_allocator_matches_oracle(cpu_lib):
+    rng = np.random.default_rng(0)
+    for trial in range(50):
+        s = rng.lognormal(0, 2, 64)
+        if trial % 5 == 0:
+            s[rng.integers(0, 64, 8)] = s[0]          # ties
+        bmin, bmax = [(1, 8), (2, 4), (1, 3)][trial % 3]
+        total = int(rng.integers(64 * bmin, 64 * bmax + 10))
+        got = _lib.bgtq_allocate(s, bmin, bmax, total)
+        assert np.array_equal(got, bgtq.greedy_allocate(s, bmin, bmax, total))
+
+
+def test_allocator_rejects_bad_arguments(cpu_lib):
+    with pytest.raises(_lib.KvqError):
+        _lib.bgtq_allocate(np.ones(4), 3, 2, 20)
+    with pytest.raises(_lib.KvqError):
+        _lib.bgtq_allocate(np.ones(4), 1, 8, 3)
+    with pytest.raises(_lib.KvqError):
+        _lib.bgtq_allocate(np.array([1.0, np.nan]), 1, 8, 4)
+
+
+def test_codebooks_match_oracle(cpu_lib):
+    table = bgtq.lloyd_max_table()
+    for b in range(1, 9):
+        got = _lib.bgtq_lloyd_max_codebook(b)
+        want = table[b - 1, : 2 ** b]
+        assert np.max(np.abs(got - want)) <= 1e-9, b
+        # the fp32 tables both sides quantise against agree bit for bit
+        for n in (2, 16, 128):
+            assert np.array_equal((got / np.sqrt(n)).astype(np.float32), (want / np.sqrt(n)).astype(np.float32)), (b, n)
+
+
+def test_device_calls_reject_bad_arguments_before_launch(cpu_lib):
+    L = cpu_lib
+    # d != 128 and null pointers are refused on the host
+    assert L.kvq_append_int2(None, None, 1, 1, 64, None, None, None, None, None, 1, None, None, None, None) == -2
+    assert L.kvq_append_int2(None, None, 1, 1, 128, None, None, None, None, None, 1, None, None, None, None) == -1
+    assert L.kvq_decode_attn_int2(None, 1, 12, 1, 128, None, 1, None, 1, None, None, None, 0.1, None, None, 0, 0,
+                                  None) == -2
+    assert L.kvq_decode_attn_int2(None, 1, 6, 4, 128, None, 1, None, 1, None, None, None, 0.1, None, None, 0, 0,
+                                  None) == -1
+    assert b"GQA" in L.kvq_last_error() or b"H_q" in L.kvq_last_error()
