@@ -18,16 +18,16 @@
 //       columns, pre-scaled by 4^-k and a per-head power of two.
 //   softmax  online, base 2, exact running maximum per head.
 //   PV  o'(j, i) = sum_s p_{s,j} scale_{s,g} c_{s,i} + sum_s p_{s,j} min_{s,g}
-//       rows = channels (codes again as fp16 subnormals), K = the 16 tokens,
-//       B = p * scale (fp16); the min term is one more MMA with A = the fp16
-//       mins of the four groups.
+//       rows = channels (codes again as fp16 subnormals), K = the 16 tokens.
+//       p is rounded to fp16 once (p^); B = p^ * scale as an exact fp16
+//       hi/lo pair (HMUL2, then HFMA2 for the remainder), so the large
+//       group minima and the code term cancel without amplifying rounding;
+//       the min term is one more MMA with A = the fp16 mins of the groups.
 //
 // Split partials (m, l, o') go to the workspace; the last CTA of a
 // (sequence, KV head) to finish (atomic ticket, no waiting) merges them,
 // applies R_v^T and writes the output.
-#include <math_constants.h>
-
-#include "kvq_common.cuh"
+#include "merge.cuh"
 
 namespace kvq {
 
@@ -43,10 +43,7 @@ struct __align__(16) DecodeSmem {
     float q[8][D];        // scaled rotated queries q~ = q R_k * scale * log2(e)
     float gsum[8][NGROUP];
     float sigma[8];       // power-of-two pre-scale per head
-    float m_part[DEC_WARPS][8];
-    float l_part[DEC_WARPS][8];
-    float o_final[8][D];
-    int is_last;
+    MergeSmem<DEC_WARPS> ms;
 };
 
 template <int NT>
@@ -65,8 +62,6 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     const int r = lane >> 2, t = lane & 3;
 
     uint32_t* err_word = reinterpret_cast<uint32_t*>(ws);
-    int32_t* tickets = reinterpret_cast<int32_t*>(ws + WS_HEADER);
-    float* partials = reinterpret_cast<float*>(ws + WS_HEADER + tickets_bytes(gridDim.z, H_kv));
 
     int ctx = __ldg(context_lens + b);
     ctx = max(0, min(ctx, max_pages * PAGE));
@@ -103,22 +98,9 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     // ---- q~ = (q R_k) * scale * log2(e) for the G heads of this KV head
     {
         const __nv_bfloat16* qb = q + ((size_t)b * H_q + (size_t)h * G) * D;
-        for (int idx = tid; idx < G * D; idx += 128) sm.o_final[idx / D][idx % D] = __bfloat162float(qb[idx]);
+        for (int idx = tid; idx < G * D; idx += 128) sm.ms.o_final[idx / D][idx % D] = __bfloat162float(qb[idx]);
         __syncthreads();
-        const float* R = Rk + (size_t)h * D * D;
-        float acc[8];
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) acc[jj] = 0.f;
-        for (int i = 0; i < D; ++i) {
-            const float rv = __ldg(R + i * D + tid);
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj)
-                if (jj < G) acc[jj] = fmaf(sm.o_final[jj][i], rv, acc[jj]);
-        }
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj)
-            if (jj < G) sm.q[jj][tid] = acc[jj] * scale_log2;
-        __syncthreads();
+        rotate_rows<DEC_WARPS>(sm.ms.o_final, Rk + (size_t)h * D * D, G, scale_log2, sm.q, sm.ms);
         // per head: power-of-two pre-scale (max |q~| * sigma in [2^14, 2^15)) and group sums
         for (int jj = warp; jj < G; jj += DEC_WARPS) {
             float mx = 0.f;
@@ -270,8 +252,10 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                 need = true;
             }
             const float mref = mrun[nt] == -CUDART_INF_F ? 0.f : mrun[nt];
-            pr[nt][0] = exp2f(lg[nt][0] - mref);
-            pr[nt][1] = exp2f(lg[nt][1] - mref);
+            // p is rounded to fp16 once; the same p^ weights the codes, the
+            // group minima and the normaliser
+            pr[nt][0] = __half2float(__float2half_rn(exp2f(lg[nt][0] - mref)));
+            pr[nt][1] = __half2float(__float2half_rn(exp2f(lg[nt][1] - mref)));
             lsum[nt] = fmaf(lsum[nt], corr[nt], pr[nt][0] + pr[nt][1]);
         }
         if (__any_sync(0xffffffffu, need)) {
@@ -311,7 +295,8 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                     Y1 = Z1;
                 }
             }
-            if (r >= G) Y0 = Y1 = 0u;
+            // NT == 1: columns 4..7 repeat heads 0..3 and carry the low part of p*scale
+            if ((NT == 1 ? (r & 3) : r) >= G) Y0 = Y1 = 0u;
             pb0 = prmt(Y0, Y1, 0x5410);  // p(2t), p(2t+1)
             pb1 = prmt(Y0, Y1, 0x7632);  // p(2t+8), p(2t+9)
         }
@@ -337,7 +322,8 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                     a[2] = prmt(lds32(tile + OFF_VM + 16 * (2 * t + 8) + 4 * r),
                                 lds32(tile + OFF_VM + 16 * (2 * t + 9) + 4 * r), 0x7632) & vm89;
                 }
-                mma_f16_16816(cmin, a, pb0, pb1);
+                const bool dup = NT == 1 && r >= 4;  // repeated columns stay out of the min term
+                mma_f16_16816(cmin, a, dup ? 0u : pb0, dup ? 0u : pb1);
             }
 
             const uint32_t v0 = lds32(tile + OFF_VC + 32 * (2 * t) + 4 * r);
@@ -351,13 +337,22 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                 const uint32_t xa = g == 0 ? A01 : g == 1 ? (A01 >> 8) : g == 2 ? A23 : (A23 >> 8);
                 const uint32_t xb = g == 0 ? B01 : g == 1 ? (B01 >> 8) : g == 2 ? B23 : (B23 >> 8);
                 const uint32_t sc01 = prmt(w0[g], w1[g], 0x5410) & vm01, sc89 = prmt(w8[g], w9[g], 0x5410) & vm89;
-                const uint32_t W0 = h2_as_u32(__hmul2(u32_as_h2(pb0), u32_as_h2(sc01)));
-                const uint32_t W1 = h2_as_u32(__hmul2(u32_as_h2(pb1), u32_as_h2(sc89)));
+                // p^ * scale exactly as an fp16 pair: hi = rn(p^ s), lo = p^ s - hi (exact)
+                const __half2 P0 = u32_as_h2(pb0), P1 = u32_as_h2(pb1);
+                const __half2 S01 = u32_as_h2(sc01), S89 = u32_as_h2(sc89);
+                const __half2 H0 = __hmul2(P0, S01), H1 = __hmul2(P1, S89);
+                const __half2 L0 = __hfma2(P0, S01, __hneg2(H0)), L1 = __hfma2(P1, S89, __hneg2(H1));
 #pragma unroll
                 for (int hs = 0; hs < 2; ++hs) {
                     const uint32_t k0 = 0x00030003u << (4 * hs), k1 = 0x00030003u << (4 * hs + 2);
                     const uint32_t a[4] = {xa & k0, xa & k1, xb & k0, xb & k1};
-                    mma_f16_16816(oacc[2 * g + hs], a, W0, W1);
+                    if constexpr (NT == 1) {
+                        const bool lo = r >= 4;
+                        mma_f16_16816(oacc[2 * g + hs], a, h2_as_u32(lo ? L0 : H0), h2_as_u32(lo ? L1 : H1));
+                    } else {
+                        mma_f16_16816(oacc[2 * g + hs], a, h2_as_u32(H0), h2_as_u32(H1));
+                        mma_f16_16816(oacc[2 * g + hs], a, h2_as_u32(L0), h2_as_u32(L1));
+                    }
                 }
             }
         }
@@ -383,6 +378,14 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             cm[g][0] = __shfl_sync(0xffffffffu, cmin[0], 4 * g + t);
             cm[g][1] = __shfl_sync(0xffffffffu, cmin[1], 4 * g + t);
         }
+        if constexpr (NT == 1) {
+            // columns 4..7 (lanes t = 2, 3) hold the low parts of heads 0..3
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) oacc[m][e] += __shfl_xor_sync(0xffffffffu, oacc[m][e], 2);
+        }
+        const bool writer = NT == 2 || t < 2;
 #pragma unroll
         for (int g = 0; g < NGROUP; ++g)
 #pragma unroll
@@ -391,11 +394,11 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                 const int ch0 = 32 * g + 4 * r + 2 * hs;     // row r, k = 2hs
                 const float f0 = ldexpf(1.f, 24 - 4 * hs);  // 2^24 / 4^(2hs)
                 const float f1 = f0 * 0.25f;                     // row r + 8, k = 2hs + 1
-                if (2 * t < G) {
+                if (writer && 2 * t < G) {
                     sm.u.o_part[warp][2 * t][ch0] = fmaf(oacc[m][0], f0, cm[g][0]);
                     sm.u.o_part[warp][2 * t][ch0 + 1] = fmaf(oacc[m][2], f1, cm[g][0]);
                 }
-                if (2 * t + 1 < G) {
+                if (writer && 2 * t + 1 < G) {
                     sm.u.o_part[warp][2 * t + 1][ch0] = fmaf(oacc[m][1], f0, cm[g][1]);
                     sm.u.o_part[warp][2 * t + 1][ch0 + 1] = fmaf(oacc[m][3], f1, cm[g][1]);
                 }
@@ -408,82 +411,15 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             l += __shfl_xor_sync(0xffffffffu, l, 16);
             const int hq = 4 * nt + t;
             if (r == 0 && hq < G) {
-                sm.m_part[warp][hq] = mrun[nt];
-                sm.l_part[warp][hq] = l;
+                sm.ms.m_part[warp][hq] = mrun[nt];
+                sm.ms.l_part[warp][hq] = l;
             }
         }
     }
     __syncthreads();
 
-    // ---------------- CTA merge -> split partial in the workspace
-    const int c = tid;
-    for (int jj = 0; jj < G; ++jj) {
-        float M = -CUDART_INF_F;
-#pragma unroll
-        for (int w = 0; w < DEC_WARPS; ++w) M = fmaxf(M, sm.m_part[w][jj]);
-        float L = 0.f, O = 0.f;
-        if (M != -CUDART_INF_F) {
-#pragma unroll
-            for (int w = 0; w < DEC_WARPS; ++w) {
-                const float f = exp2f(sm.m_part[w][jj] - M);
-                L = fmaf(sm.l_part[w][jj], f, L);
-                O = fmaf(sm.u.o_part[w][jj][c], f, O);
-            }
-        }
-        float* part = partials + (((size_t)b * H_q + (size_t)h * G + jj) * S + split) * PART_STRIDE;
-        part[4 + c] = O;
-        if (c == 0) {
-            part[0] = M;
-            part[1] = L;
-        }
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const int prev = atomicAdd(tickets + (size_t)b * H_kv + h, 1);
-        sm.is_last = prev == S - 1;
-    }
-    __syncthreads();
-    if (!sm.is_last) return;
-    __threadfence();
-
-    // ---------------- last CTA: merge the S splits, rotate back, write out
-    for (int jj = 0; jj < G; ++jj) {
-        const float* base = partials + (((size_t)b * H_q + (size_t)h * G + jj) * S) * PART_STRIDE;
-        float M = -CUDART_INF_F;
-        for (int s = 0; s < S; ++s) M = fmaxf(M, __ldcg(base + (size_t)s * PART_STRIDE));
-        float L = 0.f, O = 0.f;
-        if (M != -CUDART_INF_F) {
-            for (int s = 0; s < S; ++s) {
-                const float* ps = base + (size_t)s * PART_STRIDE;
-                const float f = exp2f(__ldcg(ps) - M);
-                L = fmaf(__ldcg(ps + 1), f, L);
-                O = fmaf(__ldcg(ps + 4 + c), f, O);
-            }
-        }
-        sm.o_final[jj][c] = L > 0.f ? O / L : 0.f;
-    }
-    __syncthreads();
-    {
-        // o_i = sum_j o'_j R_v[i][j]
-        const float4* Rrow = reinterpret_cast<const float4*>(Rv + ((size_t)h * D + c) * D);
-        float acc[8];
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) acc[jj] = 0.f;
-        for (int j4 = 0; j4 < D / 4; ++j4) {
-            const float4 rv = __ldg(Rrow + j4);
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj)
-                if (jj < G) {
-                    const float* o = &sm.o_final[jj][4 * j4];
-                    acc[jj] = fmaf(o[0], rv.x, fmaf(o[1], rv.y, fmaf(o[2], rv.z, fmaf(o[3], rv.w, acc[jj]))));
-                }
-        }
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj)
-            if (jj < G) out[((size_t)b * H_q + (size_t)h * G + jj) * D + c] = acc[jj];
-    }
-    if (tid == 0) tickets[(size_t)b * H_kv + h] = 0;
+    finish_decode<DEC_WARPS>(sm.ms, sm.u.o_part, G, H_q, H_kv, gridDim.z, b, h, split, S, ws,
+                             Rv + (size_t)h * D * D, out);
 }
 
 }  // namespace kvq
@@ -496,7 +432,8 @@ extern "C" int kvq_decode_auto_splits(int B, int H_kv, int max_pages_per_seq) {
     const long units = (long)B * H_kv;
     const long target = 152L * 3;
     long s = (target + units - 1) / units;
-    const long max_s = (max_pages_per_seq + 15) / 16;
+    long max_s = (max_pages_per_seq + 15) / 16;
+    if (max_s > MAX_SPLITS) max_s = MAX_SPLITS;
     if (s > max_s) s = max_s;
     if (s < 1) s = 1;
     return (int)s;
@@ -529,6 +466,8 @@ extern "C" kvq_status kvq_decode_attn_int2(const void* q, int B, int H_q, int H_
         reinterpret_cast<uintptr_t>(R_v) % 16)
         return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_decode_attn_int2: cache, R_v and workspace need 16-byte alignment");
     const int S = num_splits > 0 ? num_splits : kvq_decode_auto_splits(B, H_kv, max_pages_per_seq);
+    if (S > MAX_SPLITS)
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_decode_attn_int2: num_splits=%d above %d", S, MAX_SPLITS);
     const size_t need = kvq_decode_workspace_bytes(B, H_q, H_kv, max_pages_per_seq, S);
     if (workspace_bytes < need)
         return kvq_set_error(KVQ_ERR_WORKSPACE, "kvq_decode_attn_int2: workspace %zu < %zu bytes", workspace_bytes,
@@ -539,11 +478,14 @@ extern "C" kvq_status kvq_decode_attn_int2(const void* q, int B, int H_q, int H_
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (G <= 4) {
-        static_assert(sizeof(DecodeSmem) < 48 * 1024, "decode smem above the default limit");
+        cudaError_t a = cudaFuncSetAttribute(decode_int2_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (a != cudaSuccess) return kvq_check_cuda(a, "kvq_decode_attn_int2 smem attribute");
         decode_int2_kernel<1><<<grid, 128, smem, st>>>(
             static_cast<const __nv_bfloat16*>(q), H_q, H_kv, G, static_cast<const uint8_t*>(cache), num_pages,
             block_table, max_pages_per_seq, context_lens, R_k, R_v, scale_log2, out, static_cast<uint8_t*>(workspace));
     } else {
+        cudaError_t a = cudaFuncSetAttribute(decode_int2_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (a != cudaSuccess) return kvq_check_cuda(a, "kvq_decode_attn_int2 smem attribute");
         decode_int2_kernel<2><<<grid, 128, smem, st>>>(
             static_cast<const __nv_bfloat16*>(q), H_q, H_kv, G, static_cast<const uint8_t*>(cache), num_pages,
             block_table, max_pages_per_seq, context_lens, R_k, R_v, scale_log2, out, static_cast<uint8_t*>(workspace));
@@ -567,6 +509,7 @@ extern "C" kvq_status kvq_workspace_status(void* workspace, void* stream) {
         if (s != KVQ_OK) return s;
     }
     if (word & ERR_TIMEOUT) return kvq_set_error(KVQ_ERR_CUDA, "decode: an in-kernel wait timed out");
+    if (word & ERR_BAD_WIDTHS) return kvq_set_error(KVQ_ERR_INVALID_ARG, "decode: widths outside 1..8 or over budget");
     if (word & ERR_BAD_PAGE) return kvq_set_error(KVQ_ERR_BAD_BLOCK_TABLE, "decode: block table entry out of range");
     return KVQ_OK;
 }

@@ -21,7 +21,7 @@ constexpr int OFF_KC = 0, OFF_KM = 512, OFF_VC = 768, OFF_VM = 1280;
 // decode workspace: [header 256 B][tickets][partials]
 constexpr int WS_HEADER = 256;
 constexpr int PART_STRIDE = 132;  // floats per (seq, q head, split): m, l, pad, pad, o[128]
-constexpr uint32_t ERR_BAD_PAGE = 1u, ERR_TIMEOUT = 2u;
+constexpr uint32_t ERR_BAD_PAGE = 1u, ERR_TIMEOUT = 2u, ERR_BAD_WIDTHS = 4u;
 
 // give an mbarrier wait about two seconds at ~2 GHz before declaring failure
 constexpr long long WAIT_LIMIT_CYCLES = 4000000000LL;
