@@ -94,3 +94,72 @@ class Int2Layer:
         """Algorithmic cache bytes one decode reads: 96 B per attended
         token-head (codes + fp16 scale/min of K and V)."""
         return int(self.context_lens.sum().item()) * self.spec.h_kv * 96
+
+
+class BgtqLayer:
+    """One attention layer's Block-GTQ cache and parameters on `device`:
+    per-head widths from the greedy allocator (library, host) over the
+    per-block energy scores, shared TQ rotations, Lloyd-Max codebooks from
+    the library, paged cache filled with bgtq_append."""
+
+    def __init__(self, spec: Spec, layer: int, device="cuda", block_table=None, extra_pages: int = 0,
+                 codebooks=None):
+        self.spec, self.layer, self.device = spec, layer, device
+        ex = spec.extra
+        self.avg_bits, self.v_bits = int(ex.get("avg_bits", 3)), int(ex.get("v_bits", 3))
+        self.b_min, self.b_max = int(ex.get("b_min", 1)), int(ex.get("b_max", 8))
+        self.total_bits = self.avg_bits * (spec.d // 2)
+        self.scores = np.stack([inputs.block_energies(spec, layer, h) for h in range(spec.h_kv)])
+        w = np.stack([_lib.bgtq_allocate(self.scores[h], self.b_min, self.b_max, self.total_bits)
+                      for h in range(spec.h_kv)])
+        self.widths_np = w
+        self.widths = torch.as_tensor(w, dtype=torch.int8, device=device).contiguous()
+        table64, offsets = inputs.tq_rotations(spec.d, "tq", spec.name)
+        self.pi_table64, self.pi_offsets_np = table64, offsets
+        self.pi_table = torch.as_tensor(table64, dtype=torch.float32, device=device).contiguous()
+        self.pi_offsets = torch.as_tensor(offsets, dtype=torch.int64, device=device).contiguous()
+        if codebooks is None:
+            cb = np.zeros((8, 256))
+            for b in range(1, 9):
+                cb[b - 1, : 2 ** b] = _lib.bgtq_lloyd_max_codebook(b)
+            codebooks = cb
+        self.codebooks_np = np.asarray(codebooks, dtype=np.float64)
+        self.codebooks = torch.as_tensor(self.codebooks_np, dtype=torch.float64, device=device).contiguous()
+        bt = inputs.block_tables(spec, device="cpu") if block_table is None else block_table.cpu()
+        self.block_table = bt.to(device=device, dtype=torch.int32).contiguous()
+        self.num_pages = int(bt.max().item()) + 1 + extra_pages
+        self.tile = _lib.bgtq_tile_bytes(self.total_bits, self.v_bits)
+        self.cache = torch.zeros((self.num_pages, spec.h_kv, self.tile), dtype=torch.uint8, device=device)
+        self.context_lens = torch.full((spec.batch,), spec.ctx, dtype=torch.int32, device=device)
+        self.scale = 1.0 / math.sqrt(spec.d)
+
+    history_kv = Int2Layer.history_kv
+    new_kv = Int2Layer.new_kv
+    queries = Int2Layer.queries
+    slots = Int2Layer.slots
+    new_slots = Int2Layer.new_slots
+    workspace = Int2Layer.workspace
+
+    def append(self, k, v, slots, err_count=None):
+        _lib.bgtq_append(k, v, slots, self.widths, self.total_bits, self.v_bits, self.pi_table, self.pi_offsets,
+                         self.codebooks, self.cache, self.num_pages, err_count)
+
+    def prefill(self, chunk: int = 1 << 16):
+        pos = history_positions(self.spec)
+        for b in range(self.spec.batch):
+            k, v = self.history_kv(b)
+            sl = self.slots(b, pos)
+            for s in range(0, k.shape[0], chunk):
+                e = min(k.shape[0], s + chunk)
+                self.append(k[s:e].contiguous(), v[s:e].contiguous(), sl[s:e].contiguous())
+            del k, v
+
+    def decode(self, q, out, ws, num_splits: int = 0, context_lens=None):
+        _lib.bgtq_decode_attn(q, self.cache, self.num_pages, self.block_table,
+                              self.context_lens if context_lens is None else context_lens, self.widths,
+                              self.total_bits, self.v_bits, self.pi_table, self.pi_offsets, self.codebooks,
+                              self.scale, out, ws, num_splits)
+
+    def bytes_per_token_head(self) -> int:
+        """Algorithmic bytes of one cached token for one KV head."""
+        return self.tile // PAGE_SIZE

@@ -191,6 +191,38 @@ def tq_encode(x32: np.ndarray, pi32: np.ndarray, cb32: np.ndarray):
     return codes, f16_rn_sat(r), r, y
 
 
+def tq_encode_fp64_rotation(x32: np.ndarray, pi32: np.ndarray, cb32: np.ndarray):
+    """TQ-MSE with the norm and rotation taken in fp64 and rounded to fp32
+    before the code decision (for long contexts, where the fp32 chain
+    emulation is too slow; rare ties may then differ from the kernels)."""
+    x32 = np.asarray(x32, np.float32)
+    r = np.sqrt(np.sum(x32.astype(np.float64) ** 2, axis=-1)).astype(np.float32)
+    safe = np.where(r > 0, r, np.float32(1.0)).astype(np.float32)
+    u = (x32 / safe[..., None]).astype(np.float32)
+    y = (u.astype(np.float64) @ np.asarray(pi32, np.float32).astype(np.float64)).astype(np.float32)
+    codes = np.where((r > 0)[..., None], nearest_codes(y, cb32), 0)
+    return codes, f16_rn_sat(r), r, y
+
+
+def dequantize_dense(k32, v32, widths, v_bits, pis, table, exact_chain=True):
+    """Dequantised keys and values [T, d] (fp64, original basis) of one KV
+    head, without packing: grouped TQ-MSE keys (method step 3) and uniform
+    TQ-MSE values (step 4)."""
+    enc = tq_encode if exact_chain else tq_encode_fp64_rotation
+    k32 = np.asarray(k32, np.float32)
+    kh = np.zeros(k32.shape, np.float64)
+    for b, bl in width_groups(widths):
+        if not bl:
+            continue
+        n = 2 * len(bl)
+        cb = scaled_codebook(table, b, n)
+        codes, nh, _, _ = enc(gather(k32, bl), pis[n], cb)
+        scatter(tq_decode(codes, nh, pis[n], cb), bl, kh)
+    cbv = scaled_codebook(table, v_bits, D)
+    codes, nh, _, _ = enc(np.asarray(v32, np.float32), pis[D], cbv)
+    return kh, tq_decode(codes, nh, pis[D], cbv)
+
+
 def tq_decode(codes, norm_f16, pi32, cb32) -> np.ndarray:
     """x^ = r * (c[codes] Pi^T), fp64."""
     c = np.asarray(cb32, np.float32).astype(np.float64)[np.asarray(codes)]

@@ -241,7 +241,7 @@ def test_decode_rejects_small_workspace():
 
 # --------------------------------------------------------------------------- full-size sampled
 
-def _sampled_check(spec, layer_idx, samples, splits=0, token_samples=256):
+def _sampled_check(spec, layer_idx, samples, splits=0, token_samples=256, exact=False):
     layer = Int2Layer(spec, layer_idx)
     layer.prefill()
     k_new, v_new = layer.new_kv()
@@ -270,9 +270,10 @@ def _sampled_check(spec, layer_idx, samples, splits=0, token_samples=256):
             for off, n in ((int2.OFF_K_CODES + 32 * s, 32), (int2.OFF_K_META + 16 * s, 16),
                            (int2.OFF_V_CODES + 32 * s, 32), (int2.OFF_V_META + 16 * s, 16)):
                 assert np.array_equal(gpu_tiles[page, off:off + n], small[page, 0, off:off + n]), (b, h, t)
-        # attention of the sampled (sequence, KV head): oracle with fp64 rotation
+        # attention of the sampled (sequence, KV head); with exact=False the
+        # oracle decides codes from its fp64 rotation (rare ties differ)
         full = int2.new_cache(layer.num_pages, 1)
-        int2.append(full, kf, vf, slots, mu[h:h + 1], rk, rv, exact_chain=False)
+        int2.append(full, kf, vf, slots, mu[h:h + 1], rk, rv, exact_chain=exact)
         g = spec.g
         ref = int2.decode(_f64(q[b:b + 1, h * g:(h + 1) * g]), full, bt[b:b + 1], [T], mu[h:h + 1], rk, rv,
                           layer.scale, 1)
@@ -280,7 +281,9 @@ def _sampled_check(spec, layer_idx, samples, splits=0, token_samples=256):
 
 
 def test_llama8b_full_size_sampled():
-    _sampled_check(inputs.SPECS["llama8b"], 0, [(0, 0), (3, 5), (7, 7)])
+    # post-RoPE keys with heavy offsets give peaked attention, where one
+    # flipped code of a dominant token shows: decide codes exactly
+    _sampled_check(inputs.SPECS["llama8b"], 0, [(0, 0), (7, 7)], exact=True)
 
 
 def test_qwen8b_full_context_sampled_layers():
