@@ -1,0 +1,479 @@
+#!/usr/bin/env python
+"""Benchmark: packed-KV decode attention over the rotated INT2 cache.
+
+Workload (default): Qwen3-8B-shaped decode step, 36 layers x (32 q / 8 KV
+heads, d = 128), batch 1, 128K context.  One step = for every layer, the
+quantise-on-append of the new token (kvq_append_int2) followed by fused
+packed-cache decode attention (kvq_decode_attn_int2); the 72 launches are
+replayed as one CUDA graph.  Inputs are synthetic and seeded; every cache
+is prefilled through the library's own append call before timing.
+
+Prints one JSON line.  `value` is achieved algorithmic bandwidth (packed
+cache bytes + q/out + new-token traffic per step / device time per step,
+summed over ranks); `e2e` is the same metric through the C ABI with the
+step's inputs copied from pinned host memory and its outputs copied back
+inside the timed region; `roofline` is the decode kernel alone (CUDA events
+around each launch); `bgtq` is the Block-GTQ K3V3 decode at 128K measured
+the same way; `cpu_baseline` is the fp64 oracle on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import os
+
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import hashlib
+import json
+import math
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bit_kv_cache_13_gb300 import _lib, inputs  # noqa: E402
+from bit_kv_cache_13_gb300.workload import BgtqLayer, Int2Layer  # noqa: E402
+
+METRIC = "packed-KV decode attention HBM GB/s (% of 8 TB/s) and ms/step at 128K ctx"
+NOMINAL_HBM_GBS = 8000.0
+TOKEN_HEAD_BYTES = 96  # K codes 32 + K scale/min 16 + V codes 32 + V scale/min 16
+
+
+# ------------------------------------------------------------------ helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash(names) -> str:
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "bit_kv_cache_13_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, sources, per_launch_units: int):
+    """dram bytes per launch from the committed ncu summary, scaled to this
+    launch's token-heads; None if absent or taken on other kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("source_hash") != kernel_source_hash(sources):
+        return None
+    return int(rec["dram_bytes_per_token_head"] * per_launch_units)
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9 and parts[1].isdigit():
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [int(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        pw = [float(r[3]) for r in rows if r[3] not in ("", "[N/A]")]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": int(rows[0][2]), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ workload
+
+class Int2Step:
+    """All layers of one decode step, resident on the device."""
+
+    def __init__(self, spec, device):
+        self.spec = spec
+        self.layers = []
+        self.q, self.k_new, self.v_new, self.slots, self.out, self.ws = [], [], [], [], [], []
+        for l in range(spec.n_layers):
+            layer = Int2Layer(spec, l, device=device)
+            layer.prefill()
+            k, v = layer.new_kv()
+            self.layers.append(layer)
+            self.q.append(layer.queries())
+            self.k_new.append(k)
+            self.v_new.append(v)
+            self.slots.append(layer.new_slots())
+            self.out.append(torch.zeros((spec.batch, spec.h_q, spec.d), dtype=torch.float32, device=device))
+            self.ws.append(layer.workspace())
+        torch.cuda.synchronize()
+
+    def append(self, l):
+        L = self.layers[l]
+        _lib.kvq_append_int2(self.k_new[l], self.v_new[l], self.slots[l], L.mu, L.R_k, L.R_v, L.cache, L.num_pages)
+
+    def decode(self, l):
+        L = self.layers[l]
+        _lib.kvq_decode_attn_int2(self.q[l], L.cache, L.num_pages, L.block_table, L.context_lens, L.R_k, L.R_v,
+                                  L.scale, self.out[l], self.ws[l])
+
+    def run(self):
+        for l in range(len(self.layers)):
+            self.append(l)
+            self.decode(l)
+
+    # byte accounting (algorithmic)
+    def units_per_decode(self) -> int:
+        return self.spec.batch * self.spec.ctx * self.spec.h_kv
+
+    def bytes_per_decode(self) -> int:
+        s = self.spec
+        return self.units_per_decode() * TOKEN_HEAD_BYTES + s.batch * s.h_q * s.d * (2 + 4)
+
+    def bytes_per_append(self) -> int:
+        s = self.spec
+        return s.batch * s.h_kv * (2 * s.d * 2 + TOKEN_HEAD_BYTES)
+
+    def bytes_per_step(self) -> int:
+        return self.spec.n_layers * (self.bytes_per_decode() + self.bytes_per_append())
+
+    def host_io(self):
+        h2d = sum(t.numel() * t.element_size() for t in self.q + self.k_new + self.v_new + self.slots)
+        d2h = sum(t.numel() * t.element_size() for t in self.out)
+        return h2d, d2h
+
+
+def time_launches(stream, fn, n):
+    """Mean duration (ms) of fn() over n launches, CUDA events around each."""
+    evs = []
+    with torch.cuda.stream(stream):
+        for _ in range(n):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            evs.append((a, b))
+    stream.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+
+def measure_bgtq(device, stream, reps):
+    """Block-GTQ K3V3 decode at 128K (32 q / 8 KV heads, B = 1): kernel-alone
+    bandwidth of the packed stream (KB + 16 + VB + 2 bytes per token-head)."""
+    spec = inputs.SPECS["bgtq"]
+    layer = BgtqLayer(spec, 0, device=device)
+    layer.prefill()
+    k, v = layer.new_kv()
+    layer.append(k, v, layer.new_slots())
+    q = layer.queries()
+    out = torch.zeros((spec.batch, spec.h_q, spec.d), dtype=torch.float32, device=device)
+    ws = layer.workspace()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)   # evict the 120 MB cache from L2
+    for _ in range(3):
+        layer.decode(q, out, ws)
+    durs = []
+    for _ in range(reps):
+        flush.zero_()
+        durs.append(time_launches(stream, lambda: layer.decode(q, out, ws), 1))
+    ms = statistics.median(durs)
+    units = spec.batch * spec.ctx * spec.h_kv
+    nbytes = units * layer.bytes_per_token_head() + spec.batch * spec.h_q * spec.d * 6
+    peak, kind = peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": "bgtq K3V3: 32 q / 8 KV heads, batch 1, 131072 ctx, widths greedy in [1,8], sum 192",
+            "kernel": "bgtq_decode_kernel", "bytes_per_token_head": layer.bytes_per_token_head(),
+            "ms_per_decode": round(ms, 4), "value": round(gbs, 2), "unit": "GB/s",
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "peak_kind": kind,
+                         "traffic": profiled_traffic("bgtq_decode", ("bgtq.cu", "merge.cuh", "kvq_common.cuh"),
+                                                     units)},
+            "l2": "256 MB buffer written before every timed launch"}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+class OracleSample:
+    """The fp64 oracle on one (layer, KV head) of the same workload.  The
+    head's cache is built untimed; a step is the oracle's new-token append
+    plus the decode of that head's query group over the full context."""
+
+    def __init__(self, spec, layer_idx, h):
+        from oracle import int2
+        self.int2, self.spec, self.h = int2, spec, h
+        layer = Int2Layer(spec, layer_idx, device="cpu")
+        k, v = layer.history_kv(0, device="cpu")
+        self.mu = inputs.key_centre(k).numpy()[h:h + 1]
+        k_new, v_new = layer.new_kv(device="cpu")
+        self.k_new = k_new[0:1, h:h + 1].float().numpy()
+        self.v_new = v_new[0:1, h:h + 1].float().numpy()
+        g = spec.g
+        self.q = layer.queries(device="cpu").double().numpy()[0:1, h * g:(h + 1) * g]
+        T = spec.ctx
+        self.bt = layer.block_table.cpu().numpy()[0:1]
+        self.slots = np.array([self.bt[0, t // 16] * 16 + t % 16 for t in range(T)])
+        self.rk = layer.R_k[h:h + 1].cpu().numpy()
+        self.rv = layer.R_v[h:h + 1].cpu().numpy()
+        self.cache = int2.new_cache(layer.num_pages, 1)
+        int2.append(self.cache, k[:, h:h + 1].float().numpy(), v[:, h:h + 1].float().numpy(), self.slots[:-1],
+                    self.mu, self.rk, self.rv, exact_chain=False)
+        self.label = f"layer {layer_idx} kv-head {h}"
+        self.nbytes = T * TOKEN_HEAD_BYTES + g * spec.d * 6 + (2 * spec.d * 2 + TOKEN_HEAD_BYTES)
+
+    def step(self) -> float:
+        t0 = time.perf_counter()
+        self.int2.append(self.cache, self.k_new, self.v_new, self.slots[-1:], self.mu, self.rk, self.rv)
+        self.int2.decode(self.q, self.cache, self.bt, [self.spec.ctx], self.mu, self.rk, self.rv,
+                         1 / math.sqrt(self.spec.d), 1)
+        return time.perf_counter() - t0
+
+
+def oracle_baseline(spec, seconds_target=15.0):
+    """GB/s of the oracle over (layer, head) samples, ~seconds_target of work."""
+    pairs = [(0, 0), (spec.n_layers - 1, spec.h_kv - 1), (spec.n_layers // 2, 3)]
+    elapsed, nbytes, labels = 0.0, 0, []
+    for l, h in pairs:
+        smp = OracleSample(spec, l, h)
+        n = 0
+        while elapsed < seconds_target * (len(labels) + 1) / len(pairs) or n == 0:
+            elapsed += smp.step()
+            nbytes += smp.nbytes
+            n += 1
+        labels.append(f"{smp.label} x{n}")
+    return nbytes / elapsed / 1e9, elapsed, "; ".join(labels)
+
+
+# ------------------------------------------------------------------ arms
+
+def config_dict(spec, args, world, l2):
+    return {"workload": f"{spec.name}: {spec.n_layers} layers x ({spec.h_q} q / {spec.h_kv} KV heads, d={spec.d}), "
+                        f"batch {spec.batch}, {spec.ctx} ctx, INT2 K/V groups of 32 + fp16 scale/min, page 16",
+            "layers": spec.n_layers, "global_batch": spec.batch * world, "seq_len": spec.ctx,
+            "parallelism": f"replicas x{world}", "l2": l2}
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm: each step is a bounded sample of the
+    workload run by the fp64 CPU oracle."""
+    if rank != 0:
+        return
+    spec = inputs.SPECS[args.workload]
+    smp = OracleSample(spec, 0, 0)
+    times = []
+    for i in range(args.warmup + args.steps):
+        el = smp.step()
+        if i >= args.warmup:
+            times.append(el)
+    vals = [smp.nbytes / t / 1e9 for t in times]
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.median(times), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(spec, args, 1, l2="oracle on host cores"),
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"per step: new-token append + decode of one (layer, KV head) at {spec.ctx} "
+                                   f"tokens ({smp.label}); bytes = that head's packed cache + q/out"},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    _lib.load()
+    spec = inputs.SPECS[args.workload]
+    st = Int2Step(spec, device)
+    stream = torch.cuda.Stream(device=device)
+
+    # warm-up + graph capture of the whole step
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            st.run()
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            st.run()
+        for _ in range(args.warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region (device time, graph replays)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            for i in range(args.steps):
+                graph.replay()
+                ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = max_over_ranks(ev[0].elapsed_time(ev[-1]), world)
+    ms_per_step = total_ms / args.steps
+    bytes_step = st.bytes_per_step()
+    value = world * bytes_step / (ms_per_step * 1e-3) / 1e9
+    clocks = clk.summary()
+
+    # ---- decode kernel alone: events around every decode launch (eager)
+    dec_ms = []
+    for _ in range(max(2, min(args.steps, 5))):
+        for l in range(spec.n_layers):
+            with torch.cuda.stream(stream):
+                st.append(l)
+            dec_ms.append(time_launches(stream, lambda: st.decode(l), 1))
+    dec_avg_ms = statistics.mean(dec_ms)
+    peak, peak_kind = peaks()
+    achieved = st.bytes_per_decode() / (dec_avg_ms * 1e-3) / 1e9
+    traffic = profiled_traffic("decode_int2", ("decode_int2.cu", "merge.cuh", "kvq_common.cuh"),
+                               st.units_per_decode())
+
+    # ---- end to end through the C ABI with host buffers
+    h2d, d2h = st.host_io()
+    dev_in = st.q + st.k_new + st.v_new + st.slots
+    host_in = [t.cpu().pin_memory() for t in dev_in]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in st.out]
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            for hsrc, d in zip(host_in, dev_in):
+                d.copy_(hsrc, non_blocking=True)
+            graph.replay()
+            for d, hdst in zip(st.out, host_out):
+                hdst.copy_(d, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+    e2e_value = world * bytes_step / (e2e_ms * 1e-3) / 1e9
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u8 codes, fp16 scale/min, fp32 softmax/accumulate", "data": "synthetic",
+        "config": config_dict(spec, args, world, l2=f"inputs larger than L2: {bytes_step / 1e9:.2f} GB read per step"),
+        "pct_of_8TBs": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
+        "pct_of_measured_hbm": round(100.0 * value / world / peak, 2),
+        "step_ms_median": round(statistics.median(step_ms), 4),
+        "bytes_per_step": bytes_step,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": "decode_int2_kernel", "avg_launch_us": round(dec_avg_ms * 1e3, 3),
+                     "bytes_per_launch": st.bytes_per_decode()},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": 2 * spec.n_layers * args.steps,
+        "clocks": clocks,
+    }
+    del graph, st
+    torch.cuda.empty_cache()
+    if not args.no_bgtq:
+        line["bgtq"] = measure_bgtq(device, stream, reps=max(3, min(args.steps, 10)))
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, el, sample = oracle_baseline(spec)
+        line["cpu_baseline"] = {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{sample}: new-token append + decode at {spec.ctx} tokens, "
+                                          f"{el:.1f} s of fp64 numpy on one host core"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen8b", choices=["qwen8b", "llama8b"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-bgtq", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
