@@ -455,6 +455,31 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_profile_case(args):
+    """A small decode case for a full ncu capture (few MB resident): one
+    Qwen3-8B-shaped layer (32 q / 8 KV heads) at 32K context, three decode
+    launches of the chosen kernel."""
+    torch.cuda.set_device(0)
+    spec = inputs.small_spec("prof32k", h_q=32, h_kv=8, batch=1, ctx=32768, permute=True, k_kind="energy_rope",
+                             v_kind="gauss", avg_bits=3, v_bits=3, b_min=1, b_max=8)
+    out = torch.zeros((1, spec.h_q, spec.d), dtype=torch.float32, device="cuda")
+    if args.profile_case == "decode_int2":
+        L = Int2Layer(spec, 0)
+        L.prefill()
+        q, ws = L.queries(), L.workspace()
+        for _ in range(3):
+            _lib.kvq_decode_attn_int2(q, L.cache, L.num_pages, L.block_table, L.context_lens, L.R_k, L.R_v, L.scale,
+                                      out, ws)
+    else:
+        L = BgtqLayer(spec, 0)
+        L.prefill()
+        q, ws = L.queries(), L.workspace()
+        for _ in range(3):
+            L.decode(q, out, ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": args.profile_case, "ok": True}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -464,7 +489,12 @@ def main():
     ap.add_argument("--workload", default="qwen8b", choices=["qwen8b", "llama8b"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-bgtq", action="store_true")
+    ap.add_argument("--profile-case", choices=["decode_int2", "bgtq_decode"], default=None,
+                    help="run a small decode case for an ncu capture instead of the benchmark")
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args)
+        return
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
