@@ -30,6 +30,7 @@ _SIGS = {
     "kvq_decode_auto_splits": ([I, I, I], I),
     "kvq_decode_attn_int2": ([P, I, I, I, I, P, I64, P, I, P, P, P, F, P, P, SZ, I, P], I),
     "kvq_workspace_status": ([P, P], I),
+    "kvq_decode_attn_int2_noalloc": ([P, I, I, I, I, P, I64, P, I, P, P, P, F, P, I, P], I),
     "bgtq_lloyd_max_codebook": ([I, P], I),
     "bgtq_allocate": ([P, I, I, I, I64, P], I),
     "bgtq_tile_bytes": ([I, I], SZ),
@@ -128,6 +129,20 @@ def kvq_decode_attn_int2(q, cache, num_pages: int, block_table, context_lens, R_
         _dev(context_lens, torch.int32, "context_lens"), _dev(R_k, torch.float32, "R_k"),
         _dev(R_v, torch.float32, "R_v"), float(scale), _dev(out, torch.float32, "out"),
         _dev(workspace, torch.uint8, "workspace"), workspace.numel(), int(num_splits), _stream(stream)))
+
+
+def kvq_decode_attn_int2_noalloc(q, cache, num_pages: int, block_table, context_lens, R_k, R_v, scale: float,
+                                 out, num_splits: int = 0, H_kv: int | None = None, stream=None):
+    """kvq_decode_attn_int2 with the library's fixed scratch instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    B, H_q, d = q.shape
+    h_kv = R_k.shape[0] if H_kv is None else H_kv
+    _check(load().kvq_decode_attn_int2_noalloc(
+        _dev(q, torch.bfloat16, "q"), B, H_q, h_kv, d, _dev(cache, torch.uint8, "cache"), int(num_pages),
+        _dev(block_table, torch.int32, "block_table"), block_table.shape[1],
+        _dev(context_lens, torch.int32, "context_lens"), _dev(R_k, torch.float32, "R_k"),
+        _dev(R_v, torch.float32, "R_v"), float(scale), _dev(out, torch.float32, "out"), int(num_splits),
+        _stream(stream)))
 
 
 def kvq_workspace_status(workspace, stream=None) -> int:

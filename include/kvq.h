@@ -126,6 +126,32 @@ kvq_status kvq_decode_attn_int2(const void* q, int B, int H_q, int H_kv, int d,
  * when an in-kernel wait gave up. */
 kvq_status kvq_workspace_status(void* workspace, void* stream);
 
+/* The same decode attention as kvq_decode_attn_int2, for callers that cannot
+ * allocate device memory at call time: for example a serving loop whose
+ * device memory is all planned once up front, a host application that owns
+ * every device allocation through its own allocator, or code where the
+ * device-wide synchronisation cudaMalloc may cause is not acceptable.  The
+ * pages have no counterpart of this call; it is a packaging of the same
+ * kernel.
+ *   Arguments are those of kvq_decode_attn_int2 without the workspace.
+ *   Scratch: a fixed 4 MiB array inside the library's device memory, held by
+ *   every GPU that loads the library until the process exits.  A shape whose
+ *   workspace (kvq_decode_workspace_bytes) exceeds 4 MiB is rejected with
+ *   KVQ_ERR_WORKSPACE before anything is launched.
+ *   The first call on a device looks up the array's device address (once
+ *   per device, with that device current); make that first call before any
+ *   stream capture.  Each call clears the scratch counters on `stream`.
+ *   Every call shares the one array: calls whose work overlaps on the GPU
+ *   (other streams, other host threads) race and give wrong results.
+ *   In-kernel errors (out-of-range block-table entries) are not reported:
+ *   such pages are skipped.  Allocates nothing. */
+kvq_status kvq_decode_attn_int2_noalloc(const void* q, int B, int H_q, int H_kv, int d,
+                                        const void* cache, int64_t num_pages,
+                                        const int32_t* block_table, int max_pages_per_seq,
+                                        const int32_t* context_lens,
+                                        const float* R_k, const float* R_v, float scale,
+                                        float* out, int num_splits, void* stream);
+
 /* ------------------------------------------------------------- Block-GTQ */
 
 /* Host only.  Centroids (ascending, fp64) of the 2^b-level Lloyd-Max
