@@ -5,35 +5,35 @@
 // the value is rotated, w = v R_v (§3.1 Eq. 4); each group of 32 rotated
 // channels is INT2-quantised with one fp16 scale and min (§1).
 //
-// One CTA = 256 threads works on one KV head and a run of tokens.  Thread j
-// (0..127) produces rotated key channel j, thread 128 + j value channel j;
-// each keeps its column of the rotation in registers, so R is read once per
-// CTA.  A rotated coordinate is a fixed-order fp32 fma chain over the 128
-// inputs (the order the format's documentation promises).  Warp w owns one
-// 32-channel group: min/max by shuffles, exact threshold comparisons, and
-// the four 2-bit codes of a byte gathered from four neighbouring lanes.
+// One CTA = 64 threads works on one (KV head, 32-channel group) and a run of
+// tokens.  Warp 0 produces the group's 32 rotated key channels, warp 1 the
+// group's 32 rotated value channels; each thread keeps its column of the
+// rotation in registers, so R is read once per CTA and a single appended
+// token is spread over 4 CTAs per head.  A rotated coordinate is a
+// fixed-order fp32 fma chain over the 128 inputs (the order the format's
+// documentation promises).  Within the warp: min/max by shuffles, exact
+// threshold comparisons, and the four 2-bit codes of a byte gathered from
+// four neighbouring lanes.
 #include "kvq_common.cuh"
 
 namespace kvq {
 
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(64)
 append_int2_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v, int n_tok,
                    int H_kv, const int32_t* __restrict__ slot_mapping, const float* __restrict__ mu,
                    const float* __restrict__ Rk, const float* __restrict__ Rv, uint8_t* __restrict__ cache,
                    int64_t num_pages, float* __restrict__ dbg_k, float* __restrict__ dbg_v,
                    int32_t* __restrict__ err_count, int tok_per_cta) {
-    const int h = blockIdx.y;
+    const int h = blockIdx.y, grp = blockIdx.z;
     const int tid = threadIdx.x;
-    const int is_v = tid >> 7;
-    const int j = tid & (D - 1);
+    const int is_v = tid >> 5;
     const int lane = tid & 31;
-    const int grp = j >> 5;
+    const int j = 32 * grp + lane;  // output channel
 
     const float* R = (is_v ? Rv : Rk) + (size_t)h * D * D;
     float rcol[D];
 #pragma unroll
     for (int i = 0; i < D; ++i) rcol[i] = __ldg(R + i * D + j);
-    const float muj = is_v ? 0.f : __ldg(mu + h * D + j);
 
     __shared__ float xs[2][2][D];
     const int t0 = blockIdx.x * tok_per_cta;
@@ -44,18 +44,25 @@ append_int2_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
     for (int t = t0; t < t1; ++t) {
         const int slot = __ldg(slot_mapping + t);
         if (slot < 0 && slot != -1) {
-            if (tid == 0 && err_count) atomicAdd(err_count, 1);
+            if (tid == 0 && h == 0 && grp == 0 && err_count) atomicAdd(err_count, 1);
             continue;
         }
         if (slot == -1) continue;
         if ((int64_t)slot >= n_slots) {
-            if (tid == 0 && err_count) atomicAdd(err_count, 1);
+            if (tid == 0 && h == 0 && grp == 0 && err_count) atomicAdd(err_count, 1);
             continue;
         }
-        const __nv_bfloat16* src = (is_v ? v : k) + ((size_t)t * H_kv + h) * D;
-        float x = __bfloat162float(src[j]);
-        if (!is_v) x = __fsub_rn(x, muj);
-        xs[buf][is_v][j] = x;
+        // stage the token's key (centred) and value rows: 4 + 4 inputs per thread
+        {
+            const __nv_bfloat16* src = (is_v ? v : k) + ((size_t)t * H_kv + h) * D;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = lane + 32 * e;
+                float x = __bfloat162float(src[i]);
+                if (!is_v) x = __fsub_rn(x, __ldg(mu + h * D + i));
+                xs[buf][is_v][i] = x;
+            }
+        }
         __syncthreads();
 
         const float* xv = xs[buf][is_v];
@@ -124,14 +131,14 @@ extern "C" kvq_status kvq_append_int2(const void* k, const void* v, int n_tok, i
         return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_append_int2: cache not 16-byte aligned");
 
     // enough CTAs for about four waves of the 152 SMs; at most 64 tokens each
-    const int want_ctas = 152 * 4;
-    int chunks = (want_ctas + H_kv - 1) / H_kv;
+    const int want_ctas = 152 * 16;
+    int chunks = (want_ctas + 4 * H_kv - 1) / (4 * H_kv);
     chunks = chunks < 1 ? 1 : chunks;
     int per = (n_tok + chunks - 1) / chunks;
     per = per < 1 ? 1 : (per > 64 ? 64 : per);
     const int grid_x = (n_tok + per - 1) / per;
-    dim3 grid(grid_x, H_kv);
-    append_int2_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+    dim3 grid(grid_x, H_kv, NGROUP);
+    append_int2_kernel<<<grid, 64, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), n_tok, H_kv, slot_mapping,
         mu_k, R_k, R_v, static_cast<uint8_t*>(cache), num_pages, dbg_rot_k, dbg_rot_v, err_count, per);
     return kvq_check_cuda(cudaGetLastError(), "kvq_append_int2 launch");

@@ -14,6 +14,8 @@
 // query sub-vector is rotated once per CTA (q~_b = q_b Pi_n), a key
 // contributes r_b * c[code] * q~ per coordinate, and values accumulate
 // sum_s p_s r_s c[code] in the Pi_128 basis, rotated back once at the end.
+#include <mutex>
+
 #include "merge.cuh"
 
 namespace kvq {
@@ -135,7 +137,7 @@ bgtq_append_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
         const int slot = __ldg(slot_mapping + t);
         if (slot == -1) continue;
         if (slot < -1 || (int64_t)slot >= n_slots) {
-            if (tid == 0 && err_count) atomicAdd(err_count, 1);
+            if (tid == 0 && h == 0 && err_count) atomicAdd(err_count, 1);
             continue;
         }
         const __nv_bfloat16* src = (side ? v : k) + ((size_t)t * H_kv + h) * D;
@@ -189,7 +191,7 @@ struct BgDecodeSmem {
     float cb_v[256];
     float q[8][D];          // q~ in gathered key order, times scale * log2(e)
     float qin[8][D];
-    MergeSmem<BG_WARPS> ms;
+    MergeSmem<BG_WARPS, 8> ms;
     uint64_t bar[BG_WARPS][BG_STAGES];
     float o_part[BG_WARPS][8][D];
 };
@@ -403,7 +405,7 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             }
         }
     __syncthreads();
-    finish_decode<BG_WARPS>(sm.ms, sm.o_part, G, H_q, H_kv, gridDim.z, b, h, split, S, ws,
+    finish_decode<BG_WARPS, 8>(sm.ms, sm.o_part, G, H_q, H_kv, gridDim.z, b, h, split, S, ws,
                             pi_table + __ldg(pi_offsets + D), out);
 }
 
@@ -474,10 +476,24 @@ extern "C" kvq_status bgtq_decode_attn(const void* q, int B, int H_q, int H_kv, 
         return kvq_set_error(KVQ_ERR_WORKSPACE, "bgtq_decode_attn: workspace %zu < %zu bytes", workspace_bytes, need);
     const int tile = (int)bgtq_tile_bytes(total_bits, v_bits);
     const size_t smem = align_up(sizeof(BgDecodeSmem), 128) + (size_t)BG_WARPS * BG_STAGES * tile;
-    kvq_status s2 = kvq_check_cuda(
-        cudaFuncSetAttribute(bgtq_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
-        "bgtq_decode_attn smem attribute");
-    if (s2 != KVQ_OK) return s2;
+    {
+        // opt in once per device, to the largest tile any width budget gives
+        static std::mutex mu;
+        static bool done[64] = {};
+        int dev = 0;
+        kvq_status s2 = kvq_check_cuda(cudaGetDevice(&dev), "bgtq_decode_attn: cudaGetDevice");
+        if (s2 != KVQ_OK) return s2;
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 0 || dev >= 64 || !done[dev]) {
+            const size_t max_smem =
+                align_up(sizeof(BgDecodeSmem), 128) + (size_t)BG_WARPS * BG_STAGES * bgtq_tile_bytes(512, 8);
+            s2 = kvq_check_cuda(
+                cudaFuncSetAttribute(bgtq_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem),
+                "bgtq_decode_attn smem attribute");
+            if (s2 != KVQ_OK) return s2;
+            if (dev >= 0 && dev < 64) done[dev] = true;
+        }
+    }
     dim3 grid(S, H_kv, B);
     bgtq_decode_kernel<<<grid, 128, smem, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const __nv_bfloat16*>(q), H_q, H_kv, G, static_cast<const uint8_t*>(cache), num_pages, block_table,

@@ -27,23 +27,27 @@
 // Split partials (m, l, o') go to the workspace; the last CTA of a
 // (sequence, KV head) to finish (atomic ticket, no waiting) merges them,
 // applies R_v^T and writes the output.
+#include <mutex>
+
 #include "merge.cuh"
 
 namespace kvq {
 
 constexpr int DEC_WARPS = 4;
-constexpr int DEC_STAGES = 4;
+constexpr int DEC_STAGES = 8;
 
+template <int MAXG>
 struct __align__(16) DecodeSmem {
     union {
         uint8_t ring[DEC_WARPS][DEC_STAGES][INT2_TILE];  // page tiles in flight
-        float o_part[DEC_WARPS][8][D];                   // per-warp o' after the loop
+        float o_part[DEC_WARPS][MAXG][D];                // per-warp o' after the loop
     } u;
     uint64_t bar[DEC_WARPS][DEC_STAGES];
-    float q[8][D];        // scaled rotated queries q~ = q R_k * scale * log2(e)
-    float gsum[8][NGROUP];
-    float sigma[8];       // power-of-two pre-scale per head
-    MergeSmem<DEC_WARPS> ms;
+    int ntok[DEC_WARPS][DEC_STAGES];  // valid tokens of the page in each stage (0: skipped page)
+    float q[MAXG][D];     // scaled rotated queries q~ = q R_k * scale * log2(e)
+    float gsum[MAXG][NGROUP];
+    float sigma[MAXG];    // power-of-two pre-scale per head
+    MergeSmem<DEC_WARPS, MAXG> ms;
 };
 
 template <int NT>
@@ -54,7 +58,8 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                    const float* __restrict__ Rv, float scale_log2, float* __restrict__ out,
                    uint8_t* __restrict__ ws) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
+    constexpr int MAXG = 4 * NT;
+    DecodeSmem<MAXG>& sm = *reinterpret_cast<DecodeSmem<MAXG>*>(smem_raw);
 
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int S = gridDim.x;
@@ -72,35 +77,60 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     const int my_count = p_end - p_begin > warp ? (p_end - p_begin - warp + DEC_WARPS - 1) / DEC_WARPS : 0;
     const int32_t* bt = block_table + (size_t)b * max_pages;
 
-    // ---- start streaming before the query set-up
+    // ---- first, every global read of the prologue is put in flight at once:
+    // the first pages' ids (lane 0), this warp's rows of R_k, the query rows
+    auto page_id = [&](int i) { return __ldg(bt + p_begin + warp + DEC_WARPS * i); };
+    int pids[DEC_STAGES + 1];
+    if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i <= DEC_STAGES; ++i) pids[i] = i < my_count ? page_id(i) : 0;
+    }
+    float4 rr[RowPrefetch<MAXG>::N];
+    load_rows<DEC_WARPS>(Rk + (size_t)h * D * D, rr);
+    __nv_bfloat16 qv[MAXG];
+    {
+        const __nv_bfloat16* qb = q + ((size_t)b * H_q + (size_t)h * G) * D;
+#pragma unroll
+        for (int jj = 0; jj < MAXG; ++jj) qv[jj] = jj < G ? qb[jj * D + tid] : __float2bfloat16(0.f);
+    }
     if (lane == 0) {
         for (int s = 0; s < DEC_STAGES; ++s) mbar_init(&sm.bar[warp][s], 1);
         fence_mbar_init();
         fence_proxy_async_smem();
     }
     __syncwarp();
-    auto issue = [&](int i) {  // lane 0 only
+    // Lane 0 issues page i of this warp with its (already loaded) page id and
+    // records how many of its tokens are valid; the mbarrier publishes that
+    // count together with the data.
+    auto issue = [&](int i, int pid) {  // lane 0 only
         const int p = p_begin + warp + DEC_WARPS * i;
-        const int pid = __ldg(bt + p);
-        uint64_t* bar = &sm.bar[warp][i % DEC_STAGES];
+        const int st = i % DEC_STAGES;
+        uint64_t* bar = &sm.bar[warp][st];
         if (pid < 0 || (int64_t)pid >= num_pages) {
             atomicOr(err_word, ERR_BAD_PAGE);
+            sm.ntok[warp][st] = 0;
             mbar_arrive(bar);  // complete the phase without data
         } else {
+            sm.ntok[warp][st] = min(PAGE, ctx - p * PAGE);
             mbar_arrive_expect_tx(bar, INT2_TILE);
-            bulk_g2s(sm.u.ring[warp][i % DEC_STAGES], cache + ((size_t)pid * H_kv + h) * INT2_TILE, INT2_TILE,
-                     bar);
+            bulk_g2s(sm.u.ring[warp][st], cache + ((size_t)pid * H_kv + h) * INT2_TILE, INT2_TILE, bar);
         }
     };
-    if (lane == 0)
-        for (int i = 0; i < min(DEC_STAGES, my_count); ++i) issue(i);
+    int pid_next = 0;  // lane 0: page id of the next page to issue, loaded one iteration early
+    if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < DEC_STAGES; ++i)
+            if (i < my_count) issue(i, pids[i]);
+        pid_next = pids[DEC_STAGES];
+    }
 
     // ---- q~ = (q R_k) * scale * log2(e) for the G heads of this KV head
     {
-        const __nv_bfloat16* qb = q + ((size_t)b * H_q + (size_t)h * G) * D;
-        for (int idx = tid; idx < G * D; idx += 128) sm.ms.o_final[idx / D][idx % D] = __bfloat162float(qb[idx]);
+#pragma unroll
+        for (int jj = 0; jj < MAXG; ++jj)
+            if (jj < G) sm.ms.o_final[jj][tid] = __bfloat162float(qv[jj]);
         __syncthreads();
-        rotate_rows<DEC_WARPS>(sm.ms.o_final, Rk + (size_t)h * D * D, G, scale_log2, sm.q, sm.ms);
+        rotate_rows<DEC_WARPS, MAXG>(sm.ms.o_final, Rk + (size_t)h * D * D, rr, G, scale_log2, sm.q, sm.ms);
         // per head: power-of-two pre-scale (max |q~| * sigma in [2^14, 2^15)) and group sums
         for (int jj = warp; jj < G; jj += DEC_WARPS) {
             float mx = 0.f;
@@ -189,10 +219,7 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         }
         if (timed_out) break;
         const uint8_t* tile = sm.u.ring[warp][stage];
-        const int p = p_begin + warp + DEC_WARPS * i;
-        const int pid = __ldg(bt + p);
-        const bool valid = pid >= 0 && (int64_t)pid < num_pages;
-        const int n_tok = valid ? min(PAGE, ctx - p * PAGE) : 0;
+        const int n_tok = sm.ntok[warp][stage];
 
         // ---------------- QK
         float lg[NT][2];
@@ -247,15 +274,15 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
             corr[nt] = 1.f;
             if (pm > mrun[nt]) {
-                corr[nt] = exp2f(mrun[nt] - pm);  // 0 when mrun = -inf
+                corr[nt] = ex2(mrun[nt] - pm);  // 0 when mrun = -inf
                 mrun[nt] = pm;
                 need = true;
             }
             const float mref = mrun[nt] == -CUDART_INF_F ? 0.f : mrun[nt];
             // p is rounded to fp16 once; the same p^ weights the codes, the
             // group minima and the normaliser
-            pr[nt][0] = __half2float(__float2half_rn(exp2f(lg[nt][0] - mref)));
-            pr[nt][1] = __half2float(__float2half_rn(exp2f(lg[nt][1] - mref)));
+            pr[nt][0] = __half2float(__float2half_rn(ex2(lg[nt][0] - mref)));
+            pr[nt][1] = __half2float(__float2half_rn(ex2(lg[nt][1] - mref)));
             lsum[nt] = fmaf(lsum[nt], corr[nt], pr[nt][0] + pr[nt][1]);
         }
         if (__any_sync(0xffffffffu, need)) {
@@ -360,7 +387,8 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         __syncwarp();
         if (lane == 0 && i + DEC_STAGES < my_count) {
             fence_proxy_async_smem();
-            issue(i + DEC_STAGES);
+            issue(i + DEC_STAGES, pid_next);
+            if (i + DEC_STAGES + 1 < my_count) pid_next = page_id(i + DEC_STAGES + 1);
         }
     }
     if (timed_out && lane == 0) {
@@ -418,13 +446,29 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     }
     __syncthreads();
 
-    finish_decode<DEC_WARPS>(sm.ms, sm.u.o_part, G, H_q, H_kv, gridDim.z, b, h, split, S, ws,
+    finish_decode<DEC_WARPS, MAXG>(sm.ms, sm.u.o_part, G, H_q, H_kv, gridDim.z, b, h, split, S, ws,
                              Rv + (size_t)h * D * D, out);
 }
 
 }  // namespace kvq
 
 using namespace kvq;
+
+// The dynamic shared memory opt-in is a per-device attribute of the kernel:
+// set it on the first call on each device only.
+static kvq_status set_smem_once(const void* fn, int bytes, int which) {
+    static std::mutex mu;
+    static bool done[64][2] = {};
+    int dev = 0;
+    kvq_status st = kvq_check_cuda(cudaGetDevice(&dev), "kvq_decode_attn_int2: cudaGetDevice");
+    if (st != KVQ_OK) return st;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && done[dev][which]) return KVQ_OK;
+    st = kvq_check_cuda(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
+                        "kvq_decode_attn_int2 smem attribute");
+    if (st == KVQ_OK && dev >= 0 && dev < 64) done[dev][which] = true;
+    return st;
+}
 
 extern "C" int kvq_decode_auto_splits(int B, int H_kv, int max_pages_per_seq) {
     if (B <= 0 || H_kv <= 0 || max_pages_per_seq <= 0) return 1;
@@ -473,19 +517,18 @@ extern "C" kvq_status kvq_decode_attn_int2(const void* q, int B, int H_q, int H_
         return kvq_set_error(KVQ_ERR_WORKSPACE, "kvq_decode_attn_int2: workspace %zu < %zu bytes", workspace_bytes,
                              need);
     const float scale_log2 = scale * 1.4426950408889634f;
-    const size_t smem = sizeof(DecodeSmem);
+    const size_t smem = G <= 4 ? sizeof(DecodeSmem<4>) : sizeof(DecodeSmem<8>);
     dim3 grid(S, H_kv, B);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
+    kvq_status sa = set_smem_once(G <= 4 ? (const void*)decode_int2_kernel<1> : (const void*)decode_int2_kernel<2>,
+                                  (int)smem, G <= 4 ? 0 : 1);
+    if (sa != KVQ_OK) return sa;
     if (G <= 4) {
-        cudaError_t a = cudaFuncSetAttribute(decode_int2_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (a != cudaSuccess) return kvq_check_cuda(a, "kvq_decode_attn_int2 smem attribute");
         decode_int2_kernel<1><<<grid, 128, smem, st>>>(
             static_cast<const __nv_bfloat16*>(q), H_q, H_kv, G, static_cast<const uint8_t*>(cache), num_pages,
             block_table, max_pages_per_seq, context_lens, R_k, R_v, scale_log2, out, static_cast<uint8_t*>(workspace));
     } else {
-        cudaError_t a = cudaFuncSetAttribute(decode_int2_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (a != cudaSuccess) return kvq_check_cuda(a, "kvq_decode_attn_int2 smem attribute");
         decode_int2_kernel<2><<<grid, 128, smem, st>>>(
             static_cast<const __nv_bfloat16*>(q), H_q, H_kv, G, static_cast<const uint8_t*>(cache), num_pages,
             block_table, max_pages_per_seq, context_lens, R_k, R_v, scale_log2, out, static_cast<uint8_t*>(workspace));

@@ -7,8 +7,11 @@
 // publishes the CTA's split partial (m, l, o') to the workspace, and the last
 // CTA of the (sequence, KV head) to arrive -- decided by an atomic ticket,
 // nobody waits -- merges the S split partials with the log-sum-exp rule
-//     M = max_s m_s,  L = sum_s l_s 2^(m_s - M),  O = sum_s o'_s 2^(m_s - M),
-// rotates o = (O / L) Rot^T once (o_i = sum_j o'_j Rot[i][j]) and writes it.
+//     M = max_s m_s,  L = sum_s l_s 2^(m_s - M),  O = sum_s O_s 2^(m_s - M),
+// and writes o = O / L.  The output rotation o = o' Rot^T is linear, so
+// every CTA applies it to its own partial (O_s = o'_s Rot^T, o_i = sum_j
+// o'_j Rot[i][j]) before publishing it: that work runs in parallel across
+// the splits instead of in the one CTA that finishes last.
 // The ticket is reset to zero so the workspace is ready for the next call.
 // Every global read in these paths is issued many-at-a-time (warps split
 // the rows / splits, float4 loads) so their latency overlaps.
@@ -22,36 +25,59 @@ namespace kvq {
 
 constexpr int MAX_SPLITS = 256;
 
-template <int NWARPS>
+// MAXG: the largest query-head group the kernel instance handles (G <= MAXG).
+template <int NWARPS, int MAXG>
 struct MergeSmem {
-    float m_part[NWARPS][8];
-    float l_part[NWARPS][8];
-    float o_final[8][D];
-    float red[NWARPS][8][D];    // cross-warp partial sums
-    float fac[8][MAX_SPLITS];   // per-split weights 2^(m_s - M)
-    float Mh[8], Lh[8];
+    float m_part[NWARPS][MAXG];
+    float l_part[NWARPS][MAXG];
+    float o_final[MAXG][D];
+    float red[NWARPS][MAXG][D];    // cross-warp partial sums
+    float fac[MAXG][MAX_SPLITS];   // per-split maxima, then weights 2^(m_s - M)
+    float lsp[MAXG][MAX_SPLITS];   // per-split normalisers
+    float Mh[MAXG], Lh[MAXG];
     int is_last;
 };
 
 __device__ __forceinline__ float4 ldg4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
 __device__ __forceinline__ float4 ldcg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
 
-// qr[jj][c] = sum_i qin[jj][i] * R[i][c] * factor for jj < G (128 threads).
-// Warp w takes rows 32w .. 32w+31, lane takes columns 4*lane .. 4*lane+3.
-template <int NWARPS>
-__device__ __forceinline__ void rotate_rows(const float (*qin)[D], const float* __restrict__ R, int G, float factor,
-                                            float (*qr)[D], MergeSmem<NWARPS>& ms) {
+// 2^x with the hardware approximation (relative error ~2^-22); -inf gives 0.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Rows prefetched early by the prologue: all 32 of a warp's rows when the
+// head group is small, half of them for groups of 8 (register budget).
+template <int MAXG>
+struct RowPrefetch {
+    static constexpr int N = MAXG <= 4 ? 32 : 16;
+};
+
+// Rows 32w .. 32w+N-1 of R, columns 4*lane .. 4*lane+3, for warp w: issued
+// together so their latencies overlap (call early, use later).
+template <int NWARPS, int N>
+__device__ __forceinline__ void load_rows(const float* __restrict__ R, float4 (&rr)[N]) {
     static_assert(NWARPS * 32 == D, "one warp per 32 rows");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float4 acc[8];
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) acc[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 16
-    for (int ii = 0; ii < 32; ++ii) {
-        const int i = 32 * warp + ii;
-        const float4 r = ldg4(R + (size_t)i * D + 4 * lane);
+    for (int ii = 0; ii < N; ++ii) rr[ii] = ldg4(R + (size_t)(32 * warp + ii) * D + 4 * lane);
+}
+
+// qr[jj][c] = sum_i qin[jj][i] * R[i][c] * factor for jj < G (128 threads),
+// with the first N of this warp's rows of R already in rr (load_rows); the
+// rest are loaded here.
+template <int NWARPS, int MAXG, int N>
+__device__ __forceinline__ void rotate_rows(const float (*qin)[D], const float* __restrict__ R, const float4 (&rr)[N],
+                                            int G, float factor, float (*qr)[D], MergeSmem<NWARPS, MAXG>& ms) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float4 acc[MAXG];
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj)
+    for (int jj = 0; jj < MAXG; ++jj) acc[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto accumulate = [&](int i, float4 r) {
+#pragma unroll
+        for (int jj = 0; jj < MAXG; ++jj)
             if (jj < G) {
                 const float x = qin[jj][i];
                 acc[jj].x = fmaf(x, r.x, acc[jj].x);
@@ -59,9 +85,18 @@ __device__ __forceinline__ void rotate_rows(const float (*qin)[D], const float* 
                 acc[jj].z = fmaf(x, r.z, acc[jj].z);
                 acc[jj].w = fmaf(x, r.w, acc[jj].w);
             }
+    };
+#pragma unroll
+    for (int ii = 0; ii < N; ++ii) accumulate(32 * warp + ii, rr[ii]);
+    if constexpr (N < 32) {
+        float4 r2[32 - N];
+#pragma unroll
+        for (int ii = 0; ii < 32 - N; ++ii) r2[ii] = ldg4(R + (size_t)(32 * warp + N + ii) * D + 4 * lane);
+#pragma unroll
+        for (int ii = 0; ii < 32 - N; ++ii) accumulate(32 * warp + N + ii, r2[ii]);
     }
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj)
+    for (int jj = 0; jj < MAXG; ++jj)
         if (jj < G) *reinterpret_cast<float4*>(&ms.red[warp][jj][4 * lane]) = acc[jj];
     __syncthreads();
     const int c = threadIdx.x;
@@ -75,9 +110,9 @@ __device__ __forceinline__ void rotate_rows(const float (*qin)[D], const float* 
 }
 
 // 128 threads; o_part[w][jj][c] is warp w's o'.  Rot is row-major [D][D]
-// fp32, 16-byte aligned.  S <= MAX_SPLITS.
-template <int NWARPS>
-__device__ __forceinline__ void finish_decode(MergeSmem<NWARPS>& ms, const float (*o_part)[8][D], int G, int H_q,
+// fp32, 16-byte aligned.  S <= MAX_SPLITS, G <= MAXG.
+template <int NWARPS, int MAXG>
+__device__ __forceinline__ void finish_decode(MergeSmem<NWARPS, MAXG>& ms, const float (*o_part)[MAXG][D], int G, int H_q,
                                               int H_kv, int B, int b, int h, int split, int S, uint8_t* ws,
                                               const float* __restrict__ Rot, float* __restrict__ out) {
     const int c = threadIdx.x, warp = c >> 5, lane = c & 31;
@@ -85,7 +120,13 @@ __device__ __forceinline__ void finish_decode(MergeSmem<NWARPS>& ms, const float
     float* partials = reinterpret_cast<float*>(ws + WS_HEADER + tickets_bytes(B, H_kv));
     const size_t head0 = (size_t)b * H_q + (size_t)h * G;
 
-    // ---- warps -> this CTA's split partial
+    // ---- warps -> this CTA's split partial (M, L, unnormalised o')
+    // rows of Rot this warp rotates, columns 4*lane .. +3: coalesced, issued
+    // now; all 32 rows at once for small head groups, 16 at a time for 8
+    constexpr int RP = MAXG <= 4 ? 32 : 16;
+    float4 rr[RP];
+#pragma unroll
+    for (int ii = 0; ii < RP; ++ii) rr[ii] = ldg4(Rot + (size_t)(32 * warp + ii) * D + 4 * lane);
     for (int jj = 0; jj < G; ++jj) {
         float M = -CUDART_INF_F;
 #pragma unroll
@@ -99,11 +140,49 @@ __device__ __forceinline__ void finish_decode(MergeSmem<NWARPS>& ms, const float
                 O = fmaf(o_part[w][jj][c], f, O);
             }
         }
-        float* part = partials + ((head0 + jj) * S + split) * PART_STRIDE;
-        part[4 + c] = O;
+        ms.o_final[jj][c] = O;
         if (c == 0) {
-            part[0] = M;
-            part[1] = L;
+            ms.Mh[jj] = M;
+            ms.Lh[jj] = L;
+        }
+    }
+    __syncthreads();
+    // ---- rotate this partial: O_i = sum_j o'_j Rot[i][j] for i = 32*warp + lane.
+    // Each lane forms the partial dots of its 4 columns with RP of the warp's
+    // rows; a reduce-scatter over the lanes then leaves each row's full dot
+    // in one lane (31 shuffles per head and 32 rows).
+#pragma unroll
+    for (int pass = 0; pass < 32 / RP; ++pass) {
+        if (pass > 0) {
+#pragma unroll
+            for (int ii = 0; ii < RP; ++ii) rr[ii] = ldg4(Rot + (size_t)(32 * warp + RP * pass + ii) * D + 4 * lane);
+        }
+        for (int jj = 0; jj < G; ++jj) {
+            const float4 o4 = *reinterpret_cast<const float4*>(&ms.o_final[jj][4 * lane]);
+            float v[RP];
+#pragma unroll
+            for (int ii = 0; ii < RP; ++ii)
+                v[ii] = fmaf(o4.x, rr[ii].x, fmaf(o4.y, rr[ii].y, fmaf(o4.z, rr[ii].z, o4.w * rr[ii].w)));
+            if constexpr (RP == 16) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], 16);
+            }
+#pragma unroll
+            for (int off = RP / 2; off >= 1; off >>= 1) {
+                const bool upper = lane & off;
+#pragma unroll
+                for (int k = 0; k < off; ++k) {
+                    const float send = upper ? v[k] : v[k + off];
+                    const float keep = upper ? v[k + off] : v[k];
+                    v[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                }
+            }
+            float* part = partials + ((head0 + jj) * S + split) * PART_STRIDE;
+            if (RP == 32 || lane < 16) part[4 + 32 * warp + RP * pass + (lane & (RP - 1))] = v[0];
+            if (c == 0 && pass == 0) {
+                part[0] = ms.Mh[jj];
+                part[1] = ms.Lh[jj];
+            }
         }
     }
     __threadfence();
@@ -116,22 +195,26 @@ __device__ __forceinline__ void finish_decode(MergeSmem<NWARPS>& ms, const float
     if (!ms.is_last) return;
     __threadfence();
 
-    // ---- last CTA: split weights (one warp per head, lanes over splits)
+    // ---- last CTA: every split's (m, l) of the G heads, gathered at once
+#pragma unroll 4
+    for (int idx = c; idx < G * S; idx += NWARPS * 32) {
+        const int jj = idx / S, s = idx - jj * S;
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(partials + ((head0 + jj) * S + s) * PART_STRIDE));
+        ms.fac[jj][s] = ml.x;
+        ms.lsp[jj][s] = ml.y;
+    }
+    __syncthreads();
+    // split weights (one warp per head, lanes over splits, shared memory only)
     for (int jj = warp; jj < G; jj += NWARPS) {
-        const float* base = partials + (head0 + jj) * S * PART_STRIDE;
         float M = -CUDART_INF_F;
-        for (int s = lane; s < S; s += 32) {
-            const float m = __ldcg(base + (size_t)s * PART_STRIDE);
-            ms.fac[jj][s] = m;
-            M = fmaxf(M, m);
-        }
+        for (int s = lane; s < S; s += 32) M = fmaxf(M, ms.fac[jj][s]);
 #pragma unroll
         for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
         float L = 0.f;
         for (int s = lane; s < S; s += 32) {
             const float f = M == -CUDART_INF_F ? 0.f : exp2f(ms.fac[jj][s] - M);
             ms.fac[jj][s] = f;
-            L = fmaf(__ldcg(base + (size_t)s * PART_STRIDE + 1), f, L);
+            L = fmaf(ms.lsp[jj][s], f, L);
         }
 #pragma unroll
         for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
@@ -141,15 +224,16 @@ __device__ __forceinline__ void finish_decode(MergeSmem<NWARPS>& ms, const float
         }
     }
     __syncthreads();
-    // ---- weighted sum of the split outputs: warp w takes splits w, w+4, ...
+    // ---- weighted sum of the split outputs: warp w takes splits w, w+4, ...;
+    // unrolled so each lane keeps many independent loads in flight
     {
-        float4 acc[8];
+        float4 acc[MAXG];
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) acc[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
+        for (int jj = 0; jj < MAXG; ++jj) acc[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll(MAXG <= 4 ? 8 : 4)
         for (int s = warp; s < S; s += NWARPS) {
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj)
+            for (int jj = 0; jj < MAXG; ++jj)
                 if (jj < G) {
                     const float f = ms.fac[jj][s];
                     const float4 o = ldcg4(partials + ((head0 + jj) * S + s) * PART_STRIDE + 4 + 4 * lane);
@@ -160,7 +244,7 @@ __device__ __forceinline__ void finish_decode(MergeSmem<NWARPS>& ms, const float
                 }
         }
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj)
+        for (int jj = 0; jj < MAXG; ++jj)
             if (jj < G) *reinterpret_cast<float4*>(&ms.red[warp][jj][4 * lane]) = acc[jj];
     }
     __syncthreads();
@@ -169,27 +253,8 @@ __device__ __forceinline__ void finish_decode(MergeSmem<NWARPS>& ms, const float
 #pragma unroll
         for (int w = 0; w < NWARPS; ++w) s += ms.red[w][jj][c];
         const float L = ms.Lh[jj];
-        ms.o_final[jj][c] = L > 0.f ? s / L : 0.f;
+        out[(head0 + jj) * D + c] = L > 0.f ? s / L : 0.f;
     }
-    __syncthreads();
-    // ---- o_c = sum_j o'_j Rot[c][j]
-    const float* row = Rot + (size_t)c * D;
-    float acc[8];
-#pragma unroll
-    for (int jj = 0; jj < 8; ++jj) acc[jj] = 0.f;
-#pragma unroll
-    for (int j4 = 0; j4 < D / 4; ++j4) {
-        const float4 rv = ldg4(row + 4 * j4);
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj)
-            if (jj < G) {
-                const float* o = &ms.o_final[jj][4 * j4];
-                acc[jj] = fmaf(o[0], rv.x, fmaf(o[1], rv.y, fmaf(o[2], rv.z, fmaf(o[3], rv.w, acc[jj]))));
-            }
-    }
-#pragma unroll
-    for (int jj = 0; jj < 8; ++jj)
-        if (jj < G) out[(head0 + jj) * D + c] = acc[jj];
     if (c == 0) tickets[(size_t)b * H_kv + h] = 0;
 }
 

@@ -190,6 +190,10 @@ size_t bgtq_tile_bytes(int total_bits, int v_bits);
  *               every even n <= d, Pi_n at pi_table + pi_offsets[n]
  *   pi_offsets  device int64 [d + 1] (-1 for odd n)
  *   codebooks   device fp64 [8][256]: row b-1 = bgtq_lloyd_max_codebook(b)
+ *   err_count   nullable device int32: incremented once per token whose slot
+ *               lies outside [0, num_pages*16) (other than -1), and at least
+ *               once when a head's widths are outside 1..8 or over budget;
+ *               such tokens / heads are skipped
  * Key: RoPE block i = dims (i, i + d/2); blocks of equal width b form a
  * sub-vector (ascending block index, each block as its two dims) of length
  * n; r = ||x|| (fp32 fma chain of squares, correctly rounded sqrt),
