@@ -27,7 +27,7 @@ _SIGS = {
     "kvq_int2_tile_bytes": ([I], SZ),
     "kvq_append_int2": ([P, P, I, I, I, P, P, P, P, P, I64, P, P, P, P], I),
     "kvq_decode_workspace_bytes": ([I, I, I, I, I], SZ),
-    "kvq_decode_auto_splits": ([I, I, I], I),
+    "kvq_decode_auto_splits": ([I, I, I, I], I),
     "kvq_decode_attn_int2": ([P, I, I, I, I, P, I64, P, I, P, P, P, F, P, P, SZ, I, P], I),
     "kvq_workspace_status": ([P, P], I),
     "kvq_decode_attn_int2_noalloc": ([P, I, I, I, I, P, I64, P, I, P, P, P, F, P, I, P], I),
@@ -115,8 +115,8 @@ def kvq_decode_workspace_bytes(B: int, H_q: int, H_kv: int, max_pages_per_seq: i
     return load().kvq_decode_workspace_bytes(B, H_q, H_kv, max_pages_per_seq, num_splits)
 
 
-def kvq_decode_auto_splits(B: int, H_kv: int, max_pages_per_seq: int) -> int:
-    return load().kvq_decode_auto_splits(B, H_kv, max_pages_per_seq)
+def kvq_decode_auto_splits(B: int, H_q: int, H_kv: int, max_pages_per_seq: int) -> int:
+    return load().kvq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq)
 
 
 def kvq_decode_attn_int2(q, cache, num_pages: int, block_table, context_lens, R_k, R_v, scale: float,

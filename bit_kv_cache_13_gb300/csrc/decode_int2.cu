@@ -205,82 +205,92 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         mrun[nt] = -CUDART_INF_F;
         lsum[nt] = 0.f;
     }
-    bool timed_out = false;
 
-    for (int i = 0; i < my_count; ++i) {
-        const int stage = i % DEC_STAGES;
-        const uint32_t parity = (i / DEC_STAGES) & 1;
-        if (!timed_out) {
-            const bool ok = mbar_wait_bounded(&sm.bar[warp][stage], parity, WAIT_LIMIT_CYCLES);
-            if (__any_sync(0xffffffffu, !ok)) {
-                timed_out = true;
-                if (lane == 0) atomicOr(err_word, ERR_TIMEOUT);
-            }
+    // Wait for page i of this warp; false on a timeout.  On a sequence's
+    // last page the slots past the context may hold stale bytes (even NaN
+    // scales): their value scale/min words are zeroed here, so p = 0 always
+    // meets finite factors and the PV step needs no per-slot masks (the QK
+    // step drops those slots' logits by selection).
+    auto wait_page = [&](int i) -> bool {
+        const int st = i % DEC_STAGES;
+        const bool ok = mbar_wait_bounded(&sm.bar[warp][st], (i / DEC_STAGES) & 1, WAIT_LIMIT_CYCLES);
+        if (__any_sync(0xffffffffu, !ok)) {
+            if (lane == 0) atomicOr(err_word, ERR_TIMEOUT);
+            return false;
         }
-        if (timed_out) break;
-        const uint8_t* tile = sm.u.ring[warp][stage];
-        const int n_tok = sm.ntok[warp][stage];
+        const int n = sm.ntok[warp][st];
+        if (n < PAGE) {
+            if (lane >= n && lane < PAGE)
+                *reinterpret_cast<uint4*>(sm.u.ring[warp][st] + OFF_VM + 16 * lane) = make_uint4(0u, 0u, 0u, 0u);
+            __syncwarp();
+        }
+        return true;
+    };
 
-        // ---------------- QK
-        float lg[NT][2];
-        {
-            const uint2 kr = lds64(tile + OFF_KC + 32 * r + 8 * t);
-            const uint2 kr8 = lds64(tile + OFF_KC + 32 * (r + 8) + 8 * t);
-            const uint32_t P01 = prmt(kr.x, kr.y, 0x5410), P23 = prmt(kr.x, kr.y, 0x7632);
-            const uint32_t Q01 = prmt(kr8.x, kr8.y, 0x5410), Q23 = prmt(kr8.x, kr8.y, 0x7632);
-            const uint4 mr = lds128(tile + OFF_KM + 16 * r);
-            const uint4 mr8 = lds128(tile + OFF_KM + 16 * (r + 8));
-            const uint32_t mrw[4] = {mr.x, mr.y, mr.z, mr.w}, mr8w[4] = {mr8.x, mr8.y, mr8.z, mr8.w};
-            float acc_r[NT], acc_r8[NT], mn_r[NT], mn_r8[NT];
+    // ---------------- QK of page i: base-2 logits of tokens r, r + 8 for
+    // head 4*nt + t (-inf past the context) and each head's page maximum
+    auto qk_page = [&](int i, float (&lg)[NT][2], float (&pm)[NT]) {
+        const uint8_t* tile = sm.u.ring[warp][i % DEC_STAGES];
+        const int n_tok = sm.ntok[warp][i % DEC_STAGES];
+        const uint2 kr = lds64(tile + OFF_KC + 32 * r + 8 * t);
+        const uint2 kr8 = lds64(tile + OFF_KC + 32 * (r + 8) + 8 * t);
+        const uint32_t P01 = prmt(kr.x, kr.y, 0x5410), P23 = prmt(kr.x, kr.y, 0x7632);
+        const uint32_t Q01 = prmt(kr8.x, kr8.y, 0x5410), Q23 = prmt(kr8.x, kr8.y, 0x7632);
+        const uint4 mr = lds128(tile + OFF_KM + 16 * r);
+        const uint4 mr8 = lds128(tile + OFF_KM + 16 * (r + 8));
+        const uint32_t mrw[4] = {mr.x, mr.y, mr.z, mr.w}, mr8w[4] = {mr8.x, mr8.y, mr8.z, mr8.w};
+        float acc_r[NT], acc_r8[NT], mn_r[NT], mn_r8[NT];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) acc_r[nt] = acc_r8[nt] = mn_r[nt] = mn_r8[nt] = 0.f;
+        for (int nt = 0; nt < NT; ++nt) acc_r[nt] = acc_r8[nt] = mn_r[nt] = mn_r8[nt] = 0.f;
 #pragma unroll
-            for (int g = 0; g < NGROUP; ++g) {
-                const uint32_t xr = g == 0 ? P01 : g == 1 ? (P01 >> 8) : g == 2 ? P23 : (P23 >> 8);
-                const uint32_t xr8 = g == 0 ? Q01 : g == 1 ? (Q01 >> 8) : g == 2 ? Q23 : (Q23 >> 8);
-                const float2 smr = __half22float2(u32_as_h2(mrw[g]));    // (scale, min) token r
-                const float2 smr8 = __half22float2(u32_as_h2(mr8w[g]));  // token r + 8
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int hs = 0; hs < 2; ++hs) {
-                        const uint32_t m0 = 0x00030003u << (4 * hs), m1 = 0x00030003u << (4 * hs + 2);
-                        const uint32_t a[4] = {xr & m0, xr8 & m0, xr & m1, xr8 & m1};
-                        mma_f16_16816(c, a, bq[nt][2 * g + hs][0], bq[nt][2 * g + hs][1]);
-                    }
-                    acc_r[nt] = fmaf(smr.x, c[0] + c[1], acc_r[nt]);
-                    acc_r8[nt] = fmaf(smr8.x, c[2] + c[3], acc_r8[nt]);
-                    mn_r[nt] = fmaf(smr.y, gsum[nt][g], mn_r[nt]);
-                    mn_r8[nt] = fmaf(smr8.y, gsum[nt][g], mn_r8[nt]);
-                }
-            }
+        for (int g = 0; g < NGROUP; ++g) {
+            const uint32_t xr = g == 0 ? P01 : g == 1 ? (P01 >> 8) : g == 2 ? P23 : (P23 >> 8);
+            const uint32_t xr8 = g == 0 ? Q01 : g == 1 ? (Q01 >> 8) : g == 2 ? Q23 : (Q23 >> 8);
+            const float2 smr = __half22float2(u32_as_h2(mrw[g]));    // (scale, min) token r
+            const float2 smr8 = __half22float2(u32_as_h2(mr8w[g]));  // token r + 8
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                lg[nt][0] = r < n_tok ? fmaf(acc_r[nt], inv_sig[nt], mn_r[nt]) : -CUDART_INF_F;
-                lg[nt][1] = r + 8 < n_tok ? fmaf(acc_r8[nt], inv_sig[nt], mn_r8[nt]) : -CUDART_INF_F;
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int hs = 0; hs < 2; ++hs) {
+                    const uint32_t m0 = 0x00030003u << (4 * hs), m1 = 0x00030003u << (4 * hs + 2);
+                    const uint32_t a[4] = {xr & m0, xr8 & m0, xr & m1, xr8 & m1};
+                    mma_f16_16816(c, a, bq[nt][2 * g + hs][0], bq[nt][2 * g + hs][1]);
+                }
+                acc_r[nt] = fmaf(smr.x, c[0] + c[1], acc_r[nt]);
+                acc_r8[nt] = fmaf(smr8.x, c[2] + c[3], acc_r8[nt]);
+                mn_r[nt] = fmaf(smr.y, gsum[nt][g], mn_r[nt]);
+                mn_r8[nt] = fmaf(smr8.y, gsum[nt][g], mn_r8[nt]);
             }
         }
-
-        // ---------------- online softmax (base 2), head 4*nt + t
-        float corr[NT];
-        bool need = false;
-        float pr[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            float pm = fmaxf(lg[nt][0], lg[nt][1]);
-            pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
-            pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
-            pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+            lg[nt][0] = r < n_tok ? fmaf(acc_r[nt], inv_sig[nt], mn_r[nt]) : -CUDART_INF_F;
+            lg[nt][1] = r + 8 < n_tok ? fmaf(acc_r8[nt], inv_sig[nt], mn_r8[nt]) : -CUDART_INF_F;
+            float m = fmaxf(lg[nt][0], lg[nt][1]);
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+            pm[nt] = m;
+        }
+    };
+
+    // ---------------- online softmax (base 2) for one page, head 4*nt + t:
+    // raise the running maxima, rescale the accumulators when one grew, and
+    // return p^ (p rounded to fp16 once; the same p^ weights the codes, the
+    // group minima and the normaliser)
+    auto softmax_page = [&](const float (&lg)[NT][2], const float (&pm)[NT], float (&pr)[NT][2]) {
+        float corr[NT];
+        bool need = false;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
             corr[nt] = 1.f;
-            if (pm > mrun[nt]) {
-                corr[nt] = ex2(mrun[nt] - pm);  // 0 when mrun = -inf
-                mrun[nt] = pm;
+            if (pm[nt] > mrun[nt]) {
+                corr[nt] = ex2(mrun[nt] - pm[nt]);  // 0 when mrun = -inf
+                mrun[nt] = pm[nt];
                 need = true;
             }
             const float mref = mrun[nt] == -CUDART_INF_F ? 0.f : mrun[nt];
-            // p is rounded to fp16 once; the same p^ weights the codes, the
-            // group minima and the normaliser
             pr[nt][0] = __half2float(__float2half_rn(ex2(lg[nt][0] - mref)));
             pr[nt][1] = __half2float(__float2half_rn(ex2(lg[nt][1] - mref)));
             lsum[nt] = fmaf(lsum[nt], corr[nt], pr[nt][0] + pr[nt][1]);
@@ -307,8 +317,12 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             cmin[1] *= cB;
             cmin[3] *= cB;
         }
+    };
 
-        // ---------------- P in the PV B layout: column n = r (head n), rows = tokens 2t, 2t+1 | 2t+8, 2t+9
+    // ---------------- PV of page i with its weights p^
+    auto pv_page = [&](int i, const float (&pr)[NT][2]) {
+        const uint8_t* tile = sm.u.ring[warp][i % DEC_STAGES];
+        // P in the PV B layout: column n = r (head n), rows = tokens 2t, 2t+1 | 2t+8, 2t+9
         uint32_t pb0, pb1;
         {
             const uint32_t X0 = pack_half2(pr[0][0], pr[0][1]);  // (token r, token r+8) of head t
@@ -327,69 +341,87 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             pb0 = prmt(Y0, Y1, 0x5410);  // p(2t), p(2t+1)
             pb1 = prmt(Y0, Y1, 0x7632);  // p(2t+8), p(2t+9)
         }
+        const uint4 m0 = lds128(tile + OFF_VM + 16 * (2 * t));
+        const uint4 m1 = lds128(tile + OFF_VM + 16 * (2 * t + 1));
+        const uint4 m8 = lds128(tile + OFF_VM + 16 * (2 * t + 8));
+        const uint4 m9 = lds128(tile + OFF_VM + 16 * (2 * t + 9));
+        const uint32_t w0[4] = {m0.x, m0.y, m0.z, m0.w}, w1[4] = {m1.x, m1.y, m1.z, m1.w};
+        const uint32_t w8[4] = {m8.x, m8.y, m8.z, m8.w}, w9[4] = {m9.x, m9.y, m9.z, m9.w};
 
-        // ---------------- PV
+        // min term: rows = groups (rows 4..15 are never read), K = tokens
         {
-            const uint4 m0 = lds128(tile + OFF_VM + 16 * (2 * t));
-            const uint4 m1 = lds128(tile + OFF_VM + 16 * (2 * t + 1));
-            const uint4 m8 = lds128(tile + OFF_VM + 16 * (2 * t + 8));
-            const uint4 m9 = lds128(tile + OFF_VM + 16 * (2 * t + 9));
-            const uint32_t w0[4] = {m0.x, m0.y, m0.z, m0.w}, w1[4] = {m1.x, m1.y, m1.z, m1.w};
-            const uint32_t w8[4] = {m8.x, m8.y, m8.z, m8.w}, w9[4] = {m9.x, m9.y, m9.z, m9.w};
-            // slots past the context may hold stale bytes (even NaN scales): zero their fp16 words
-            const uint32_t vm01 = (2 * t < n_tok ? 0x0000ffffu : 0u) | (2 * t + 1 < n_tok ? 0xffff0000u : 0u);
-            const uint32_t vm89 = (2 * t + 8 < n_tok ? 0x0000ffffu : 0u) | (2 * t + 9 < n_tok ? 0xffff0000u : 0u);
+            const int gr = 4 * (r & 3);
+            uint32_t a[4] = {0u, 0u, 0u, 0u};
+            a[0] = prmt(lds32(tile + OFF_VM + 16 * (2 * t) + gr), lds32(tile + OFF_VM + 16 * (2 * t + 1) + gr), 0x7632);
+            a[2] = prmt(lds32(tile + OFF_VM + 16 * (2 * t + 8) + gr), lds32(tile + OFF_VM + 16 * (2 * t + 9) + gr),
+                        0x7632);
+            mma_f16_16816(cmin, a, pb0, pb1);
+        }
 
-            // min term: rows = groups (r < 4), K = tokens
-            {
-                uint32_t a[4] = {0u, 0u, 0u, 0u};
-                if (r < NGROUP) {
-                    a[0] = prmt(lds32(tile + OFF_VM + 16 * (2 * t) + 4 * r),
-                                lds32(tile + OFF_VM + 16 * (2 * t + 1) + 4 * r), 0x7632) & vm01;
-                    a[2] = prmt(lds32(tile + OFF_VM + 16 * (2 * t + 8) + 4 * r),
-                                lds32(tile + OFF_VM + 16 * (2 * t + 9) + 4 * r), 0x7632) & vm89;
-                }
-                const bool dup = NT == 1 && r >= 4;  // repeated columns stay out of the min term
-                mma_f16_16816(cmin, a, dup ? 0u : pb0, dup ? 0u : pb1);
-            }
-
-            const uint32_t v0 = lds32(tile + OFF_VC + 32 * (2 * t) + 4 * r);
-            const uint32_t v1 = lds32(tile + OFF_VC + 32 * (2 * t + 1) + 4 * r);
-            const uint32_t v8 = lds32(tile + OFF_VC + 32 * (2 * t + 8) + 4 * r);
-            const uint32_t v9 = lds32(tile + OFF_VC + 32 * (2 * t + 9) + 4 * r);
-            const uint32_t A01 = prmt(v0, v1, 0x5410), A23 = prmt(v0, v1, 0x7632);
-            const uint32_t B01 = prmt(v8, v9, 0x5410), B23 = prmt(v8, v9, 0x7632);
+        const uint32_t v0 = lds32(tile + OFF_VC + 32 * (2 * t) + 4 * r);
+        const uint32_t v1 = lds32(tile + OFF_VC + 32 * (2 * t + 1) + 4 * r);
+        const uint32_t v8 = lds32(tile + OFF_VC + 32 * (2 * t + 8) + 4 * r);
+        const uint32_t v9 = lds32(tile + OFF_VC + 32 * (2 * t + 9) + 4 * r);
+        const uint32_t A01 = prmt(v0, v1, 0x5410), A23 = prmt(v0, v1, 0x7632);
+        const uint32_t B01 = prmt(v8, v9, 0x5410), B23 = prmt(v8, v9, 0x7632);
+        const __half2 P0 = u32_as_h2(pb0), P1 = u32_as_h2(pb1);
 #pragma unroll
-            for (int g = 0; g < NGROUP; ++g) {
-                const uint32_t xa = g == 0 ? A01 : g == 1 ? (A01 >> 8) : g == 2 ? A23 : (A23 >> 8);
-                const uint32_t xb = g == 0 ? B01 : g == 1 ? (B01 >> 8) : g == 2 ? B23 : (B23 >> 8);
-                const uint32_t sc01 = prmt(w0[g], w1[g], 0x5410) & vm01, sc89 = prmt(w8[g], w9[g], 0x5410) & vm89;
-                // p^ * scale exactly as an fp16 pair: hi = rn(p^ s), lo = p^ s - hi (exact)
-                const __half2 P0 = u32_as_h2(pb0), P1 = u32_as_h2(pb1);
-                const __half2 S01 = u32_as_h2(sc01), S89 = u32_as_h2(sc89);
-                const __half2 H0 = __hmul2(P0, S01), H1 = __hmul2(P1, S89);
-                const __half2 L0 = __hfma2(P0, S01, __hneg2(H0)), L1 = __hfma2(P1, S89, __hneg2(H1));
+        for (int g = 0; g < NGROUP; ++g) {
+            const uint32_t xa = g == 0 ? A01 : g == 1 ? (A01 >> 8) : g == 2 ? A23 : (A23 >> 8);
+            const uint32_t xb = g == 0 ? B01 : g == 1 ? (B01 >> 8) : g == 2 ? B23 : (B23 >> 8);
+            // p^ * scale exactly as an fp16 pair: hi = rn(p^ s), lo = p^ s - hi (exact)
+            const __half2 S01 = u32_as_h2(prmt(w0[g], w1[g], 0x5410)), S89 = u32_as_h2(prmt(w8[g], w9[g], 0x5410));
+            const __half2 H0 = __hmul2(P0, S01), H1 = __hmul2(P1, S89);
+            const __half2 L0 = __hfma2(P0, S01, __hneg2(H0)), L1 = __hfma2(P1, S89, __hneg2(H1));
 #pragma unroll
-                for (int hs = 0; hs < 2; ++hs) {
-                    const uint32_t k0 = 0x00030003u << (4 * hs), k1 = 0x00030003u << (4 * hs + 2);
-                    const uint32_t a[4] = {xa & k0, xa & k1, xb & k0, xb & k1};
-                    if constexpr (NT == 1) {
-                        const bool lo = r >= 4;
-                        mma_f16_16816(oacc[2 * g + hs], a, h2_as_u32(lo ? L0 : H0), h2_as_u32(lo ? L1 : H1));
-                    } else {
-                        mma_f16_16816(oacc[2 * g + hs], a, h2_as_u32(H0), h2_as_u32(H1));
-                        mma_f16_16816(oacc[2 * g + hs], a, h2_as_u32(L0), h2_as_u32(L1));
-                    }
+            for (int hs = 0; hs < 2; ++hs) {
+                const uint32_t k0 = 0x00030003u << (4 * hs), k1 = 0x00030003u << (4 * hs + 2);
+                const uint32_t a[4] = {xa & k0, xa & k1, xb & k0, xb & k1};
+                if constexpr (NT == 1) {
+                    const bool lo = r >= 4;
+                    mma_f16_16816(oacc[2 * g + hs], a, h2_as_u32(lo ? L0 : H0), h2_as_u32(lo ? L1 : H1));
+                } else {
+                    mma_f16_16816(oacc[2 * g + hs], a, h2_as_u32(H0), h2_as_u32(H1));
+                    mma_f16_16816(oacc[2 * g + hs], a, h2_as_u32(L0), h2_as_u32(L1));
                 }
             }
         }
+    };
 
+    // Hand page i's stage back: issue the page DEC_STAGES ahead into it.
+    auto release_page = [&](int i) {
         __syncwarp();
         if (lane == 0 && i + DEC_STAGES < my_count) {
             fence_proxy_async_smem();
             issue(i + DEC_STAGES, pid_next);
             if (i + DEC_STAGES + 1 < my_count) pid_next = page_id(i + DEC_STAGES + 1);
         }
+    };
+
+    // Software pipeline over the warp's pages: the QK of page i + 1 does not
+    // depend on the softmax or PV of page i, and the two sit in one
+    // straight-line block so their instruction streams interleave.
+    bool timed_out = false;
+    float lg[NT][2], pm[NT];
+    if (my_count > 0) {
+        timed_out = !wait_page(0);
+        if (!timed_out) qk_page(0, lg, pm);
+    }
+    for (int i = 0; i + 1 < my_count && !timed_out; ++i) {
+        float pr[NT][2];
+        softmax_page(lg, pm, pr);
+        if (!wait_page(i + 1)) {
+            timed_out = true;
+            break;
+        }
+        pv_page(i, pr);
+        qk_page(i + 1, lg, pm);  // lg, pm of page i are spent (pr holds what PV needs)
+        release_page(i);
+    }
+    if (!timed_out && my_count > 0) {
+        float pr[NT][2];
+        softmax_page(lg, pm, pr);
+        pv_page(my_count - 1, pr);
     }
     if (timed_out && lane == 0) {
         // let copies still in flight land before the shared memory is reused
@@ -470,11 +502,12 @@ static kvq_status set_smem_once(const void* fn, int bytes, int which) {
     return st;
 }
 
-extern "C" int kvq_decode_auto_splits(int B, int H_kv, int max_pages_per_seq) {
-    if (B <= 0 || H_kv <= 0 || max_pages_per_seq <= 0) return 1;
-    // about three resident CTAs per SM of the 152; at least 16 pages per split
+extern "C" int kvq_decode_auto_splits(int B, int H_q, int H_kv, int max_pages_per_seq) {
+    if (B <= 0 || H_kv <= 0 || H_q < H_kv || max_pages_per_seq <= 0) return 1;
+    // one wave of resident CTAs: 3 per SM of the 152 for GQA groups up to 4,
+    // 2 for larger groups; at least 16 pages per split
     const long units = (long)B * H_kv;
-    const long target = 152L * 3;
+    const long target = 152L * (H_q / H_kv <= 4 ? 3 : 2);
     long s = (target + units - 1) / units;
     long max_s = (max_pages_per_seq + 15) / 16;
     if (max_s > MAX_SPLITS) max_s = MAX_SPLITS;
@@ -485,7 +518,7 @@ extern "C" int kvq_decode_auto_splits(int B, int H_kv, int max_pages_per_seq) {
 
 extern "C" size_t kvq_decode_workspace_bytes(int B, int H_q, int H_kv, int max_pages_per_seq, int num_splits) {
     if (B <= 0 || H_q <= 0 || H_kv <= 0) return 0;
-    const int S = num_splits > 0 ? num_splits : kvq_decode_auto_splits(B, H_kv, max_pages_per_seq);
+    const int S = num_splits > 0 ? num_splits : kvq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
     return WS_HEADER + tickets_bytes(B, H_kv) + (size_t)B * H_q * S * PART_STRIDE * sizeof(float);
 }
 
@@ -509,7 +542,7 @@ extern "C" kvq_status kvq_decode_attn_int2(const void* q, int B, int H_q, int H_
     if (reinterpret_cast<uintptr_t>(cache) % 16 || reinterpret_cast<uintptr_t>(workspace) % 16 ||
         reinterpret_cast<uintptr_t>(R_v) % 16)
         return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_decode_attn_int2: cache, R_v and workspace need 16-byte alignment");
-    const int S = num_splits > 0 ? num_splits : kvq_decode_auto_splits(B, H_kv, max_pages_per_seq);
+    const int S = num_splits > 0 ? num_splits : kvq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
     if (S > MAX_SPLITS)
         return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_decode_attn_int2: num_splits=%d above %d", S, MAX_SPLITS);
     const size_t need = kvq_decode_workspace_bytes(B, H_q, H_kv, max_pages_per_seq, S);

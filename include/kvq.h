@@ -97,8 +97,10 @@ kvq_status kvq_append_int2(const void* k, const void* v, int n_tok, int H_kv, in
  * counters at zero again. */
 size_t kvq_decode_workspace_bytes(int B, int H_q, int H_kv, int max_pages_per_seq, int num_splits);
 
-/* The split count the automatic choice (num_splits = 0) uses. */
-int kvq_decode_auto_splits(int B, int H_kv, int max_pages_per_seq);
+/* The split count the automatic choice (num_splits = 0) uses: one wave of
+ * resident CTAs over the (sequence, KV head) pairs, at least 16 pages per
+ * split, at most 256. */
+int kvq_decode_auto_splits(int B, int H_q, int H_kv, int max_pages_per_seq);
 
 /* Fused packed-cache decode attention over the INT2 cache.
  *   q            device bf16 [B][H_q][d]
