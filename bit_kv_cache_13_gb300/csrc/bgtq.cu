@@ -468,7 +468,7 @@ extern "C" kvq_status bgtq_decode_attn(const void* q, int B, int H_q, int H_kv, 
         return kvq_set_error(KVQ_ERR_INVALID_ARG, "bgtq_decode_attn: null pointer");
     if (reinterpret_cast<uintptr_t>(cache) % 16 || reinterpret_cast<uintptr_t>(workspace) % 16)
         return kvq_set_error(KVQ_ERR_INVALID_ARG, "bgtq_decode_attn: cache and workspace need 16-byte alignment");
-    const int S = num_splits > 0 ? num_splits : kvq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
+    const int S = num_splits > 0 ? num_splits : bgtq_decode_auto_splits(B, H_kv, max_pages_per_seq);
     if (S > MAX_SPLITS)
         return kvq_set_error(KVQ_ERR_INVALID_ARG, "bgtq_decode_attn: num_splits=%d above %d", S, MAX_SPLITS);
     const size_t need = kvq_decode_workspace_bytes(B, H_q, H_kv, max_pages_per_seq, S);

@@ -6,9 +6,11 @@
 // the output is rotated back once (o = o' R_v^T).  The kernel reads only the
 // packed codes and fp16 (scale, min) pairs.
 //
-// Grid (split, kv_head, seq); 4 warps per CTA, each warp streaming its own
-// pages of the split through a 4-stage ring of 1536-byte tiles filled by
-// bulk async copies (cp.async.bulk + mbarrier).  Per page (16 tokens):
+// Grid (split, kv_head, seq) with one large CTA per SM (12 warps for head
+// groups up to 4, 8 for groups of 8).  Each warp streams pages through its
+// own 8-stage ring of 1536-byte tiles filled by bulk async copies
+// (cp.async.bulk + mbarrier).  The pages of a (sequence, KV head) are dealt
+// round-robin over all warps of its split CTAs.  Per page (16 tokens):
 //
 //   QK  logit(s, j) = sum_g [ scale_{s,g} <q'_{j,g}, c_{s,g}> + min_{s,g} S_{j,g} ]
 //       The 2-bit codes c are fed to mma.sync m16n8k16 as exact fp16
@@ -23,6 +25,7 @@
 //       hi/lo pair (HMUL2, then HFMA2 for the remainder), so the large
 //       group minima and the code term cancel without amplifying rounding;
 //       the min term is one more MMA with A = the fp16 mins of the groups.
+//   The QK of page i + 1 and the softmax/PV of page i are software-pipelined.
 //
 // Split partials (m, l, o') go to the workspace; the last CTA of a
 // (sequence, KV head) to finish (atomic ticket, no waiting) merges them,
@@ -33,25 +36,32 @@
 
 namespace kvq {
 
-constexpr int DEC_WARPS = 4;
 constexpr int DEC_STAGES = 8;
 
-template <int MAXG>
+// Warps per CTA.  Each of the SM's four schedulers owns a quarter of its
+// 64K registers: three warps of 168 registers fit one (head groups up to 4),
+// while groups of 8 need more registers per thread and run two per scheduler.
+template <int NT>
+struct DecWarps {
+    static constexpr int NW = NT == 1 ? 12 : 8;
+};
+
+template <int NW, int MAXG>
 struct __align__(16) DecodeSmem {
     union {
-        uint8_t ring[DEC_WARPS][DEC_STAGES][INT2_TILE];  // page tiles in flight
-        float o_part[DEC_WARPS][MAXG][D];                // per-warp o' after the loop
+        uint8_t ring[NW][DEC_STAGES][INT2_TILE];  // page tiles in flight
+        float o_part[NW][MAXG][D];                // per-warp o' after the loop
     } u;
-    uint64_t bar[DEC_WARPS][DEC_STAGES];
-    int ntok[DEC_WARPS][DEC_STAGES];  // valid tokens of the page in each stage (0: skipped page)
-    float q[MAXG][D];     // scaled rotated queries q~ = q R_k * scale * log2(e)
+    uint64_t bar[NW][DEC_STAGES];
+    int ntok[NW][DEC_STAGES];  // valid tokens of the page in each stage (0: skipped page)
+    float q[MAXG][D];          // scaled rotated queries q~ = q R_k * scale * log2(e)
     float gsum[MAXG][NGROUP];
-    float sigma[MAXG];    // power-of-two pre-scale per head
-    MergeSmem<DEC_WARPS, MAXG> ms;
+    float sigma[MAXG];         // power-of-two pre-scale per head
+    MergeSmem<NW, MAXG> ms;
 };
 
 template <int NT>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(DecWarps<NT>::NW * 32, 1)
 decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G, const uint8_t* __restrict__ cache,
                    int64_t num_pages, const int32_t* __restrict__ block_table, int max_pages,
                    const int32_t* __restrict__ context_lens, const float* __restrict__ Rk,
@@ -59,10 +69,11 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                    uint8_t* __restrict__ ws) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     constexpr int MAXG = 4 * NT;
-    DecodeSmem<MAXG>& sm = *reinterpret_cast<DecodeSmem<MAXG>*>(smem_raw);
+    constexpr int NW = DecWarps<NT>::NW;
+    DecodeSmem<NW, MAXG>& sm = *reinterpret_cast<DecodeSmem<NW, MAXG>*>(smem_raw);
 
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int S = gridDim.x;
+    const int S = gridDim.x, B = gridDim.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r = lane >> 2, t = lane & 3;
 
@@ -71,27 +82,34 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     int ctx = __ldg(context_lens + b);
     ctx = max(0, min(ctx, max_pages * PAGE));
     const int n_pages = (ctx + PAGE - 1) / PAGE;
-    const int pps = (n_pages + S - 1) / S;
-    const int p_begin = min(split * pps, n_pages);
-    const int p_end = min(p_begin + pps, n_pages);
-    const int my_count = p_end - p_begin > warp ? (p_end - p_begin - warp + DEC_WARPS - 1) / DEC_WARPS : 0;
     const int32_t* bt = block_table + (size_t)b * max_pages;
+    // Page schedule: the pages of a (sequence, KV head) are dealt round-robin
+    // over all S * NW warps of its split CTAs, so warp k0 = split * NW + warp
+    // takes pages k0, k0 + KS, k0 + 2 KS, ...  Every warp gets the same
+    // number of pages to within one, and page ids come from anywhere in the
+    // sequence (the block table scatters them over the cache anyway).
+    const int KS = S * NW, k0 = split * NW + warp;
+    const int my_count = n_pages > k0 ? (n_pages - k0 + KS - 1) / KS : 0;
+    auto page_of = [&](int j) { return k0 + KS * j; };
 
     // ---- first, every global read of the prologue is put in flight at once:
     // the first pages' ids (lane 0), this warp's rows of R_k, the query rows
-    auto page_id = [&](int i) { return __ldg(bt + p_begin + warp + DEC_WARPS * i); };
     int pids[DEC_STAGES + 1];
     if (lane == 0) {
 #pragma unroll
-        for (int i = 0; i <= DEC_STAGES; ++i) pids[i] = i < my_count ? page_id(i) : 0;
+        for (int j = 0; j <= DEC_STAGES; ++j) pids[j] = j < my_count ? __ldg(bt + page_of(j)) : 0;
     }
-    float4 rr[RowPrefetch<MAXG>::N];
-    load_rows<DEC_WARPS>(Rk + (size_t)h * D * D, rr);
-    __nv_bfloat16 qv[MAXG];
+    float4 rr[RowPrefetch<NW, MAXG>::N];
+    load_rows<NW>(Rk + (size_t)h * D * D, rr);
+    constexpr int QPT = (MAXG * D + NW * 32 - 1) / (NW * 32);  // query values per thread
+    float qv[QPT];
     {
         const __nv_bfloat16* qb = q + ((size_t)b * H_q + (size_t)h * G) * D;
 #pragma unroll
-        for (int jj = 0; jj < MAXG; ++jj) qv[jj] = jj < G ? qb[jj * D + tid] : __float2bfloat16(0.f);
+        for (int k = 0; k < QPT; ++k) {
+            const int idx = tid + k * NW * 32;
+            qv[k] = idx < G * D ? __bfloat162float(qb[idx]) : 0.f;
+        }
     }
     if (lane == 0) {
         for (int s = 0; s < DEC_STAGES; ++s) mbar_init(&sm.bar[warp][s], 1);
@@ -99,11 +117,10 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         fence_proxy_async_smem();
     }
     __syncwarp();
-    // Lane 0 issues page i of this warp with its (already loaded) page id and
-    // records how many of its tokens are valid; the mbarrier publishes that
-    // count together with the data.
-    auto issue = [&](int i, int pid) {  // lane 0 only
-        const int p = p_begin + warp + DEC_WARPS * i;
+    // Lane 0 issues the warp's i-th page (sequence page p) with its (already
+    // loaded) page id and records how many of its tokens are valid; the
+    // mbarrier publishes that count together with the data.
+    auto issue = [&](int i, int p, int pid) {  // lane 0 only
         const int st = i % DEC_STAGES;
         uint64_t* bar = &sm.bar[warp][st];
         if (pid < 0 || (int64_t)pid >= num_pages) {
@@ -116,23 +133,25 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             bulk_g2s(sm.u.ring[warp][st], cache + ((size_t)pid * H_kv + h) * INT2_TILE, INT2_TILE, bar);
         }
     };
-    int pid_next = 0;  // lane 0: page id of the next page to issue, loaded one iteration early
+    int pid_next = 0;  // lane 0: page id of the next page to issue, loaded one release early
     if (lane == 0) {
 #pragma unroll
-        for (int i = 0; i < DEC_STAGES; ++i)
-            if (i < my_count) issue(i, pids[i]);
+        for (int j = 0; j < DEC_STAGES; ++j)
+            if (j < my_count) issue(j, page_of(j), pids[j]);
         pid_next = pids[DEC_STAGES];
     }
 
     // ---- q~ = (q R_k) * scale * log2(e) for the G heads of this KV head
     {
 #pragma unroll
-        for (int jj = 0; jj < MAXG; ++jj)
-            if (jj < G) sm.ms.o_final[jj][tid] = __bfloat162float(qv[jj]);
+        for (int k = 0; k < QPT; ++k) {
+            const int idx = tid + k * NW * 32;
+            if (idx < G * D) sm.ms.o_final[idx / D][idx % D] = qv[k];
+        }
         __syncthreads();
-        rotate_rows<DEC_WARPS, MAXG>(sm.ms.o_final, Rk + (size_t)h * D * D, rr, G, scale_log2, sm.q, sm.ms);
+        rotate_rows<NW, MAXG>(sm.ms.o_final, Rk + (size_t)h * D * D, rr, G, scale_log2, sm.q, sm.ms);
         // per head: power-of-two pre-scale (max |q~| * sigma in [2^14, 2^15)) and group sums
-        for (int jj = warp; jj < G; jj += DEC_WARPS) {
+        for (int jj = warp; jj < G; jj += NW) {
             float mx = 0.f;
             float gs[NGROUP];
 #pragma unroll
@@ -388,13 +407,14 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         }
     };
 
-    // Hand page i's stage back: issue the page DEC_STAGES ahead into it.
+    // Hand page i's stage back: issue the page DEC_STAGES ahead into it and
+    // start loading the id of the one after.
     auto release_page = [&](int i) {
         __syncwarp();
         if (lane == 0 && i + DEC_STAGES < my_count) {
             fence_proxy_async_smem();
-            issue(i + DEC_STAGES, pid_next);
-            if (i + DEC_STAGES + 1 < my_count) pid_next = page_id(i + DEC_STAGES + 1);
+            issue(i + DEC_STAGES, page_of(i + DEC_STAGES), pid_next);
+            if (i + DEC_STAGES + 1 < my_count) pid_next = __ldg(bt + page_of(i + DEC_STAGES + 1));
         }
     };
 
@@ -407,7 +427,8 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         timed_out = !wait_page(0);
         if (!timed_out) qk_page(0, lg, pm);
     }
-    for (int i = 0; i + 1 < my_count && !timed_out; ++i) {
+    int i = 0;
+    for (; i + 1 < my_count && !timed_out; ++i) {
         float pr[NT][2];
         softmax_page(lg, pm, pr);
         if (!wait_page(i + 1)) {
@@ -421,7 +442,7 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     if (!timed_out && my_count > 0) {
         float pr[NT][2];
         softmax_page(lg, pm, pr);
-        pv_page(my_count - 1, pr);
+        pv_page(i, pr);
     }
     if (timed_out && lane == 0) {
         // let copies still in flight land before the shared memory is reused
@@ -478,7 +499,7 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     }
     __syncthreads();
 
-    finish_decode<DEC_WARPS, MAXG>(sm.ms, sm.u.o_part, G, H_q, H_kv, gridDim.z, b, h, split, S, ws,
+    finish_decode<NW, MAXG>(sm.ms, sm.u.o_part, G, H_q, H_kv, B, b, h, split, S, ws,
                              Rv + (size_t)h * D * D, out);
 }
 
@@ -504,11 +525,23 @@ static kvq_status set_smem_once(const void* fn, int bytes, int which) {
 
 extern "C" int kvq_decode_auto_splits(int B, int H_q, int H_kv, int max_pages_per_seq) {
     if (B <= 0 || H_kv <= 0 || H_q < H_kv || max_pages_per_seq <= 0) return 1;
-    // one wave of resident CTAs: 3 per SM of the 152 for GQA groups up to 4,
-    // 2 for larger groups; at least 16 pages per split
+    // one CTA per SM of the 152 over the (sequence, KV head) pairs; at
+    // least 32 pages per split (the CTAs have 10-12 warps)
     const long units = (long)B * H_kv;
-    const long target = 152L * (H_q / H_kv <= 4 ? 3 : 2);
-    long s = (target + units - 1) / units;
+    long s = (152L + units - 1) / units;
+    long max_s = (max_pages_per_seq + 31) / 32;
+    if (max_s > MAX_SPLITS) max_s = MAX_SPLITS;
+    if (s > max_s) s = max_s;
+    if (s < 1) s = 1;
+    return (int)s;
+}
+
+// The Block-GTQ decode runs 4-warp CTAs, several per SM: its automatic
+// split count aims at three CTAs per SM, at least 16 pages per split.
+int bgtq_decode_auto_splits(int B, int H_kv, int max_pages_per_seq) {
+    if (B <= 0 || H_kv <= 0 || max_pages_per_seq <= 0) return 1;
+    const long units = (long)B * H_kv;
+    long s = (152L * 3 + units - 1) / units;
     long max_s = (max_pages_per_seq + 15) / 16;
     if (max_s > MAX_SPLITS) max_s = MAX_SPLITS;
     if (s > max_s) s = max_s;
@@ -518,7 +551,12 @@ extern "C" int kvq_decode_auto_splits(int B, int H_q, int H_kv, int max_pages_pe
 
 extern "C" size_t kvq_decode_workspace_bytes(int B, int H_q, int H_kv, int max_pages_per_seq, int num_splits) {
     if (B <= 0 || H_q <= 0 || H_kv <= 0) return 0;
-    const int S = num_splits > 0 ? num_splits : kvq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
+    int S = num_splits;
+    if (S <= 0) {  // room for the automatic choice of either decode entry point
+        S = kvq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
+        const int Sb = bgtq_decode_auto_splits(B, H_kv, max_pages_per_seq);
+        if (Sb > S) S = Sb;
+    }
     return WS_HEADER + tickets_bytes(B, H_kv) + (size_t)B * H_q * S * PART_STRIDE * sizeof(float);
 }
 
@@ -550,7 +588,8 @@ extern "C" kvq_status kvq_decode_attn_int2(const void* q, int B, int H_q, int H_
         return kvq_set_error(KVQ_ERR_WORKSPACE, "kvq_decode_attn_int2: workspace %zu < %zu bytes", workspace_bytes,
                              need);
     const float scale_log2 = scale * 1.4426950408889634f;
-    const size_t smem = G <= 4 ? sizeof(DecodeSmem<4>) : sizeof(DecodeSmem<8>);
+    constexpr int NW1 = DecWarps<1>::NW, NW2 = DecWarps<2>::NW;
+    const size_t smem = G <= 4 ? sizeof(DecodeSmem<NW1, 4>) : sizeof(DecodeSmem<NW2, 8>);
     dim3 grid(S, H_kv, B);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
@@ -558,11 +597,11 @@ extern "C" kvq_status kvq_decode_attn_int2(const void* q, int B, int H_q, int H_
                                   (int)smem, G <= 4 ? 0 : 1);
     if (sa != KVQ_OK) return sa;
     if (G <= 4) {
-        decode_int2_kernel<1><<<grid, 128, smem, st>>>(
+        decode_int2_kernel<1><<<grid, NW1 * 32, smem, st>>>(
             static_cast<const __nv_bfloat16*>(q), H_q, H_kv, G, static_cast<const uint8_t*>(cache), num_pages,
             block_table, max_pages_per_seq, context_lens, R_k, R_v, scale_log2, out, static_cast<uint8_t*>(workspace));
     } else {
-        decode_int2_kernel<2><<<grid, 128, smem, st>>>(
+        decode_int2_kernel<2><<<grid, NW2 * 32, smem, st>>>(
             static_cast<const __nv_bfloat16*>(q), H_q, H_kv, G, static_cast<const uint8_t*>(cache), num_pages,
             block_table, max_pages_per_seq, context_lens, R_k, R_v, scale_log2, out, static_cast<uint8_t*>(workspace));
     }

@@ -55,7 +55,8 @@ extern "C" kvq_status kvq_decode_attn_int2_noalloc(const void* q, int B, int H_q
     if (B <= 0 || H_q <= 0 || H_kv <= 0 || max_pages_per_seq <= 0 || num_splits < 0)
         return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_decode_attn_int2_noalloc: B=%d H_q=%d H_kv=%d max_pages=%d",
                              B, H_q, H_kv, max_pages_per_seq);
-    const size_t need = kvq_decode_workspace_bytes(B, H_q, H_kv, max_pages_per_seq, num_splits);
+    const int S = num_splits > 0 ? num_splits : kvq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
+    const size_t need = kvq_decode_workspace_bytes(B, H_q, H_kv, max_pages_per_seq, S);
     if (need > kNoallocScratchBytes)
         return kvq_set_error(KVQ_ERR_WORKSPACE,
                              "kvq_decode_attn_int2_noalloc: this shape needs %zu bytes of scratch, above the fixed "
@@ -70,5 +71,5 @@ extern "C" kvq_status kvq_decode_attn_int2_noalloc(const void* q, int B, int H_q
                         "kvq_decode_attn_int2_noalloc: clearing scratch");
     if (st != KVQ_OK) return st;
     return kvq_decode_attn_int2(q, B, H_q, H_kv, d, cache, num_pages, block_table, max_pages_per_seq, context_lens,
-                                R_k, R_v, scale, out, scratch, kNoallocScratchBytes, num_splits, stream);
+                                R_k, R_v, scale, out, scratch, kNoallocScratchBytes, S, stream);
 }

@@ -28,7 +28,16 @@ constexpr long long WAIT_LIMIT_CYCLES = 4000000000LL;
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// one int32 split ticket per (sequence, KV head), zero between calls
 __host__ __device__ inline size_t tickets_bytes(int B, int H_kv) { return align_up((size_t)B * H_kv * 4, 256); }
+
+}  // namespace kvq
+
+// Automatic split count of the Block-GTQ decode (host; defined beside the
+// INT2 rule, which kvq_decode_auto_splits exports).
+int bgtq_decode_auto_splits(int B, int H_kv, int max_pages_per_seq);
+
+namespace kvq {
 
 // ---------------------------------------------------------------- PTX
 

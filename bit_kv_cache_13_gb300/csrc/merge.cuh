@@ -15,6 +15,10 @@
 // The ticket is reset to zero so the workspace is ready for the next call.
 // Every global read in these paths is issued many-at-a-time (warps split
 // the rows / splits, float4 loads) so their latency overlaps.
+//
+// NW is the CTA's warp count.  A 128 x 128 rotation is shared by
+// RotSplit<NW>::NR warps of RotSplit<NW>::RPW rows each: all four warps of a
+// 4-warp CTA (32 rows each), eight warps of a larger one (16 rows each).
 #pragma once
 
 #include <math_constants.h>
@@ -25,15 +29,29 @@ namespace kvq {
 
 constexpr int MAX_SPLITS = 256;
 
+template <int NW>
+struct RotSplit {
+    static constexpr int NR = NW < 8 ? NW : 8;
+    static constexpr int RPW = D / NR;
+    static_assert(NR * RPW == D && (RPW == 16 || RPW == 32), "rotation split");
+};
+
+// Rows of R a rotating warp holds in registers at once: all of its rows,
+// except 16 of 32 for head groups of 8 (register budget).
+template <int NW, int MAXG>
+struct RowPrefetch {
+    static constexpr int N = (RotSplit<NW>::RPW == 32 && MAXG > 4) ? 16 : RotSplit<NW>::RPW;
+};
+
 // MAXG: the largest query-head group the kernel instance handles (G <= MAXG).
-template <int NWARPS, int MAXG>
+template <int NW, int MAXG>
 struct MergeSmem {
-    float m_part[NWARPS][MAXG];
-    float l_part[NWARPS][MAXG];
+    float m_part[NW][MAXG];
+    float l_part[NW][MAXG];
     float o_final[MAXG][D];
-    float red[NWARPS][MAXG][D];    // cross-warp partial sums
-    float fac[MAXG][MAX_SPLITS];   // per-split maxima, then weights 2^(m_s - M)
-    float lsp[MAXG][MAX_SPLITS];   // per-split normalisers
+    float red[RotSplit<NW>::NR][MAXG][D];  // cross-warp partial sums
+    float fac[MAXG][MAX_SPLITS];           // per-split maxima, then weights 2^(m_s - M)
+    float lsp[MAXG][MAX_SPLITS];           // per-split normalisers
     float Mh[MAXG], Lh[MAXG];
     int is_last;
 };
@@ -48,93 +66,91 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// Rows prefetched early by the prologue: all 32 of a warp's rows when the
-// head group is small, half of them for groups of 8 (register budget).
-template <int MAXG>
-struct RowPrefetch {
-    static constexpr int N = MAXG <= 4 ? 32 : 16;
-};
-
-// Rows 32w .. 32w+N-1 of R, columns 4*lane .. 4*lane+3, for warp w: issued
-// together so their latencies overlap (call early, use later).
-template <int NWARPS, int N>
+// The first N rows of this warp's share of R (rows RPW*w .. RPW*w+N-1),
+// columns 4*lane .. 4*lane+3, for the rotating warps w < NR: issued together
+// so their latencies overlap (call early, use later).
+template <int NW, int N>
 __device__ __forceinline__ void load_rows(const float* __restrict__ R, float4 (&rr)[N]) {
-    static_assert(NWARPS * 32 == D, "one warp per 32 rows");
+    constexpr int NR = RotSplit<NW>::NR, RPW = RotSplit<NW>::RPW;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp >= NR) return;
 #pragma unroll
-    for (int ii = 0; ii < N; ++ii) rr[ii] = ldg4(R + (size_t)(32 * warp + ii) * D + 4 * lane);
+    for (int ii = 0; ii < N; ++ii) rr[ii] = ldg4(R + (size_t)(RPW * warp + ii) * D + 4 * lane);
 }
 
-// qr[jj][c] = sum_i qin[jj][i] * R[i][c] * factor for jj < G (128 threads),
-// with the first N of this warp's rows of R already in rr (load_rows); the
-// rest are loaded here.
-template <int NWARPS, int MAXG, int N>
+// qr[jj][c] = sum_i qin[jj][i] * R[i][c] * factor for jj < G (all NW warps
+// call it), with the first N of each rotating warp's rows of R already in rr
+// (load_rows); the rest are loaded here.
+template <int NW, int MAXG, int N>
 __device__ __forceinline__ void rotate_rows(const float (*qin)[D], const float* __restrict__ R, const float4 (&rr)[N],
-                                            int G, float factor, float (*qr)[D], MergeSmem<NWARPS, MAXG>& ms) {
+                                            int G, float factor, float (*qr)[D], MergeSmem<NW, MAXG>& ms) {
+    constexpr int NR = RotSplit<NW>::NR, RPW = RotSplit<NW>::RPW;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float4 acc[MAXG];
+    if (warp < NR) {
+        float4 acc[MAXG];
 #pragma unroll
-    for (int jj = 0; jj < MAXG; ++jj) acc[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
-    auto accumulate = [&](int i, float4 r) {
+        for (int jj = 0; jj < MAXG; ++jj) acc[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
+        auto accumulate = [&](int i, float4 r) {
+#pragma unroll
+            for (int jj = 0; jj < MAXG; ++jj)
+                if (jj < G) {
+                    const float x = qin[jj][i];
+                    acc[jj].x = fmaf(x, r.x, acc[jj].x);
+                    acc[jj].y = fmaf(x, r.y, acc[jj].y);
+                    acc[jj].z = fmaf(x, r.z, acc[jj].z);
+                    acc[jj].w = fmaf(x, r.w, acc[jj].w);
+                }
+        };
+#pragma unroll
+        for (int ii = 0; ii < N; ++ii) accumulate(RPW * warp + ii, rr[ii]);
+        if constexpr (N < RPW) {
+            float4 r2[RPW - N];
+#pragma unroll
+            for (int ii = 0; ii < RPW - N; ++ii) r2[ii] = ldg4(R + (size_t)(RPW * warp + N + ii) * D + 4 * lane);
+#pragma unroll
+            for (int ii = 0; ii < RPW - N; ++ii) accumulate(RPW * warp + N + ii, r2[ii]);
+        }
 #pragma unroll
         for (int jj = 0; jj < MAXG; ++jj)
-            if (jj < G) {
-                const float x = qin[jj][i];
-                acc[jj].x = fmaf(x, r.x, acc[jj].x);
-                acc[jj].y = fmaf(x, r.y, acc[jj].y);
-                acc[jj].z = fmaf(x, r.z, acc[jj].z);
-                acc[jj].w = fmaf(x, r.w, acc[jj].w);
-            }
-    };
-#pragma unroll
-    for (int ii = 0; ii < N; ++ii) accumulate(32 * warp + ii, rr[ii]);
-    if constexpr (N < 32) {
-        float4 r2[32 - N];
-#pragma unroll
-        for (int ii = 0; ii < 32 - N; ++ii) r2[ii] = ldg4(R + (size_t)(32 * warp + N + ii) * D + 4 * lane);
-#pragma unroll
-        for (int ii = 0; ii < 32 - N; ++ii) accumulate(32 * warp + N + ii, r2[ii]);
+            if (jj < G) *reinterpret_cast<float4*>(&ms.red[warp][jj][4 * lane]) = acc[jj];
     }
-#pragma unroll
-    for (int jj = 0; jj < MAXG; ++jj)
-        if (jj < G) *reinterpret_cast<float4*>(&ms.red[warp][jj][4 * lane]) = acc[jj];
     __syncthreads();
-    const int c = threadIdx.x;
-    for (int jj = 0; jj < G; ++jj) {
+    for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
+        const int jj = idx / D, c = idx % D;
         float s = 0.f;
 #pragma unroll
-        for (int w = 0; w < NWARPS; ++w) s += ms.red[w][jj][c];
+        for (int w = 0; w < NR; ++w) s += ms.red[w][jj][c];
         qr[jj][c] = s * factor;
     }
     __syncthreads();
 }
 
-// 128 threads; o_part[w][jj][c] is warp w's o'.  Rot is row-major [D][D]
+// NW*32 threads; o_part[w][jj][c] is warp w's o'.  Rot is row-major [D][D]
 // fp32, 16-byte aligned.  S <= MAX_SPLITS, G <= MAXG.
-template <int NWARPS, int MAXG>
-__device__ __forceinline__ void finish_decode(MergeSmem<NWARPS, MAXG>& ms, const float (*o_part)[MAXG][D], int G, int H_q,
+template <int NW, int MAXG>
+__device__ __forceinline__ void finish_decode(MergeSmem<NW, MAXG>& ms, const float (*o_part)[MAXG][D], int G, int H_q,
                                               int H_kv, int B, int b, int h, int split, int S, uint8_t* ws,
                                               const float* __restrict__ Rot, float* __restrict__ out) {
-    const int c = threadIdx.x, warp = c >> 5, lane = c & 31;
+    constexpr int NR = RotSplit<NW>::NR, RPW = RotSplit<NW>::RPW, RP = RowPrefetch<NW, MAXG>::N;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int32_t* tickets = reinterpret_cast<int32_t*>(ws + WS_HEADER);
     float* partials = reinterpret_cast<float*>(ws + WS_HEADER + tickets_bytes(B, H_kv));
     const size_t head0 = (size_t)b * H_q + (size_t)h * G;
+    const size_t unit = (size_t)b * H_kv + h;
 
     // ---- warps -> this CTA's split partial (M, L, unnormalised o')
-    // rows of Rot this warp rotates, columns 4*lane .. +3: coalesced, issued
-    // now; all 32 rows at once for small head groups, 16 at a time for 8
-    constexpr int RP = MAXG <= 4 ? 32 : 16;
+    // rows of Rot this warp rotates, columns 4*lane .. +3: coalesced, issued now
     float4 rr[RP];
-#pragma unroll
-    for (int ii = 0; ii < RP; ++ii) rr[ii] = ldg4(Rot + (size_t)(32 * warp + ii) * D + 4 * lane);
-    for (int jj = 0; jj < G; ++jj) {
+    load_rows<NW, RP>(Rot, rr);
+    for (int idx = tid; idx < G * D; idx += NW * 32) {
+        const int jj = idx / D, c = idx % D;
         float M = -CUDART_INF_F;
 #pragma unroll
-        for (int w = 0; w < NWARPS; ++w) M = fmaxf(M, ms.m_part[w][jj]);
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, ms.m_part[w][jj]);
         float L = 0.f, O = 0.f;
         if (M != -CUDART_INF_F) {
 #pragma unroll
-            for (int w = 0; w < NWARPS; ++w) {
+            for (int w = 0; w < NW; ++w) {
                 const float f = exp2f(ms.m_part[w][jj] - M);
                 L = fmaf(ms.l_part[w][jj], f, L);
                 O = fmaf(o_part[w][jj][c], f, O);
@@ -147,48 +163,52 @@ __device__ __forceinline__ void finish_decode(MergeSmem<NWARPS, MAXG>& ms, const
         }
     }
     __syncthreads();
-    // ---- rotate this partial: O_i = sum_j o'_j Rot[i][j] for i = 32*warp + lane.
-    // Each lane forms the partial dots of its 4 columns with RP of the warp's
+    // ---- rotate this partial: O_i = sum_j o'_j Rot[i][j] for the rows i of
+    // this warp.  Each lane forms the partial dots of its 4 columns with RP
     // rows; a reduce-scatter over the lanes then leaves each row's full dot
-    // in one lane (31 shuffles per head and 32 rows).
+    // in one lane (RP - 1 shuffles per head and RP rows, after a fold of the
+    // two half-warps when RP = 16).
+    if (warp < NR) {
 #pragma unroll
-    for (int pass = 0; pass < 32 / RP; ++pass) {
-        if (pass > 0) {
+        for (int pass = 0; pass < RPW / RP; ++pass) {
+            if (pass > 0) {
 #pragma unroll
-            for (int ii = 0; ii < RP; ++ii) rr[ii] = ldg4(Rot + (size_t)(32 * warp + RP * pass + ii) * D + 4 * lane);
-        }
-        for (int jj = 0; jj < G; ++jj) {
-            const float4 o4 = *reinterpret_cast<const float4*>(&ms.o_final[jj][4 * lane]);
-            float v[RP];
-#pragma unroll
-            for (int ii = 0; ii < RP; ++ii)
-                v[ii] = fmaf(o4.x, rr[ii].x, fmaf(o4.y, rr[ii].y, fmaf(o4.z, rr[ii].z, o4.w * rr[ii].w)));
-            if constexpr (RP == 16) {
-#pragma unroll
-                for (int k = 0; k < 16; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], 16);
+                for (int ii = 0; ii < RP; ++ii)
+                    rr[ii] = ldg4(Rot + (size_t)(RPW * warp + RP * pass + ii) * D + 4 * lane);
             }
+            for (int jj = 0; jj < G; ++jj) {
+                const float4 o4 = *reinterpret_cast<const float4*>(&ms.o_final[jj][4 * lane]);
+                float v[RP];
 #pragma unroll
-            for (int off = RP / 2; off >= 1; off >>= 1) {
-                const bool upper = lane & off;
+                for (int ii = 0; ii < RP; ++ii)
+                    v[ii] = fmaf(o4.x, rr[ii].x, fmaf(o4.y, rr[ii].y, fmaf(o4.z, rr[ii].z, o4.w * rr[ii].w)));
+                if constexpr (RP == 16) {
 #pragma unroll
-                for (int k = 0; k < off; ++k) {
-                    const float send = upper ? v[k] : v[k + off];
-                    const float keep = upper ? v[k + off] : v[k];
-                    v[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                    for (int k = 0; k < 16; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], 16);
                 }
-            }
-            float* part = partials + ((head0 + jj) * S + split) * PART_STRIDE;
-            if (RP == 32 || lane < 16) part[4 + 32 * warp + RP * pass + (lane & (RP - 1))] = v[0];
-            if (c == 0 && pass == 0) {
-                part[0] = ms.Mh[jj];
-                part[1] = ms.Lh[jj];
+#pragma unroll
+                for (int off = RP / 2; off >= 1; off >>= 1) {
+                    const bool upper = lane & off;
+#pragma unroll
+                    for (int k = 0; k < off; ++k) {
+                        const float send = upper ? v[k] : v[k + off];
+                        const float keep = upper ? v[k + off] : v[k];
+                        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                    }
+                }
+                float* part = partials + ((head0 + jj) * S + split) * PART_STRIDE;
+                if (RP == 32 || lane < 16) part[4 + RPW * warp + RP * pass + (lane & (RP - 1))] = v[0];
+                if (tid == 0 && pass == 0) {
+                    part[0] = ms.Mh[jj];
+                    part[1] = ms.Lh[jj];
+                }
             }
         }
     }
     __threadfence();
     __syncthreads();
-    if (c == 0) {
-        const int prev = atomicAdd(tickets + (size_t)b * H_kv + h, 1);
+    if (tid == 0) {
+        const int prev = atomicAdd(tickets + unit, 1);
         ms.is_last = prev == S - 1;
     }
     __syncthreads();
@@ -196,8 +216,7 @@ __device__ __forceinline__ void finish_decode(MergeSmem<NWARPS, MAXG>& ms, const
     __threadfence();
 
     // ---- last CTA: every split's (m, l) of the G heads, gathered at once
-#pragma unroll 4
-    for (int idx = c; idx < G * S; idx += NWARPS * 32) {
+    for (int idx = tid; idx < G * S; idx += NW * 32) {
         const int jj = idx / S, s = idx - jj * S;
         const float2 ml = __ldcg(reinterpret_cast<const float2*>(partials + ((head0 + jj) * S + s) * PART_STRIDE));
         ms.fac[jj][s] = ml.x;
@@ -205,7 +224,7 @@ __device__ __forceinline__ void finish_decode(MergeSmem<NWARPS, MAXG>& ms, const
     }
     __syncthreads();
     // split weights (one warp per head, lanes over splits, shared memory only)
-    for (int jj = warp; jj < G; jj += NWARPS) {
+    for (int jj = warp; jj < G; jj += NW) {
         float M = -CUDART_INF_F;
         for (int s = lane; s < S; s += 32) M = fmaxf(M, ms.fac[jj][s]);
 #pragma unroll
@@ -224,14 +243,14 @@ __device__ __forceinline__ void finish_decode(MergeSmem<NWARPS, MAXG>& ms, const
         }
     }
     __syncthreads();
-    // ---- weighted sum of the split outputs: warp w takes splits w, w+4, ...;
-    // unrolled so each lane keeps many independent loads in flight
-    {
+    // ---- weighted sum of the split outputs: warp w < NR takes splits
+    // w, w + NR, ...; unrolled so each lane keeps many independent loads in flight
+    if (warp < NR) {
         float4 acc[MAXG];
 #pragma unroll
         for (int jj = 0; jj < MAXG; ++jj) acc[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll(MAXG <= 4 ? 8 : 4)
-        for (int s = warp; s < S; s += NWARPS) {
+        for (int s = warp; s < S; s += NR) {
 #pragma unroll
             for (int jj = 0; jj < MAXG; ++jj)
                 if (jj < G) {
@@ -248,14 +267,15 @@ __device__ __forceinline__ void finish_decode(MergeSmem<NWARPS, MAXG>& ms, const
             if (jj < G) *reinterpret_cast<float4*>(&ms.red[warp][jj][4 * lane]) = acc[jj];
     }
     __syncthreads();
-    for (int jj = 0; jj < G; ++jj) {
+    for (int idx = tid; idx < G * D; idx += NW * 32) {
+        const int jj = idx / D, c = idx % D;
         float s = 0.f;
 #pragma unroll
-        for (int w = 0; w < NWARPS; ++w) s += ms.red[w][jj][c];
+        for (int w = 0; w < NR; ++w) s += ms.red[w][jj][c];
         const float L = ms.Lh[jj];
         out[(head0 + jj) * D + c] = L > 0.f ? s / L : 0.f;
     }
-    if (c == 0) tickets[(size_t)b * H_kv + h] = 0;
+    if (tid == 0) tickets[unit] = 0;
 }
 
 }  // namespace kvq

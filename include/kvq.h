@@ -91,15 +91,18 @@ kvq_status kvq_append_int2(const void* k, const void* v, int n_tok, int H_kv, in
                            void* stream);
 
 /* Bytes of decode workspace for B sequences, H_q query heads, H_kv KV heads
- * and num_splits split-K partitions (num_splits = 0: the number the
- * automatic choice would take for max_pages_per_seq pages).  The workspace
- * must be zero-filled once before its first use; every call leaves its
- * counters at zero again. */
+ * and num_splits split-K partitions (num_splits = 0: room for the automatic
+ * choice of either decode entry point, kvq_decode_attn_int2 or
+ * bgtq_decode_attn, at max_pages_per_seq pages).  The workspace holds an
+ * error word, a split ticket per (sequence, KV head) and the split partials.
+ * It must be zero-filled once before its first use; every call leaves its
+ * tickets at zero again. */
 size_t kvq_decode_workspace_bytes(int B, int H_q, int H_kv, int max_pages_per_seq, int num_splits);
 
-/* The split count the automatic choice (num_splits = 0) uses: one wave of
- * resident CTAs over the (sequence, KV head) pairs, at least 16 pages per
- * split, at most 256. */
+/* The split count kvq_decode_attn_int2's automatic choice (num_splits = 0)
+ * uses: one CTA per SM (152) over the (sequence, KV head) pairs, at least 32
+ * pages per split, at most 256.  bgtq_decode_attn, whose CTAs are smaller,
+ * aims at three CTAs per SM and at least 16 pages per split. */
 int kvq_decode_auto_splits(int B, int H_q, int H_kv, int max_pages_per_seq);
 
 /* Fused packed-cache decode attention over the INT2 cache.
