@@ -457,12 +457,14 @@ def run_ours(args, world, rank, local):
 
 
 def run_profile_case(args):
-    """A small decode case for a full ncu capture (few MB resident): one
-    Qwen3-8B-shaped layer (32 q / 8 KV heads) at 32K context, three decode
-    launches of the chosen kernel."""
+    """A decode case for a full ncu capture: one Qwen3-8B-shaped layer
+    (32 q / 8 KV heads) at --profile-ctx tokens (default 32K; 131072 is one
+    layer of the benchmark step, ~100 MB of cache), three decode launches of
+    the chosen kernel."""
     torch.cuda.set_device(0)
-    spec = inputs.small_spec("prof32k", h_q=32, h_kv=8, batch=1, ctx=32768, permute=True, k_kind="energy_rope",
-                             v_kind="gauss", avg_bits=3, v_bits=3, b_min=1, b_max=8)
+    spec = inputs.small_spec(f"prof{args.profile_ctx // 1024}k", h_q=32, h_kv=8, batch=1, ctx=args.profile_ctx,
+                             permute=True, k_kind="energy_rope", v_kind="gauss", avg_bits=3, v_bits=3, b_min=1,
+                             b_max=8)
     out = torch.zeros((1, spec.h_q, spec.d), dtype=torch.float32, device="cuda")
     if args.profile_case == "decode_int2":
         L = Int2Layer(spec, 0)
@@ -492,6 +494,7 @@ def main():
     ap.add_argument("--no-bgtq", action="store_true")
     ap.add_argument("--profile-case", choices=["decode_int2", "bgtq_decode"], default=None,
                     help="run a small decode case for an ncu capture instead of the benchmark")
+    ap.add_argument("--profile-ctx", type=int, default=32768, help="context length of the --profile-case layer")
     args = ap.parse_args()
     if args.profile_case:
         run_profile_case(args)

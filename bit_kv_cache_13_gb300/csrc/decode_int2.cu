@@ -94,13 +94,25 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
 
     // ---- first, every global read of the prologue is put in flight at once:
     // the first pages' ids (lane 0), this warp's rows of R_k, the query rows
-    int pids[DEC_STAGES + 1];
+    int pids[DEC_STAGES + 2];
     if (lane == 0) {
 #pragma unroll
-        for (int j = 0; j <= DEC_STAGES; ++j) pids[j] = j < my_count ? __ldg(bt + page_of(j)) : 0;
+        for (int j = 0; j < DEC_STAGES + 2; ++j) pids[j] = j < my_count ? __ldg(bt + page_of(j)) : 0;
+    }
+    {
+        // the rest of this sequence's block table is read one entry at a
+        // time during the loop: have L2 fetch it now
+        const char* btc = reinterpret_cast<const char*>(bt);
+        const int lines = (n_pages * 4 + 127) / 128;
+        for (int l = split * NW * 32 + tid; l < lines; l += S * NW * 32) prefetch_l2_keep(btc + 128 * l);
     }
     float4 rr[RowPrefetch<NW, MAXG>::N];
     load_rows<NW>(Rk + (size_t)h * D * D, rr);
+    {
+        // R_v is read only after the loop: have L2 fetch it now and keep it
+        const char* rv = reinterpret_cast<const char*>(Rv + (size_t)h * D * D);
+        for (int l = tid; l < D * D * 4 / 128; l += NW * 32) prefetch_l2_keep(rv + 128 * l);
+    }
     constexpr int QPT = (MAXG * D + NW * 32 - 1) / (NW * 32);  // query values per thread
     float qv[QPT];
     {
@@ -133,12 +145,14 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             bulk_g2s(sm.u.ring[warp][st], cache + ((size_t)pid * H_kv + h) * INT2_TILE, INT2_TILE, bar);
         }
     };
-    int pid_next = 0;  // lane 0: page id of the next page to issue, loaded one release early
+    // lane 0: ids of the next two pages to issue, each loaded two releases early
+    int pid_next = 0, pid_after = 0;
     if (lane == 0) {
 #pragma unroll
         for (int j = 0; j < DEC_STAGES; ++j)
             if (j < my_count) issue(j, page_of(j), pids[j]);
         pid_next = pids[DEC_STAGES];
+        pid_after = pids[DEC_STAGES + 1];
     }
 
     // ---- q~ = (q R_k) * scale * log2(e) for the G heads of this KV head
@@ -408,13 +422,14 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     };
 
     // Hand page i's stage back: issue the page DEC_STAGES ahead into it and
-    // start loading the id of the one after.
+    // start loading the id of the page two after that.
     auto release_page = [&](int i) {
         __syncwarp();
         if (lane == 0 && i + DEC_STAGES < my_count) {
             fence_proxy_async_smem();
             issue(i + DEC_STAGES, page_of(i + DEC_STAGES), pid_next);
-            if (i + DEC_STAGES + 1 < my_count) pid_next = __ldg(bt + page_of(i + DEC_STAGES + 1));
+            pid_next = pid_after;
+            if (i + DEC_STAGES + 2 < my_count) pid_after = __ldg(bt + page_of(i + DEC_STAGES + 2));
         }
     };
 

@@ -86,6 +86,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
 }
 
+// Ask L2 to fetch the 128-byte line at p and keep it ahead of streaming data.
+__device__ __forceinline__ void prefetch_l2_keep(const void* p) {
+    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
+}
+
 // 1-D bulk copy global -> shared (16-byte aligned, size multiple of 16),
 // completion signalled as transaction bytes on `bar`.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

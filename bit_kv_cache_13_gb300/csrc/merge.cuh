@@ -142,25 +142,29 @@ __device__ __forceinline__ void finish_decode(MergeSmem<NW, MAXG>& ms, const flo
     // rows of Rot this warp rotates, columns 4*lane .. +3: coalesced, issued now
     float4 rr[RP];
     load_rows<NW, RP>(Rot, rr);
-    for (int idx = tid; idx < G * D; idx += NW * 32) {
-        const int jj = idx / D, c = idx % D;
+    // per (warp, head) weight 2^(m_w - M) in place of m_w, and the head's M, L
+    if (tid < G) {
+        const int jj = tid;
         float M = -CUDART_INF_F;
 #pragma unroll
         for (int w = 0; w < NW; ++w) M = fmaxf(M, ms.m_part[w][jj]);
-        float L = 0.f, O = 0.f;
-        if (M != -CUDART_INF_F) {
+        float L = 0.f;
 #pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                const float f = exp2f(ms.m_part[w][jj] - M);
-                L = fmaf(ms.l_part[w][jj], f, L);
-                O = fmaf(o_part[w][jj][c], f, O);
-            }
+        for (int w = 0; w < NW; ++w) {
+            const float f = M == -CUDART_INF_F ? 0.f : ex2(ms.m_part[w][jj] - M);
+            ms.m_part[w][jj] = f;
+            L = fmaf(ms.l_part[w][jj], f, L);
         }
+        ms.Mh[jj] = M;
+        ms.Lh[jj] = L;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < G * D; idx += NW * 32) {
+        const int jj = idx / D, c = idx % D;
+        float O = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) O = fmaf(o_part[w][jj][c], ms.m_part[w][jj], O);
         ms.o_final[jj][c] = O;
-        if (c == 0) {
-            ms.Mh[jj] = M;
-            ms.Lh[jj] = L;
-        }
     }
     __syncthreads();
     // ---- rotate this partial: O_i = sum_j o'_j Rot[i][j] for the rows i of
@@ -215,65 +219,56 @@ __device__ __forceinline__ void finish_decode(MergeSmem<NW, MAXG>& ms, const flo
     if (!ms.is_last) return;
     __threadfence();
 
-    // ---- last CTA: every split's (m, l) of the G heads, gathered at once
-    for (int idx = tid; idx < G * S; idx += NW * 32) {
-        const int jj = idx / S, s = idx - jj * S;
-        const float2 ml = __ldcg(reinterpret_cast<const float2*>(partials + ((head0 + jj) * S + s) * PART_STRIDE));
-        ms.fac[jj][s] = ml.x;
-        ms.lsp[jj][s] = ml.y;
-    }
-    __syncthreads();
-    // split weights (one warp per head, lanes over splits, shared memory only)
+    // ---- last CTA: merge the S split partials of each head in one pass.
+    // Warp jj takes head jj; the first run of split outputs is loaded
+    // together with the (m, l) pairs, the weights 2^(m_s - M) pass through
+    // shared memory, and each lane sums its 4 channels over the runs.
+    constexpr int CH = NW >= 8 ? 32 : 16;  // split outputs in flight per lane
     for (int jj = warp; jj < G; jj += NW) {
+        const float* ph = partials + (head0 + jj) * S * PART_STRIDE;
+        float4 ov[CH];
+        auto load_run = [&](int s0) {
+#pragma unroll
+            for (int k = 0; k < CH; ++k)
+                ov[k] = s0 + k < S ? ldcg4(ph + (size_t)(s0 + k) * PART_STRIDE + 4 + 4 * lane)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+        };
+        load_run(0);
         float M = -CUDART_INF_F;
-        for (int s = lane; s < S; s += 32) M = fmaxf(M, ms.fac[jj][s]);
+        for (int s = lane; s < S; s += 32) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(ph + (size_t)s * PART_STRIDE));
+            ms.fac[jj][s] = ml.x;
+            ms.lsp[jj][s] = ml.y;
+            M = fmaxf(M, ml.x);
+        }
 #pragma unroll
         for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
         float L = 0.f;
         for (int s = lane; s < S; s += 32) {
-            const float f = M == -CUDART_INF_F ? 0.f : exp2f(ms.fac[jj][s] - M);
+            const float f = M == -CUDART_INF_F ? 0.f : ex2(ms.fac[jj][s] - M);
             ms.fac[jj][s] = f;
             L = fmaf(ms.lsp[jj][s], f, L);
         }
 #pragma unroll
         for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-        if (lane == 0) {
-            ms.Mh[jj] = M;
-            ms.Lh[jj] = L;
+        __syncwarp();
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s0 = 0; s0 < S; s0 += CH) {
+            if (s0 > 0) load_run(s0);
+#pragma unroll
+            for (int k = 0; k < CH; ++k) {
+                const float f = s0 + k < S ? ms.fac[jj][s0 + k] : 0.f;
+                acc.x = fmaf(f, ov[k].x, acc.x);
+                acc.y = fmaf(f, ov[k].y, acc.y);
+                acc.z = fmaf(f, ov[k].z, acc.z);
+                acc.w = fmaf(f, ov[k].w, acc.w);
+            }
         }
-    }
-    __syncthreads();
-    // ---- weighted sum of the split outputs: warp w < NR takes splits
-    // w, w + NR, ...; unrolled so each lane keeps many independent loads in flight
-    if (warp < NR) {
-        float4 acc[MAXG];
-#pragma unroll
-        for (int jj = 0; jj < MAXG; ++jj) acc[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll(MAXG <= 4 ? 8 : 4)
-        for (int s = warp; s < S; s += NR) {
-#pragma unroll
-            for (int jj = 0; jj < MAXG; ++jj)
-                if (jj < G) {
-                    const float f = ms.fac[jj][s];
-                    const float4 o = ldcg4(partials + ((head0 + jj) * S + s) * PART_STRIDE + 4 + 4 * lane);
-                    acc[jj].x = fmaf(f, o.x, acc[jj].x);
-                    acc[jj].y = fmaf(f, o.y, acc[jj].y);
-                    acc[jj].z = fmaf(f, o.z, acc[jj].z);
-                    acc[jj].w = fmaf(f, o.w, acc[jj].w);
-                }
-        }
-#pragma unroll
-        for (int jj = 0; jj < MAXG; ++jj)
-            if (jj < G) *reinterpret_cast<float4*>(&ms.red[warp][jj][4 * lane]) = acc[jj];
-    }
-    __syncthreads();
-    for (int idx = tid; idx < G * D; idx += NW * 32) {
-        const int jj = idx / D, c = idx % D;
-        float s = 0.f;
-#pragma unroll
-        for (int w = 0; w < NR; ++w) s += ms.red[w][jj][c];
-        const float L = ms.Lh[jj];
-        out[(head0 + jj) * D + c] = L > 0.f ? s / L : 0.f;
+        float* o = out + (head0 + jj) * D + 4 * lane;
+        o[0] = L > 0.f ? acc.x / L : 0.f;
+        o[1] = L > 0.f ? acc.y / L : 0.f;
+        o[2] = L > 0.f ? acc.z / L : 0.f;
+        o[3] = L > 0.f ? acc.w / L : 0.f;
     }
     if (tid == 0) tickets[unit] = 0;
 }
