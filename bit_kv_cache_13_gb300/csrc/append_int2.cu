@@ -24,6 +24,8 @@ append_int2_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
                    const float* __restrict__ Rk, const float* __restrict__ Rv, uint8_t* __restrict__ cache,
                    int64_t num_pages, float* __restrict__ dbg_k, float* __restrict__ dbg_v,
                    int32_t* __restrict__ err_count, int tok_per_cta) {
+    griddep_wait();  // k, v, the slot mapping or the cache may come from the previous kernel
+    griddep_launch_dependents();
     const int h = blockIdx.y, grp = blockIdx.z;
     const int tid = threadIdx.x;
     const int is_v = tid >> 5;
@@ -138,8 +140,9 @@ extern "C" kvq_status kvq_append_int2(const void* k, const void* v, int n_tok, i
     per = per < 1 ? 1 : (per > 64 ? 64 : per);
     const int grid_x = (n_tok + per - 1) / per;
     dim3 grid(grid_x, H_kv, NGROUP);
-    append_int2_kernel<<<grid, 64, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), n_tok, H_kv, slot_mapping,
-        mu_k, R_k, R_v, static_cast<uint8_t*>(cache), num_pages, dbg_rot_k, dbg_rot_v, err_count, per);
-    return kvq_check_cuda(cudaGetLastError(), "kvq_append_int2 launch");
+    return kvq_check_cuda(launch_pdl(append_int2_kernel, grid, dim3(64), 0, static_cast<cudaStream_t>(stream),
+                                     static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), n_tok,
+                                     H_kv, slot_mapping, mu_k, R_k, R_v, static_cast<uint8_t*>(cache), num_pages,
+                                     dbg_rot_k, dbg_rot_v, err_count, per),
+                          "kvq_append_int2 launch");
 }

@@ -406,7 +406,7 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         }
     __syncthreads();
     finish_decode<BG_WARPS, 8>(sm.ms, sm.o_part, G, H_q, H_kv, gridDim.z, b, h, split, S, ws,
-                            pi_table + __ldg(pi_offsets + D), out);
+                               pi_table + __ldg(pi_offsets + D), out);
 }
 
 }  // namespace kvq

@@ -79,6 +79,7 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
 
     uint32_t* err_word = reinterpret_cast<uint32_t*>(ws);
 
+    griddep_wait();  // every input may come from the previous kernel in the stream
     int ctx = __ldg(context_lens + b);
     ctx = max(0, min(ctx, max_pages * PAGE));
     const int n_pages = (ctx + PAGE - 1) / PAGE;
@@ -92,12 +93,44 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     const int my_count = n_pages > k0 ? (n_pages - k0 + KS - 1) / KS : 0;
     auto page_of = [&](int j) { return k0 + KS * j; };
 
-    // ---- first, every global read of the prologue is put in flight at once:
-    // the first pages' ids (lane 0), this warp's rows of R_k, the query rows
-    int pids[DEC_STAGES + 2];
     if (lane == 0) {
+        for (int s = 0; s < DEC_STAGES; ++s) mbar_init(&sm.bar[warp][s], 1);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    __syncwarp();
+    // Lane 0 issues the warp's i-th page (sequence page p) with its (already
+    // loaded) page id and records how many of its tokens are valid; the
+    // mbarrier publishes that count together with the data.
+    auto issue = [&](int i, int p, int pid) {  // lane 0 only
+        const int st = i % DEC_STAGES;
+        uint64_t* bar = &sm.bar[warp][st];
+        if (pid < 0 || (int64_t)pid >= num_pages) {
+            atomicOr(err_word, ERR_BAD_PAGE);
+            sm.ntok[warp][st] = 0;
+            mbar_arrive(bar);  // complete the phase without data
+        } else {
+            sm.ntok[warp][st] = min(PAGE, ctx - p * PAGE);
+            mbar_arrive_expect_tx(bar, INT2_TILE);
+            bulk_g2s(sm.u.ring[warp][st], cache + ((size_t)pid * H_kv + h) * INT2_TILE, INT2_TILE, bar);
+        }
+    };
+    // ---- first the page ids of the first pages and their copies (lane 0),
+    // with no other load ahead of them; the rest of the prologue overlaps the
+    // copies.  Lane 0 keeps the ids of the next two pages to issue, each
+    // loaded two releases before its use.
+    int pid_next = 0, pid_after = 0;
+    if (lane == 0) {
+        // bounded by the block table's row length, not the context, so these
+        // loads need not wait for context_lens
+        int pids[DEC_STAGES + 2];
 #pragma unroll
-        for (int j = 0; j < DEC_STAGES + 2; ++j) pids[j] = j < my_count ? __ldg(bt + page_of(j)) : 0;
+        for (int j = 0; j < DEC_STAGES + 2; ++j) pids[j] = page_of(j) < max_pages ? __ldg(bt + page_of(j)) : 0;
+#pragma unroll
+        for (int j = 0; j < DEC_STAGES; ++j)
+            if (j < my_count) issue(j, page_of(j), pids[j]);
+        pid_next = pids[DEC_STAGES];
+        pid_after = pids[DEC_STAGES + 1];
     }
     {
         // the rest of this sequence's block table is read one entry at a
@@ -122,37 +155,6 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             const int idx = tid + k * NW * 32;
             qv[k] = idx < G * D ? __bfloat162float(qb[idx]) : 0.f;
         }
-    }
-    if (lane == 0) {
-        for (int s = 0; s < DEC_STAGES; ++s) mbar_init(&sm.bar[warp][s], 1);
-        fence_mbar_init();
-        fence_proxy_async_smem();
-    }
-    __syncwarp();
-    // Lane 0 issues the warp's i-th page (sequence page p) with its (already
-    // loaded) page id and records how many of its tokens are valid; the
-    // mbarrier publishes that count together with the data.
-    auto issue = [&](int i, int p, int pid) {  // lane 0 only
-        const int st = i % DEC_STAGES;
-        uint64_t* bar = &sm.bar[warp][st];
-        if (pid < 0 || (int64_t)pid >= num_pages) {
-            atomicOr(err_word, ERR_BAD_PAGE);
-            sm.ntok[warp][st] = 0;
-            mbar_arrive(bar);  // complete the phase without data
-        } else {
-            sm.ntok[warp][st] = min(PAGE, ctx - p * PAGE);
-            mbar_arrive_expect_tx(bar, INT2_TILE);
-            bulk_g2s(sm.u.ring[warp][st], cache + ((size_t)pid * H_kv + h) * INT2_TILE, INT2_TILE, bar);
-        }
-    };
-    // lane 0: ids of the next two pages to issue, each loaded two releases early
-    int pid_next = 0, pid_after = 0;
-    if (lane == 0) {
-#pragma unroll
-        for (int j = 0; j < DEC_STAGES; ++j)
-            if (j < my_count) issue(j, page_of(j), pids[j]);
-        pid_next = pids[DEC_STAGES];
-        pid_after = pids[DEC_STAGES + 1];
     }
 
     // ---- q~ = (q R_k) * scale * log2(e) for the G heads of this KV head
@@ -464,6 +466,9 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         for (int s = 0; s < DEC_STAGES; ++s) (void)mbar_wait_bounded(&sm.bar[warp][s], 0, 1000000LL);
     }
 
+    // the next kernel in the stream may be scheduled once every CTA is here
+    griddep_launch_dependents();
+
     // ---------------- warp partial -> shared memory
     __syncthreads();  // all warps are done with the ring (o_part aliases it)
     {
@@ -514,8 +519,7 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     }
     __syncthreads();
 
-    finish_decode<NW, MAXG>(sm.ms, sm.u.o_part, G, H_q, H_kv, B, b, h, split, S, ws,
-                             Rv + (size_t)h * D * D, out);
+    finish_decode<NW, MAXG>(sm.ms, sm.u.o_part, G, H_q, H_kv, B, b, h, split, S, ws, Rv + (size_t)h * D * D, out);
 }
 
 }  // namespace kvq
@@ -607,20 +611,14 @@ extern "C" kvq_status kvq_decode_attn_int2(const void* q, int B, int H_q, int H_
     const size_t smem = G <= 4 ? sizeof(DecodeSmem<NW1, 4>) : sizeof(DecodeSmem<NW2, 8>);
     dim3 grid(S, H_kv, B);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
     kvq_status sa = set_smem_once(G <= 4 ? (const void*)decode_int2_kernel<1> : (const void*)decode_int2_kernel<2>,
                                   (int)smem, G <= 4 ? 0 : 1);
     if (sa != KVQ_OK) return sa;
-    if (G <= 4) {
-        decode_int2_kernel<1><<<grid, NW1 * 32, smem, st>>>(
-            static_cast<const __nv_bfloat16*>(q), H_q, H_kv, G, static_cast<const uint8_t*>(cache), num_pages,
-            block_table, max_pages_per_seq, context_lens, R_k, R_v, scale_log2, out, static_cast<uint8_t*>(workspace));
-    } else {
-        decode_int2_kernel<2><<<grid, NW2 * 32, smem, st>>>(
-            static_cast<const __nv_bfloat16*>(q), H_q, H_kv, G, static_cast<const uint8_t*>(cache), num_pages,
-            block_table, max_pages_per_seq, context_lens, R_k, R_v, scale_log2, out, static_cast<uint8_t*>(workspace));
-    }
-    e = cudaGetLastError();
+    const cudaError_t e =
+        launch_pdl(G <= 4 ? decode_int2_kernel<1> : decode_int2_kernel<2>, grid, dim3((G <= 4 ? NW1 : NW2) * 32), smem,
+                   st, static_cast<const __nv_bfloat16*>(q), H_q, H_kv, G, static_cast<const uint8_t*>(cache),
+                   num_pages, block_table, max_pages_per_seq, context_lens, R_k, R_v, scale_log2, out,
+                   static_cast<uint8_t*>(workspace));
     return kvq_check_cuda(e, "kvq_decode_attn_int2 launch");
 }
 

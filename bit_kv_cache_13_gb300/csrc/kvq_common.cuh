@@ -31,6 +31,22 @@ __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a -
 // one int32 split ticket per (sequence, KV head), zero between calls
 __host__ __device__ inline size_t tickets_bytes(int B, int H_kv) { return align_up((size_t)B * H_kv * 4, 256); }
 
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 }  // namespace kvq
 
 // Automatic split count of the Block-GTQ decode (host; defined beside the
@@ -85,6 +101,25 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
         if (clock64() - t0 > limit) return false;
     }
 }
+
+// atomicAdd at GPU scope with acquire-release order: writes ordered before it
+// (in the CTA, by a preceding __syncthreads) are visible to any thread that
+// acquires the value it leaves, and reads ordered after it see what the
+// earlier adders released.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int32_t* p, int v) {
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// Programmatic dependent launch.  Every kernel of this library is launched
+// with programmatic stream serialization (launch_pdl): it may be scheduled
+// while the kernel before it in the stream is still finishing, so it calls
+// griddep_wait() before its first read of global memory that kernel may have
+// written (a no-op when launched without the attribute), and calls
+// griddep_launch_dependents() once the kernel after it may be scheduled.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Ask L2 to fetch the 128-byte line at p and keep it ahead of streaming data.
 __device__ __forceinline__ void prefetch_l2_keep(const void* p) {

@@ -171,7 +171,8 @@ __device__ __forceinline__ void finish_decode(MergeSmem<NW, MAXG>& ms, const flo
     // this warp.  Each lane forms the partial dots of its 4 columns with RP
     // rows; a reduce-scatter over the lanes then leaves each row's full dot
     // in one lane (RP - 1 shuffles per head and RP rows, after a fold of the
-    // two half-warps when RP = 16).
+    // two half-warps when RP = 16).  Heads go two at a time so their shuffle
+    // chains overlap (the second of a pair past G is computed and dropped).
     if (warp < NR) {
 #pragma unroll
         for (int pass = 0; pass < RPW / RP; ++pass) {
@@ -180,44 +181,59 @@ __device__ __forceinline__ void finish_decode(MergeSmem<NW, MAXG>& ms, const flo
                 for (int ii = 0; ii < RP; ++ii)
                     rr[ii] = ldg4(Rot + (size_t)(RPW * warp + RP * pass + ii) * D + 4 * lane);
             }
-            for (int jj = 0; jj < G; ++jj) {
-                const float4 o4 = *reinterpret_cast<const float4*>(&ms.o_final[jj][4 * lane]);
-                float v[RP];
+            for (int jj = 0; jj < G; jj += 2) {
+                const int jb = jj + 1 < MAXG ? jj + 1 : jj;
+                const float4 oa = *reinterpret_cast<const float4*>(&ms.o_final[jj][4 * lane]);
+                const float4 ob = *reinterpret_cast<const float4*>(&ms.o_final[jb][4 * lane]);
+                float va[RP], vb[RP];
 #pragma unroll
-                for (int ii = 0; ii < RP; ++ii)
-                    v[ii] = fmaf(o4.x, rr[ii].x, fmaf(o4.y, rr[ii].y, fmaf(o4.z, rr[ii].z, o4.w * rr[ii].w)));
+                for (int ii = 0; ii < RP; ++ii) {
+                    va[ii] = fmaf(oa.x, rr[ii].x, fmaf(oa.y, rr[ii].y, fmaf(oa.z, rr[ii].z, oa.w * rr[ii].w)));
+                    vb[ii] = fmaf(ob.x, rr[ii].x, fmaf(ob.y, rr[ii].y, fmaf(ob.z, rr[ii].z, ob.w * rr[ii].w)));
+                }
                 if constexpr (RP == 16) {
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], 16);
+                    for (int k = 0; k < 16; ++k) {
+                        va[k] += __shfl_xor_sync(0xffffffffu, va[k], 16);
+                        vb[k] += __shfl_xor_sync(0xffffffffu, vb[k], 16);
+                    }
                 }
 #pragma unroll
                 for (int off = RP / 2; off >= 1; off >>= 1) {
                     const bool upper = lane & off;
 #pragma unroll
                     for (int k = 0; k < off; ++k) {
-                        const float send = upper ? v[k] : v[k + off];
-                        const float keep = upper ? v[k + off] : v[k];
-                        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                        const float sa = upper ? va[k] : va[k + off], ka = upper ? va[k + off] : va[k];
+                        const float sb = upper ? vb[k] : vb[k + off], kb = upper ? vb[k + off] : vb[k];
+                        va[k] = ka + __shfl_xor_sync(0xffffffffu, sa, off);
+                        vb[k] = kb + __shfl_xor_sync(0xffffffffu, sb, off);
                     }
                 }
-                float* part = partials + ((head0 + jj) * S + split) * PART_STRIDE;
-                if (RP == 32 || lane < 16) part[4 + RPW * warp + RP * pass + (lane & (RP - 1))] = v[0];
+                const int row = 4 + RPW * warp + RP * pass + (lane & (RP - 1));
+                float* pa = partials + ((head0 + jj) * S + split) * PART_STRIDE;
+                if (RP == 32 || lane < 16) pa[row] = va[0];
                 if (tid == 0 && pass == 0) {
-                    part[0] = ms.Mh[jj];
-                    part[1] = ms.Lh[jj];
+                    pa[0] = ms.Mh[jj];
+                    pa[1] = ms.Lh[jj];
+                }
+                if (jj + 1 < G) {
+                    float* pb = partials + ((head0 + jj + 1) * S + split) * PART_STRIDE;
+                    if (RP == 32 || lane < 16) pb[row] = vb[0];
+                    if (tid == 0 && pass == 0) {
+                        pb[0] = ms.Mh[jj + 1];
+                        pb[1] = ms.Lh[jj + 1];
+                    }
                 }
             }
         }
     }
-    __threadfence();
+    // publish: the barrier orders every thread's partial writes before
+    // thread 0's release-acquire ticket; in the last CTA, the barrier after
+    // the ticket orders all its reads of the other partials after it
     __syncthreads();
-    if (tid == 0) {
-        const int prev = atomicAdd(tickets + unit, 1);
-        ms.is_last = prev == S - 1;
-    }
+    if (tid == 0) ms.is_last = atomic_add_acq_rel_gpu(tickets + unit, 1) == S - 1;
     __syncthreads();
     if (!ms.is_last) return;
-    __threadfence();
 
     // ---- last CTA: merge the S split partials of each head in one pass.
     // Warp jj takes head jj; the first run of split outputs is loaded
