@@ -42,7 +42,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from bit_kv_cache_13_gb300 import _lib, inputs  # noqa: E402
-from bit_kv_cache_13_gb300.workload import BgtqLayer, Int2Layer  # noqa: E402
+from bit_kv_cache_13_gb300.workload import BgtqLayer, Int2Layer, history_positions  # noqa: E402
 
 METRIC = "packed-KV decode attention HBM GB/s (% of 8 TB/s) and ms/step at 128K ctx"
 NOMINAL_HBM_GBS = 8000.0
@@ -263,6 +263,37 @@ def measure_bgtq(device, stream, reps):
             "l2": "256 MB buffer written before every timed launch"}
 
 
+# 128 fp32 lanes per SM x 152 SMs x 2 flop per fma at the 2070 MHz maximum SM clock
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+
+
+def measure_append_prefill(spec, device, stream, reps):
+    """Batched prefill append: one layer's whole 128K-token history through
+    kvq_append_int2 in one call (8 KV heads).  The rotation is a fixed-order
+    fp32 fma chain of 128 steps per coordinate (16K fma per token-head and
+    side), so the bound is fp32 fma issue, not HBM."""
+    layer = Int2Layer(spec, 0, device=device)
+    k, v = layer.history_kv(0)
+    layer.mu = inputs.key_centre(k).to(device).contiguous()
+    sl = layer.slots(0, history_positions(spec)).contiguous()
+    k, v = k.contiguous(), v.contiguous()
+    call = lambda: _lib.kvq_append_int2(k, v, sl, layer.mu, layer.R_k, layer.R_v, layer.cache, layer.num_pages)
+    call()
+    ms = statistics.median(time_launches(stream, call, 1) for _ in range(reps))
+    th = k.shape[0] * spec.h_kv
+    tflops = th * 2 * 2 * spec.d * spec.d / (ms * 1e-3) / 1e12
+    out = {"workload": f"{spec.name}: one layer, {k.shape[0]} tokens x {spec.h_kv} KV heads appended in one call",
+           "kernel": "append_int2_kernel", "ms_per_layer": round(ms, 4),
+           "value": round(th / (ms * 1e-3) / 1e6, 2), "unit": "M token-heads/s",
+           "roofline": {"bound": "alu", "achieved": round(tflops, 3), "peak": round(FP32_PEAK_TFLOPS, 1),
+                        "unit": "TFLOP/s", "frac": round(tflops / FP32_PEAK_TFLOPS, 4),
+                        "peak_kind": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz"},
+           "bytes_per_token_head": {"read": 2 * 2 * spec.d, "written": 96}}
+    del layer, k, v
+    torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------------ CPU oracle
 
 class OracleSample:
@@ -447,6 +478,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.empty_cache()
     if not args.no_bgtq:
         line["bgtq"] = measure_bgtq(device, stream, reps=max(3, min(args.steps, 10)))
+    line["append_prefill"] = measure_append_prefill(spec, device, stream, reps=3)
     if rank == 0 and not args.no_cpu_baseline:
         gbs, el, sample = oracle_baseline(spec)
         line["cpu_baseline"] = {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",

@@ -211,11 +211,20 @@ def read_tokens(cache, page_ids, n_tokens, h):
 # packed-cache decode attention
 # --------------------------------------------------------------------------
 
-def decode(q, cache, block_table, ctx_lens, mu32, rk32, rv32, scale, h_kv):
+def decode(q, cache, block_table, ctx_lens, mu32, rk32, rv32, scale, h_kv, window=None):
     """Decode attention over the packed INT2 cache, fp64, as the plain
     definition: the effective cached key and value of Eq. (4),
         k~_s = Q2((k_s - mu) R_k) R_k^T + mu,   v~_s = Q2(v_s R_v) R_v^T,
     then Eqs. (1)-(2) over s < ctx_lens[b] with logit scale `scale`.
+
+    window: None, or (k_win, v_win, win_lens) with k_win, v_win
+    [B, W, H_kv, d] (bf16 values) and win_lens[B] <= W.  The INT2 paper keeps
+    a small window of tokens in BF16 (§3.1; the Block-GTQ page keeps 4 sink
+    and 128 recent tokens, Table 6).  Window tokens are attended exactly, in
+    the original basis, together with the cached tokens: the softmax runs
+    over the union of the s < ctx_lens[b] cached tokens and the first
+    win_lens[b] window tokens.  A window token is not also in the INT2
+    range; which tokens go where is the caller's choice.
 
     q: [B, H_q, d] (bf16 values); mu32 [H_kv, d]; rk32, rv32 [H_kv, d, d].
     Returns [B, H_q, d].  (Adding mu back shifts every logit of a query by
@@ -236,6 +245,11 @@ def decode(q, cache, block_table, ctx_lens, mu32, rk32, rv32, scale, h_kv):
             kz, vw = read_tokens(cache, block_table[b], T, h)
             kt[:, h] = kz @ rk[h].T + mu[h]
             vt[:, h] = vw @ rv[h].T
+        if window is not None:
+            k_win, v_win, win_lens = window
+            wl = int(win_lens[b])
+            kt = np.concatenate([kt, np.asarray(k_win[b, :wl], np.float64)], axis=0)
+            vt = np.concatenate([vt, np.asarray(v_win[b, :wl], np.float64)], axis=0)
         out[b] = attention.gqa_decode(q[b], kt, vt, sc)
     return out
 

@@ -253,3 +253,120 @@ def test_seventy_b_kv_byte_count():
     per_token = 80 * 8 * 128 * 2 * 2
     assert per_token == 320 * 1024
     assert per_token * 131072 == 40 * 1024 ** 3
+
+
+# ---------------------------------------------------------------- BF16 window
+
+def _lattice_tokens_identity(rng, T, mu):
+    """Tokens k = z + mu (R = I) whose 32-channel groups are exactly the four
+    INT2 levels m + c*s of their own min/max, so the INT2 round trip is
+    exact; every value is a small multiple of 1/4, exact in bf16 and fp32."""
+    z = np.zeros((T, 128))
+    for t in range(T):
+        for g in range(4):
+            m = 0.25 * rng.integers(-8, 8)
+            s = 0.25 * rng.integers(1, 5)
+            c = rng.integers(0, 4, 32)
+            c[0], c[1] = 0, 3
+            z[t, 32 * g: 32 * g + 32] = m + s * c
+    return z + mu
+
+
+def _split_window(k, v, w):
+    """The last w tokens as a one-sequence window [1, w, H_kv, d]."""
+    T = k.shape[0]
+    return k[:T - w], v[:T - w], (k[None, T - w:], v[None, T - w:], [w])
+
+
+def test_window_token_equals_exact_int2_token():
+    # A token whose INT2 encoding is exact (R = I, lattice groups) attends
+    # the same from the packed cache as from the BF16 window, so moving the
+    # last w tokens into the window leaves the output unchanged.
+    rng = np.random.default_rng(21)
+    T, w, g = 35, 6, 4
+    mu = (0.25 * rng.integers(-8, 8, (1, 128))).astype(np.float32)
+    k = _lattice_tokens_identity(rng, T, mu[0].astype(np.float64))[:, None].astype(np.float32)
+    v = _lattice_tokens_identity(rng, T, 0.0)[:, None].astype(np.float32)
+    eye = np.eye(128, dtype=np.float32)[None]
+    q = rng.standard_normal((1, g, 128))
+    full = int2.new_cache(3, 1)
+    int2.append(full, k, v, np.arange(T), mu, eye, eye)
+    want = int2.decode(q, full, np.array([[0, 1, 2]]), [T], mu, eye, eye, 0.125, 1)
+    kh, vh, win = _split_window(k, v, w)
+    part = int2.new_cache(3, 1)
+    int2.append(part, kh, vh, np.arange(T - w), mu, eye, eye)
+    got = int2.decode(q, part, np.array([[0, 1, 2]]), [T - w], mu, eye, eye, 0.125, 1, window=win)
+    assert np.max(np.abs(got - want)) <= 1e-12 * np.max(np.abs(want))
+
+
+def test_window_token_matches_rotated_lattice_token():
+    # Same move with a Haar-Hadamard R and a non-zero centre: the cached keys
+    # are lattice points in the rotated basis, so the window and the cache
+    # agree to the fp32 rounding of k = z R^T + mu.
+    rng = np.random.default_rng(22)
+    T, w, g = 40, 9, 3
+    rk = inputs.head_rotation(128, "k", 0).astype(np.float32)[None]
+    rv = inputs.head_rotation(128, "v", 0).astype(np.float32)[None]
+    mu = (rng.standard_normal((1, 128)) * 3).astype(np.float32)
+    k, _ = _lattice_keys(rng, T, mu[0].astype(np.float64), rk[0].astype(np.float64))
+    v, _ = _lattice_keys(rng, T, 0.0, rv[0].astype(np.float64))
+    k = k[:, None].astype(np.float32)
+    v = v[:, None].astype(np.float32)
+    q = rng.standard_normal((1, g, 128))
+    bt = np.array([[4, 1, 3]], np.int32)
+    slots = lambda n: np.array([bt[0, t // 16] * 16 + t % 16 for t in range(n)])
+    full = int2.new_cache(6, 1)
+    int2.append(full, k, v, slots(T), mu, rk, rv)
+    want = int2.decode(q, full, bt, [T], mu, rk, rv, 1 / math.sqrt(128), 1)
+    kh, vh, win = _split_window(k, v, w)
+    part = int2.new_cache(6, 1)
+    int2.append(part, kh, vh, slots(T - w), mu, rk, rv)
+    got = int2.decode(q, part, bt, [T - w], mu, rk, rv, 1 / math.sqrt(128), 1, window=win)
+    assert np.max(np.abs(got - want)) <= 1e-4 * np.max(np.abs(want))
+
+
+def test_window_alone_is_plain_attention():
+    # No cached tokens: the output is textbook attention over the window.
+    rng = np.random.default_rng(23)
+    W, h_kv, g = 7, 2, 4
+    kw = rng.standard_normal((1, W, h_kv, 128)).astype(np.float32)
+    vw = rng.standard_normal((1, W, h_kv, 128)).astype(np.float32)
+    eye = np.stack([np.eye(128, dtype=np.float32)] * h_kv)
+    q = rng.standard_normal((1, h_kv * g, 128))
+    cache = int2.new_cache(1, h_kv)
+    got = int2.decode(q, cache, np.array([[0]]), [0], np.zeros((h_kv, 128)), eye, eye, 0.1, h_kv,
+                      window=(kw, vw, [W]))
+    for j in range(h_kv * g):
+        a = kw[0, :, j // g].astype(np.float64) @ q[0, j] * float(np.float32(0.1))
+        e = np.exp(a - a.max())
+        want = (e[:, None] * vw[0, :, j // g]).sum(0) / e.sum()
+        assert np.max(np.abs(got[0, j] - want)) <= 1e-12 * np.max(np.abs(want))
+
+
+def test_window_lengths_are_per_sequence():
+    # Ragged windows: sequence b attends exactly its first win_lens[b] window
+    # tokens (zero-length windows included); entries past that are ignored.
+    rng = np.random.default_rng(24)
+    B, W, T = 3, 5, 20
+    k = rng.standard_normal((B, T, 1, 128)).astype(np.float32)
+    v = rng.standard_normal((B, T, 1, 128)).astype(np.float32)
+    kw = rng.standard_normal((B, W, 1, 128)).astype(np.float32)
+    vw = rng.standard_normal((B, W, 1, 128)).astype(np.float32)
+    rk = inputs.head_rotation(128, "w").astype(np.float32)[None]
+    mu = np.zeros((1, 128), np.float32)
+    q = rng.standard_normal((B, 2, 128))
+    cache = int2.new_cache(2 * B, 1)
+    bt = np.array([[2 * b, 2 * b + 1] for b in range(B)], np.int32)
+    for b in range(B):
+        int2.append(cache, k[b], v[b], [bt[b, t // 16] * 16 + t % 16 for t in range(T)], mu, rk, rk)
+    lens = [0, 3, 5]
+    got = int2.decode(q, cache, bt, [T] * B, mu, rk, rk, 0.1, 1, window=(kw, vw, lens))
+    for b in range(B):
+        poisoned = kw.copy()
+        poisoned[b, lens[b]:] = 1e4                      # beyond the length: must not matter
+        one = int2.decode(q[b:b + 1], cache, bt[b:b + 1], [T], mu, rk, rk, 0.1, 1,
+                          window=(poisoned[b:b + 1], vw[b:b + 1], [lens[b]]))
+        assert np.array_equal(got[b], one[0])
+        if lens[b] == 0:
+            plain = int2.decode(q[b:b + 1], cache, bt[b:b + 1], [T], mu, rk, rk, 0.1, 1)
+            assert np.array_equal(got[b], plain[0])
