@@ -29,6 +29,7 @@ _SIGS = {
     "kvq_decode_workspace_bytes": ([I, I, I, I, I], SZ),
     "kvq_decode_auto_splits": ([I, I, I, I], I),
     "kvq_decode_attn_int2": ([P, I, I, I, I, P, I64, P, I, P, P, P, F, P, P, SZ, I, P], I),
+    "kvq_decode_attn_int2_window": ([P, I, I, I, I, P, I64, P, I, P, P, P, P, P, P, P, I, F, P, P, SZ, I, P], I),
     "kvq_workspace_status": ([P, P], I),
     "kvq_decode_attn_int2_noalloc": ([P, I, I, I, I, P, I64, P, I, P, P, P, F, P, I, P], I),
     "bgtq_lloyd_max_codebook": ([I, P], I),
@@ -129,6 +130,23 @@ def kvq_decode_attn_int2(q, cache, num_pages: int, block_table, context_lens, R_
         _dev(context_lens, torch.int32, "context_lens"), _dev(R_k, torch.float32, "R_k"),
         _dev(R_v, torch.float32, "R_v"), float(scale), _dev(out, torch.float32, "out"),
         _dev(workspace, torch.uint8, "workspace"), workspace.numel(), int(num_splits), _stream(stream)))
+
+
+def kvq_decode_attn_int2_window(q, cache, num_pages: int, block_table, context_lens, R_k, R_v, mu_k, win_k, win_v,
+                                win_lens, scale: float, out, workspace, num_splits: int = 0, H_kv: int | None = None,
+                                stream=None):
+    """kvq_decode_attn_int2 over the cache plus a BF16 window (win_k, win_v:
+    [B, win_max, H_kv, d] bf16; win_lens: [B] int32)."""
+    B, H_q, d = q.shape
+    h_kv = R_k.shape[0] if H_kv is None else H_kv
+    _check(load().kvq_decode_attn_int2_window(
+        _dev(q, torch.bfloat16, "q"), B, H_q, h_kv, d, _dev(cache, torch.uint8, "cache"), int(num_pages),
+        _dev(block_table, torch.int32, "block_table"), block_table.shape[1],
+        _dev(context_lens, torch.int32, "context_lens"), _dev(R_k, torch.float32, "R_k"),
+        _dev(R_v, torch.float32, "R_v"), _dev(mu_k, torch.float32, "mu_k"), _dev(win_k, torch.bfloat16, "win_k"),
+        _dev(win_v, torch.bfloat16, "win_v"), _dev(win_lens, torch.int32, "win_lens"), win_k.shape[1], float(scale),
+        _dev(out, torch.float32, "out"), _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+        int(num_splits), _stream(stream)))
 
 
 def kvq_decode_attn_int2_noalloc(q, cache, num_pages: int, block_table, context_lens, R_k, R_v, scale: float,

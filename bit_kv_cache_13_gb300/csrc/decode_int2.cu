@@ -60,12 +60,88 @@ struct __align__(16) DecodeSmem {
     MergeSmem<NW, MAXG> ms;
 };
 
+// BF16 window (the INT2 paper keeps a small BF16 window, §3.1; the
+// Block-GTQ page keeps 4 sink and 128 recent tokens, Table 6): the first
+// win_lens[b] rows of win_k / win_v [B][win_max][H_kv][d] are attended
+// exactly, in the original basis, with the logit q . (k - mu) * scale: the
+// same shift by -q . mu that centring gives the cached keys, so the two
+// parts share one softmax.  Each warp runs an online softmax over tokens
+// warp, warp + NW, ...; lanes hold 4 channels; results go to the per-warp
+// partial slots the split finish merges.
+template <int NW, int MAXG>
+__device__ __forceinline__ void window_partials(float (*o_part)[MAXG][D], MergeSmem<NW, MAXG>& ms,
+                                                const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G, int b,
+                                                int h, const float* __restrict__ mu,
+                                                const __nv_bfloat16* __restrict__ win_k,
+                                                const __nv_bfloat16* __restrict__ win_v,
+                                                const int32_t* __restrict__ win_lens, int win_max, float scale_log2) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wl = max(0, min(__ldg(win_lens + b), win_max));
+    float qv[MAXG][4], mc[4];
+    const __nv_bfloat16* qb = q + ((size_t)b * H_q + (size_t)h * G) * D + 4 * lane;
+#pragma unroll
+    for (int jj = 0; jj < MAXG; ++jj)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) qv[jj][e] = jj < G ? __bfloat162float(qb[(size_t)jj * D + e]) : 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) mc[e] = __ldg(mu + (size_t)h * D + 4 * lane + e);
+    float m_w[MAXG], l_w[MAXG], o_w[MAXG][4];
+#pragma unroll
+    for (int jj = 0; jj < MAXG; ++jj) {
+        m_w[jj] = -CUDART_INF_F;
+        l_w[jj] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o_w[jj][e] = 0.f;
+    }
+    for (int t = warp; t < wl; t += NW) {
+        const size_t row = (((size_t)b * win_max + t) * H_kv + h) * D + 4 * lane;
+        const uint2 kr = __ldg(reinterpret_cast<const uint2*>(win_k + row));
+        const uint2 vr = __ldg(reinterpret_cast<const uint2*>(win_v + row));
+        const float2 k01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kr.x));
+        const float2 k23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kr.y));
+        const float2 v01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vr.x));
+        const float2 v23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vr.y));
+        const float kc[4] = {__fsub_rn(k01.x, mc[0]), __fsub_rn(k01.y, mc[1]), __fsub_rn(k23.x, mc[2]),
+                             __fsub_rn(k23.y, mc[3])};
+        const float vc[4] = {v01.x, v01.y, v23.x, v23.y};
+#pragma unroll
+        for (int jj = 0; jj < MAXG; ++jj) {
+            if (jj >= G) continue;
+            float dot = qv[jj][0] * kc[0];
+#pragma unroll
+            for (int e = 1; e < 4; ++e) dot = fmaf(qv[jj][e], kc[e], dot);
+#pragma unroll
+            for (int o = 16; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+            const float lg = dot * scale_log2;
+            const float mn = fmaxf(m_w[jj], lg);
+            const float corr = ex2(m_w[jj] - mn);  // 0 while nothing was seen
+            const float p = ex2(lg - mn);
+            l_w[jj] = fmaf(l_w[jj], corr, p);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o_w[jj][e] = fmaf(o_w[jj][e], corr, p * vc[e]);
+            m_w[jj] = mn;
+        }
+    }
+#pragma unroll
+    for (int jj = 0; jj < MAXG; ++jj)
+        if (jj < G) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o_part[warp][jj][4 * lane + e] = o_w[jj][e];
+            if (lane == 0) {
+                ms.m_part[warp][jj] = m_w[jj];
+                ms.l_part[warp][jj] = l_w[jj];
+            }
+        }
+}
+
 template <int NT>
 __global__ void __launch_bounds__(DecWarps<NT>::NW * 32, 1)
 decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G, const uint8_t* __restrict__ cache,
                    int64_t num_pages, const int32_t* __restrict__ block_table, int max_pages,
                    const int32_t* __restrict__ context_lens, const float* __restrict__ Rk,
-                   const float* __restrict__ Rv, float scale_log2, float* __restrict__ out,
+                   const float* __restrict__ Rv, const float* __restrict__ mu,
+                   const __nv_bfloat16* __restrict__ win_k, const __nv_bfloat16* __restrict__ win_v,
+                   const int32_t* __restrict__ win_lens, int win_max, float scale_log2, float* __restrict__ out,
                    uint8_t* __restrict__ ws) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     constexpr int MAXG = 4 * NT;
@@ -80,6 +156,16 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     uint32_t* err_word = reinterpret_cast<uint32_t*>(ws);
 
     griddep_wait();  // every input may come from the previous kernel in the stream
+    if (win_k && split == S - 1) {
+        // the last split attends the BF16 window instead of cache pages
+        griddep_launch_dependents();
+        window_partials<NW, MAXG>(sm.u.o_part, sm.ms, q, H_q, H_kv, G, b, h, mu, win_k, win_v, win_lens, win_max,
+                                  scale_log2);
+        __syncthreads();
+        finish_decode<NW, MAXG>(sm.ms, sm.u.o_part, G, H_q, H_kv, B, b, h, split, S, ws, nullptr, out);
+        return;
+    }
+    const int S_pages = win_k ? S - 1 : S;  // splits that stream cache pages
     int ctx = __ldg(context_lens + b);
     ctx = max(0, min(ctx, max_pages * PAGE));
     const int n_pages = (ctx + PAGE - 1) / PAGE;
@@ -89,7 +175,7 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     // takes pages k0, k0 + KS, k0 + 2 KS, ...  Every warp gets the same
     // number of pages to within one, and page ids come from anywhere in the
     // sequence (the block table scatters them over the cache anyway).
-    const int KS = S * NW, k0 = split * NW + warp;
+    const int KS = S_pages * NW, k0 = split * NW + warp;
     const int my_count = n_pages > k0 ? (n_pages - k0 + KS - 1) / KS : 0;
     auto page_of = [&](int j) { return k0 + KS * j; };
 
@@ -137,7 +223,7 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         // time during the loop: have L2 fetch it now
         const char* btc = reinterpret_cast<const char*>(bt);
         const int lines = (n_pages * 4 + 127) / 128;
-        for (int l = split * NW * 32 + tid; l < lines; l += S * NW * 32) prefetch_l2_keep(btc + 128 * l);
+        for (int l = split * NW * 32 + tid; l < lines; l += S_pages * NW * 32) prefetch_l2_keep(btc + 128 * l);
     }
     float4 rr[RowPrefetch<NW, MAXG>::N];
     load_rows<NW>(Rk + (size_t)h * D * D, rr);
@@ -571,41 +657,48 @@ int bgtq_decode_auto_splits(int B, int H_kv, int max_pages_per_seq) {
 extern "C" size_t kvq_decode_workspace_bytes(int B, int H_q, int H_kv, int max_pages_per_seq, int num_splits) {
     if (B <= 0 || H_q <= 0 || H_kv <= 0) return 0;
     int S = num_splits;
-    if (S <= 0) {  // room for the automatic choice of either decode entry point
-        S = kvq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
+    if (S <= 0) {  // room for the automatic choice of every decode entry point
+        S = kvq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq) + 1;  // + 1: a BF16 window split
         const int Sb = bgtq_decode_auto_splits(B, H_kv, max_pages_per_seq);
         if (Sb > S) S = Sb;
     }
     return WS_HEADER + tickets_bytes(B, H_kv) + (size_t)B * H_q * S * PART_STRIDE * sizeof(float);
 }
 
-extern "C" kvq_status kvq_decode_attn_int2(const void* q, int B, int H_q, int H_kv, int d, const void* cache,
-                                           int64_t num_pages, const int32_t* block_table, int max_pages_per_seq,
-                                           const int32_t* context_lens, const float* R_k, const float* R_v,
-                                           float scale, float* out, void* workspace, size_t workspace_bytes,
-                                           int num_splits, void* stream) {
-    if (d != D) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "kvq_decode_attn_int2: d=%d (only 128)", d);
+// Validation and launch shared by the two INT2 decode entry points; `win_k`
+// null means no BF16 window.
+static kvq_status decode_int2_launch(const char* fn, const void* q, int B, int H_q, int H_kv, int d,
+                                     const void* cache, int64_t num_pages, const int32_t* block_table,
+                                     int max_pages_per_seq, const int32_t* context_lens, const float* R_k,
+                                     const float* R_v, const float* mu_k, const void* win_k, const void* win_v,
+                                     const int32_t* win_lens, int win_max, float scale, float* out, void* workspace,
+                                     size_t workspace_bytes, int num_splits, void* stream) {
+    if (d != D) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "%s: d=%d (only 128)", fn, d);
     if (B <= 0 || H_kv <= 0 || H_q <= 0 || H_q % H_kv || max_pages_per_seq <= 0 || num_pages <= 0 ||
         num_splits < 0)
-        return kvq_set_error(KVQ_ERR_INVALID_ARG,
-                             "kvq_decode_attn_int2: B=%d H_q=%d H_kv=%d max_pages=%d num_pages=%lld splits=%d", B,
-                             H_q, H_kv, max_pages_per_seq, (long long)num_pages, num_splits);
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: B=%d H_q=%d H_kv=%d max_pages=%d num_pages=%lld splits=%d",
+                             fn, B, H_q, H_kv, max_pages_per_seq, (long long)num_pages, num_splits);
     const int G = H_q / H_kv;
-    if (G > 8) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "kvq_decode_attn_int2: GQA group %d > 8", G);
-    if (B > 65535 || H_kv > 65535)
-        return kvq_set_error(KVQ_ERR_UNSUPPORTED, "kvq_decode_attn_int2: B or H_kv above 65535");
+    if (G > 8) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "%s: GQA group %d > 8", fn, G);
+    if (B > 65535 || H_kv > 65535) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "%s: B or H_kv above 65535", fn);
     if (!q || !cache || !block_table || !context_lens || !R_k || !R_v || !out || !workspace)
-        return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_decode_attn_int2: null pointer");
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: null pointer", fn);
     if (reinterpret_cast<uintptr_t>(cache) % 16 || reinterpret_cast<uintptr_t>(workspace) % 16 ||
         reinterpret_cast<uintptr_t>(R_v) % 16)
-        return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_decode_attn_int2: cache, R_v and workspace need 16-byte alignment");
-    const int S = num_splits > 0 ? num_splits : kvq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: cache, R_v and workspace need 16-byte alignment", fn);
+    if (win_k) {
+        if (win_max <= 0 || !win_v || !win_lens || !mu_k)
+            return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: window needs win_max > 0, win_v, win_lens and mu_k", fn);
+        if (reinterpret_cast<uintptr_t>(win_k) % 16 || reinterpret_cast<uintptr_t>(win_v) % 16)
+            return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: win_k and win_v need 16-byte alignment", fn);
+    }
+    const int S_pages = num_splits > 0 ? num_splits : kvq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
+    const int S = S_pages + (win_k ? 1 : 0);
     if (S > MAX_SPLITS)
-        return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_decode_attn_int2: num_splits=%d above %d", S, MAX_SPLITS);
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: %d splits above %d", fn, S, MAX_SPLITS);
     const size_t need = kvq_decode_workspace_bytes(B, H_q, H_kv, max_pages_per_seq, S);
     if (workspace_bytes < need)
-        return kvq_set_error(KVQ_ERR_WORKSPACE, "kvq_decode_attn_int2: workspace %zu < %zu bytes", workspace_bytes,
-                             need);
+        return kvq_set_error(KVQ_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, workspace_bytes, need);
     const float scale_log2 = scale * 1.4426950408889634f;
     constexpr int NW1 = DecWarps<1>::NW, NW2 = DecWarps<2>::NW;
     const size_t smem = G <= 4 ? sizeof(DecodeSmem<NW1, 4>) : sizeof(DecodeSmem<NW2, 8>);
@@ -617,9 +710,33 @@ extern "C" kvq_status kvq_decode_attn_int2(const void* q, int B, int H_q, int H_
     const cudaError_t e =
         launch_pdl(G <= 4 ? decode_int2_kernel<1> : decode_int2_kernel<2>, grid, dim3((G <= 4 ? NW1 : NW2) * 32), smem,
                    st, static_cast<const __nv_bfloat16*>(q), H_q, H_kv, G, static_cast<const uint8_t*>(cache),
-                   num_pages, block_table, max_pages_per_seq, context_lens, R_k, R_v, scale_log2, out,
-                   static_cast<uint8_t*>(workspace));
-    return kvq_check_cuda(e, "kvq_decode_attn_int2 launch");
+                   num_pages, block_table, max_pages_per_seq, context_lens, R_k, R_v, mu_k,
+                   static_cast<const __nv_bfloat16*>(win_k), static_cast<const __nv_bfloat16*>(win_v), win_lens,
+                   win_max, scale_log2, out, static_cast<uint8_t*>(workspace));
+    return kvq_check_cuda(e, "decode launch");
+}
+
+extern "C" kvq_status kvq_decode_attn_int2(const void* q, int B, int H_q, int H_kv, int d, const void* cache,
+                                           int64_t num_pages, const int32_t* block_table, int max_pages_per_seq,
+                                           const int32_t* context_lens, const float* R_k, const float* R_v,
+                                           float scale, float* out, void* workspace, size_t workspace_bytes,
+                                           int num_splits, void* stream) {
+    return decode_int2_launch("kvq_decode_attn_int2", q, B, H_q, H_kv, d, cache, num_pages, block_table,
+                              max_pages_per_seq, context_lens, R_k, R_v, nullptr, nullptr, nullptr, nullptr, 0, scale,
+                              out, workspace, workspace_bytes, num_splits, stream);
+}
+
+extern "C" kvq_status kvq_decode_attn_int2_window(const void* q, int B, int H_q, int H_kv, int d, const void* cache,
+                                                  int64_t num_pages, const int32_t* block_table,
+                                                  int max_pages_per_seq, const int32_t* context_lens,
+                                                  const float* R_k, const float* R_v, const float* mu_k,
+                                                  const void* win_k, const void* win_v, const int32_t* win_lens,
+                                                  int win_max, float scale, float* out, void* workspace,
+                                                  size_t workspace_bytes, int num_splits, void* stream) {
+    if (!win_k) return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_decode_attn_int2_window: null win_k");
+    return decode_int2_launch("kvq_decode_attn_int2_window", q, B, H_q, H_kv, d, cache, num_pages, block_table,
+                              max_pages_per_seq, context_lens, R_k, R_v, mu_k, win_k, win_v, win_lens, win_max, scale,
+                              out, workspace, workspace_bytes, num_splits, stream);
 }
 
 extern "C" kvq_status kvq_workspace_status(void* workspace, void* stream) {

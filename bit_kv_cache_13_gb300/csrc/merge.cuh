@@ -126,7 +126,8 @@ __device__ __forceinline__ void rotate_rows(const float (*qin)[D], const float* 
 }
 
 // NW*32 threads; o_part[w][jj][c] is warp w's o'.  Rot is row-major [D][D]
-// fp32, 16-byte aligned.  S <= MAX_SPLITS, G <= MAXG.
+// fp32, 16-byte aligned, or null when o' is already in the output basis.
+// S <= MAX_SPLITS, G <= MAXG.
 template <int NW, int MAXG>
 __device__ __forceinline__ void finish_decode(MergeSmem<NW, MAXG>& ms, const float (*o_part)[MAXG][D], int G, int H_q,
                                               int H_kv, int B, int b, int h, int split, int S, uint8_t* ws,
@@ -141,7 +142,7 @@ __device__ __forceinline__ void finish_decode(MergeSmem<NW, MAXG>& ms, const flo
     // ---- warps -> this CTA's split partial (M, L, unnormalised o')
     // rows of Rot this warp rotates, columns 4*lane .. +3: coalesced, issued now
     float4 rr[RP];
-    load_rows<NW, RP>(Rot, rr);
+    if (Rot) load_rows<NW, RP>(Rot, rr);
     // per (warp, head) weight 2^(m_w - M) in place of m_w, and the head's M, L
     if (tid < G) {
         const int jj = tid;
@@ -173,7 +174,18 @@ __device__ __forceinline__ void finish_decode(MergeSmem<NW, MAXG>& ms, const flo
     // in one lane (RP - 1 shuffles per head and RP rows, after a fold of the
     // two half-warps when RP = 16).  Heads go two at a time so their shuffle
     // chains overlap (the second of a pair past G is computed and dropped).
-    if (warp < NR) {
+    if (!Rot) {
+        // already in the output basis: publish o' as it is
+        for (int idx = tid; idx < G * D; idx += NW * 32) {
+            const int jj = idx / D, c = idx % D;
+            float* part = partials + ((head0 + jj) * S + split) * PART_STRIDE;
+            part[4 + c] = ms.o_final[jj][c];
+            if (c == 0) {
+                part[0] = ms.Mh[jj];
+                part[1] = ms.Lh[jj];
+            }
+        }
+    } else if (warp < NR) {
 #pragma unroll
         for (int pass = 0; pass < RPW / RP; ++pass) {
             if (pass > 0) {

@@ -92,8 +92,8 @@ kvq_status kvq_append_int2(const void* k, const void* v, int n_tok, int H_kv, in
 
 /* Bytes of decode workspace for B sequences, H_q query heads, H_kv KV heads
  * and num_splits split-K partitions (num_splits = 0: room for the automatic
- * choice of either decode entry point, kvq_decode_attn_int2 or
- * bgtq_decode_attn, at max_pages_per_seq pages).  The workspace holds an
+ * choice of every decode entry point, kvq_decode_attn_int2, its BF16-window
+ * form or bgtq_decode_attn, at max_pages_per_seq pages).  The workspace holds an
  * error word, a split ticket per (sequence, KV head) and the split partials.
  * It must be zero-filled once before its first use; every call leaves its
  * tickets at zero again. */
@@ -125,6 +125,36 @@ kvq_status kvq_decode_attn_int2(const void* q, int B, int H_q, int H_kv, int d,
                                 const float* R_k, const float* R_v, float scale,
                                 float* out, void* workspace, size_t workspace_bytes,
                                 int num_splits, void* stream);
+
+/* Decode attention over the INT2 cache together with a BF16 window of
+ * tokens kept unquantised.  "Output-Aware Rotation for INT2 KV-Cache
+ * Quantization" §3.1 retains a small BF16 window; the Block-GTQ page keeps
+ * 4 sink and 128 recent tokens in fp16 (Table 6).  The softmax runs over
+ * the union of the context_lens[b] cached tokens and the first win_lens[b]
+ * window tokens; a window token must not also be in the cached range (the
+ * cached range need not start at the sequence's first token: keys are
+ * stored after RoPE, so sinks and recent tokens can simply live in the
+ * window).
+ *   Arguments as kvq_decode_attn_int2, plus:
+ *   mu_k      device fp32 [H_kv][d], the key centre append used: window
+ *             logits are q . (k - mu_k) * scale, the same shift centring gives
+ *             the cached keys
+ *   win_k, win_v  device bf16 [B][win_max][H_kv][d], original basis (not
+ *             centred, not rotated), 16-byte aligned
+ *   win_lens  device int32 [B], clamped to [0, win_max]
+ *   win_max   > 0
+ * The window takes one split of its own: the workspace must hold
+ * num_splits + 1 partials (kvq_decode_workspace_bytes(..., num_splits + 1);
+ * with num_splits = 0, kvq_decode_workspace_bytes(..., 0) already does). */
+kvq_status kvq_decode_attn_int2_window(const void* q, int B, int H_q, int H_kv, int d,
+                                       const void* cache, int64_t num_pages,
+                                       const int32_t* block_table, int max_pages_per_seq,
+                                       const int32_t* context_lens,
+                                       const float* R_k, const float* R_v, const float* mu_k,
+                                       const void* win_k, const void* win_v,
+                                       const int32_t* win_lens, int win_max, float scale,
+                                       float* out, void* workspace, size_t workspace_bytes,
+                                       int num_splits, void* stream);
 
 /* Reads (synchronously, on `stream`) and clears the error word a decode call
  * left in its workspace: KVQ_OK, KVQ_ERR_BAD_BLOCK_TABLE, or KVQ_ERR_CUDA
