@@ -278,6 +278,22 @@ def gen_values(spec: Spec, layer: int, batch_idx: int, n: int, device="cpu",
     return out
 
 
+def gen_prefix_queries(spec: Spec, layer: int, positions: torch.Tensor, device="cpu") -> torch.Tensor:
+    """Queries [n, H_q, d] bf16 of a calibration prefix at the given
+    positions (post-RoPE for the RoPE workloads), drawn like the decode
+    queries: per-block standard deviations from the head's energy scores."""
+    n = positions.numel()
+    out = torch.empty((n, spec.h_q, spec.d), dtype=torch.bfloat16, device=device)
+    for j in range(spec.h_q):
+        g = torch_gen(device, spec.name, layer, j, "qcal")
+        z = torch.randn((n, spec.d), generator=g, device=device, dtype=torch.float32)
+        z = _scaled(z, query_params(spec, layer, j // spec.g))
+        if spec.k_kind in ("offset_rope", "energy_rope"):
+            z = rope_apply(z, positions.to(device), spec.rope_theta)
+        out[:, j] = to_bf16(z)
+    return out
+
+
 def gen_queries(spec: Spec, layer: int, device="cpu") -> torch.Tensor:
     """Decode queries [B, H_q, d] bf16 (post-RoPE at position ctx-1 for the
     RoPE workloads)."""

@@ -19,6 +19,8 @@ Follows "RoPE-Aware Bit Allocation for KV-Cache Quantization":
       bits per dimension; values use uniform-width TQ-MSE.
   core method: the RoPE logit is a sum over 2-D blocks and the key-error
       logit bound is |K(q,k) - K(q,k^)| <= sum_i ||q(i)|| ||e_k(i)||.
+  method step (1): label-free block energy scores from a calibration
+      prefix, s_i = 1/2 E||q(i)||^2 + 1/2 E||k(i)||^2 (energy_scores).
 
 Readings (the pages leave these open): block i is the rotate-half pair of
 dims (i, i + d/2); x_b lists the blocks of G_b in ascending order, each as
@@ -124,6 +126,32 @@ def nearest_codes(y32: np.ndarray, cb32: np.ndarray) -> np.ndarray:
 # --------------------------------------------------------------------------
 # greedy RoPE-block allocator
 # --------------------------------------------------------------------------
+
+def energy_scores(q, k, h_kv: int):
+    """Block energy scores of a calibration prefix (method step (1)):
+        s_{h,i} = 1/2 E_{t, g in G(h)} ||q_{t,g}(i)||^2 + 1/2 E_t ||k_{t,h}(i)||^2,
+    block i = dims (i, i + d/2), G(h) the query heads reading KV head h; and
+    the paired estimate
+        s*_{h,i} = E_{t, g in G(h)} ||q_{t,g}(i)|| ||k_{t,h}(i)||,
+    which AM-GM (||q|| ||k|| <= (||q||^2 + ||k||^2) / 2, token by token)
+    keeps at or below s (technical novelty (2): s* <= s).
+
+    q: [T, H_q, d], k: [T, H_kv, d] (bf16 values); returns (s, s_star), each
+    [H_kv, d/2] fp64.  T = 0 gives zeros.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    T, h_q, d = q.shape
+    L = d // 2
+    g = h_q // h_kv
+    if T == 0:
+        return np.zeros((h_kv, L)), np.zeros((h_kv, L))
+    qn = (q[..., :L] ** 2 + q[..., L:] ** 2).reshape(T, h_kv, g, L)   # ||q_{t,g}(i)||^2
+    kn = k[..., :L] ** 2 + k[..., L:] ** 2                               # ||k_{t,h}(i)||^2
+    s = 0.5 * qn.mean(axis=(0, 2)) + 0.5 * kn.mean(axis=0)
+    s_star = (np.sqrt(qn) * np.sqrt(kn)[:, :, None, :]).mean(axis=(0, 2))
+    return s, s_star
+
 
 def greedy_allocate(scores, b_min: int, b_max: int, total_bits: int) -> np.ndarray:
     """Integer widths b_i in [b_min, b_max] with sum <= total_bits.

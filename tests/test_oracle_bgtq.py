@@ -205,3 +205,70 @@ def test_decode_close_to_plain_attention_at_high_width(table):
     got = bgtq.decode(q, cache, np.array([[0, 1]]), [T], widths, 8, total, pis, table, 0.1, h_kv)
     want = attention.gqa_decode(q[0], k, v, float(np.float32(0.1)))
     assert np.max(np.abs(got[0] - want)) <= 0.02 * np.max(np.abs(want))
+
+
+# ------------------------------------------------------ calibration energy scores
+
+def test_energy_scores_hand_example():
+    # d = 4: block 0 = dims (0, 2), block 1 = dims (1, 3); two tokens, two
+    # query heads on one KV head.
+    q = np.array([[[1, 2, 2, 0], [0, 0, 3, 4]],
+                  [[3, 0, 4, 1], [1, 1, 1, 1]]], dtype=np.float64)      # [T=2, H_q=2, 4]
+    k = np.array([[[2, 0, 0, 1]], [[0, 3, 4, 0]]], dtype=np.float64)    # [T=2, H_kv=1, 4]
+    s, s_star = bgtq.energy_scores(q, k, 1)
+    # ||q(0)||^2: t0 = (1, 2)->5, (0, 3)->9; t1 = (3, 4)->25, (1, 1)->2 -> mean 41/4
+    # ||q(1)||^2: t0 = (2, 0)->4, (0, 4)->16; t1 = (0, 1)->1, (1, 1)->2 -> mean 23/4
+    # ||k(0)||^2: t0 = (2, 0)->4; t1 = (0, 4)->16 -> mean 10;  ||k(1)||^2: 1, 9 -> mean 5
+    assert np.allclose(s, [[0.5 * 41 / 4 + 0.5 * 10, 0.5 * 23 / 4 + 0.5 * 5]], rtol=0, atol=1e-15)
+    pairs0 = [math.sqrt(5) * 2, 3 * 2, 5 * 4, math.sqrt(2) * 4]
+    pairs1 = [2 * 1, 4 * 1, 1 * 3, math.sqrt(2) * 3]
+    assert np.allclose(s_star, [[sum(pairs0) / 4, sum(pairs1) / 4]], rtol=1e-15, atol=0)
+
+
+def test_energy_scores_am_gm_bound():
+    rng = np.random.default_rng(31)
+    q = rng.standard_normal((200, 8, 128)) * rng.lognormal(0, 1.5, 128)
+    k = rng.standard_normal((200, 2, 128)) * rng.lognormal(0, 1.5, 128)
+    s, s_star = bgtq.energy_scores(q, k, 2)
+    assert np.all(s_star <= s * (1 + 1e-15))
+    assert np.any(s_star < 0.9 * s)                   # the bound is not tight in general
+
+
+def test_energy_scores_equal_when_queries_are_the_keys():
+    # AM-GM holds with equality when ||q(i)|| = ||k(i)|| token by token.
+    rng = np.random.default_rng(32)
+    k = rng.standard_normal((50, 3, 128))
+    s, s_star = bgtq.energy_scores(k.copy(), k, 3)
+    assert np.allclose(s_star, s, rtol=1e-14, atol=0)
+    assert np.allclose(s, ((k[..., :64] ** 2 + k[..., 64:] ** 2)).mean(axis=0), rtol=1e-14, atol=0)
+
+
+def test_energy_scores_invariant_under_rope():
+    # Rotate-half RoPE turns block i = dims (i, i + 64) by a 2x2 rotation,
+    # which keeps every block norm: scores from pre- and post-RoPE vectors
+    # agree (a wrong pairing of dims would break this).
+    rng = np.random.default_rng(33)
+    T = 64
+    q = torch.as_tensor(rng.standard_normal((T, 4, 128)))
+    k = torch.as_tensor(rng.standard_normal((T, 1, 128)) * 3)
+    pos = torch.as_tensor(rng.integers(0, 100000, T))
+    qr = torch.stack([inputs.rope_apply(q[:, j], pos, 5e5) for j in range(4)], dim=1)
+    kr = inputs.rope_apply(k[:, 0], pos, 5e5)[:, None]
+    a = bgtq.energy_scores(q.numpy(), k.numpy(), 1)
+    b = bgtq.energy_scores(qr.numpy(), kr.numpy(), 1)
+    for x, y in zip(a, b):
+        assert np.allclose(x, y, rtol=1e-12, atol=0)
+
+
+def test_energy_scores_recover_the_generators_block_energies():
+    # The Block-GTQ workload draws q and k block i with E||.(i)||^2 = s_i;
+    # 4096 calibration tokens recover every s_i to well within 10 % (the
+    # relative standard error is about 1/sqrt(T) = 1.6 %).
+    spec = inputs.small_spec("cal", h_q=8, h_kv=2, batch=1, ctx=4096, k_kind="energy_rope")
+    pos = torch.arange(4096)
+    q = inputs.gen_prefix_queries(spec, 0, pos).float().numpy()
+    k = inputs.gen_keys(spec, 0, 0, pos).float().numpy()
+    s, _ = bgtq.energy_scores(q, k, 2)
+    for h in range(2):
+        want = inputs.block_energies(spec, 0, h)
+        assert np.max(np.abs(s[h] / want - 1)) < 0.1
