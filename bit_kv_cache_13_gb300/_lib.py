@@ -31,6 +31,7 @@ _SIGS = {
     "kvq_decode_attn_int2": ([P, I, I, I, I, P, I64, P, I, P, P, P, F, P, P, SZ, I, P], I),
     "kvq_decode_attn_int2_window": ([P, I, I, I, I, P, I64, P, I, P, P, P, P, P, P, P, I, F, P, P, SZ, I, P], I),
     "kvq_workspace_status": ([P, P], I),
+    "bgtq_energy_scores": ([P, P, I, I, I, I, P, P, P], I),
     "kvq_decode_attn_int2_noalloc": ([P, I, I, I, I, P, I64, P, I, P, P, P, F, P, I, P], I),
     "bgtq_lloyd_max_codebook": ([I, P], I),
     "bgtq_allocate": ([P, I, I, I, I64, P], I),
@@ -170,6 +171,15 @@ def kvq_workspace_status(workspace, stream=None) -> int:
 
 
 # -------------------------------------------------------------- Block-GTQ
+
+def bgtq_energy_scores(q, k, H_kv: int, scores, paired=None, stream=None):
+    """Calibration block energy scores (and the paired AM-GM estimate) of
+    q [T, H_q, d] and k [T, H_kv, d] bf16 into fp64 [H_kv, d/2] tensors."""
+    T, H_q, d = q.shape
+    _check(load().bgtq_energy_scores(
+        _dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"), T, H_q, H_kv, d,
+        _dev(scores, torch.float64, "scores"), None if paired is None else _dev(paired, torch.float64, "paired"),
+        _stream(stream)))
 
 def bgtq_lloyd_max_codebook(b: int):
     import numpy as np

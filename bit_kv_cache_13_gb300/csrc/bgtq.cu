@@ -409,9 +409,90 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                                pi_table + __ldg(pi_offsets + D), out);
 }
 
+// ------------------------------------------------------------- calibration
+
+// Method step (1): s_{h,i} = 1/2 E_{t,g in G(h)} ||q_{t,g}(i)||^2 +
+// 1/2 E_t ||k_{t,h}(i)||^2 over a calibration prefix, block i = dims
+// (i, i + d/2); and the paired estimate s*_{h,i} = E_{t,g} ||q(i)|| ||k(i)||
+// (AM-GM keeps it at or below s).  CTA (h, chunk) takes tokens
+// chunk * CAL_TOK .. + CAL_TOK: thread (i, lane4) every 4th of them.
+// Products of bf16 values are exact in fp64 and the sums are fp64 (the
+// paired term takes fp32 square roots); the 4 token lanes combine in a fixed
+// order, and each CTA adds its share (already divided by the token counts)
+// into the outputs with fp64 atomics.
+constexpr int CAL_TOK = 256;
+
+__global__ void __launch_bounds__(256)
+bgtq_energy_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int T, int H_q, int H_kv,
+                   double* __restrict__ scores, double* __restrict__ paired) {
+    griddep_wait();
+    griddep_launch_dependents();
+    constexpr int L = D / 2;
+    const int h = blockIdx.x, chunk = blockIdx.y;
+    const int i = threadIdx.x % L, lane4 = threadIdx.x / L;
+    const int G = H_q / H_kv;
+    const int t0 = chunk * CAL_TOK, t1 = min(T, t0 + CAL_TOK);
+    double qs = 0.0, ks = 0.0, ps = 0.0;
+    for (int t = t0 + lane4; t < t1; t += 4) {
+        const __nv_bfloat16* kr = k + ((size_t)t * H_kv + h) * D;
+        const double ka = __bfloat162float(kr[i]), kb = __bfloat162float(kr[i + L]);
+        const double kn = fma(ka, ka, kb * kb);  // bf16 products are exact in fp64
+        ks += kn;
+        const float kroot = sqrtf((float)kn);
+        for (int g = 0; g < G; ++g) {
+            const __nv_bfloat16* qr = q + ((size_t)t * H_q + (size_t)h * G + g) * D;
+            const double qa = __bfloat162float(qr[i]), qb = __bfloat162float(qr[i + L]);
+            const double qn = fma(qa, qa, qb * qb);
+            qs += qn;
+            ps += (double)(sqrtf((float)qn) * kroot);
+        }
+    }
+    __shared__ double red[3][4][L];
+    red[0][lane4][i] = qs;
+    red[1][lane4][i] = ks;
+    red[2][lane4][i] = ps;
+    __syncthreads();
+    if (lane4 == 0) {
+        double a = 0.0, b = 0.0, c = 0.0;
+#pragma unroll
+        for (int l = 0; l < 4; ++l) {
+            a += red[0][l][i];
+            b += red[1][l][i];
+            c += red[2][l][i];
+        }
+        const double n_q = (double)T * G, n_k = (double)T;
+        atomicAdd(scores + (size_t)h * L + i, 0.5 * a / n_q + 0.5 * b / n_k);
+        if (paired) atomicAdd(paired + (size_t)h * L + i, c / n_q);
+    }
+}
+
 }  // namespace kvq
 
 using namespace kvq;
+
+extern "C" kvq_status bgtq_energy_scores(const void* q, const void* k, int T, int H_q, int H_kv, int d,
+                                         double* scores, double* paired, void* stream) {
+    if (d != D) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "bgtq_energy_scores: d=%d (only 128)", d);
+    if (T < 0 || H_kv <= 0 || H_q <= 0 || H_q % H_kv || H_kv > 65535)
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "bgtq_energy_scores: T=%d H_q=%d H_kv=%d", T, H_q, H_kv);
+    if (!scores || (T > 0 && (!q || !k)))
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "bgtq_energy_scores: null pointer");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t bytes = (size_t)H_kv * (D / 2) * sizeof(double);
+    kvq_status s = kvq_check_cuda(cudaMemsetAsync(scores, 0, bytes, st), "bgtq_energy_scores: clearing scores");
+    if (s != KVQ_OK) return s;
+    if (paired) {
+        s = kvq_check_cuda(cudaMemsetAsync(paired, 0, bytes, st), "bgtq_energy_scores: clearing paired");
+        if (s != KVQ_OK) return s;
+    }
+    if (T == 0) return KVQ_OK;
+    const int chunks = (T + CAL_TOK - 1) / CAL_TOK;
+    if (chunks > 65535) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "bgtq_energy_scores: T=%d too long", T);
+    return kvq_check_cuda(launch_pdl(bgtq_energy_kernel, dim3(H_kv, chunks), dim3(256), 0, st,
+                                     static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), T,
+                                     H_q, H_kv, scores, paired),
+                          "bgtq_energy_scores launch");
+}
 
 static kvq_status check_bgtq_common(const char* fn, int d, int H_kv, int total_bits, int v_bits,
                                     const float* pi_table) {

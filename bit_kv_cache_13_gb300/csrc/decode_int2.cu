@@ -134,7 +134,9 @@ __device__ __forceinline__ void window_partials(float (*o_part)[MAXG][D], MergeS
         }
 }
 
-template <int NT>
+// WIN: the grid's last split attends the BF16 window (a separate
+// instantiation, so the plain decode carries none of it).
+template <int NT, bool WIN>
 __global__ void __launch_bounds__(DecWarps<NT>::NW * 32, 1)
 decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G, const uint8_t* __restrict__ cache,
                    int64_t num_pages, const int32_t* __restrict__ block_table, int max_pages,
@@ -156,16 +158,18 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     uint32_t* err_word = reinterpret_cast<uint32_t*>(ws);
 
     griddep_wait();  // every input may come from the previous kernel in the stream
-    if (win_k && split == S - 1) {
-        // the last split attends the BF16 window instead of cache pages
-        griddep_launch_dependents();
-        window_partials<NW, MAXG>(sm.u.o_part, sm.ms, q, H_q, H_kv, G, b, h, mu, win_k, win_v, win_lens, win_max,
-                                  scale_log2);
-        __syncthreads();
-        finish_decode<NW, MAXG>(sm.ms, sm.u.o_part, G, H_q, H_kv, B, b, h, split, S, ws, nullptr, out);
-        return;
+    if constexpr (WIN) {
+        if (split == S - 1) {
+            // the last split attends the BF16 window instead of cache pages
+            griddep_launch_dependents();
+            window_partials<NW, MAXG>(sm.u.o_part, sm.ms, q, H_q, H_kv, G, b, h, mu, win_k, win_v, win_lens, win_max,
+                                      scale_log2);
+            __syncthreads();
+            finish_decode<NW, MAXG, false>(sm.ms, sm.u.o_part, G, H_q, H_kv, B, b, h, split, S, ws, nullptr, out);
+            return;
+        }
     }
-    const int S_pages = win_k ? S - 1 : S;  // splits that stream cache pages
+    const int S_pages = WIN ? S - 1 : S;  // splits that stream cache pages
     int ctx = __ldg(context_lens + b);
     ctx = max(0, min(ctx, max_pages * PAGE));
     const int n_pages = (ctx + PAGE - 1) / PAGE;
@@ -616,7 +620,7 @@ using namespace kvq;
 // set it on the first call on each device only.
 static kvq_status set_smem_once(const void* fn, int bytes, int which) {
     static std::mutex mu;
-    static bool done[64][2] = {};
+    static bool done[64][4] = {};
     int dev = 0;
     kvq_status st = kvq_check_cuda(cudaGetDevice(&dev), "kvq_decode_attn_int2: cudaGetDevice");
     if (st != KVQ_OK) return st;
@@ -704,15 +708,16 @@ static kvq_status decode_int2_launch(const char* fn, const void* q, int B, int H
     const size_t smem = G <= 4 ? sizeof(DecodeSmem<NW1, 4>) : sizeof(DecodeSmem<NW2, 8>);
     dim3 grid(S, H_kv, B);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    kvq_status sa = set_smem_once(G <= 4 ? (const void*)decode_int2_kernel<1> : (const void*)decode_int2_kernel<2>,
-                                  (int)smem, G <= 4 ? 0 : 1);
+    auto* kern = G <= 4 ? (win_k ? decode_int2_kernel<1, true> : decode_int2_kernel<1, false>)
+                        : (win_k ? decode_int2_kernel<2, true> : decode_int2_kernel<2, false>);
+    kvq_status sa = set_smem_once((const void*)kern, (int)smem, (G <= 4 ? 0 : 2) + (win_k ? 1 : 0));
     if (sa != KVQ_OK) return sa;
     const cudaError_t e =
-        launch_pdl(G <= 4 ? decode_int2_kernel<1> : decode_int2_kernel<2>, grid, dim3((G <= 4 ? NW1 : NW2) * 32), smem,
-                   st, static_cast<const __nv_bfloat16*>(q), H_q, H_kv, G, static_cast<const uint8_t*>(cache),
-                   num_pages, block_table, max_pages_per_seq, context_lens, R_k, R_v, mu_k,
-                   static_cast<const __nv_bfloat16*>(win_k), static_cast<const __nv_bfloat16*>(win_v), win_lens,
-                   win_max, scale_log2, out, static_cast<uint8_t*>(workspace));
+        launch_pdl(kern, grid, dim3((G <= 4 ? NW1 : NW2) * 32), smem, st, static_cast<const __nv_bfloat16*>(q), H_q,
+                   H_kv, G, static_cast<const uint8_t*>(cache), num_pages, block_table, max_pages_per_seq,
+                   context_lens, R_k, R_v, mu_k, static_cast<const __nv_bfloat16*>(win_k),
+                   static_cast<const __nv_bfloat16*>(win_v), win_lens, win_max, scale_log2, out,
+                   static_cast<uint8_t*>(workspace));
     return kvq_check_cuda(e, "decode launch");
 }
 

@@ -126,9 +126,9 @@ __device__ __forceinline__ void rotate_rows(const float (*qin)[D], const float* 
 }
 
 // NW*32 threads; o_part[w][jj][c] is warp w's o'.  Rot is row-major [D][D]
-// fp32, 16-byte aligned, or null when o' is already in the output basis.
-// S <= MAX_SPLITS, G <= MAXG.
-template <int NW, int MAXG>
+// fp32, 16-byte aligned; with ROTATE false, o' is already in the output
+// basis and Rot is not read.  S <= MAX_SPLITS, G <= MAXG.
+template <int NW, int MAXG, bool ROTATE = true>
 __device__ __forceinline__ void finish_decode(MergeSmem<NW, MAXG>& ms, const float (*o_part)[MAXG][D], int G, int H_q,
                                               int H_kv, int B, int b, int h, int split, int S, uint8_t* ws,
                                               const float* __restrict__ Rot, float* __restrict__ out) {
@@ -142,7 +142,7 @@ __device__ __forceinline__ void finish_decode(MergeSmem<NW, MAXG>& ms, const flo
     // ---- warps -> this CTA's split partial (M, L, unnormalised o')
     // rows of Rot this warp rotates, columns 4*lane .. +3: coalesced, issued now
     float4 rr[RP];
-    if (Rot) load_rows<NW, RP>(Rot, rr);
+    if constexpr (ROTATE) load_rows<NW, RP>(Rot, rr);
     // per (warp, head) weight 2^(m_w - M) in place of m_w, and the head's M, L
     if (tid < G) {
         const int jj = tid;
@@ -174,7 +174,7 @@ __device__ __forceinline__ void finish_decode(MergeSmem<NW, MAXG>& ms, const flo
     // in one lane (RP - 1 shuffles per head and RP rows, after a fold of the
     // two half-warps when RP = 16).  Heads go two at a time so their shuffle
     // chains overlap (the second of a pair past G is computed and dropped).
-    if (!Rot) {
+    if constexpr (!ROTATE) {
         // already in the output basis: publish o' as it is
         for (int idx = tid; idx < G * D; idx += NW * 32) {
             const int jj = idx / D, c = idx % D;

@@ -195,6 +195,24 @@ kvq_status kvq_decode_attn_int2_noalloc(const void* q, int B, int H_q, int H_kv,
  * sub-vector at width b uses fp32(c / sqrt(n)). */
 kvq_status bgtq_lloyd_max_codebook(int b, double* centroids_out);
 
+/* Block energy scores of a calibration prefix ("RoPE-Aware Bit Allocation
+ * for KV-Cache Quantization", method step (1)): for KV head h and RoPE block
+ * i = dims (i, i + d/2),
+ *   scores[h][i] = 1/2 mean_{t < T, g in G(h)} ||q_{t,g}(i)||^2
+ *                + 1/2 mean_{t < T} ||k_{t,h}(i)||^2,
+ * G(h) the H_q/H_kv query heads reading KV head h (contiguous), and the
+ * paired estimate (technical novelty (2): AM-GM gives paired <= scores)
+ *   paired[h][i] = mean_{t, g in G(h)} ||q_{t,g}(i)|| ||k_{t,h}(i)||.
+ *   q       device bf16 [T][H_q][d], post-RoPE calibration queries
+ *   k       device bf16 [T][H_kv][d], post-RoPE calibration keys
+ *   scores  device fp64 [H_kv][d/2], written (the input of bgtq_allocate)
+ *   paired  device fp64 [H_kv][d/2] or null
+ * Products of bf16 values are exact in fp64 and sums are fp64 (scores to
+ * ~1e-15 relative); the paired estimate takes fp32 square roots (~1e-7
+ * relative).  T = 0 gives zeros. */
+kvq_status bgtq_energy_scores(const void* q, const void* k, int T, int H_q, int H_kv, int d,
+                              double* scores, double* paired, void* stream);
+
 /* Host only.  Greedy RoPE-block width allocation (Theorem 1): every block
  * starts at b_min; one bit at a time goes to the block with the largest
  * marginal gain (3/4) s_i 4^-b_i among blocks below b_max (ties: lowest
