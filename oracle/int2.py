@@ -8,9 +8,10 @@ Follows "Output-Aware Rotation for INT2 KV-Cache Quantization":
       quantisation, which shifts every logit of a query by the same constant
       and leaves the softmax unchanged.
   §3.1 Eq. (4): D_{R,c}(z) = Q2(zR; c, G) R^T, with R orthogonal, clip ratio
-      c and group size G.  Readings used here: c = 1 (plain min/max range),
-      G = 32 consecutive rotated channels of one token, asymmetric levels
-      min + code*scale, scale = (max - min)/3, both stored as fp16.
+      c and group size G.  Readings used here: c scales the group's range
+      ends (c = 1, the plain min/max range, by default), G = 32 consecutive
+      rotated channels of one token, asymmetric levels min + code*scale,
+      scale = (max - min)/3, both stored as fp16.
   §3 Eqs. (1)-(2): decode attention; the cache is consumed in the rotated
       basis: <q, k~> = <qR_k, Q2(z)> and o = (sum_s p_s Q2(w_s)) R_v^T.
 
@@ -44,15 +45,20 @@ META_BYTES = 16
 # quantiser Q2 (one group of 32 rotated values)
 # --------------------------------------------------------------------------
 
-def quant_params(x32: np.ndarray):
+def quant_params(x32: np.ndarray, clip: float = 1.0):
     """fp16 (scale, min) of each group along the last axis (length 32).
 
-    Taken in the kernel's precision: max - min and the division by 3 are
-    fp32 operations rounded to nearest, then rounded to fp16 (saturating).
+    Clip ratio c (§3.1, Q2(.; c, G)): the group's range ends are scaled,
+    min_c = c*min and max_c = c*max (fp32 products), so for c < 1 values
+    beyond the clipped range saturate at the end codes; c = 1 is the plain
+    min/max range.  Taken in the kernel's precision: the products, max - min
+    and the division by 3 are fp32 operations rounded to nearest, then
+    rounded to fp16 (saturating).
     """
     x32 = np.asarray(x32, dtype=np.float32)
-    mn = x32.min(axis=-1)
-    mx = x32.max(axis=-1)
+    c = np.float32(clip)
+    mn = (c * x32.min(axis=-1)).astype(np.float32)
+    mx = (c * x32.max(axis=-1)).astype(np.float32)
     rng = (mx - mn).astype(np.float32)
     s = (rng / np.float32(3.0)).astype(np.float32)
     return f16_rn_sat(s), f16_rn_sat(mn)
@@ -71,14 +77,25 @@ def quant_codes(x32: np.ndarray, scale_h: np.ndarray, min_h: np.ndarray) -> np.n
     return np.where(sc == 0.0, 0, code).astype(np.uint8)
 
 
-def quantize(z32: np.ndarray):
+def quantize(z32: np.ndarray, clip: float = 1.0):
     """Q2 of rotated vectors [..., 128] -> (codes [...,128] u8,
-    scale [...,4] f16, min [...,4] f16)."""
+    scale [...,4] f16, min [...,4] f16), clip ratio `clip`."""
     z32 = np.asarray(z32, dtype=np.float32)
     g = z32.reshape(z32.shape[:-1] + (N_GROUPS, GROUP))
-    scale_h, min_h = quant_params(g)
+    scale_h, min_h = quant_params(g, clip)
     codes = quant_codes(g, scale_h, min_h)
     return codes.reshape(z32.shape), scale_h, min_h
+
+
+def dequantize_f32(codes: np.ndarray, scale_h: np.ndarray, min_h: np.ndarray) -> np.ndarray:
+    """min + code*scale as one fp32 fused multiply-add (exact product, one
+    rounding of the sum), [..., 128] fp32: the value a reader of the cache
+    gets in fp32."""
+    c = np.asarray(codes, dtype=np.float64)
+    c = c.reshape(c.shape[:-1] + (N_GROUPS, GROUP))
+    out = (np.asarray(min_h, np.float16).astype(np.float64)[..., None]
+           + c * np.asarray(scale_h, np.float16).astype(np.float64)[..., None])   # exact in fp64
+    return out.astype(np.float32).reshape(out.shape[:-2] + (D,))
 
 
 def dequantize(codes: np.ndarray, scale_h: np.ndarray, min_h: np.ndarray) -> np.ndarray:
@@ -160,11 +177,12 @@ def new_cache(num_pages: int, h_kv: int) -> np.ndarray:
     return np.zeros((num_pages, h_kv, TILE_BYTES), dtype=np.uint8)
 
 
-def append(cache, k, v, slot_mapping, mu32, rk32, rv32, exact_chain=True):
+def append(cache, k, v, slot_mapping, mu32, rk32, rv32, exact_chain=True, clip=1.0):
     """Quantise-on-append into the paged cache (in place).
 
     k, v: [n, H_kv, d] (bf16 values); slot_mapping[n] = page*16 + slot,
-    -1 skips the token; mu32 [H_kv, d]; rk32, rv32 [H_kv, d, d] fp32.
+    -1 skips the token; mu32 [H_kv, d]; rk32, rv32 [H_kv, d, d] fp32;
+    clip: the clip ratio c of Q2 (keys and values alike).
     Returns dict with the fp32 rotated vectors z, w ([n, H_kv, d]).
     """
     k = np.asarray(k)
@@ -180,7 +198,7 @@ def append(cache, k, v, slot_mapping, mu32, rk32, rv32, exact_chain=True):
         z_all[keep, h] = z32
         w_all[keep, h] = w32
         for src, off_c, off_m in ((z32, OFF_K_CODES, OFF_K_META), (w32, OFF_V_CODES, OFF_V_META)):
-            codes, sc, mn = quantize(src)
+            codes, sc, mn = quantize(src, clip)
             recs = pack_codes(codes)
             metas = pack_meta(sc, mn)
             for i, slot in enumerate(sm[keep]):

@@ -370,3 +370,51 @@ def test_window_lengths_are_per_sequence():
         if lens[b] == 0:
             plain = int2.decode(q[b:b + 1], cache, bt[b:b + 1], [T], mu, rk, rk, 0.1, 1)
             assert np.array_equal(got[b], plain[0])
+
+
+# ---------------------------------------------------------------- clip ratio
+
+def test_clip_one_is_the_plain_range():
+    rng = np.random.default_rng(41)
+    x = (rng.standard_normal((50, 4, 32)) * 3 + 1).astype(np.float32)
+    for a, b in zip(int2.quant_params(x), int2.quant_params(x, 1.0)):
+        assert np.array_equal(a, b)
+
+
+def test_clipped_codes_are_the_nearest_level():
+    # With c < 1 the four levels span [c*min, c*max] (to fp16 rounding) and
+    # every value takes the nearest of them, ties low: values beyond the
+    # clipped range saturate at code 0 or 3.
+    rng = np.random.default_rng(42)
+    for c in (0.5, 0.8, 0.95):
+        for _ in range(100):
+            x = (rng.standard_normal(32) * rng.uniform(0.1, 20) + rng.normal(0, 5)).astype(np.float32)
+            sc, mn = int2.quant_params(x, c)
+            lo = float(np.float32(np.float32(c) * x.min()))
+            hi = float(np.float32(np.float32(c) * x.max()))
+            assert float(mn) == float(np.float16(lo))
+            assert abs(float(mn) + 3 * float(sc) - hi) <= 2e-3 * max(abs(hi), abs(lo)) + 1e-6
+            got = int2.quant_codes(x, sc, mn)
+            assert np.array_equal(got, _brute_codes(x, sc, mn))
+            if float(sc) > 0:
+                assert np.all(got[x >= hi] == 3) and np.all(got[x <= lo] == 0)
+
+
+def test_clipping_lowers_the_error_of_heavy_tailed_groups():
+    # Student-t (3 dof) groups: a few large values stretch the plain range;
+    # a clip ratio somewhat below 1 gives a lower mean squared error.
+    rng = np.random.default_rng(43)
+    x = rng.standard_t(3, size=(4000, 4, 32)).astype(np.float32)
+    def mse(c):
+        codes, sc, mn = int2.quantize(x.reshape(4000, 128), c)
+        return float(np.mean((int2.dequantize(codes, sc, mn) - x.reshape(4000, 128)) ** 2))
+    assert mse(0.8) < 0.95 * mse(1.0)
+
+
+def test_dequantize_f32_is_the_rounded_fp64_value():
+    rng = np.random.default_rng(44)
+    z = (rng.standard_normal((20, 128)) * 5).astype(np.float32)
+    codes, sc, mn = int2.quantize(z)
+    d32 = int2.dequantize_f32(codes, sc, mn)
+    assert d32.dtype == np.float32
+    assert np.array_equal(d32, int2.dequantize(codes, sc, mn).astype(np.float32))
