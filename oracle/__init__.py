@@ -20,6 +20,8 @@ Modules
              RoPE-block bit allocation (Theorem 1), grouped encoding and the
              packed Block-GTQ cache (RoPE-Aware Bit Allocation for KV-Cache
              Quantization, prerequisites and method steps (1)-(4)).
+  diagnostics  output-space error of a quantised cache: E_rec, E_out and
+             the key/value split (Output-Aware Rotation, §3.2 Eqs. 5-10).
 
 Every function is pinned by tests under tests/ that do not re-derive its
 formula: closed forms, textbook values, invariants, brute force and exact
