@@ -31,6 +31,8 @@ _SIGS = {
     "kvq_decode_attn_int2": ([P, I, I, I, I, P, I64, P, I, P, P, P, F, P, P, SZ, I, P], I),
     "kvq_decode_attn_int2_window": ([P, I, I, I, I, P, I64, P, I, P, P, P, P, P, P, P, I, F, P, P, SZ, I, P], I),
     "kvq_workspace_status": ([P, P], I),
+    "kvq_append_int2_clip": ([P, P, I, I, I, P, P, P, P, F, P, I64, P, P, P, P], I),
+    "kvq_dequant_int2": ([P, I64, I, I, P, I, P, P, P], I),
     "bgtq_energy_scores": ([P, P, I, I, I, I, P, P, P], I),
     "kvq_decode_attn_int2_noalloc": ([P, I, I, I, I, P, I64, P, I, P, P, P, F, P, I, P], I),
     "bgtq_lloyd_max_codebook": ([I, P], I),
@@ -111,6 +113,28 @@ def kvq_append_int2(k, v, slot_mapping, mu_k, R_k, R_v, cache, num_pages: int,
         _dev(cache, torch.uint8, "cache"), int(num_pages),
         _dev(dbg_rot_k, torch.float32, "dbg_rot_k"), _dev(dbg_rot_v, torch.float32, "dbg_rot_v"),
         _dev(err_count, torch.int32, "err_count"), _stream(stream)))
+
+
+def kvq_append_int2_clip(k, v, slot_mapping, mu_k, R_k, R_v, clip: float, cache, num_pages: int,
+                         dbg_rot_k=None, dbg_rot_v=None, err_count=None, stream=None):
+    """kvq_append_int2 with clip ratio c in (0, 1] (c = 1: the plain call)."""
+    n_tok, h_kv, d = k.shape
+    _check(load().kvq_append_int2_clip(
+        _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"), n_tok, h_kv, d,
+        _dev(slot_mapping, torch.int32, "slot_mapping"), _dev(mu_k, torch.float32, "mu_k"),
+        _dev(R_k, torch.float32, "R_k"), _dev(R_v, torch.float32, "R_v"), float(clip),
+        _dev(cache, torch.uint8, "cache"), int(num_pages),
+        _dev(dbg_rot_k, torch.float32, "dbg_rot_k"), _dev(dbg_rot_v, torch.float32, "dbg_rot_v"),
+        _dev(err_count, torch.int32, "err_count"), _stream(stream)))
+
+
+def kvq_dequant_int2(cache, num_pages: int, H_kv: int, slot_mapping, k_rot=None, v_rot=None, stream=None):
+    """Dequantised rotated vectors [n, H_kv, d] fp32 of the cached tokens at
+    slot_mapping [n]."""
+    n = slot_mapping.shape[0]
+    _check(load().kvq_dequant_int2(
+        _dev(cache, torch.uint8, "cache"), int(num_pages), H_kv, 128, _dev(slot_mapping, torch.int32, "slot_mapping"),
+        n, _dev(k_rot, torch.float32, "k_rot"), _dev(v_rot, torch.float32, "v_rot"), _stream(stream)))
 
 
 def kvq_decode_workspace_bytes(B: int, H_q: int, H_kv: int, max_pages_per_seq: int, num_splits: int = 0) -> int:

@@ -23,7 +23,7 @@ append_int2_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
                    int H_kv, const int32_t* __restrict__ slot_mapping, const float* __restrict__ mu,
                    const float* __restrict__ Rk, const float* __restrict__ Rv, uint8_t* __restrict__ cache,
                    int64_t num_pages, float* __restrict__ dbg_k, float* __restrict__ dbg_v,
-                   int32_t* __restrict__ err_count, int tok_per_cta) {
+                   int32_t* __restrict__ err_count, int tok_per_cta, float clip) {
     griddep_wait();  // k, v, the slot mapping or the cache may come from the previous kernel
     griddep_launch_dependents();
     const int h = blockIdx.y, grp = blockIdx.z;
@@ -83,6 +83,9 @@ append_int2_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
             mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         }
+        // clip ratio c (Q2(.; c, G)): the range ends scale to c*min, c*max
+        mn = __fmul_rn(clip, mn);
+        mx = __fmul_rn(clip, mx);
         const __half sh = f16_sat(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
         const __half mh = f16_sat(mn);
         const float scf = __half2float(sh), mnf = __half2float(mh);
@@ -117,15 +120,17 @@ using namespace kvq;
 
 extern "C" size_t kvq_int2_tile_bytes(int d) { return d == D ? (size_t)INT2_TILE : 0; }
 
-extern "C" kvq_status kvq_append_int2(const void* k, const void* v, int n_tok, int H_kv, int d,
+static kvq_status append_int2_launch(const void* k, const void* v, int n_tok, int H_kv, int d,
                                       const int32_t* slot_mapping, const float* mu_k, const float* R_k,
                                       const float* R_v, void* cache, int64_t num_pages, float* dbg_rot_k,
-                                      float* dbg_rot_v, int32_t* err_count, void* stream) {
+                                      float* dbg_rot_v, int32_t* err_count, float clip, void* stream) {
     if (d != D) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "kvq_append_int2: d=%d (only 128)", d);
     if (n_tok < 0 || H_kv <= 0 || num_pages <= 0)
         return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_append_int2: n_tok=%d H_kv=%d num_pages=%lld", n_tok,
                              H_kv, (long long)num_pages);
     if (H_kv > 65535) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "kvq_append_int2: H_kv=%d too large", H_kv);
+    if (!(clip > 0.f && clip <= 1.f))
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_append_int2: clip ratio %g outside (0, 1]", (double)clip);
     if (n_tok == 0) return KVQ_OK;
     if (!k || !v || !slot_mapping || !mu_k || !R_k || !R_v || !cache)
         return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_append_int2: null pointer");
@@ -143,6 +148,72 @@ extern "C" kvq_status kvq_append_int2(const void* k, const void* v, int n_tok, i
     return kvq_check_cuda(launch_pdl(append_int2_kernel, grid, dim3(64), 0, static_cast<cudaStream_t>(stream),
                                      static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), n_tok,
                                      H_kv, slot_mapping, mu_k, R_k, R_v, static_cast<uint8_t*>(cache), num_pages,
-                                     dbg_rot_k, dbg_rot_v, err_count, per),
+                                     dbg_rot_k, dbg_rot_v, err_count, per, clip),
                           "kvq_append_int2 launch");
+}
+
+extern "C" kvq_status kvq_append_int2(const void* k, const void* v, int n_tok, int H_kv, int d,
+                                      const int32_t* slot_mapping, const float* mu_k, const float* R_k,
+                                      const float* R_v, void* cache, int64_t num_pages, float* dbg_rot_k,
+                                      float* dbg_rot_v, int32_t* err_count, void* stream) {
+    return append_int2_launch(k, v, n_tok, H_kv, d, slot_mapping, mu_k, R_k, R_v, cache, num_pages, dbg_rot_k,
+                              dbg_rot_v, err_count, 1.0f, stream);
+}
+
+extern "C" kvq_status kvq_append_int2_clip(const void* k, const void* v, int n_tok, int H_kv, int d,
+                                           const int32_t* slot_mapping, const float* mu_k, const float* R_k,
+                                           const float* R_v, float clip, void* cache, int64_t num_pages,
+                                           float* dbg_rot_k, float* dbg_rot_v, int32_t* err_count, void* stream) {
+    return append_int2_launch(k, v, n_tok, H_kv, d, slot_mapping, mu_k, R_k, R_v, cache, num_pages, dbg_rot_k,
+                              dbg_rot_v, err_count, clip, stream);
+}
+
+namespace kvq {
+
+// Reads cached tokens back: thread (token, head, side, channel) forms
+// min + code * scale with one fp32 fused multiply-add.
+__global__ void __launch_bounds__(256)
+dequant_int2_kernel(const uint8_t* __restrict__ cache, int64_t num_pages, int H_kv,
+                    const int32_t* __restrict__ slot_mapping, int n, float* __restrict__ k_rot,
+                    float* __restrict__ v_rot) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int t = blockIdx.x, h = blockIdx.y;
+    const int side = threadIdx.x >> 7, j = threadIdx.x & (D - 1);
+    float* dst = side ? v_rot : k_rot;
+    if (!dst) return;
+    const int slot = __ldg(slot_mapping + t);
+    float val = 0.f;
+    if (slot >= 0 && (int64_t)slot < num_pages * PAGE) {
+        const int page = slot / PAGE, s = slot % PAGE;
+        const uint8_t* tile = cache + ((size_t)page * H_kv + h) * INT2_TILE;
+        // channel j = 32 g + 4 b + c sits in byte 4 b + g, bits 2c
+        const int g = j >> 5, b = (j >> 2) & 7, c = j & 3;
+        const int code = (tile[(side ? OFF_VC : OFF_KC) + 32 * s + 4 * b + g] >> (2 * c)) & 3;
+        const uint32_t meta = *reinterpret_cast<const uint32_t*>(tile + (side ? OFF_VM : OFF_KM) + 16 * s + 4 * g);
+        const float sc = __half2float(__ushort_as_half((unsigned short)(meta & 0xffffu)));
+        const float mn = __half2float(__ushort_as_half((unsigned short)(meta >> 16)));
+        val = __fmaf_rn((float)code, sc, mn);
+    }
+    dst[((size_t)t * H_kv + h) * D + j] = val;
+}
+
+}  // namespace kvq
+
+extern "C" kvq_status kvq_dequant_int2(const void* cache, int64_t num_pages, int H_kv, int d,
+                                       const int32_t* slot_mapping, int n, float* k_rot, float* v_rot,
+                                       void* stream) {
+    if (d != D) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "kvq_dequant_int2: d=%d (only 128)", d);
+    if (n < 0 || H_kv <= 0 || H_kv > 65535 || num_pages <= 0 || n > 0x7fffffff)
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_dequant_int2: n=%d H_kv=%d num_pages=%lld", n, H_kv,
+                             (long long)num_pages);
+    if (n == 0) return KVQ_OK;
+    if (!cache || !slot_mapping || (!k_rot && !v_rot))
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_dequant_int2: null pointer");
+    if (reinterpret_cast<uintptr_t>(cache) % 16)
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_dequant_int2: cache not 16-byte aligned");
+    return kvq_check_cuda(launch_pdl(dequant_int2_kernel, dim3(n, H_kv), dim3(256), 0,
+                                     static_cast<cudaStream_t>(stream), static_cast<const uint8_t*>(cache),
+                                     num_pages, H_kv, slot_mapping, n, k_rot, v_rot),
+                          "kvq_dequant_int2 launch");
 }

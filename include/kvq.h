@@ -90,6 +90,30 @@ kvq_status kvq_append_int2(const void* k, const void* v, int n_tok, int H_kv, in
                            float* dbg_rot_k, float* dbg_rot_v, int32_t* err_count,
                            void* stream);
 
+/* kvq_append_int2 with clip ratio c of Q2(.; c, G) ("Output-Aware Rotation
+ * for INT2 KV-Cache Quantization" §3.1, Eq. (4) names c without a value):
+ * each group's range ends scale to c*min and c*max (fp32 products), so
+ * values beyond the clipped range saturate at codes 0 and 3.  0 < clip <= 1;
+ * clip = 1 is kvq_append_int2 exactly.  Other arguments as kvq_append_int2. */
+kvq_status kvq_append_int2_clip(const void* k, const void* v, int n_tok, int H_kv, int d,
+                                const int32_t* slot_mapping, const float* mu_k,
+                                const float* R_k, const float* R_v, float clip,
+                                void* cache, int64_t num_pages,
+                                float* dbg_rot_k, float* dbg_rot_v, int32_t* err_count,
+                                void* stream);
+
+/* Reads cached tokens back: the dequantised rotated key and value vectors
+ * of the tokens at slot_mapping[0..n), each coordinate min + code * scale as
+ * one fp32 fused multiply-add (the Q2(zR) of Eq. (4), still in the rotated
+ * basis: multiply by R^T, and add mu for keys, for the original basis).
+ *   cache         as written by the append calls (num_pages pages)
+ *   slot_mapping  device int32 [n]; a slot outside the cache gives zeros
+ *   k_rot, v_rot  device fp32 [n][H_kv][d], either may be null
+ * Enqueued on `stream`. */
+kvq_status kvq_dequant_int2(const void* cache, int64_t num_pages, int H_kv, int d,
+                            const int32_t* slot_mapping, int n, float* k_rot, float* v_rot,
+                            void* stream);
+
 /* Bytes of decode workspace for B sequences, H_q query heads, H_kv KV heads
  * and num_splits split-K partitions (num_splits = 0: room for the automatic
  * choice of every decode entry point, kvq_decode_attn_int2, its BF16-window
