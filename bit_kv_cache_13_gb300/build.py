@@ -15,7 +15,7 @@ SRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libkvq.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["append_int2.cu", "decode_int2.cu", "decode_int2_noalloc.cu", "bgtq.cu", "host.cpp"]
+SOURCES = ["append_int2.cu", "decode_int2.cu", "decode_int2_noalloc.cu", "bgtq.cu", "bgtq_decode.cu", "host.cpp"]
 
 
 def nvcc() -> str:

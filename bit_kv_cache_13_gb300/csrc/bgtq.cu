@@ -1,5 +1,6 @@
-// Block-GTQ: grouped TQ-MSE key codes with per-RoPE-block widths, uniform
-// TQ-MSE value codes, and fused decode attention over the packed cache.
+// Block-GTQ: quantise-on-append (grouped TQ-MSE key codes with per-RoPE-block
+// widths, uniform TQ-MSE value codes) and the calibration energy scores; the
+// fused decode is in bgtq_decode.cu.
 //
 // "RoPE-Aware Bit Allocation for KV-Cache Quantization":
 //   prerequisites (TQ-MSE): normalise x, rotate by a shared orthogonal Pi,
@@ -7,75 +8,11 @@
 //   method step (3): RoPE blocks of equal width b form one sub-vector (the
 //     blocks' post-RoPE coordinates concatenated) encoded at b bits/dim;
 //   method step (4): values use uniform-width TQ-MSE;
-//   Figure 2: persistent HBM holds packed code streams plus norms; the fused
-//     kernel decodes only the current tile into kernel-local temporaries.
-//
-// Decode works in the TQ basis: <q_b, r c Pi^T> = r <q_b Pi, c>, so each
-// query sub-vector is rotated once per CTA (q~_b = q_b Pi_n), a key
-// contributes r_b * c[code] * q~ per coordinate, and values accumulate
-// sum_s p_s r_s c[code] in the Pi_128 basis, rotated back once at the end.
-#include <mutex>
+//   Figure 2: persistent HBM holds packed code streams plus norms.
 
-#include "merge.cuh"
+#include "bgtq_common.cuh"
 
 namespace kvq {
-
-// Per-head layout of the grouped key sub-vectors (built from the widths).
-struct BgtqLayout {
-    int16_t dim[D];      // gathered position -> original dimension
-    int16_t start[9];    // first position of the width-b group
-    int16_t n[9];        // length of the width-b group (2 * blocks)
-    int16_t bitstart[9]; // first code bit of the width-b group
-    int total_bits;      // sum over positions of the widths
-    int ok;              // widths all in 1..8
-};
-
-// Thread 0 fills the layout: groups in ascending width, blocks ascending
-// inside a group, each block as (dim i, dim i + 64).
-__device__ void build_layout(const int8_t* __restrict__ w, BgtqLayout& L) {
-    int pos = 0, bit = 0, ok = 1;
-    for (int i = 0; i < D / 2; ++i) ok &= (w[i] >= 1 && w[i] <= 8);
-    for (int b = 1; b <= 8; ++b) {
-        L.start[b] = (int16_t)pos;
-        L.bitstart[b] = (int16_t)bit;
-        for (int i = 0; i < D / 2; ++i)
-            if (w[i] == b) {
-                L.dim[pos++] = (int16_t)i;
-                L.dim[pos++] = (int16_t)(i + D / 2);
-            }
-        L.n[b] = (int16_t)(pos - L.start[b]);
-        bit += b * L.n[b];
-    }
-    L.total_bits = bit;
-    L.ok = ok && pos == D;
-}
-
-__host__ __device__ inline int bgtq_kb(int total_bits) { return 4 * ((2 * total_bits + 31) / 32); }
-
-// Scaled codebook fp32(C_b[c] / sqrt(n)), computed in fp64 then rounded once.
-__device__ __forceinline__ float scaled_centroid(const double* __restrict__ cb, int b, int c, int n) {
-    return __double2float_rn(cb[(b - 1) * 256 + c] / sqrt((double)n));
-}
-
-// Number of midpoints (c_k + c_{k+1}) / 2 (exact in fp64) strictly below y:
-// the nearest centroid, ties to the lower index.
-__device__ __forceinline__ int nearest_code(float y, const float* __restrict__ c, int levels) {
-    int lo = 0, hi = levels - 1;
-    const double yd = (double)y;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        const double m = 0.5 * ((double)c[mid] + (double)c[mid + 1]);
-        if (m < yd) lo = mid + 1; else hi = mid;
-    }
-    return lo;
-}
-
-// Group of gathered position p (1..8).
-__device__ __forceinline__ int group_of(const BgtqLayout& L, int p) {
-    int b = 1;
-    while (b < 8 && !(p >= L.start[b] && p < L.start[b] + L.n[b])) ++b;
-    return b;
-}
 
 // ------------------------------------------------------------------ append
 
@@ -180,235 +117,6 @@ bgtq_append_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
     }
 }
 
-// ------------------------------------------------------------------ decode
-
-constexpr int BG_WARPS = 4;
-constexpr int BG_STAGES = 4;
-
-struct BgDecodeSmem {
-    BgtqLayout L;
-    float cb_k[8][256];
-    float cb_v[256];
-    float q[8][D];          // q~ in gathered key order, times scale * log2(e)
-    float qin[8][D];
-    MergeSmem<BG_WARPS, 8> ms;
-    uint64_t bar[BG_WARPS][BG_STAGES];
-    float o_part[BG_WARPS][8][D];
-};
-
-__global__ void __launch_bounds__(128)
-bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G, const uint8_t* __restrict__ cache,
-                   int64_t num_pages, const int32_t* __restrict__ block_table, int max_pages,
-                   const int32_t* __restrict__ context_lens, const int8_t* __restrict__ widths, int total_bits,
-                   int v_bits, const float* __restrict__ pi_table, const int64_t* __restrict__ pi_offsets,
-                   const double* __restrict__ codebooks, float scale_log2, float* __restrict__ out,
-                   uint8_t* __restrict__ ws, int tile_bytes) {
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    BgDecodeSmem& sm = *reinterpret_cast<BgDecodeSmem*>(smem_raw);
-    uint8_t* ring = smem_raw + align_up(sizeof(BgDecodeSmem), 128);
-
-    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z, S = gridDim.x;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    uint32_t* err_word = reinterpret_cast<uint32_t*>(ws);
-
-    int ctx = __ldg(context_lens + b);
-    ctx = max(0, min(ctx, max_pages * PAGE));
-    const int n_pages = (ctx + PAGE - 1) / PAGE;
-    const int pps = (n_pages + S - 1) / S;
-    const int p_begin = min(split * pps, n_pages), p_end = min(p_begin + pps, n_pages);
-    const int my_count = p_end - p_begin > warp ? (p_end - p_begin - warp + BG_WARPS - 1) / BG_WARPS : 0;
-    const int32_t* bt = block_table + (size_t)b * max_pages;
-    uint8_t* my_ring = ring + (size_t)warp * BG_STAGES * tile_bytes;
-
-    if (lane == 0) {
-        for (int s = 0; s < BG_STAGES; ++s) mbar_init(&sm.bar[warp][s], 1);
-        fence_mbar_init();
-        fence_proxy_async_smem();
-    }
-    __syncwarp();
-    auto issue = [&](int i) {  // lane 0 only
-        const int p = p_begin + warp + BG_WARPS * i;
-        const int pid = __ldg(bt + p);
-        uint64_t* bar = &sm.bar[warp][i % BG_STAGES];
-        if (pid < 0 || (int64_t)pid >= num_pages) {
-            atomicOr(err_word, ERR_BAD_PAGE);
-            mbar_arrive(bar);
-        } else {
-            mbar_arrive_expect_tx(bar, tile_bytes);
-            bulk_g2s(my_ring + (size_t)(i % BG_STAGES) * tile_bytes, cache + ((size_t)pid * H_kv + h) * tile_bytes,
-                     tile_bytes, bar);
-        }
-    };
-    if (lane == 0)
-        for (int i = 0; i < min(BG_STAGES, my_count); ++i) issue(i);
-
-    // ---- per-head layout, codebooks and rotated queries
-    if (tid == 0) build_layout(widths + h * (D / 2), sm.L);
-    const __nv_bfloat16* qb = q + ((size_t)b * H_q + (size_t)h * G) * D;
-    for (int idx = tid; idx < G * D; idx += 128) sm.qin[idx / D][idx % D] = __bfloat162float(qb[idx]);
-    __syncthreads();
-    const bool layout_ok = sm.L.ok && sm.L.total_bits <= 2 * total_bits;
-    if (!layout_ok && tid == 0) atomicOr(err_word, ERR_BAD_WIDTHS);
-    for (int idx = tid; idx < 8 * 256; idx += 128) {
-        const int bb = idx / 256 + 1, c = idx % 256;
-        if (c < (1 << bb) && sm.L.n[bb] > 0) sm.cb_k[bb - 1][c] = scaled_centroid(codebooks, bb, c, sm.L.n[bb]);
-    }
-    for (int c = tid; c < (1 << v_bits); c += 128) sm.cb_v[c] = scaled_centroid(codebooks, v_bits, c, D);
-    if (layout_ok) {
-        // q~ at gathered position p = tid: sum_i q[dim(st + i)] Pi_n[i][p - st]
-        const int p = tid;
-        const int bb = group_of(sm.L, p);
-        const int st = sm.L.start[bb], n = sm.L.n[bb], j = p - st;
-        const float* pi = pi_table + __ldg(pi_offsets + n);
-        float acc[8];
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) acc[jj] = 0.f;
-#pragma unroll 16
-        for (int i = 0; i < n; ++i) {
-            const float pv = __ldg(pi + (size_t)i * n + j);
-            const int dm = sm.L.dim[st + i];
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj)
-                if (jj < G) acc[jj] = fmaf(sm.qin[jj][dm], pv, acc[jj]);
-        }
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj)
-            if (jj < G) sm.q[jj][p] = acc[jj] * scale_log2;
-    }
-    __syncthreads();
-
-    const int kb = bgtq_kb(total_bits), vb = 16 * v_bits;
-    const int off_kn = PAGE * kb, off_vc = off_kn + PAGE * 16, off_vn = off_vc + PAGE * vb;
-    const int s_tok = lane & 15, half = lane >> 4;
-    const uint32_t vmask = (1u << v_bits) - 1u;
-
-    float mrun[8], lsum[8], oacc[8][4];
-#pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-        mrun[jj] = -CUDART_INF_F;
-        lsum[jj] = 0.f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) oacc[jj][e] = 0.f;
-    }
-    bool timed_out = false;
-
-    for (int i = 0; i < my_count; ++i) {
-        const int stage = i % BG_STAGES;
-        const uint32_t parity = (i / BG_STAGES) & 1;
-        if (!timed_out) {
-            const bool okw = mbar_wait_bounded(&sm.bar[warp][stage], parity, WAIT_LIMIT_CYCLES);
-            if (__any_sync(0xffffffffu, !okw)) {
-                timed_out = true;
-                if (lane == 0) atomicOr(err_word, ERR_TIMEOUT);
-            }
-        }
-        if (timed_out) break;
-        const uint8_t* tile = my_ring + (size_t)stage * tile_bytes;
-        const int pg = p_begin + warp + BG_WARPS * i;
-        const int pid = __ldg(bt + pg);
-        const bool valid = layout_ok && pid >= 0 && (int64_t)pid < num_pages;
-        const int n_tok = valid ? min(PAGE, ctx - pg * PAGE) : 0;
-
-        // ---- QK: lane = (token s_tok, gathered positions of parity `half`)
-        float dot[8];
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) dot[jj] = 0.f;
-        if (valid) {
-            const uint8_t* rec = tile + s_tok * kb;
-            const __half* kn = reinterpret_cast<const __half*>(tile + off_kn + 16 * s_tok);
-            for (int bb = 1; bb <= 8; ++bb) {
-                const int n = sm.L.n[bb];
-                if (n == 0) continue;
-                const float rb = __half2float(kn[bb - 1]);
-                const int st = sm.L.start[bb], bs = sm.L.bitstart[bb];
-                const uint32_t mask = (1u << bb) - 1u;
-                const float* cb = sm.cb_k[bb - 1];
-                for (int e = half; e < n; e += 2) {
-                    const int bit = bs + e * bb;
-                    const uint32_t lo = lds32(rec + 4 * (bit >> 5)), hi = lds32(rec + 4 * (bit >> 5) + 4);
-                    const uint32_t code = __funnelshift_r(lo, hi, bit & 31) & mask;
-                    const float val = rb * cb[code];
-                    const int p = st + e;
-#pragma unroll
-                    for (int jj = 0; jj < 8; ++jj)
-                        if (jj < G) dot[jj] = fmaf(val, sm.q[jj][p], dot[jj]);
-                }
-            }
-        }
-        // ---- online softmax over the page's 16 tokens (lanes s and s + 16 agree)
-        float pr[8], corr[8];
-        bool need = false;
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-            pr[jj] = 0.f;
-            corr[jj] = 1.f;
-            if (jj >= G) continue;
-            float lg = dot[jj] + __shfl_xor_sync(0xffffffffu, dot[jj], 16);
-            lg = s_tok < n_tok ? lg : -CUDART_INF_F;
-            float pm = lg;
-#pragma unroll
-            for (int o = 1; o < 16; o <<= 1) pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, o));
-            if (pm > mrun[jj]) {
-                corr[jj] = exp2f(mrun[jj] - pm);
-                mrun[jj] = pm;
-                need = true;
-            }
-            const float mref = mrun[jj] == -CUDART_INF_F ? 0.f : mrun[jj];
-            pr[jj] = exp2f(lg - mref);
-            float ps = half == 0 ? pr[jj] : 0.f;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-            lsum[jj] = fmaf(lsum[jj], corr[jj], ps);
-        }
-        if (need) {
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) oacc[jj][e] *= corr[jj];
-        }
-        // ---- PV: lane owns channels 4*lane .. 4*lane+3 (4*v_bits contiguous bits)
-        const int vbit = 4 * lane * v_bits;
-        for (int s = 0; s < n_tok; ++s) {
-            const uint8_t* vrec = tile + off_vc + s * vb;
-            const uint32_t lo = lds32(vrec + 4 * (vbit >> 5));
-            const uint32_t hi = (vbit >> 5) + 1 < vb / 4 ? lds32(vrec + 4 * (vbit >> 5) + 4) : 0u;
-            const uint32_t codes = __funnelshift_r(lo, hi, vbit & 31);
-            const float rv = __half2float(reinterpret_cast<const __half*>(tile + off_vn)[s]);
-            float cv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) cv[e] = sm.cb_v[(codes >> (e * v_bits)) & vmask];
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                if (jj >= G) continue;
-                const float wgt = __shfl_sync(0xffffffffu, pr[jj], s) * rv;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) oacc[jj][e] = fmaf(wgt, cv[e], oacc[jj][e]);
-            }
-        }
-        __syncwarp();
-        if (lane == 0 && i + BG_STAGES < my_count) {
-            fence_proxy_async_smem();
-            issue(i + BG_STAGES);
-        }
-    }
-    if (timed_out && lane == 0)
-        for (int s = 0; s < BG_STAGES; ++s) (void)mbar_wait_bounded(&sm.bar[warp][s], 0, 1000000LL);
-
-#pragma unroll
-    for (int jj = 0; jj < 8; ++jj)
-        if (jj < G) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sm.o_part[warp][jj][4 * lane + e] = oacc[jj][e];
-            if (lane == 0) {
-                sm.ms.m_part[warp][jj] = mrun[jj];
-                sm.ms.l_part[warp][jj] = lsum[jj];
-            }
-        }
-    __syncthreads();
-    finish_decode<BG_WARPS, 8>(sm.ms, sm.o_part, G, H_q, H_kv, gridDim.z, b, h, split, S, ws,
-                               pi_table + __ldg(pi_offsets + D), out);
-}
-
 // ------------------------------------------------------------- calibration
 
 // Method step (1): s_{h,i} = 1/2 E_{t,g in G(h)} ||q_{t,g}(i)||^2 +
@@ -494,8 +202,7 @@ extern "C" kvq_status bgtq_energy_scores(const void* q, const void* k, int T, in
                           "bgtq_energy_scores launch");
 }
 
-static kvq_status check_bgtq_common(const char* fn, int d, int H_kv, int total_bits, int v_bits,
-                                    const float* pi_table) {
+kvq_status bgtq_check_common(const char* fn, int d, int H_kv, int total_bits, int v_bits, const float* pi_table) {
     if (d != D) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "%s: d=%d (only 128)", fn, d);
     if (H_kv <= 0 || H_kv > 65535) return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: H_kv=%d", fn, H_kv);
     if (bgtq_tile_bytes(total_bits, v_bits) == 0)
@@ -510,7 +217,7 @@ extern "C" kvq_status bgtq_append(const void* k, const void* v, int n_tok, int H
                                   const int8_t* widths, int total_bits, int v_bits, const float* pi_table,
                                   const int64_t* pi_offsets, const double* codebooks, void* cache, int64_t num_pages,
                                   int32_t* err_count, void* stream) {
-    kvq_status st = check_bgtq_common("bgtq_append", d, H_kv, total_bits, v_bits, pi_table);
+    kvq_status st = bgtq_check_common("bgtq_append", d, H_kv, total_bits, v_bits, pi_table);
     if (st != KVQ_OK) return st;
     if (n_tok < 0 || num_pages <= 0)
         return kvq_set_error(KVQ_ERR_INVALID_ARG, "bgtq_append: n_tok=%d num_pages=%lld", n_tok, (long long)num_pages);
@@ -529,56 +236,4 @@ extern "C" kvq_status bgtq_append(const void* k, const void* v, int n_tok, int H
         total_bits, v_bits, pi_table, pi_offsets, codebooks, static_cast<uint8_t*>(cache), num_pages, err_count, per,
         tile);
     return kvq_check_cuda(cudaGetLastError(), "bgtq_append launch");
-}
-
-extern "C" kvq_status bgtq_decode_attn(const void* q, int B, int H_q, int H_kv, int d, const void* cache,
-                                       int64_t num_pages, const int32_t* block_table, int max_pages_per_seq,
-                                       const int32_t* context_lens, const int8_t* widths, int total_bits, int v_bits,
-                                       const float* pi_table, const int64_t* pi_offsets, const double* codebooks,
-                                       float scale, float* out, void* workspace, size_t workspace_bytes,
-                                       int num_splits, void* stream) {
-    kvq_status st = check_bgtq_common("bgtq_decode_attn", d, H_kv, total_bits, v_bits, pi_table);
-    if (st != KVQ_OK) return st;
-    if (B <= 0 || B > 65535 || H_q <= 0 || H_q % H_kv || max_pages_per_seq <= 0 || num_pages <= 0 || num_splits < 0)
-        return kvq_set_error(KVQ_ERR_INVALID_ARG, "bgtq_decode_attn: B=%d H_q=%d H_kv=%d max_pages=%d", B, H_q, H_kv,
-                             max_pages_per_seq);
-    const int G = H_q / H_kv;
-    if (G > 8) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "bgtq_decode_attn: GQA group %d > 8", G);
-    if (!q || !cache || !block_table || !context_lens || !widths || !pi_table || !pi_offsets || !codebooks || !out ||
-        !workspace)
-        return kvq_set_error(KVQ_ERR_INVALID_ARG, "bgtq_decode_attn: null pointer");
-    if (reinterpret_cast<uintptr_t>(cache) % 16 || reinterpret_cast<uintptr_t>(workspace) % 16)
-        return kvq_set_error(KVQ_ERR_INVALID_ARG, "bgtq_decode_attn: cache and workspace need 16-byte alignment");
-    const int S = num_splits > 0 ? num_splits : bgtq_decode_auto_splits(B, H_kv, max_pages_per_seq);
-    if (S > MAX_SPLITS)
-        return kvq_set_error(KVQ_ERR_INVALID_ARG, "bgtq_decode_attn: num_splits=%d above %d", S, MAX_SPLITS);
-    const size_t need = kvq_decode_workspace_bytes(B, H_q, H_kv, max_pages_per_seq, S);
-    if (workspace_bytes < need)
-        return kvq_set_error(KVQ_ERR_WORKSPACE, "bgtq_decode_attn: workspace %zu < %zu bytes", workspace_bytes, need);
-    const int tile = (int)bgtq_tile_bytes(total_bits, v_bits);
-    const size_t smem = align_up(sizeof(BgDecodeSmem), 128) + (size_t)BG_WARPS * BG_STAGES * tile;
-    {
-        // opt in once per device, to the largest tile any width budget gives
-        static std::mutex mu;
-        static bool done[64] = {};
-        int dev = 0;
-        kvq_status s2 = kvq_check_cuda(cudaGetDevice(&dev), "bgtq_decode_attn: cudaGetDevice");
-        if (s2 != KVQ_OK) return s2;
-        std::lock_guard<std::mutex> lock(mu);
-        if (dev < 0 || dev >= 64 || !done[dev]) {
-            const size_t max_smem =
-                align_up(sizeof(BgDecodeSmem), 128) + (size_t)BG_WARPS * BG_STAGES * bgtq_tile_bytes(512, 8);
-            s2 = kvq_check_cuda(
-                cudaFuncSetAttribute(bgtq_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem),
-                "bgtq_decode_attn smem attribute");
-            if (s2 != KVQ_OK) return s2;
-            if (dev >= 0 && dev < 64) done[dev] = true;
-        }
-    }
-    dim3 grid(S, H_kv, B);
-    bgtq_decode_kernel<<<grid, 128, smem, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const __nv_bfloat16*>(q), H_q, H_kv, G, static_cast<const uint8_t*>(cache), num_pages, block_table,
-        max_pages_per_seq, context_lens, widths, total_bits, v_bits, pi_table, pi_offsets, codebooks,
-        scale * 1.4426950408889634f, out, static_cast<uint8_t*>(workspace), tile);
-    return kvq_check_cuda(cudaGetLastError(), "bgtq_decode_attn launch");
 }

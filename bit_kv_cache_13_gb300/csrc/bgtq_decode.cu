@@ -1,0 +1,428 @@
+// Fused decode attention over the packed Block-GTQ cache.
+//
+// "RoPE-Aware Bit Allocation for KV-Cache Quantization", Figure 2 and core
+// method: the kernel reads only the packed code streams and fp16 norms of
+// the current tile and decodes them in registers.  Decode works in the TQ
+// basis, <q_b, r c Pi^T> = r <q_b Pi, c>: each query sub-vector is rotated
+// once per CTA (q~_b = q_b Pi_n), a key contributes r_b C_b[code] q~ per
+// coordinate, and values accumulate sum_s p_s r_s C_v[code] in the Pi_128
+// basis, rotated back once at the end.
+//
+// Grid (split, kv_head, seq) with one CTA per SM (12 warps for head groups
+// up to 4, 8 for groups of 8); the pages of a (sequence, KV head) are dealt
+// round-robin over all warps of its CTAs and streamed through per-warp rings
+// of bulk async copies, as in the INT2 decode.  Per page (16 tokens):
+//   QK  lane l owns gathered positions 4l .. 4l+3 (two RoPE blocks).  Their
+//       q~ for every head stays in registers, and their four codes are
+//       contiguous bits of a token's stream (groups are laid out in
+//       ascending width), cut out by one funnel shift and four bit-field
+//       extracts.  C_b[code] comes from the shared-memory codebook and is
+//       scaled by the token's group norm r_b.  The lanes' partial dots of 8
+//       tokens at a time go through a padded shared-memory transpose and are
+//       summed by column, which leaves each lane the logit of one token for
+//       one head (two heads for groups of 8).
+//   softmax  online, base 2, exact running maximum per head.
+//   PV  lane l owns channels 4l .. 4l+3: four codes cut from the value
+//       stream, C_v[code] r_v weighted by p of every head, fp32 fma.
+#include <mutex>
+
+#include "bgtq_common.cuh"
+
+namespace kvq {
+
+constexpr int BG_MAX_STAGES = 8;
+
+template <int MAXG>
+struct BgWarps {
+    static constexpr int NW = MAXG <= 4 ? 12 : 8;
+};
+
+// values per lane after one 8-token transpose, and the transpose row length
+// (padded so that the rows of 8 consecutive lanes fall in distinct banks)
+template <int MAXG>
+struct BgTr {
+    static constexpr int VPL = MAXG / 4;
+    static constexpr int W = 8 * MAXG + 4;
+};
+
+template <int NW, int MAXG>
+struct __align__(16) BgDecodeSmem {
+    union {
+        float tr[NW][32][BgTr<MAXG>::W];  // per-warp transpose of partial dots
+        float o_part[NW][MAXG][D];        // per-warp o' after the loop
+    } u;
+    float pb[NW][PAGE][MAXG];  // softmax weights of the warp's current page
+    float qt[MAXG][D];         // q~ in gathered order, times scale * log2(e)
+    float qin[MAXG][D];
+    float cb_k[8][256];        // C_b / sqrt(n_b) per width b (fp32)
+    float cb_v[256];           // C_v / sqrt(128)
+    uint64_t bar[NW][BG_MAX_STAGES];
+    int ntok[NW][BG_MAX_STAGES];
+    BgtqLayout L;
+    MergeSmem<NW, MAXG> ms;
+};
+
+__device__ __forceinline__ uint32_t bfe(uint32_t x, uint32_t pos, uint32_t len) {
+    uint32_t y;
+    asm("bfe.u32 %0, %1, %2, %3;" : "=r"(y) : "r"(x), "r"(pos), "r"(len));
+    return y;
+}
+
+template <int MAXG>
+__global__ void __launch_bounds__(BgWarps<MAXG>::NW * 32, 1)
+bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G, const uint8_t* __restrict__ cache,
+                   int64_t num_pages, const int32_t* __restrict__ block_table, int max_pages,
+                   const int32_t* __restrict__ context_lens, const int8_t* __restrict__ widths, int total_bits,
+                   int v_bits, const float* __restrict__ pi_table, const int64_t* __restrict__ pi_offsets,
+                   const double* __restrict__ codebooks, float scale_log2, float* __restrict__ out,
+                   uint8_t* __restrict__ ws, int n_stages) {
+    constexpr int NW = BgWarps<MAXG>::NW;
+    constexpr int VPL = BgTr<MAXG>::VPL;
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    BgDecodeSmem<NW, MAXG>& sm = *reinterpret_cast<BgDecodeSmem<NW, MAXG>*>(smem_raw);
+    const BgtqTile tl(total_bits, v_bits);
+    uint8_t* my_ring = smem_raw + align_up(sizeof(BgDecodeSmem<NW, MAXG>), 128) +
+                       (size_t)(threadIdx.x >> 5) * n_stages * tl.bytes;
+
+    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int S = gridDim.x, B = gridDim.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint32_t* err_word = reinterpret_cast<uint32_t*>(ws);
+
+    griddep_wait();  // every input may come from the previous kernel in the stream
+    int ctx = __ldg(context_lens + b);
+    ctx = max(0, min(ctx, max_pages * PAGE));
+    const int n_pages = (ctx + PAGE - 1) / PAGE;
+    const int32_t* bt = block_table + (size_t)b * max_pages;
+    // pages dealt round-robin over all S * NW warps of the (sequence, KV head)
+    const int KS = S * NW, k0 = split * NW + warp;
+    const int my_count = n_pages > k0 ? (n_pages - k0 + KS - 1) / KS : 0;
+    auto page_of = [&](int j) { return k0 + KS * j; };
+
+    if (lane == 0) {
+        for (int s = 0; s < n_stages; ++s) mbar_init(&sm.bar[warp][s], 1);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    __syncwarp();
+    auto issue = [&](int i, int p, int pid) {  // lane 0 only
+        const int st = i % n_stages;
+        uint64_t* bar = &sm.bar[warp][st];
+        if (pid < 0 || (int64_t)pid >= num_pages) {
+            atomicOr(err_word, ERR_BAD_PAGE);
+            sm.ntok[warp][st] = 0;
+            mbar_arrive(bar);
+        } else {
+            sm.ntok[warp][st] = min(PAGE, ctx - p * PAGE);
+            mbar_arrive_expect_tx(bar, tl.bytes);
+            bulk_g2s(my_ring + (size_t)st * tl.bytes, cache + ((size_t)pid * H_kv + h) * tl.bytes, tl.bytes, bar);
+        }
+    };
+    int pid_next = 0;
+    if (lane == 0) {
+        for (int j = 0; j < n_stages && j < my_count; ++j) issue(j, page_of(j), __ldg(bt + page_of(j)));
+        if (n_stages < my_count) pid_next = __ldg(bt + page_of(n_stages));
+    }
+    {
+        // the block table and the output rotation are read later: have L2 keep them
+        const char* btc = reinterpret_cast<const char*>(bt);
+        const int lines = (n_pages * 4 + 127) / 128;
+        for (int l = split * NW * 32 + tid; l < lines; l += S * NW * 32) prefetch_l2_keep(btc + 128 * l);
+        const char* rot = reinterpret_cast<const char*>(pi_table + __ldg(pi_offsets + D));
+        for (int l = tid; l < D * D * 4 / 128; l += NW * 32) prefetch_l2_keep(rot + 128 * l);
+    }
+
+    // ---- per-head layout, codebooks and rotated queries
+    if (tid == 0) build_layout(widths + h * (D / 2), sm.L);
+    const __nv_bfloat16* qb = q + ((size_t)b * H_q + (size_t)h * G) * D;
+    for (int idx = tid; idx < G * D; idx += NW * 32) sm.qin[idx / D][idx % D] = __bfloat162float(qb[idx]);
+    __syncthreads();
+    const bool layout_ok = sm.L.ok && sm.L.total_bits <= 2 * total_bits;
+    if (!layout_ok && tid == 0) atomicOr(err_word, ERR_BAD_WIDTHS);
+    for (int idx = tid; idx < 8 * 256; idx += NW * 32) {
+        const int bb = idx / 256 + 1, c = idx % 256;
+        if (c < (1 << bb) && sm.L.n[bb] > 0) sm.cb_k[bb - 1][c] = scaled_centroid(codebooks, bb, c, sm.L.n[bb]);
+    }
+    for (int c = tid; c < (1 << v_bits); c += NW * 32) sm.cb_v[c] = scaled_centroid(codebooks, v_bits, c, D);
+    if (tid < D) {
+        // q~ at gathered position p = tid: sum_i q[dim(st + i)] Pi_n[i][p - st]
+        const int p = tid;
+        float acc[MAXG];
+#pragma unroll
+        for (int jj = 0; jj < MAXG; ++jj) acc[jj] = 0.f;
+        if (layout_ok) {
+            const int bb = group_of(sm.L, p);
+            const int st = sm.L.start[bb], n = sm.L.n[bb], j = p - st;
+            const float* pi = pi_table + __ldg(pi_offsets + n);
+#pragma unroll 16
+            for (int i = 0; i < n; ++i) {
+                const float pv = __ldg(pi + (size_t)i * n + j);
+                const int dm = sm.L.dim[st + i];
+#pragma unroll
+                for (int jj = 0; jj < MAXG; ++jj)
+                    if (jj < G) acc[jj] = fmaf(sm.qin[jj][dm], pv, acc[jj]);
+            }
+        }
+#pragma unroll
+        for (int jj = 0; jj < MAXG; ++jj) sm.qt[jj][p] = jj < G ? acc[jj] * scale_log2 : 0.f;
+    }
+    __syncthreads();
+
+    // ---- this lane's key positions 4l .. 4l+3: blocks A (4l, 4l+1) and B
+    const int p0 = 4 * lane;
+    int wA = 1, wB = 1, bitA = 0;
+    if (layout_ok) {
+        wA = group_of(sm.L, p0);
+        wB = group_of(sm.L, p0 + 2);
+        bitA = sm.L.bitstart[wA] + (p0 - sm.L.start[wA]) * wA;
+    }
+    const int kwi = bitA >> 5, ksh = bitA & 31;
+    const uint32_t posB0 = 2 * wA, posB1 = 2 * wA + wB;
+    const float* cbA = sm.cb_k[wA - 1];
+    const float* cbB = sm.cb_k[wB - 1];
+    float qv[MAXG][4];
+#pragma unroll
+    for (int jj = 0; jj < MAXG; ++jj)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) qv[jj][e] = sm.qt[jj][p0 + e];
+    // ---- this lane's value channels 4l .. 4l+3 (4 v_bits contiguous bits)
+    const int vbit = 4 * v_bits * lane;
+    const int vwi = vbit >> 5, vsh = vbit & 31;
+
+    float o[MAXG][4];
+    float mrun[VPL], lsum[VPL];
+#pragma unroll
+    for (int jj = 0; jj < MAXG; ++jj)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[jj][e] = 0.f;
+#pragma unroll
+    for (int e = 0; e < VPL; ++e) {
+        mrun[e] = -CUDART_INF_F;
+        lsum[e] = 0.f;
+    }
+    float(*tr)[BgTr<MAXG>::W] = sm.u.tr[warp];
+    bool timed_out = false;
+
+    for (int i = 0; i < my_count; ++i) {
+        const int stage = i % n_stages;
+        const bool ok = mbar_wait_bounded(&sm.bar[warp][stage], (i / n_stages) & 1, WAIT_LIMIT_CYCLES);
+        if (__any_sync(0xffffffffu, !ok)) {
+            timed_out = true;
+            if (lane == 0) atomicOr(err_word, ERR_TIMEOUT);
+            break;
+        }
+        const uint8_t* tile = my_ring + (size_t)stage * tl.bytes;
+        const int n_tok = layout_ok ? sm.ntok[warp][stage] : 0;
+
+        // ---- QK, 8 tokens at a time: partial dots -> transpose -> column sums
+        float lg[2][VPL];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll 2
+            for (int u = 0; u < 8; ++u) {
+                const int s = 8 * half + u;
+                float part[MAXG];
+                if (s < n_tok) {
+                    const uint32_t* rec = reinterpret_cast<const uint32_t*>(tile + s * tl.kb);
+                    const uint32_t x = __funnelshift_r(rec[kwi], rec[kwi + 1], ksh);
+                    const __half* nr = reinterpret_cast<const __half*>(tile + tl.off_kn + 16 * s);
+                    const float rA = __half2float(nr[wA - 1]), rB = __half2float(nr[wB - 1]);
+                    const float v0 = cbA[bfe(x, 0, wA)] * rA, v1 = cbA[bfe(x, wA, wA)] * rA;
+                    const float v2 = cbB[bfe(x, posB0, wB)] * rB, v3 = cbB[bfe(x, posB1, wB)] * rB;
+#pragma unroll
+                    for (int jj = 0; jj < MAXG; ++jj)
+                        part[jj] = fmaf(qv[jj][0], v0, fmaf(qv[jj][1], v1, fmaf(qv[jj][2], v2, qv[jj][3] * v3)));
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < MAXG; ++jj) part[jj] = 0.f;
+                }
+#pragma unroll
+                for (int c = 0; c < MAXG; c += 4)
+                    *reinterpret_cast<float4*>(&tr[lane][u * MAXG + c]) =
+                        make_float4(part[c], part[c + 1], part[c + 2], part[c + 3]);
+            }
+            __syncwarp();
+            // lane l sums column VPL*l + e over the 32 rows: token 8*half + l/4,
+            // head VPL*(l%4) + e
+            float acc[VPL];
+#pragma unroll
+            for (int e = 0; e < VPL; ++e) acc[e] = 0.f;
+#pragma unroll 8
+            for (int m = 0; m < 32; ++m) {
+                if constexpr (VPL == 1) {
+                    acc[0] += tr[m][lane];
+                } else {
+                    const float2 t2 = *reinterpret_cast<const float2*>(&tr[m][2 * lane]);
+                    acc[0] += t2.x;
+                    acc[1] += t2.y;
+                }
+            }
+            __syncwarp();
+            const int s = 8 * half + (lane >> 2);
+#pragma unroll
+            for (int e = 0; e < VPL; ++e) lg[half][e] = s < n_tok ? acc[e] : -CUDART_INF_F;
+        }
+
+        // ---- online softmax (base 2): this lane's heads VPL*(l%4) + e
+        float corr[VPL];
+        bool need = false;
+#pragma unroll
+        for (int e = 0; e < VPL; ++e) {
+            float pm = fmaxf(lg[0][e], lg[1][e]);
+            pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
+            pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
+            pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+            corr[e] = 1.f;
+            if (pm > mrun[e]) {
+                corr[e] = ex2(mrun[e] - pm);
+                mrun[e] = pm;
+                need = true;
+            }
+            const float mref = mrun[e] == -CUDART_INF_F ? 0.f : mrun[e];
+            const int jj = VPL * (lane & 3) + e;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const float p = ex2(lg[half][e] - mref);
+                lsum[e] = fmaf(lsum[e], half == 0 ? corr[e] : 1.f, p);
+                sm.pb[warp][8 * half + (lane >> 2)][jj] = p;
+            }
+        }
+        if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+            for (int jj = 0; jj < MAXG; ++jj) {
+                const float c = __shfl_sync(0xffffffffu, corr[jj % VPL], jj / VPL);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[jj][e] *= c;
+            }
+        }
+        __syncwarp();
+
+        // ---- PV: this lane's channels 4l .. 4l+3
+        for (int s = 0; s < n_tok; ++s) {
+            const uint32_t* vr = reinterpret_cast<const uint32_t*>(tile + tl.off_vc + s * tl.vb);
+            const uint32_t x = __funnelshift_r(vr[vwi], vr[vwi + 1], vsh);
+            const float rv = __half2float(reinterpret_cast<const __half*>(tile + tl.off_vn)[s]);
+            float cv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) cv[e] = sm.cb_v[bfe(x, e * v_bits, v_bits)];
+#pragma unroll
+            for (int c = 0; c < MAXG; c += 4) {
+                const float4 p4 = *reinterpret_cast<const float4*>(&sm.pb[warp][s][c]);
+                const float w[4] = {p4.x * rv, p4.y * rv, p4.z * rv, p4.w * rv};
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[c + u][e] = fmaf(w[u], cv[e], o[c + u][e]);
+            }
+        }
+
+        __syncwarp();
+        if (lane == 0 && i + n_stages < my_count) {
+            fence_proxy_async_smem();
+            issue(i + n_stages, page_of(i + n_stages), pid_next);
+            if (i + n_stages + 1 < my_count) pid_next = __ldg(bt + page_of(i + n_stages + 1));
+        }
+    }
+    if (timed_out && lane == 0)
+        for (int s = 0; s < n_stages; ++s) (void)mbar_wait_bounded(&sm.bar[warp][s], 0, 1000000LL);
+    griddep_launch_dependents();
+
+    // ---- warp partial: normalisers summed over the lanes of each head
+#pragma unroll
+    for (int e = 0; e < VPL; ++e) {
+        lsum[e] += __shfl_xor_sync(0xffffffffu, lsum[e], 4);
+        lsum[e] += __shfl_xor_sync(0xffffffffu, lsum[e], 8);
+        lsum[e] += __shfl_xor_sync(0xffffffffu, lsum[e], 16);
+    }
+    __syncthreads();  // all warps are done with the transpose buffers (o_part aliases them)
+#pragma unroll
+    for (int jj = 0; jj < MAXG; ++jj)
+        if (jj < G) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sm.u.o_part[warp][jj][4 * lane + e] = o[jj][e];
+        }
+    if (lane < 4) {
+#pragma unroll
+        for (int e = 0; e < VPL; ++e) {
+            const int jj = VPL * lane + e;
+            if (jj < G) {
+                sm.ms.m_part[warp][jj] = mrun[e];
+                sm.ms.l_part[warp][jj] = lsum[e];
+            }
+        }
+    }
+    __syncthreads();
+    finish_decode<NW, MAXG>(sm.ms, sm.u.o_part, G, H_q, H_kv, B, b, h, split, S, ws, pi_table + __ldg(pi_offsets + D),
+                            out);
+}
+
+}  // namespace kvq
+
+using namespace kvq;
+
+// one CTA per SM, as the INT2 decode (kvq_decode_auto_splits)
+int bgtq_decode_auto_splits(int B, int H_q, int H_kv, int max_pages_per_seq) {
+    return kvq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
+}
+
+extern "C" kvq_status bgtq_decode_attn(const void* q, int B, int H_q, int H_kv, int d, const void* cache,
+                                       int64_t num_pages, const int32_t* block_table, int max_pages_per_seq,
+                                       const int32_t* context_lens, const int8_t* widths, int total_bits, int v_bits,
+                                       const float* pi_table, const int64_t* pi_offsets, const double* codebooks,
+                                       float scale, float* out, void* workspace, size_t workspace_bytes,
+                                       int num_splits, void* stream) {
+    kvq_status st = bgtq_check_common("bgtq_decode_attn", d, H_kv, total_bits, v_bits, pi_table);
+    if (st != KVQ_OK) return st;
+    if (B <= 0 || B > 65535 || H_q <= 0 || H_q % H_kv || max_pages_per_seq <= 0 || num_pages <= 0 || num_splits < 0)
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "bgtq_decode_attn: B=%d H_q=%d H_kv=%d max_pages=%d", B, H_q, H_kv,
+                             max_pages_per_seq);
+    const int G = H_q / H_kv;
+    if (G > 8) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "bgtq_decode_attn: GQA group %d > 8", G);
+    if (!q || !cache || !block_table || !context_lens || !widths || !pi_table || !pi_offsets || !codebooks || !out ||
+        !workspace)
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "bgtq_decode_attn: null pointer");
+    if (reinterpret_cast<uintptr_t>(cache) % 16 || reinterpret_cast<uintptr_t>(workspace) % 16)
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "bgtq_decode_attn: cache and workspace need 16-byte alignment");
+    const int S = num_splits > 0 ? num_splits : bgtq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
+    if (S > MAX_SPLITS)
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "bgtq_decode_attn: num_splits=%d above %d", S, MAX_SPLITS);
+    const size_t need = kvq_decode_workspace_bytes(B, H_q, H_kv, max_pages_per_seq, S);
+    if (workspace_bytes < need)
+        return kvq_set_error(KVQ_ERR_WORKSPACE, "bgtq_decode_attn: workspace %zu < %zu bytes", workspace_bytes, need);
+
+    const int tile = (int)bgtq_tile_bytes(total_bits, v_bits);
+    constexpr size_t kSmemMax = 227 * 1024;
+    const bool small = G <= 4;
+    const int NW = small ? BgWarps<4>::NW : BgWarps<8>::NW;
+    const size_t fixed = align_up(small ? sizeof(BgDecodeSmem<BgWarps<4>::NW, 4>) : sizeof(BgDecodeSmem<BgWarps<8>::NW, 8>),
+                                  128);
+    int n_stages = (int)((kSmemMax - fixed) / ((size_t)NW * tile));
+    n_stages = n_stages > BG_MAX_STAGES ? BG_MAX_STAGES : n_stages;
+    if (n_stages < 2)
+        return kvq_set_error(KVQ_ERR_UNSUPPORTED, "bgtq_decode_attn: %d-byte tiles leave no room for two stages", tile);
+    const size_t smem = fixed + (size_t)NW * n_stages * tile;
+    const void* fn = small ? (const void*)bgtq_decode_kernel<4> : (const void*)bgtq_decode_kernel<8>;
+    {
+        // opt in once per device and kernel, to the full shared-memory size
+        static std::mutex mu;
+        static bool done[64][2] = {};
+        int dev = 0;
+        kvq_status s2 = kvq_check_cuda(cudaGetDevice(&dev), "bgtq_decode_attn: cudaGetDevice");
+        if (s2 != KVQ_OK) return s2;
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 0 || dev >= 64 || !done[dev][small ? 0 : 1]) {
+            s2 = kvq_check_cuda(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMax),
+                                "bgtq_decode_attn smem attribute");
+            if (s2 != KVQ_OK) return s2;
+            if (dev >= 0 && dev < 64) done[dev][small ? 0 : 1] = true;
+        }
+    }
+    dim3 grid(S, H_kv, B);
+    const cudaError_t e =
+        launch_pdl(small ? bgtq_decode_kernel<4> : bgtq_decode_kernel<8>, grid, dim3(NW * 32), smem,
+                   static_cast<cudaStream_t>(stream), static_cast<const __nv_bfloat16*>(q), H_q, H_kv, G,
+                   static_cast<const uint8_t*>(cache), num_pages, block_table, max_pages_per_seq, context_lens, widths,
+                   total_bits, v_bits, pi_table, pi_offsets, codebooks, scale * 1.4426950408889634f, out,
+                   static_cast<uint8_t*>(workspace), n_stages);
+    return kvq_check_cuda(e, "bgtq_decode_attn launch");
+}

@@ -645,25 +645,12 @@ extern "C" int kvq_decode_auto_splits(int B, int H_q, int H_kv, int max_pages_pe
     return (int)s;
 }
 
-// The Block-GTQ decode runs 4-warp CTAs, several per SM: its automatic
-// split count aims at three CTAs per SM, at least 16 pages per split.
-int bgtq_decode_auto_splits(int B, int H_kv, int max_pages_per_seq) {
-    if (B <= 0 || H_kv <= 0 || max_pages_per_seq <= 0) return 1;
-    const long units = (long)B * H_kv;
-    long s = (152L * 3 + units - 1) / units;
-    long max_s = (max_pages_per_seq + 15) / 16;
-    if (max_s > MAX_SPLITS) max_s = MAX_SPLITS;
-    if (s > max_s) s = max_s;
-    if (s < 1) s = 1;
-    return (int)s;
-}
-
 extern "C" size_t kvq_decode_workspace_bytes(int B, int H_q, int H_kv, int max_pages_per_seq, int num_splits) {
     if (B <= 0 || H_q <= 0 || H_kv <= 0) return 0;
     int S = num_splits;
     if (S <= 0) {  // room for the automatic choice of every decode entry point
         S = kvq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq) + 1;  // + 1: a BF16 window split
-        const int Sb = bgtq_decode_auto_splits(B, H_kv, max_pages_per_seq);
+        const int Sb = bgtq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
         if (Sb > S) S = Sb;
     }
     return WS_HEADER + tickets_bytes(B, H_kv) + (size_t)B * H_q * S * PART_STRIDE * sizeof(float);

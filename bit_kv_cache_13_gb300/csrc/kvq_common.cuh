@@ -49,9 +49,8 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 
 }  // namespace kvq
 
-// Automatic split count of the Block-GTQ decode (host; defined beside the
-// INT2 rule, which kvq_decode_auto_splits exports).
-int bgtq_decode_auto_splits(int B, int H_kv, int max_pages_per_seq);
+// Automatic split count of the Block-GTQ decode (host).
+int bgtq_decode_auto_splits(int B, int H_q, int H_kv, int max_pages_per_seq);
 
 namespace kvq {
 
