@@ -258,7 +258,7 @@ def measure_bgtq(device, stream, reps):
             "ms_per_decode": round(ms, 4), "value": round(gbs, 2), "unit": "GB/s",
             "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4), "peak_kind": kind,
-                         "traffic": profiled_traffic("bgtq_decode", ("bgtq.cu", "merge.cuh", "kvq_common.cuh"),
+                         "traffic": profiled_traffic("bgtq_decode", ("bgtq_decode.cu", "bgtq_common.cuh", "merge.cuh", "kvq_common.cuh"),
                                                      units)},
             "l2": "256 MB buffer written before every timed launch"}
 

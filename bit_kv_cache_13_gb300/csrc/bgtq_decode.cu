@@ -31,6 +31,9 @@
 namespace kvq {
 
 constexpr int BG_MAX_STAGES = 8;
+// Codebook rows 264 floats apart: width b's table starts 8(b-1) banks on, so
+// lanes of different widths reading small codes hit different banks.
+constexpr int BG_CB_STRIDE = 264;
 
 template <int MAXG>
 struct BgWarps {
@@ -54,7 +57,7 @@ struct __align__(16) BgDecodeSmem {
     float pb[NW][PAGE][MAXG];  // softmax weights of the warp's current page
     float qt[MAXG][D];         // q~ in gathered order, times scale * log2(e)
     float qin[MAXG][D];
-    float cb_k[8][256];        // C_b / sqrt(n_b) per width b (fp32)
+    float cb_k[8][BG_CB_STRIDE];  // C_b / sqrt(n_b) per width b (fp32), rows bank-skewed
     float cb_v[256];           // C_v / sqrt(128)
     uint64_t bar[NW][BG_MAX_STAGES];
     int ntok[NW][BG_MAX_STAGES];
@@ -215,31 +218,45 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         const int n_tok = layout_ok ? sm.ntok[warp][stage] : 0;
 
         // ---- QK, 8 tokens at a time: partial dots -> transpose -> column sums
+        auto partial = [&](int s, float (&part)[MAXG]) {
+            const uint32_t* rec = reinterpret_cast<const uint32_t*>(tile + s * tl.kb);
+            const uint32_t x = __funnelshift_r(rec[kwi], rec[kwi + 1], ksh);
+            const __half* nr = reinterpret_cast<const __half*>(tile + tl.off_kn + 16 * s);
+            const float rA = __half2float(nr[wA - 1]), rB = __half2float(nr[wB - 1]);
+            const float v0 = cbA[bfe(x, 0, wA)] * rA, v1 = cbA[bfe(x, wA, wA)] * rA;
+            const float v2 = cbB[bfe(x, posB0, wB)] * rB, v3 = cbB[bfe(x, posB1, wB)] * rB;
+#pragma unroll
+            for (int jj = 0; jj < MAXG; ++jj)
+                part[jj] = fmaf(qv[jj][0], v0, fmaf(qv[jj][1], v1, fmaf(qv[jj][2], v2, qv[jj][3] * v3)));
+        };
+        auto store = [&](int u, const float (&part)[MAXG]) {
+#pragma unroll
+            for (int c = 0; c < MAXG; c += 4)
+                *reinterpret_cast<float4*>(&tr[lane][u * MAXG + c]) =
+                    make_float4(part[c], part[c + 1], part[c + 2], part[c + 3]);
+        };
+        const bool full = n_tok == PAGE;  // warp-uniform: every page but a sequence's last
         float lg[2][VPL];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-#pragma unroll 2
-            for (int u = 0; u < 8; ++u) {
-                const int s = 8 * half + u;
-                float part[MAXG];
-                if (s < n_tok) {
-                    const uint32_t* rec = reinterpret_cast<const uint32_t*>(tile + s * tl.kb);
-                    const uint32_t x = __funnelshift_r(rec[kwi], rec[kwi + 1], ksh);
-                    const __half* nr = reinterpret_cast<const __half*>(tile + tl.off_kn + 16 * s);
-                    const float rA = __half2float(nr[wA - 1]), rB = __half2float(nr[wB - 1]);
-                    const float v0 = cbA[bfe(x, 0, wA)] * rA, v1 = cbA[bfe(x, wA, wA)] * rA;
-                    const float v2 = cbB[bfe(x, posB0, wB)] * rB, v3 = cbB[bfe(x, posB1, wB)] * rB;
+            if (full) {
 #pragma unroll
-                    for (int jj = 0; jj < MAXG; ++jj)
-                        part[jj] = fmaf(qv[jj][0], v0, fmaf(qv[jj][1], v1, fmaf(qv[jj][2], v2, qv[jj][3] * v3)));
-                } else {
-#pragma unroll
-                    for (int jj = 0; jj < MAXG; ++jj) part[jj] = 0.f;
+                for (int u = 0; u < 8; ++u) {
+                    float part[MAXG];
+                    partial(8 * half + u, part);
+                    store(u, part);
                 }
+            } else {
+                for (int u = 0; u < 8; ++u) {
+                    float part[MAXG];
+                    if (8 * half + u < n_tok) {
+                        partial(8 * half + u, part);
+                    } else {
 #pragma unroll
-                for (int c = 0; c < MAXG; c += 4)
-                    *reinterpret_cast<float4*>(&tr[lane][u * MAXG + c]) =
-                        make_float4(part[c], part[c + 1], part[c + 2], part[c + 3]);
+                        for (int jj = 0; jj < MAXG; ++jj) part[jj] = 0.f;
+                    }
+                    store(u, part);
+                }
             }
             __syncwarp();
             // lane l sums column VPL*l + e over the 32 rows: token 8*half + l/4,
@@ -298,6 +315,7 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         __syncwarp();
 
         // ---- PV: this lane's channels 4l .. 4l+3
+#pragma unroll 2
         for (int s = 0; s < n_tok; ++s) {
             const uint32_t* vr = reinterpret_cast<const uint32_t*>(tile + tl.off_vc + s * tl.vb);
             const uint32_t x = __funnelshift_r(vr[vwi], vr[vwi + 1], vsh);
