@@ -24,7 +24,6 @@ append_int2_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
                    const float* __restrict__ Rk, const float* __restrict__ Rv, uint8_t* __restrict__ cache,
                    int64_t num_pages, float* __restrict__ dbg_k, float* __restrict__ dbg_v,
                    int32_t* __restrict__ err_count, int tok_per_cta, float clip) {
-    griddep_wait();  // k, v, the slot mapping or the cache may come from the previous kernel
     griddep_launch_dependents();
     const int h = blockIdx.y, grp = blockIdx.z;
     const int tid = threadIdx.x;
@@ -32,10 +31,13 @@ append_int2_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
     const int lane = tid & 31;
     const int j = 32 * grp + lane;  // output channel
 
+    // the rotations are constants of the layer: loaded while the previous
+    // kernel in the stream may still be running
     const float* R = (is_v ? Rv : Rk) + (size_t)h * D * D;
     float rcol[D];
 #pragma unroll
     for (int i = 0; i < D; ++i) rcol[i] = __ldg(R + i * D + j);
+    griddep_wait();  // k, v, the slot mapping or the cache may come from the previous kernel
 
     __shared__ float xs[2][2][D];
     const int t0 = blockIdx.x * tok_per_cta;

@@ -157,7 +157,16 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
 
     uint32_t* err_word = reinterpret_cast<uint32_t*>(ws);
 
-    griddep_wait();  // every input may come from the previous kernel in the stream
+    // The rotations are constants of the layer: this warp's rows of R_k are
+    // loaded, and R_v (read only after the loop) fetched into L2, while the
+    // previous kernel in the stream may still be running.
+    float4 rr[RowPrefetch<NW, MAXG>::N];
+    load_rows<NW>(Rk + (size_t)h * D * D, rr);
+    {
+        const char* rv = reinterpret_cast<const char*>(Rv + (size_t)h * D * D);
+        for (int l = tid; l < D * D * 4 / 128; l += NW * 32) prefetch_l2_keep(rv + 128 * l);
+    }
+    griddep_wait();  // every other input may come from the previous kernel in the stream
     if constexpr (WIN) {
         if (split == S - 1) {
             // the last split attends the BF16 window instead of cache pages
@@ -228,13 +237,6 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         const char* btc = reinterpret_cast<const char*>(bt);
         const int lines = (n_pages * 4 + 127) / 128;
         for (int l = split * NW * 32 + tid; l < lines; l += S_pages * NW * 32) prefetch_l2_keep(btc + 128 * l);
-    }
-    float4 rr[RowPrefetch<NW, MAXG>::N];
-    load_rows<NW>(Rk + (size_t)h * D * D, rr);
-    {
-        // R_v is read only after the loop: have L2 fetch it now and keep it
-        const char* rv = reinterpret_cast<const char*>(Rv + (size_t)h * D * D);
-        for (int l = tid; l < D * D * 4 / 128; l += NW * 32) prefetch_l2_keep(rv + 128 * l);
     }
     constexpr int QPT = (MAXG * D + NW * 32 - 1) / (NW * 32);  // query values per thread
     float qv[QPT];

@@ -31,6 +31,12 @@
  *    int32 physical page ids; context_lens [B] int32 tokens to attend.
  *  - Query head j reads KV head j / (H_q / H_kv) (contiguous GQA groups).
  *  - slot_mapping[t] = page * 16 + slot; -1 skips token t.
+ *  - Kernels are launched with programmatic dependent launch: a call's
+ *    kernel may start while the kernel before it in the stream is still
+ *    running, and waits for it before reading its inputs.  The INT2
+ *    rotations R_k and R_v are the exception: they are constants of a
+ *    layer and are read before that wait, so the kernel issued immediately
+ *    before an INT2 call in the same stream must not write them.
  */
 #ifndef KVQ_H
 #define KVQ_H
