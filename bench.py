@@ -252,6 +252,35 @@ def time_launches(stream, fn, n):
     return statistics.mean(a.elapsed_time(b) for a, b in evs)
 
 
+def measure_int2_gqa8(device, stream, reps):
+    """INT2 decode on the GQA-8 sweep shape (64 q / 8 KV heads, Llama-3-70B
+    style) at batch 8 and 131072 tokens: 805 MB of cache per launch, larger
+    than L2, launches back to back."""
+    spec = inputs.sweep70b_spec(8, 131072)
+    layer = Int2Layer(spec, 0, device=device)
+    layer.prefill()
+    q = layer.queries()
+    out = torch.zeros((spec.batch, spec.h_q, spec.d), dtype=torch.float32, device=device)
+    ws = layer.workspace()
+    call = lambda: _lib.kvq_decode_attn_int2(q, layer.cache, layer.num_pages, layer.block_table,
+                                             layer.context_lens, layer.R_k, layer.R_v, layer.scale, out, ws)
+    for _ in range(3):
+        call()
+    ms = statistics.median(time_launches(stream, call, 5) for _ in range(reps))
+    nbytes = layer.packed_bytes_per_decode() + spec.batch * spec.h_q * spec.d * 6
+    peak, kind = peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out_line = {"workload": "sweep70b: 64 q / 8 KV heads, batch 8, 131072 ctx, INT2 cache",
+                "kernel": "decode_int2_kernel<2>", "ms_per_decode": round(ms, 4), "value": round(gbs, 2),
+                "unit": "GB/s", "splits": _lib.kvq_decode_auto_splits(spec.batch, spec.h_q, spec.h_kv,
+                                                                      layer.block_table.shape[1]),
+                "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peak, "unit": "GB/s",
+                             "frac": round(gbs / peak, 4), "peak_kind": kind}}
+    del layer
+    torch.cuda.empty_cache()
+    return out_line
+
+
 def measure_bgtq(device, stream, reps):
     """Block-GTQ K3V3 decode at 128K (32 q / 8 KV heads, B = 1): kernel-alone
     bandwidth of the packed stream (KB + 16 + VB + 2 bytes per token-head)."""
@@ -498,6 +527,7 @@ def run_ours(args, world, rank, local):
     if not args.no_bgtq:
         line["bgtq"] = measure_bgtq(device, stream, reps=max(3, min(args.steps, 10)))
     line["append_prefill"] = measure_append_prefill(spec, device, stream, reps=3)
+    line["gqa8"] = measure_int2_gqa8(device, stream, reps=3)
     if rank == 0 and not args.no_cpu_baseline:
         gbs, el, sample = oracle_baseline(spec)
         line["cpu_baseline"] = {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",

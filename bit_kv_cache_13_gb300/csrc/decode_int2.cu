@@ -636,10 +636,11 @@ static kvq_status set_smem_once(const void* fn, int bytes, int which) {
 
 extern "C" int kvq_decode_auto_splits(int B, int H_q, int H_kv, int max_pages_per_seq) {
     if (B <= 0 || H_kv <= 0 || H_q < H_kv || max_pages_per_seq <= 0) return 1;
-    // one CTA per SM of the 152 over the (sequence, KV head) pairs; at
-    // least 32 pages per split (the CTAs have 10-12 warps)
+    // at most one wave of CTAs, one per SM of the 152, over the (sequence,
+    // KV head) pairs (a CTA past the wave would run alone in a second one);
+    // at least 32 pages per split (the CTAs have 8-12 warps)
     const long units = (long)B * H_kv;
-    long s = (152L + units - 1) / units;
+    long s = 152L / units;
     long max_s = (max_pages_per_seq + 31) / 32;
     if (max_s > MAX_SPLITS) max_s = MAX_SPLITS;
     if (s > max_s) s = max_s;

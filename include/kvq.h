@@ -129,10 +129,10 @@ kvq_status kvq_dequant_int2(const void* cache, int64_t num_pages, int H_kv, int 
  * tickets at zero again. */
 size_t kvq_decode_workspace_bytes(int B, int H_q, int H_kv, int max_pages_per_seq, int num_splits);
 
-/* The split count kvq_decode_attn_int2's automatic choice (num_splits = 0)
- * uses: one CTA per SM (152) over the (sequence, KV head) pairs, at least 32
- * pages per split, at most 256.  bgtq_decode_attn, whose CTAs are smaller,
- * aims at three CTAs per SM and at least 16 pages per split. */
+/* The split count the automatic choice (num_splits = 0) of the decode calls
+ * uses: the most splits that keep B * H_kv * splits within one wave of one
+ * CTA per SM (152), at least 1, at most one split per 32 pages and at most
+ * 256. */
 int kvq_decode_auto_splits(int B, int H_q, int H_kv, int max_pages_per_seq);
 
 /* Fused packed-cache decode attention over the INT2 cache.
