@@ -36,7 +36,10 @@
 
 namespace kvq {
 
-constexpr int DEC_STAGES = 8;
+constexpr int DEC_STAGES = 8;  // page slots per warp
+constexpr int DEC_PAIR = 2;    // pages per mbarrier phase
+constexpr int DEC_UNITS = DEC_STAGES / DEC_PAIR;
+static_assert(DEC_PAIR == 2, "the unit code is written for page pairs");
 
 // Warps per CTA.  Each of the SM's four schedulers owns a quarter of its
 // 64K registers: three warps of 168 registers fit one (head groups up to 4),
@@ -52,7 +55,7 @@ struct __align__(16) DecodeSmem {
         uint8_t ring[NW][DEC_STAGES][INT2_TILE];  // page tiles in flight
         float o_part[NW][MAXG][D];                // per-warp o' after the loop
     } u;
-    uint64_t bar[NW][DEC_STAGES];
+    uint64_t bar[NW][DEC_UNITS];
     int ntok[NW][DEC_STAGES];  // valid tokens of the page in each stage (0: skipped page)
     float q[MAXG][D];          // scaled rotated queries q~ = q R_k * scale * log2(e)
     float gsum[MAXG][NGROUP];
@@ -192,53 +195,9 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     const int my_count = n_pages > k0 ? (n_pages - k0 + KS - 1) / KS : 0;
     auto page_of = [&](int j) { return k0 + KS * j; };
 
-    if (lane == 0) {
-        for (int s = 0; s < DEC_STAGES; ++s) mbar_init(&sm.bar[warp][s], 1);
-        fence_mbar_init();
-        fence_proxy_async_smem();
-    }
-    __syncwarp();
-    // Lane 0 issues the warp's i-th page (sequence page p) with its (already
-    // loaded) page id and records how many of its tokens are valid; the
-    // mbarrier publishes that count together with the data.
-    auto issue = [&](int i, int p, int pid) {  // lane 0 only
-        const int st = i % DEC_STAGES;
-        uint64_t* bar = &sm.bar[warp][st];
-        if (pid < 0 || (int64_t)pid >= num_pages) {
-            atomicOr(err_word, ERR_BAD_PAGE);
-            sm.ntok[warp][st] = 0;
-            mbar_arrive(bar);  // complete the phase without data
-        } else {
-            sm.ntok[warp][st] = min(PAGE, ctx - p * PAGE);
-            mbar_arrive_expect_tx(bar, INT2_TILE);
-            bulk_g2s(sm.u.ring[warp][st], cache + ((size_t)pid * H_kv + h) * INT2_TILE, INT2_TILE, bar);
-        }
-    };
-    // ---- first the page ids of the first pages and their copies (lane 0),
-    // with no other load ahead of them; the rest of the prologue overlaps the
-    // copies.  Lane 0 keeps the ids of the next two pages to issue, each
-    // loaded two releases before its use.
-    int pid_next = 0, pid_after = 0;
-    if (lane == 0) {
-        // bounded by the block table's row length, not the context, so these
-        // loads need not wait for context_lens
-        int pids[DEC_STAGES + 2];
-#pragma unroll
-        for (int j = 0; j < DEC_STAGES + 2; ++j) pids[j] = page_of(j) < max_pages ? __ldg(bt + page_of(j)) : 0;
-#pragma unroll
-        for (int j = 0; j < DEC_STAGES; ++j)
-            if (j < my_count) issue(j, page_of(j), pids[j]);
-        pid_next = pids[DEC_STAGES];
-        pid_after = pids[DEC_STAGES + 1];
-    }
-    {
-        // the rest of this sequence's block table is read one entry at a
-        // time during the loop: have L2 fetch it now
-        const char* btc = reinterpret_cast<const char*>(bt);
-        const int lines = (n_pages * 4 + 127) / 128;
-        for (int l = split * NW * 32 + tid; l < lines; l += S_pages * NW * 32) prefetch_l2_keep(btc + 128 * l);
-    }
     constexpr int QPT = (MAXG * D + NW * 32 - 1) / (NW * 32);  // query values per thread
+    // the query loads go out before lane 0 waits for its page ids, so the
+    // two global round trips overlap
     float qv[QPT];
     {
         const __nv_bfloat16* qb = q + ((size_t)b * H_q + (size_t)h * G) * D;
@@ -247,6 +206,81 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             const int idx = tid + k * NW * 32;
             qv[k] = idx < G * D ? __bfloat162float(qb[idx]) : 0.f;
         }
+    }
+    // Pages travel in units of DEC_PAIR: unit u holds the warp's pages
+    // DEC_PAIR u .. DEC_PAIR u + DEC_PAIR - 1 (ring slots j % DEC_STAGES) on
+    // one mbarrier phase, so a unit costs one wait and one release.
+    const int n_units = (my_count + DEC_PAIR - 1) / DEC_PAIR;
+    if (lane == 0) {
+        for (int s = 0; s < DEC_UNITS; ++s) mbar_init(&sm.bar[warp][s], 1);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    __syncwarp();
+    // Lane 0 issues unit u with its (already loaded) page ids and records how
+    // many tokens of each page are valid (0 for a slot past the warp's pages
+    // or with a bad page id); the mbarrier publishes the counts with the data.
+    auto issue_unit = [&](int u, const int (&pid)[DEC_PAIR]) {  // lane 0 only
+        const int st = u % DEC_UNITS;
+        uint64_t* bar = &sm.bar[warp][st];
+        bool ok[DEC_PAIR];
+        uint32_t tx = 0;
+#pragma unroll
+        for (int e = 0; e < DEC_PAIR; ++e) {
+            const int j = DEC_PAIR * u + e;
+            int n = 0;
+            ok[e] = false;
+            if (j < my_count) {
+                if (pid[e] < 0 || (int64_t)pid[e] >= num_pages) {
+                    atomicOr(err_word, ERR_BAD_PAGE);
+                } else {
+                    ok[e] = true;
+                    n = min(PAGE, ctx - page_of(j) * PAGE);
+                    tx += INT2_TILE;
+                }
+            }
+            sm.ntok[warp][DEC_PAIR * st + e] = n;
+        }
+        if (tx == 0) {
+            mbar_arrive(bar);  // complete the phase without data
+        } else {
+            mbar_arrive_expect_tx(bar, tx);
+#pragma unroll
+            for (int e = 0; e < DEC_PAIR; ++e)
+                if (ok[e])
+                    bulk_g2s(sm.u.ring[warp][DEC_PAIR * st + e], cache + ((size_t)pid[e] * H_kv + h) * INT2_TILE,
+                             INT2_TILE, bar);
+        }
+    };
+    // ---- first the page ids of the first units and their copies (lane 0);
+    // the rest of the prologue overlaps the copies.  Lane 0 keeps the ids of
+    // the next unit to issue, loaded one release before their use.
+    int pid_next[DEC_PAIR];
+    int n_issued = 0;  // units issued so far (lane 0)
+#pragma unroll
+    for (int e = 0; e < DEC_PAIR; ++e) pid_next[e] = 0;
+    if (lane == 0) {
+        // bounded by the block table's row length, not the context, so these
+        // loads need not wait for context_lens
+        int pids[DEC_STAGES + DEC_PAIR];
+#pragma unroll
+        for (int j = 0; j < DEC_STAGES + DEC_PAIR; ++j) pids[j] = page_of(j) < max_pages ? __ldg(bt + page_of(j)) : 0;
+#pragma unroll
+        for (int u = 0; u < DEC_UNITS; ++u)
+            if (u < n_units) {
+                const int pu[DEC_PAIR] = {pids[DEC_PAIR * u], pids[DEC_PAIR * u + 1]};
+                issue_unit(u, pu);
+                n_issued = u + 1;
+            }
+#pragma unroll
+        for (int e = 0; e < DEC_PAIR; ++e) pid_next[e] = pids[DEC_STAGES + e];
+    }
+    {
+        // the rest of this sequence's block table is read one entry at a
+        // time during the loop: have L2 fetch it now
+        const char* btc = reinterpret_cast<const char*>(bt);
+        const int lines = (n_pages * 4 + 127) / 128;
+        for (int l = split * NW * 32 + tid; l < lines; l += S_pages * NW * 32) prefetch_l2_keep(btc + 128 * l);
     }
 
     // ---- q~ = (q R_k) * scale * log2(e) for the G heads of this KV head
@@ -333,30 +367,33 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         lsum[nt] = 0.f;
     }
 
-    // Wait for page i of this warp; false on a timeout.  On a sequence's
+    // Wait for unit u of this warp; false on a timeout.  On a sequence's
     // last page the slots past the context may hold stale bytes (even NaN
-    // scales): their value scale/min words are zeroed here, so p = 0 always
-    // meets finite factors and the PV step needs no per-slot masks (the QK
-    // step drops those slots' logits by selection).
-    auto wait_page = [&](int i) -> bool {
-        const int st = i % DEC_STAGES;
-        const bool ok = mbar_wait_bounded(&sm.bar[warp][st], (i / DEC_STAGES) & 1, WAIT_LIMIT_CYCLES);
+    // scales), and so does a slot with no page: their value scale/min words
+    // are zeroed here (lanes 16e + row cover slot e of the unit), so p = 0
+    // always meets finite factors and the PV step needs no per-slot masks
+    // (the QK step drops those slots' logits by selection).
+    auto wait_unit = [&](int u) -> bool {
+        const int st = u % DEC_UNITS;
+        const bool ok = mbar_wait_bounded(&sm.bar[warp][st], (u / DEC_UNITS) & 1, WAIT_LIMIT_CYCLES);
         if (__any_sync(0xffffffffu, !ok)) {
             if (lane == 0) atomicOr(err_word, ERR_TIMEOUT);
             return false;
         }
-        const int n = sm.ntok[warp][st];
-        if (n < PAGE) {
-            if (lane >= n && lane < PAGE)
-                *reinterpret_cast<uint4*>(sm.u.ring[warp][st] + OFF_VM + 16 * lane) = make_uint4(0u, 0u, 0u, 0u);
+        const int e = lane >> 4, row = lane & 15;
+        const int n = sm.ntok[warp][DEC_PAIR * st + e];
+        if (__any_sync(0xffffffffu, n < PAGE)) {
+            if (row >= n)
+                *reinterpret_cast<uint4*>(sm.u.ring[warp][DEC_PAIR * st + e] + OFF_VM + 16 * row) =
+                    make_uint4(0u, 0u, 0u, 0u);
             __syncwarp();
         }
         return true;
     };
 
     // ---------------- QK of page i: base-2 logits of tokens r, r + 8 for
-    // head 4*nt + t (-inf past the context) and each head's page maximum
-    auto qk_page = [&](int i, float (&lg)[NT][2], float (&pm)[NT]) {
+    // head 4*nt + t (-inf past the context)
+    auto qk_page = [&](int i, float (&lg)[NT][2]) {
         const uint8_t* tile = sm.u.ring[warp][i % DEC_STAGES];
         const int n_tok = sm.ntok[warp][i % DEC_STAGES];
         const uint2 kr = lds64(tile + OFF_KC + 32 * r + 8 * t);
@@ -394,7 +431,16 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         for (int nt = 0; nt < NT; ++nt) {
             lg[nt][0] = r < n_tok ? fmaf(acc_r[nt], inv_sig[nt], mn_r[nt]) : -CUDART_INF_F;
             lg[nt][1] = r + 8 < n_tok ? fmaf(acc_r8[nt], inv_sig[nt], mn_r8[nt]) : -CUDART_INF_F;
-            float m = fmaxf(lg[nt][0], lg[nt][1]);
+        }
+    };
+
+    // QK of unit u and each head's maximum over its pages
+    auto qk_unit = [&](int u, float (&lg)[DEC_PAIR][NT][2], float (&pm)[NT]) {
+#pragma unroll
+        for (int e = 0; e < DEC_PAIR; ++e) qk_page(DEC_PAIR * u + e, lg[e]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            float m = fmaxf(fmaxf(lg[0][nt][0], lg[0][nt][1]), fmaxf(lg[1][nt][0], lg[1][nt][1]));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
@@ -402,11 +448,11 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         }
     };
 
-    // ---------------- online softmax (base 2) for one page, head 4*nt + t:
+    // ---------------- online softmax (base 2) for one unit, head 4*nt + t:
     // raise the running maxima, rescale the accumulators when one grew, and
     // return p^ (p rounded to fp16 once; the same p^ weights the codes, the
     // group minima and the normaliser)
-    auto softmax_page = [&](const float (&lg)[NT][2], const float (&pm)[NT], float (&pr)[NT][2]) {
+    auto softmax_unit = [&](const float (&lg)[DEC_PAIR][NT][2], const float (&pm)[NT], float (&pr)[DEC_PAIR][NT][2]) {
         float corr[NT];
         bool need = false;
 #pragma unroll
@@ -418,9 +464,12 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                 need = true;
             }
             const float mref = mrun[nt] == -CUDART_INF_F ? 0.f : mrun[nt];
-            pr[nt][0] = __half2float(__float2half_rn(ex2(lg[nt][0] - mref)));
-            pr[nt][1] = __half2float(__float2half_rn(ex2(lg[nt][1] - mref)));
-            lsum[nt] = fmaf(lsum[nt], corr[nt], pr[nt][0] + pr[nt][1]);
+#pragma unroll
+            for (int e = 0; e < DEC_PAIR; ++e) {
+                pr[e][nt][0] = __half2float(__float2half_rn(ex2(lg[e][nt][0] - mref)));
+                pr[e][nt][1] = __half2float(__float2half_rn(ex2(lg[e][nt][1] - mref)));
+            }
+            lsum[nt] = fmaf(lsum[nt], corr[nt], (pr[0][nt][0] + pr[0][nt][1]) + (pr[1][nt][0] + pr[1][nt][1]));
         }
         if (__any_sync(0xffffffffu, need)) {
             // PV columns 2t, 2t+1 hold heads 2t, 2t+1, whose maxima live in lanes (2t)&3, (2t+1)&3
@@ -515,47 +564,55 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         }
     };
 
-    // Hand page i's stage back: issue the page DEC_STAGES ahead into it and
-    // start loading the id of the page two after that.
-    auto release_page = [&](int i) {
+    // Hand unit u's slots back: issue the unit DEC_UNITS ahead into them and
+    // load the page ids of the unit after that.
+    auto release_unit = [&](int u) {
         __syncwarp();
-        if (lane == 0 && i + DEC_STAGES < my_count) {
+        if (lane == 0 && u + DEC_UNITS < n_units) {
             fence_proxy_async_smem();
-            issue(i + DEC_STAGES, page_of(i + DEC_STAGES), pid_next);
-            pid_next = pid_after;
-            if (i + DEC_STAGES + 2 < my_count) pid_after = __ldg(bt + page_of(i + DEC_STAGES + 2));
+            issue_unit(u + DEC_UNITS, pid_next);
+            n_issued = u + DEC_UNITS + 1;
+            const int j = DEC_PAIR * (u + DEC_UNITS + 1);
+#pragma unroll
+            for (int e = 0; e < DEC_PAIR; ++e)
+                if (j + e < my_count) pid_next[e] = __ldg(bt + page_of(j + e));
         }
     };
 
-    // Software pipeline over the warp's pages: the QK of page i + 1 does not
-    // depend on the softmax or PV of page i, and the two sit in one
+    // Software pipeline over the warp's units: the QK of unit u + 1 does not
+    // depend on the softmax or PV of unit u, and the two sit in one
     // straight-line block so their instruction streams interleave.
-    bool timed_out = false;
-    float lg[NT][2], pm[NT];
-    if (my_count > 0) {
-        timed_out = !wait_page(0);
-        if (!timed_out) qk_page(0, lg, pm);
+    int u_fail = -1;  // the unit whose wait timed out
+    float lg[DEC_PAIR][NT][2], pm[NT];
+    if (n_units > 0) {
+        if (wait_unit(0))
+            qk_unit(0, lg, pm);
+        else
+            u_fail = 0;
     }
-    int i = 0;
-    for (; i + 1 < my_count && !timed_out; ++i) {
-        float pr[NT][2];
-        softmax_page(lg, pm, pr);
-        if (!wait_page(i + 1)) {
-            timed_out = true;
+    int u = 0;
+    for (; u + 1 < n_units && u_fail < 0; ++u) {
+        float pr[DEC_PAIR][NT][2];
+        softmax_unit(lg, pm, pr);
+        if (!wait_unit(u + 1)) {
+            u_fail = u + 1;
             break;
         }
-        pv_page(i, pr);
-        qk_page(i + 1, lg, pm);  // lg, pm of page i are spent (pr holds what PV needs)
-        release_page(i);
+#pragma unroll
+        for (int e = 0; e < DEC_PAIR; ++e) pv_page(DEC_PAIR * u + e, pr[e]);
+        qk_unit(u + 1, lg, pm);  // lg, pm of unit u are spent (pr holds what PV needs)
+        release_unit(u);
     }
-    if (!timed_out && my_count > 0) {
-        float pr[NT][2];
-        softmax_page(lg, pm, pr);
-        pv_page(i, pr);
+    if (u_fail < 0 && n_units > 0) {
+        float pr[DEC_PAIR][NT][2];
+        softmax_unit(lg, pm, pr);
+#pragma unroll
+        for (int e = 0; e < DEC_PAIR; ++e) pv_page(DEC_PAIR * u + e, pr[e]);
     }
-    if (timed_out && lane == 0) {
+    if (u_fail >= 0 && lane == 0) {
         // let copies still in flight land before the shared memory is reused
-        for (int s = 0; s < DEC_STAGES; ++s) (void)mbar_wait_bounded(&sm.bar[warp][s], 0, 1000000LL);
+        for (int v = u_fail; v < n_issued; ++v)
+            (void)mbar_wait_bounded(&sm.bar[warp][v % DEC_UNITS], (v / DEC_UNITS) & 1, 1000000LL);
     }
 
     // the next kernel in the stream may be scheduled once every CTA is here
