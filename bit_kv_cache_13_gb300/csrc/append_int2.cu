@@ -110,8 +110,14 @@ append_int2_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
         uint8_t* rec = tile + (is_v ? OFF_VC : OFF_KC) + 32 * s;
         if ((lane & 3) == 0) rec[4 * (lane >> 2) + grp] = (uint8_t)bits;
         if (lane == 0) {
-            const uint32_t meta = (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(mh) << 16);
-            *reinterpret_cast<uint32_t*>(tile + (is_v ? OFF_VM : OFF_KM) + 16 * s + 4 * grp) = meta;
+            if (is_v) {
+                uint8_t* m = tile + vm_scale_off(s, grp);
+                *reinterpret_cast<__half*>(m) = sh;
+                *reinterpret_cast<__half*>(m + VM_MINS) = mh;
+            } else {
+                const uint32_t meta = (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(mh) << 16);
+                *reinterpret_cast<uint32_t*>(tile + OFF_KM + 16 * s + 4 * grp) = meta;
+            }
         }
     }
 }
@@ -192,9 +198,9 @@ dequant_int2_kernel(const uint8_t* __restrict__ cache, int64_t num_pages, int H_
         // channel j = 32 g + 4 b + c sits in byte 4 b + g, bits 2c
         const int g = j >> 5, b = (j >> 2) & 7, c = j & 3;
         const int code = (tile[(side ? OFF_VC : OFF_KC) + 32 * s + 4 * b + g] >> (2 * c)) & 3;
-        const uint32_t meta = *reinterpret_cast<const uint32_t*>(tile + (side ? OFF_VM : OFF_KM) + 16 * s + 4 * g);
-        const float sc = __half2float(__ushort_as_half((unsigned short)(meta & 0xffffu)));
-        const float mn = __half2float(__ushort_as_half((unsigned short)(meta >> 16)));
+        const uint8_t* m = side ? tile + vm_scale_off(s, g) : tile + OFF_KM + 16 * s + 4 * g;
+        const float sc = __half2float(*reinterpret_cast<const __half*>(m));
+        const float mn = __half2float(*reinterpret_cast<const __half*>(m + (side ? VM_MINS : 2)));
         val = __fmaf_rn((float)code, sc, mn);
     }
     dst[((size_t)t * H_kv + h) * D + j] = val;

@@ -8,7 +8,7 @@
 //
 // Grid (split, kv_head, seq) with one large CTA per SM (12 warps for head
 // groups up to 4, 8 for groups of 8).  Each warp streams pages through its
-// own 8-stage ring of 1536-byte tiles filled by bulk async copies
+// own 9-slot ring of 1536-byte tiles filled by bulk async copies
 // (cp.async.bulk + mbarrier).  The pages of a (sequence, KV head) are dealt
 // round-robin over all warps of its split CTAs.  Per page (16 tokens):
 //
@@ -25,7 +25,9 @@
 //       hi/lo pair (HMUL2, then HFMA2 for the remainder), so the large
 //       group minima and the code term cancel without amplifying rounding;
 //       the min term is one more MMA with A = the fp16 mins of the groups.
-//   The QK of page i + 1 and the softmax/PV of page i are software-pipelined.
+//   Pages travel in units of three (one mbarrier phase, one wait, one
+//   release, one softmax rescale per unit); the QK of unit u + 1 and the
+//   softmax/PV of unit u are software-pipelined.
 //
 // Split partials (m, l, o') go to the workspace; the last CTA of a
 // (sequence, KV head) to finish (atomic ticket, no waiting) merges them,
@@ -36,10 +38,10 @@
 
 namespace kvq {
 
-constexpr int DEC_STAGES = 8;  // page slots per warp
-constexpr int DEC_PAIR = 2;    // pages per mbarrier phase
-constexpr int DEC_UNITS = DEC_STAGES / DEC_PAIR;
-static_assert(DEC_PAIR == 2, "the unit code is written for page pairs");
+constexpr int DEC_STAGES = 9;  // page slots per warp
+constexpr int UNIT_PAGES = 3;  // pages per mbarrier phase (one wait, one release)
+constexpr int DEC_UNITS = DEC_STAGES / UNIT_PAGES;
+static_assert(DEC_STAGES % UNIT_PAGES == 0, "a unit is a whole number of page slots");
 
 // Warps per CTA.  Each of the SM's four schedulers owns a quarter of its
 // 64K registers: three warps of 168 registers fit one (head groups up to 4),
@@ -207,10 +209,10 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             qv[k] = idx < G * D ? __bfloat162float(qb[idx]) : 0.f;
         }
     }
-    // Pages travel in units of DEC_PAIR: unit u holds the warp's pages
-    // DEC_PAIR u .. DEC_PAIR u + DEC_PAIR - 1 (ring slots j % DEC_STAGES) on
+    // Pages travel in units of UNIT_PAGES: unit u holds the warp's pages
+    // UNIT_PAGES u .. UNIT_PAGES u + UNIT_PAGES - 1 (ring slots j % DEC_STAGES) on
     // one mbarrier phase, so a unit costs one wait and one release.
-    const int n_units = (my_count + DEC_PAIR - 1) / DEC_PAIR;
+    const int n_units = (my_count + UNIT_PAGES - 1) / UNIT_PAGES;
     if (lane == 0) {
         for (int s = 0; s < DEC_UNITS; ++s) mbar_init(&sm.bar[warp][s], 1);
         fence_mbar_init();
@@ -220,14 +222,14 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     // Lane 0 issues unit u with its (already loaded) page ids and records how
     // many tokens of each page are valid (0 for a slot past the warp's pages
     // or with a bad page id); the mbarrier publishes the counts with the data.
-    auto issue_unit = [&](int u, const int (&pid)[DEC_PAIR]) {  // lane 0 only
+    auto issue_unit = [&](int u, const int (&pid)[UNIT_PAGES]) {  // lane 0 only
         const int st = u % DEC_UNITS;
         uint64_t* bar = &sm.bar[warp][st];
-        bool ok[DEC_PAIR];
+        bool ok[UNIT_PAGES];
         uint32_t tx = 0;
 #pragma unroll
-        for (int e = 0; e < DEC_PAIR; ++e) {
-            const int j = DEC_PAIR * u + e;
+        for (int e = 0; e < UNIT_PAGES; ++e) {
+            const int j = UNIT_PAGES * u + e;
             int n = 0;
             ok[e] = false;
             if (j < my_count) {
@@ -239,41 +241,43 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                     tx += INT2_TILE;
                 }
             }
-            sm.ntok[warp][DEC_PAIR * st + e] = n;
+            sm.ntok[warp][UNIT_PAGES * st + e] = n;
         }
         if (tx == 0) {
             mbar_arrive(bar);  // complete the phase without data
         } else {
             mbar_arrive_expect_tx(bar, tx);
 #pragma unroll
-            for (int e = 0; e < DEC_PAIR; ++e)
+            for (int e = 0; e < UNIT_PAGES; ++e)
                 if (ok[e])
-                    bulk_g2s(sm.u.ring[warp][DEC_PAIR * st + e], cache + ((size_t)pid[e] * H_kv + h) * INT2_TILE,
+                    bulk_g2s(sm.u.ring[warp][UNIT_PAGES * st + e], cache + ((size_t)pid[e] * H_kv + h) * INT2_TILE,
                              INT2_TILE, bar);
         }
     };
     // ---- first the page ids of the first units and their copies (lane 0);
     // the rest of the prologue overlaps the copies.  Lane 0 keeps the ids of
     // the next unit to issue, loaded one release before their use.
-    int pid_next[DEC_PAIR];
+    int pid_next[UNIT_PAGES];
     int n_issued = 0;  // units issued so far (lane 0)
 #pragma unroll
-    for (int e = 0; e < DEC_PAIR; ++e) pid_next[e] = 0;
+    for (int e = 0; e < UNIT_PAGES; ++e) pid_next[e] = 0;
     if (lane == 0) {
         // bounded by the block table's row length, not the context, so these
         // loads need not wait for context_lens
-        int pids[DEC_STAGES + DEC_PAIR];
+        int pids[DEC_STAGES + UNIT_PAGES];
 #pragma unroll
-        for (int j = 0; j < DEC_STAGES + DEC_PAIR; ++j) pids[j] = page_of(j) < max_pages ? __ldg(bt + page_of(j)) : 0;
+        for (int j = 0; j < DEC_STAGES + UNIT_PAGES; ++j) pids[j] = page_of(j) < max_pages ? __ldg(bt + page_of(j)) : 0;
 #pragma unroll
         for (int u = 0; u < DEC_UNITS; ++u)
             if (u < n_units) {
-                const int pu[DEC_PAIR] = {pids[DEC_PAIR * u], pids[DEC_PAIR * u + 1]};
+                int pu[UNIT_PAGES];
+#pragma unroll
+                for (int e = 0; e < UNIT_PAGES; ++e) pu[e] = pids[UNIT_PAGES * u + e];
                 issue_unit(u, pu);
                 n_issued = u + 1;
             }
 #pragma unroll
-        for (int e = 0; e < DEC_PAIR; ++e) pid_next[e] = pids[DEC_STAGES + e];
+        for (int e = 0; e < UNIT_PAGES; ++e) pid_next[e] = pids[DEC_STAGES + e];
     }
     {
         // the rest of this sequence's block table is read one entry at a
@@ -370,7 +374,7 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     // Wait for unit u of this warp; false on a timeout.  On a sequence's
     // last page the slots past the context may hold stale bytes (even NaN
     // scales), and so does a slot with no page: their value scale/min words
-    // are zeroed here (lanes 16e + row cover slot e of the unit), so p = 0
+    // are zeroed here, so p = 0
     // always meets finite factors and the PV step needs no per-slot masks
     // (the QK step drops those slots' logits by selection).
     auto wait_unit = [&](int u) -> bool {
@@ -380,12 +384,19 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             if (lane == 0) atomicOr(err_word, ERR_TIMEOUT);
             return false;
         }
-        const int e = lane >> 4, row = lane & 15;
-        const int n = sm.ntok[warp][DEC_PAIR * st + e];
-        if (__any_sync(0xffffffffu, n < PAGE)) {
-            if (row >= n)
-                *reinterpret_cast<uint4*>(sm.u.ring[warp][DEC_PAIR * st + e] + OFF_VM + 16 * row) =
-                    make_uint4(0u, 0u, 0u, 0u);
+        bool short_page = false;
+#pragma unroll
+        for (int e = 0; e < UNIT_PAGES; ++e) short_page |= sm.ntok[warp][UNIT_PAGES * st + e] < PAGE;
+        if (short_page) {  // warp-uniform
+            // 64 meta words per page (32 scale, 32 min words of slot pairs):
+            // clear the halves of slots at or past the page's token count
+            for (int k = lane; k < UNIT_PAGES * 64; k += 32) {
+                const int e = k >> 6, w = k & 63, pair = (w & 31) >> 2;
+                const int n = sm.ntok[warp][UNIT_PAGES * st + e];
+                const uint32_t keep = (2 * pair < n ? 0x0000ffffu : 0u) | (2 * pair + 1 < n ? 0xffff0000u : 0u);
+                uint32_t* word = reinterpret_cast<uint32_t*>(sm.u.ring[warp][UNIT_PAGES * st + e] + OFF_VM) + w;
+                if (keep != 0xffffffffu) *word &= keep;
+            }
             __syncwarp();
         }
         return true;
@@ -435,12 +446,14 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     };
 
     // QK of unit u and each head's maximum over its pages
-    auto qk_unit = [&](int u, float (&lg)[DEC_PAIR][NT][2], float (&pm)[NT]) {
+    auto qk_unit = [&](int u, float (&lg)[UNIT_PAGES][NT][2], float (&pm)[NT]) {
 #pragma unroll
-        for (int e = 0; e < DEC_PAIR; ++e) qk_page(DEC_PAIR * u + e, lg[e]);
+        for (int e = 0; e < UNIT_PAGES; ++e) qk_page(UNIT_PAGES * u + e, lg[e]);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            float m = fmaxf(fmaxf(lg[0][nt][0], lg[0][nt][1]), fmaxf(lg[1][nt][0], lg[1][nt][1]));
+            float m = fmaxf(lg[0][nt][0], lg[0][nt][1]);
+#pragma unroll
+            for (int e = 1; e < UNIT_PAGES; ++e) m = fmaxf(m, fmaxf(lg[e][nt][0], lg[e][nt][1]));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
@@ -452,7 +465,7 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     // raise the running maxima, rescale the accumulators when one grew, and
     // return p^ (p rounded to fp16 once; the same p^ weights the codes, the
     // group minima and the normaliser)
-    auto softmax_unit = [&](const float (&lg)[DEC_PAIR][NT][2], const float (&pm)[NT], float (&pr)[DEC_PAIR][NT][2]) {
+    auto softmax_unit = [&](const float (&lg)[UNIT_PAGES][NT][2], const float (&pm)[NT], float (&pr)[UNIT_PAGES][NT][2]) {
         float corr[NT];
         bool need = false;
 #pragma unroll
@@ -465,11 +478,14 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             }
             const float mref = mrun[nt] == -CUDART_INF_F ? 0.f : mrun[nt];
 #pragma unroll
-            for (int e = 0; e < DEC_PAIR; ++e) {
+            for (int e = 0; e < UNIT_PAGES; ++e) {
                 pr[e][nt][0] = __half2float(__float2half_rn(ex2(lg[e][nt][0] - mref)));
                 pr[e][nt][1] = __half2float(__float2half_rn(ex2(lg[e][nt][1] - mref)));
             }
-            lsum[nt] = fmaf(lsum[nt], corr[nt], (pr[0][nt][0] + pr[0][nt][1]) + (pr[1][nt][0] + pr[1][nt][1]));
+            float ps = pr[0][nt][0] + pr[0][nt][1];
+#pragma unroll
+            for (int e = 1; e < UNIT_PAGES; ++e) ps += pr[e][nt][0] + pr[e][nt][1];
+            lsum[nt] = fmaf(lsum[nt], corr[nt], ps);
         }
         if (__any_sync(0xffffffffu, need)) {
             // PV columns 2t, 2t+1 hold heads 2t, 2t+1, whose maxima live in lanes (2t)&3, (2t+1)&3
@@ -517,20 +533,16 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             pb0 = prmt(Y0, Y1, 0x5410);  // p(2t), p(2t+1)
             pb1 = prmt(Y0, Y1, 0x7632);  // p(2t+8), p(2t+9)
         }
-        const uint4 m0 = lds128(tile + OFF_VM + 16 * (2 * t));
-        const uint4 m1 = lds128(tile + OFF_VM + 16 * (2 * t + 1));
-        const uint4 m8 = lds128(tile + OFF_VM + 16 * (2 * t + 8));
-        const uint4 m9 = lds128(tile + OFF_VM + 16 * (2 * t + 9));
-        const uint32_t w0[4] = {m0.x, m0.y, m0.z, m0.w}, w1[4] = {m1.x, m1.y, m1.z, m1.w};
-        const uint32_t w8[4] = {m8.x, m8.y, m8.z, m8.w}, w9[4] = {m9.x, m9.y, m9.z, m9.w};
+        // value scales of tokens (2t, 2t+1) and (2t+8, 2t+9), one word per group
+        const uint4 sA = lds128(tile + OFF_VM + 16 * t);
+        const uint4 sB = lds128(tile + OFF_VM + 16 * (t + 4));
+        const uint32_t wA[4] = {sA.x, sA.y, sA.z, sA.w}, wB[4] = {sB.x, sB.y, sB.z, sB.w};
 
         // min term: rows = groups (rows 4..15 are never read), K = tokens
         {
-            const int gr = 4 * (r & 3);
             uint32_t a[4] = {0u, 0u, 0u, 0u};
-            a[0] = prmt(lds32(tile + OFF_VM + 16 * (2 * t) + gr), lds32(tile + OFF_VM + 16 * (2 * t + 1) + gr), 0x7632);
-            a[2] = prmt(lds32(tile + OFF_VM + 16 * (2 * t + 8) + gr), lds32(tile + OFF_VM + 16 * (2 * t + 9) + gr),
-                        0x7632);
+            a[0] = lds32(tile + OFF_VM + VM_MINS + 16 * t + 4 * (r & 3));
+            a[2] = lds32(tile + OFF_VM + VM_MINS + 16 * (t + 4) + 4 * (r & 3));
             mma_f16_16816(cmin, a, pb0, pb1);
         }
 
@@ -546,7 +558,7 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             const uint32_t xa = g == 0 ? A01 : g == 1 ? (A01 >> 8) : g == 2 ? A23 : (A23 >> 8);
             const uint32_t xb = g == 0 ? B01 : g == 1 ? (B01 >> 8) : g == 2 ? B23 : (B23 >> 8);
             // p^ * scale exactly as an fp16 pair: hi = rn(p^ s), lo = p^ s - hi (exact)
-            const __half2 S01 = u32_as_h2(prmt(w0[g], w1[g], 0x5410)), S89 = u32_as_h2(prmt(w8[g], w9[g], 0x5410));
+            const __half2 S01 = u32_as_h2(wA[g]), S89 = u32_as_h2(wB[g]);
             const __half2 H0 = __hmul2(P0, S01), H1 = __hmul2(P1, S89);
             const __half2 L0 = __hfma2(P0, S01, __hneg2(H0)), L1 = __hfma2(P1, S89, __hneg2(H1));
 #pragma unroll
@@ -572,9 +584,9 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             fence_proxy_async_smem();
             issue_unit(u + DEC_UNITS, pid_next);
             n_issued = u + DEC_UNITS + 1;
-            const int j = DEC_PAIR * (u + DEC_UNITS + 1);
+            const int j = UNIT_PAGES * (u + DEC_UNITS + 1);
 #pragma unroll
-            for (int e = 0; e < DEC_PAIR; ++e)
+            for (int e = 0; e < UNIT_PAGES; ++e)
                 if (j + e < my_count) pid_next[e] = __ldg(bt + page_of(j + e));
         }
     };
@@ -583,7 +595,7 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     // depend on the softmax or PV of unit u, and the two sit in one
     // straight-line block so their instruction streams interleave.
     int u_fail = -1;  // the unit whose wait timed out
-    float lg[DEC_PAIR][NT][2], pm[NT];
+    float lg[UNIT_PAGES][NT][2], pm[NT];
     if (n_units > 0) {
         if (wait_unit(0))
             qk_unit(0, lg, pm);
@@ -592,22 +604,22 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     }
     int u = 0;
     for (; u + 1 < n_units && u_fail < 0; ++u) {
-        float pr[DEC_PAIR][NT][2];
+        float pr[UNIT_PAGES][NT][2];
         softmax_unit(lg, pm, pr);
         if (!wait_unit(u + 1)) {
             u_fail = u + 1;
             break;
         }
 #pragma unroll
-        for (int e = 0; e < DEC_PAIR; ++e) pv_page(DEC_PAIR * u + e, pr[e]);
+        for (int e = 0; e < UNIT_PAGES; ++e) pv_page(UNIT_PAGES * u + e, pr[e]);
         qk_unit(u + 1, lg, pm);  // lg, pm of unit u are spent (pr holds what PV needs)
         release_unit(u);
     }
     if (u_fail < 0 && n_units > 0) {
-        float pr[DEC_PAIR][NT][2];
+        float pr[UNIT_PAGES][NT][2];
         softmax_unit(lg, pm, pr);
 #pragma unroll
-        for (int e = 0; e < DEC_PAIR; ++e) pv_page(DEC_PAIR * u + e, pr[e]);
+        for (int e = 0; e < UNIT_PAGES; ++e) pv_page(UNIT_PAGES * u + e, pr[e]);
     }
     if (u_fail >= 0 && lane == 0) {
         // let copies still in flight land before the shared memory is reused

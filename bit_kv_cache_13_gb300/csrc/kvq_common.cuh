@@ -17,6 +17,12 @@ constexpr int NGROUP = 4;       // INT2 groups of 32 channels
 // INT2 tile of one (page, KV head)
 constexpr int INT2_TILE = 1536;
 constexpr int OFF_KC = 0, OFF_KM = 512, OFF_VC = 768, OFF_VM = 1280;
+// Key meta: per slot 16 bytes, one (fp16 scale, fp16 min) word per group.
+// Value meta: pair-major, so a word holds one group's scales (or mins) of
+// slots 2j and 2j + 1 -- the order the PV step multiplies them in:
+// scales at OFF_VM + 16 j + 4 g (+2 for the odd slot), mins VM_MINS later.
+constexpr int VM_MINS = 128;
+__host__ __device__ constexpr int vm_scale_off(int s, int g) { return OFF_VM + 16 * (s >> 1) + 4 * g + 2 * (s & 1); }
 
 // decode workspace: [header 256 B][tickets][partials]
 constexpr int WS_HEADER = 256;

@@ -66,10 +66,13 @@ const char* kvq_last_error(void);
  *   [   0,  512) K codes, 16 slots x 32 B
  *   [ 512,  768) K meta, 16 slots x 4 groups x (fp16 scale, fp16 min)
  *   [ 768, 1280) V codes
- *   [1280, 1536) V meta
+ *   [1280, 1408) V scales, 8 slot pairs x 4 groups x (fp16 of slot 2j, of slot 2j+1)
+ *   [1408, 1536) V mins, the same layout
  * The cache is tiles[num_pages][H_kv].  A 32-byte code record stores
  * channel 32*g + 4*b + c (g = 0..3 group, b = 0..7, c = 0..3) in bits
- * 2c..2c+1 of byte 4*b + g.  Returns 0 for unsupported d. */
+ * 2c..2c+1 of byte 4*b + g.  The value scale of slot s, group g is at byte
+ * 1280 + 16*(s/2) + 4*g + 2*(s%2), its min 128 bytes later.  Returns 0 for
+ * unsupported d. */
 size_t kvq_int2_tile_bytes(int d);
 
 /* Quantise-on-append of n_tok tokens into the INT2 cache.

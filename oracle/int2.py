@@ -19,10 +19,13 @@ Cache format (one 1536-byte tile per (page, KV head); pages of 16 slots):
   [   0,  512) K codes  16 slots x 32 B
   [ 512,  768) K meta   16 slots x 4 groups x (scale fp16, min fp16)
   [ 768, 1280) V codes  16 slots x 32 B
-  [1280, 1536) V meta   as K meta
+  [1280, 1408) V scales 8 slot pairs x 4 groups x (fp16 of slot 2j, of slot 2j+1)
+  [1408, 1536) V mins   the same for the mins
   cache[page][kv_head] tiles, row-major.  Code record of a 128-channel
   rotated vector: byte 4*b + g (b = 0..7, g = 0..3) holds channels
-  32*g + 4*b + c (c = 0..3) in bits 2c..2c+1.
+  32*g + 4*b + c (c = 0..3) in bits 2c..2c+1.  The value meta is stored
+  pair-major (a 4-byte word holds one group's scales, or mins, of two
+  adjacent slots): a layout choice of this library, not of the method.
 """
 from __future__ import annotations
 
@@ -148,6 +151,19 @@ def unpack_meta(raw: np.ndarray):
     return h[..., 0], h[..., 1]
 
 
+def meta_bytes(side: int, s: int) -> np.ndarray:
+    """Tile byte offsets of slot s's 16-byte meta record (pack_meta order:
+    per group scale lo, hi, min lo, hi) for side 0 (keys) or 1 (values)."""
+    if side == 0:
+        return OFF_K_META + META_BYTES * s + np.arange(META_BYTES)
+    pair, half = divmod(s, 2)
+    idx = []
+    for g in range(N_GROUPS):
+        base = OFF_V_META + 16 * pair + 4 * g + 2 * half
+        idx += [base, base + 1, base + 128, base + 129]
+    return np.asarray(idx)
+
+
 # --------------------------------------------------------------------------
 # quantise-on-append
 # --------------------------------------------------------------------------
@@ -197,14 +213,14 @@ def append(cache, k, v, slot_mapping, mu32, rk32, rv32, exact_chain=True, clip=1
         w32, _ = rotate_values(v[keep, h], rv32[h], exact_chain)
         z_all[keep, h] = z32
         w_all[keep, h] = w32
-        for src, off_c, off_m in ((z32, OFF_K_CODES, OFF_K_META), (w32, OFF_V_CODES, OFF_V_META)):
+        for side, src, off_c in ((0, z32, OFF_K_CODES), (1, w32, OFF_V_CODES)):
             codes, sc, mn = quantize(src, clip)
             recs = pack_codes(codes)
             metas = pack_meta(sc, mn)
             for i, slot in enumerate(sm[keep]):
                 page, s = divmod(int(slot), PAGE)
                 cache[page, h, off_c + CODE_BYTES * s: off_c + CODE_BYTES * (s + 1)] = recs[i]
-                cache[page, h, off_m + META_BYTES * s: off_m + META_BYTES * (s + 1)] = metas[i]
+                cache[page, h, meta_bytes(side, s)] = metas[i]
     return {"z": z_all, "w": w_all}
 
 
@@ -216,13 +232,13 @@ def read_tokens(cache, page_ids, n_tokens, h):
     n_pages = (n_tokens + PAGE - 1) // PAGE
     tiles = cache[np.asarray(page_ids[:n_pages], dtype=np.int64), h]      # [P, 1536]
 
-    def side(off_c, off_m):
+    def side(which, off_c):
         recs = tiles[:, off_c: off_c + PAGE * CODE_BYTES].reshape(-1, CODE_BYTES)
-        meta = tiles[:, off_m: off_m + PAGE * META_BYTES].reshape(-1, META_BYTES)
+        meta = tiles[:, np.stack([meta_bytes(which, s) for s in range(PAGE)])].reshape(-1, META_BYTES)
         sc, mn = unpack_meta(meta)
         return dequantize(unpack_codes(recs), sc, mn)[:n_tokens]
 
-    return side(OFF_K_CODES, OFF_K_META), side(OFF_V_CODES, OFF_V_META)
+    return side(0, OFF_K_CODES), side(1, OFF_V_CODES)
 
 
 # --------------------------------------------------------------------------

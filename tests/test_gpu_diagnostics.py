@@ -48,9 +48,10 @@ def test_clipped_append_and_read_back_bit_exact(clip):
         for side, got in ((0, zk), (1, zv)):
             n = k.shape[0]
             tiles = cache[bt[: (n + 15) // 16], h]
-            off_c, off_m = (int2.OFF_K_CODES, int2.OFF_K_META) if side == 0 else (int2.OFF_V_CODES, int2.OFF_V_META)
+            off_c = int2.OFF_K_CODES if side == 0 else int2.OFF_V_CODES
             recs = tiles[:, off_c: off_c + 16 * 32].reshape(-1, 32)[:n]
-            sc, mn = int2.unpack_meta(tiles[:, off_m: off_m + 16 * 16].reshape(-1, 16)[:n])
+            meta = tiles[:, np.stack([int2.meta_bytes(side, s) for s in range(16)])].reshape(-1, 16)[:n]
+            sc, mn = int2.unpack_meta(meta)
             want = int2.dequantize_f32(int2.unpack_codes(recs), sc, mn)
             assert np.array_equal(got[:, h].cpu().numpy(), want)
 

@@ -193,8 +193,8 @@ def test_decode_shapes_on_oracle_cache(h_q, h_kv, ctxs, splits, permute):
         if T % 16:
             tile = cache_gpu[bt[b, (T - 1) // 16]]
             for s in range(T % 16, 16):
-                tile[:, int2.OFF_K_META + 16 * s: int2.OFF_K_META + 16 * s + 16] = 0xFF
-                tile[:, int2.OFF_V_META + 16 * s: int2.OFF_V_META + 16 * s + 16] = 0xFF
+                tile[:, int2.meta_bytes(0, s)] = 0xFF
+                tile[:, int2.meta_bytes(1, s)] = 0xFF
                 tile[:, int2.OFF_V_CODES + 32 * s: int2.OFF_V_CODES + 32 * s + 32] = 0xFF
     layer.cache.copy_(torch.as_tensor(cache_gpu))
     cl = torch.as_tensor(ctx_lens, device="cuda")
@@ -267,9 +267,9 @@ def _sampled_check(spec, layer_idx, samples, splits=0, token_samples=256, exact=
         gpu_tiles = layer.cache[:, h].cpu().numpy()
         for t in idx:
             page, s = divmod(int(slots[t]), 16)
-            for off, n in ((int2.OFF_K_CODES + 32 * s, 32), (int2.OFF_K_META + 16 * s, 16),
-                           (int2.OFF_V_CODES + 32 * s, 32), (int2.OFF_V_META + 16 * s, 16)):
-                assert np.array_equal(gpu_tiles[page, off:off + n], small[page, 0, off:off + n]), (b, h, t)
+            for idx in (int2.OFF_K_CODES + 32 * s + np.arange(32), int2.meta_bytes(0, s),
+                        int2.OFF_V_CODES + 32 * s + np.arange(32), int2.meta_bytes(1, s)):
+                assert np.array_equal(gpu_tiles[page, idx], small[page, 0, idx]), (b, h, t)
         # attention of the sampled (sequence, KV head); with exact=False the
         # oracle decides codes from its fp64 rotation (rare ties differ)
         full = int2.new_cache(layer.num_pages, 1)

@@ -57,8 +57,8 @@ def test_window_decode_matches_oracle(h_q, h_kv, ctxs, wins, win_max, splits):
         if T % 16:
             tile = cache_gpu[bt[b, (T - 1) // 16]]
             for s in range(T % 16, 16):
-                tile[:, int2.OFF_K_META + 16 * s: int2.OFF_K_META + 16 * s + 16] = 0xFF
-                tile[:, int2.OFF_V_META + 16 * s: int2.OFF_V_META + 16 * s + 16] = 0xFF
+                tile[:, int2.meta_bytes(0, s)] = 0xFF
+                tile[:, int2.meta_bytes(1, s)] = 0xFF
     layer.cache.copy_(torch.as_tensor(cache_gpu))
     kw = _bf16_round((rng.standard_normal((B, win_max, h_kv, 128)) * 2 + mu * 0.5).astype(np.float32))
     vw = _bf16_round(rng.standard_normal((B, win_max, h_kv, 128)).astype(np.float32))

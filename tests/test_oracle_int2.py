@@ -149,6 +149,26 @@ def test_pack_layout_and_roundtrip():
     assert np.array_equal(s2, sc) and np.array_equal(m2, mn)
 
 
+def test_meta_placement_covers_the_tile():
+    """Key meta: one 16-byte record per slot; value meta: pair-major words
+    (scales of slots 2j, 2j+1 of one group, then the same for the mins)."""
+    for side, lo in ((0, int2.OFF_K_META), (1, int2.OFF_V_META)):
+        allb = np.concatenate([int2.meta_bytes(side, s) for s in range(int2.PAGE)])
+        assert sorted(allb.tolist()) == list(range(lo, lo + 256))
+    assert int2.meta_bytes(0, 3).tolist() == list(range(512 + 48, 512 + 64))
+    # slot 3 = pair 1, upper half; group 2: scale bytes 1280 + 16 + 8 + 2, min bytes 128 further
+    assert int2.meta_bytes(1, 3)[8:12].tolist() == [1306, 1307, 1434, 1435]
+    assert int2.meta_bytes(1, 0)[:4].tolist() == [1280, 1281, 1408, 1409]
+    # a tile written by append: slot 5's value scales sit in the pair-2 words
+    cache = int2.new_cache(1, 1)
+    w = np.zeros((6, 1, 128), np.float32)
+    w[5, 0, :32] = np.linspace(0.0, 3.0, 32)         # group 0: min 0, scale 1
+    int2.append(cache, np.zeros_like(w), w, np.arange(6), np.zeros((1, 128), np.float32),
+                np.eye(128, dtype=np.float32)[None], np.eye(128, dtype=np.float32)[None])
+    word = cache[0, 0, 1280 + 16 * 2: 1280 + 16 * 2 + 4].view(np.float16)
+    assert word.tolist() == [0.0, 1.0]                 # (slot 4, slot 5) scales of group 0
+
+
 # ---------------------------------------------------------------- end to end
 
 def _lattice_keys(rng, n, mu, r):
