@@ -171,6 +171,17 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         const char* rv = reinterpret_cast<const char*>(Rv + (size_t)h * D * D);
         for (int l = tid; l < D * D * 4 / 128; l += NW * 32) prefetch_l2_keep(rv + 128 * l);
     }
+    {
+        // The inputs the prologue reads first -- this warp's first block-table
+        // entries, the context length, the query rows -- are only prefetched
+        // into L2 here; the loads that use them follow the wait.
+        const int S_pf = WIN ? S - 1 : S, k0_pf = split * NW + warp;
+        const int j = k0_pf + S_pf * NW * lane;
+        if (lane < DEC_STAGES + UNIT_PAGES && j < max_pages) prefetch_l2(block_table + (size_t)b * max_pages + j);
+        if (tid == 0) prefetch_l2(context_lens + b);
+        const char* qc = reinterpret_cast<const char*>(q + ((size_t)b * H_q + (size_t)h * G) * D);
+        if (tid < (G * D * 2 + 127) / 128) prefetch_l2(qc + 128 * tid);
+    }
     griddep_wait();  // every other input may come from the previous kernel in the stream
     if constexpr (WIN) {
         if (split == S - 1) {
@@ -254,30 +265,23 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                              INT2_TILE, bar);
         }
     };
-    // ---- first the page ids of the first units and their copies (lane 0);
-    // the rest of the prologue overlaps the copies.  Lane 0 keeps the ids of
+    // ---- the page ids of the first units (lane 0).  Their copies are
+    // issued after the query rotation, which runs while the ids arrive; the
+    // copies then fly during the B-fragment setup.  Lane 0 keeps the ids of
     // the next unit to issue, loaded one release before their use.
     int pid_next[UNIT_PAGES];
     int n_issued = 0;  // units issued so far (lane 0)
 #pragma unroll
     for (int e = 0; e < UNIT_PAGES; ++e) pid_next[e] = 0;
+    int pids[DEC_STAGES + UNIT_PAGES];
+#pragma unroll
+    for (int j = 0; j < DEC_STAGES + UNIT_PAGES; ++j) pids[j] = 0;
     if (lane == 0) {
         // bounded by the block table's row length, not the context, so these
         // loads need not wait for context_lens
-        int pids[DEC_STAGES + UNIT_PAGES];
 #pragma unroll
-        for (int j = 0; j < DEC_STAGES + UNIT_PAGES; ++j) pids[j] = page_of(j) < max_pages ? __ldg(bt + page_of(j)) : 0;
-#pragma unroll
-        for (int u = 0; u < DEC_UNITS; ++u)
-            if (u < n_units) {
-                int pu[UNIT_PAGES];
-#pragma unroll
-                for (int e = 0; e < UNIT_PAGES; ++e) pu[e] = pids[UNIT_PAGES * u + e];
-                issue_unit(u, pu);
-                n_issued = u + 1;
-            }
-#pragma unroll
-        for (int e = 0; e < UNIT_PAGES; ++e) pid_next[e] = pids[DEC_STAGES + e];
+        for (int j = 0; j < DEC_STAGES + UNIT_PAGES; ++j)
+            if (page_of(j) < max_pages) pids[j] = __ldg(bt + page_of(j));
     }
     {
         // the rest of this sequence's block table is read one entry at a
@@ -296,6 +300,19 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         }
         __syncthreads();
         rotate_rows<NW, MAXG>(sm.ms.o_final, Rk + (size_t)h * D * D, rr, G, scale_log2, sm.q, sm.ms);
+        if (lane == 0) {
+#pragma unroll
+            for (int u = 0; u < DEC_UNITS; ++u)
+                if (u < n_units) {
+                    int pu[UNIT_PAGES];
+#pragma unroll
+                    for (int e = 0; e < UNIT_PAGES; ++e) pu[e] = pids[UNIT_PAGES * u + e];
+                    issue_unit(u, pu);
+                    n_issued = u + 1;
+                }
+#pragma unroll
+            for (int e = 0; e < UNIT_PAGES; ++e) pid_next[e] = pids[DEC_STAGES + e];
+        }
         // per head: power-of-two pre-scale (max |q~| * sigma in [2^14, 2^15)) and group sums
         for (int jj = warp; jj < G; jj += NW) {
             float mx = 0.f;

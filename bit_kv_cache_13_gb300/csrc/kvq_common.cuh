@@ -127,6 +127,11 @@ __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wa
 __device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Ask L2 to fetch the 128-byte line at p and keep it ahead of streaming data.
+// Fetch a line into L2 without returning data.  L2 is the point of
+// coherence for global memory, so a prefetch issued before
+// griddepcontrol.wait cannot hand a later load a stale value: a write the
+// previous kernel makes afterwards lands in L2 too.
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 __device__ __forceinline__ void prefetch_l2_keep(const void* p) {
     asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
 }
