@@ -21,9 +21,15 @@
 //       tokens at a time go through a padded shared-memory transpose and are
 //       summed by column, which leaves each lane the logit of one token for
 //       one head (two heads for groups of 8).
-//   softmax  online, base 2, exact running maximum per head.
-//   PV  lane l owns channels 4l .. 4l+3: four codes cut from the value
-//       stream, C_v[code] r_v weighted by p of every head, fp32 fma.
+//   softmax  online, base 2, exact running maximum per head; p is rounded to
+//       fp16 once (p^), and the same p^ weights the values and the
+//       normaliser.
+//   PV  mma.sync m16n8k16 with rows = channels, K = the 16 tokens.  Lane
+//       (r, t) owns channels 16r .. 16r+15 (one contiguous 16 v_bits-bit
+//       field of each token's value stream): the MMA row pair (r, r + 8) of
+//       chunk m is channels 16r + 2m, 16r + 2m + 1.  A = C_v[code] / sqrt(128)
+//       as fp16 from a shared-memory table; B = p^ r_v as an exact fp16
+//       hi/lo pair (HMUL2, then HFMA2 for the remainder) in the N columns.
 #include <mutex>
 
 #include "bgtq_common.cuh"
@@ -54,7 +60,8 @@ struct __align__(16) BgDecodeSmem {
         float tr[NW][32][BgTr<MAXG>::W];  // per-warp transpose of partial dots
         float o_part[NW][MAXG][D];        // per-warp o' after the loop
     } u;
-    float pb[NW][PAGE][MAXG];  // softmax weights of the warp's current page
+    __half pbh[NW][MAXG][PAGE];  // p^ of the warp's current page, head-major
+    __half cb_vh[256];         // C_v / sqrt(128) as fp16 (PV A operand)
     float qt[MAXG][D];         // q~ in gathered order, times scale * log2(e)
     float qin[MAXG][D];
     float cb_k[8][BG_CB_STRIDE];  // C_b / sqrt(n_b) per width b (fp32), rows bank-skewed
@@ -71,7 +78,7 @@ __device__ __forceinline__ uint32_t bfe(uint32_t x, uint32_t pos, uint32_t len) 
     return y;
 }
 
-template <int MAXG>
+template <int MAXG, int VB>
 __global__ void __launch_bounds__(BgWarps<MAXG>::NW * 32, 1)
 bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G, const uint8_t* __restrict__ cache,
                    int64_t num_pages, const int32_t* __restrict__ block_table, int max_pages,
@@ -83,7 +90,7 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     constexpr int VPL = BgTr<MAXG>::VPL;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     BgDecodeSmem<NW, MAXG>& sm = *reinterpret_cast<BgDecodeSmem<NW, MAXG>*>(smem_raw);
-    const BgtqTile tl(total_bits, v_bits);
+    const BgtqTile tl(total_bits, VB);
     uint8_t* my_ring = smem_raw + align_up(sizeof(BgDecodeSmem<NW, MAXG>), 128) +
                        (size_t)(threadIdx.x >> 5) * n_stages * tl.bytes;
 
@@ -146,7 +153,10 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         const int bb = idx / 256 + 1, c = idx % 256;
         if (c < (1 << bb) && sm.L.n[bb] > 0) sm.cb_k[bb - 1][c] = scaled_centroid(codebooks, bb, c, sm.L.n[bb]);
     }
-    for (int c = tid; c < (1 << v_bits); c += NW * 32) sm.cb_v[c] = scaled_centroid(codebooks, v_bits, c, D);
+    for (int c = tid; c < (1 << VB); c += NW * 32) {
+        sm.cb_v[c] = scaled_centroid(codebooks, VB, c, D);
+        sm.cb_vh[c] = __float2half_rn(sm.cb_v[c]);
+    }
     if (tid < D) {
         // q~ at gathered position p = tid: sum_i q[dim(st + i)] Pi_n[i][p - st]
         const int p = tid;
@@ -188,16 +198,21 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     for (int jj = 0; jj < MAXG; ++jj)
 #pragma unroll
         for (int e = 0; e < 4; ++e) qv[jj][e] = sm.qt[jj][p0 + e];
-    // ---- this lane's value channels 4l .. 4l+3 (4 v_bits contiguous bits)
-    const int vbit = 4 * v_bits * lane;
-    const int vwi = vbit >> 5, vsh = vbit & 31;
+    // ---- this lane's value field: channels 16r .. 16r+15, the 16 VB bits
+    // at bit 16 VB r of a token's value stream, in VW words from vword on
+    // (shifted down by vshift = 0 or 16)
+    const int r = lane >> 2, t = lane & 3;
+    constexpr int VW = (VB + 1) / 2;
+    const int vword = (VB * r) >> 1, vshift = 16 * ((VB * r) & 1);
 
-    float o[MAXG][4];
+    // PV accumulators: chunk m, C fragment (row r, r + 8 = channels 16r + 2m,
+    // 16r + 2m + 1; columns 2t, 2t + 1)
+    float oacc[8][4];
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) oacc[m][e] = 0.f;
     float mrun[VPL], lsum[VPL];
-#pragma unroll
-    for (int jj = 0; jj < MAXG; ++jj)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[jj][e] = 0.f;
 #pragma unroll
     for (int e = 0; e < VPL; ++e) {
         mrun[e] = -CUDART_INF_F;
@@ -299,38 +314,93 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             const int jj = VPL * (lane & 3) + e;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                const float p = ex2(lg[half][e] - mref);
-                lsum[e] = fmaf(lsum[e], half == 0 ? corr[e] : 1.f, p);
-                sm.pb[warp][8 * half + (lane >> 2)][jj] = p;
+                const __half ph = __float2half_rn(ex2(lg[half][e] - mref));
+                lsum[e] = fmaf(lsum[e], half == 0 ? corr[e] : 1.f, __half2float(ph));
+                sm.pbh[warp][jj][8 * half + (lane >> 2)] = ph;
             }
         }
         if (__any_sync(0xffffffffu, need)) {
+            // PV columns 2t, 2t + 1: heads (2t) & 3, (2t + 1) & 3 for groups up
+            // to 4 (columns 4..7 hold the low parts), heads 2t, 2t + 1 for 8
+            float cA, cB;
+            if constexpr (VPL == 1) {
+                cA = __shfl_sync(0xffffffffu, corr[0], (2 * t) & 3);
+                cB = __shfl_sync(0xffffffffu, corr[0], (2 * t + 1) & 3);
+            } else {
+                cA = __shfl_sync(0xffffffffu, corr[0], t);
+                cB = __shfl_sync(0xffffffffu, corr[1], t);
+            }
 #pragma unroll
-            for (int jj = 0; jj < MAXG; ++jj) {
-                const float c = __shfl_sync(0xffffffffu, corr[jj % VPL], jj / VPL);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) o[jj][e] *= c;
+            for (int m = 0; m < 8; ++m) {
+                oacc[m][0] *= cA;
+                oacc[m][2] *= cA;
+                oacc[m][1] *= cB;
+                oacc[m][3] *= cB;
             }
         }
         __syncwarp();
 
-        // ---- PV: this lane's channels 4l .. 4l+3
-#pragma unroll 2
-        for (int s = 0; s < n_tok; ++s) {
-            const uint32_t* vr = reinterpret_cast<const uint32_t*>(tile + tl.off_vc + s * tl.vb);
-            const uint32_t x = __funnelshift_r(vr[vwi], vr[vwi + 1], vsh);
-            const float rv = __half2float(reinterpret_cast<const __half*>(tile + tl.off_vn)[s]);
-            float cv[4];
+        // ---- PV: B = p^ r_v for column n = r (head r & 3, hi for r < 4 and
+        // lo for r >= 4; head r, hi then lo, for groups of 8); rows k =
+        // tokens 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1).  Slots past the context
+        // get r_v = 0 (their p^ is 0, but a stale norm may be NaN).
+        {
+            const int hq = VPL == 1 ? (r & 3) : r;
+            const uint32_t* vn = reinterpret_cast<const uint32_t*>(tile + tl.off_vn);
+            uint32_t R0 = vn[t], R1 = vn[t + 4];
+            if (!full) {
+                const uint32_t lo16 = 0x0000ffffu, hi16 = 0xffff0000u;
+                R0 &= (2 * t < n_tok ? lo16 : 0u) | (2 * t + 1 < n_tok ? hi16 : 0u);
+                R1 &= (2 * t + 8 < n_tok ? lo16 : 0u) | (2 * t + 9 < n_tok ? hi16 : 0u);
+            }
+            uint32_t P0 = 0u, P1 = 0u;
+            if (hq < G) {
+                P0 = lds32(&sm.pbh[warp][hq][2 * t]);
+                P1 = lds32(&sm.pbh[warp][hq][2 * t + 8]);
+            }
+            const __half2 H0 = __hmul2(u32_as_h2(P0), u32_as_h2(R0)), H1 = __hmul2(u32_as_h2(P1), u32_as_h2(R1));
+            const __half2 L0 = __hfma2(u32_as_h2(P0), u32_as_h2(R0), __hneg2(H0));
+            const __half2 L1 = __hfma2(u32_as_h2(P1), u32_as_h2(R1), __hneg2(H1));
+            uint32_t bh0 = h2_as_u32(H0), bh1 = h2_as_u32(H1), bl0 = h2_as_u32(L0), bl1 = h2_as_u32(L1);
+            if constexpr (VPL == 1) {
+                if (r >= 4) {
+                    bh0 = bl0;
+                    bh1 = bl1;
+                }
+            }
+
+            // this lane's value fields of tokens 2t, 2t+1, 2t+8, 2t+9, aligned
+            uint32_t f[4][VW];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) cv[e] = sm.cb_v[bfe(x, e * v_bits, v_bits)];
+            for (int k = 0; k < 4; ++k) {
+                const int s_tok = 2 * t + (k & 1) + 8 * (k >> 1);
+                const uint32_t* vr = reinterpret_cast<const uint32_t*>(tile + tl.off_vc + s_tok * tl.vb) + vword;
+                uint32_t w[VW];
 #pragma unroll
-            for (int c = 0; c < MAXG; c += 4) {
-                const float4 p4 = *reinterpret_cast<const float4*>(&sm.pb[warp][s][c]);
-                const float w[4] = {p4.x * rv, p4.y * rv, p4.z * rv, p4.w * rv};
+                for (int q2 = 0; q2 < VW; ++q2) w[q2] = vr[q2];
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
+                for (int q2 = 0; q2 < VW; ++q2) f[k][q2] = __funnelshift_r(w[q2], q2 + 1 < VW ? w[q2 + 1] : 0u, vshift);
+            }
+            // code of channel 16r + i in field k
+            auto code = [&](int k, int i) -> uint32_t {
+                const int bit = VB * i, wi = bit >> 5, sh = bit & 31;
+                uint32_t x = f[k][wi] >> sh;
+                if (sh + VB > 32) x |= f[k][wi + 1] << (32 - sh);
+                return x & ((1u << VB) - 1u);
+            };
+            const unsigned short* cbv = reinterpret_cast<const unsigned short*>(sm.cb_vh);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) o[c + u][e] = fmaf(w[u], cv[e], o[c + u][e]);
+            for (int m = 0; m < 8; ++m) {
+                uint32_t hv[4][2];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    hv[k][0] = cbv[code(k, 2 * m)];
+                    hv[k][1] = cbv[code(k, 2 * m + 1)];
+                }
+                const uint32_t a[4] = {hv[0][0] | (hv[1][0] << 16), hv[0][1] | (hv[1][1] << 16),
+                                       hv[2][0] | (hv[3][0] << 16), hv[2][1] | (hv[3][1] << 16)};
+                mma_f16_16816(oacc[m], a, bh0, bh1);
+                if constexpr (VPL == 2) mma_f16_16816(oacc[m], a, bl0, bl1);
             }
         }
 
@@ -353,12 +423,27 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         lsum[e] += __shfl_xor_sync(0xffffffffu, lsum[e], 16);
     }
     __syncthreads();  // all warps are done with the transpose buffers (o_part aliases them)
+    if constexpr (VPL == 1) {
+        // columns 4..7 (lanes t = 2, 3) hold the low parts of heads 0..3
 #pragma unroll
-    for (int jj = 0; jj < MAXG; ++jj)
-        if (jj < G) {
+        for (int m = 0; m < 8; ++m)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sm.u.o_part[warp][jj][4 * lane + e] = o[jj][e];
+            for (int e = 0; e < 4; ++e) oacc[m][e] += __shfl_xor_sync(0xffffffffu, oacc[m][e], 2);
+    }
+    if (VPL == 2 || t < 2) {
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int c0 = 16 * r + 2 * m;
+            if (2 * t < G) {
+                sm.u.o_part[warp][2 * t][c0] = oacc[m][0];
+                sm.u.o_part[warp][2 * t][c0 + 1] = oacc[m][2];
+            }
+            if (2 * t + 1 < G) {
+                sm.u.o_part[warp][2 * t + 1][c0] = oacc[m][1];
+                sm.u.o_part[warp][2 * t + 1][c0 + 1] = oacc[m][3];
+            }
         }
+    }
     if (lane < 4) {
 #pragma unroll
         for (int e = 0; e < VPL; ++e) {
@@ -377,6 +462,16 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
 }  // namespace kvq
 
 using namespace kvq;
+
+namespace {
+// instances by (head group up to 4 / up to 8, value width 1..8)
+using BgKernel = decltype(&bgtq_decode_kernel<4, 1>);
+const BgKernel kBgKernels[2][8] = {
+    {bgtq_decode_kernel<4, 1>, bgtq_decode_kernel<4, 2>, bgtq_decode_kernel<4, 3>, bgtq_decode_kernel<4, 4>,
+     bgtq_decode_kernel<4, 5>, bgtq_decode_kernel<4, 6>, bgtq_decode_kernel<4, 7>, bgtq_decode_kernel<4, 8>},
+    {bgtq_decode_kernel<8, 1>, bgtq_decode_kernel<8, 2>, bgtq_decode_kernel<8, 3>, bgtq_decode_kernel<8, 4>,
+     bgtq_decode_kernel<8, 5>, bgtq_decode_kernel<8, 6>, bgtq_decode_kernel<8, 7>, bgtq_decode_kernel<8, 8>}};
+}  // namespace
 
 // one CTA per SM, as the INT2 decode (kvq_decode_auto_splits)
 int bgtq_decode_auto_splits(int B, int H_q, int H_kv, int max_pages_per_seq) {
@@ -419,25 +514,27 @@ extern "C" kvq_status bgtq_decode_attn(const void* q, int B, int H_q, int H_kv, 
     if (n_stages < 2)
         return kvq_set_error(KVQ_ERR_UNSUPPORTED, "bgtq_decode_attn: %d-byte tiles leave no room for two stages", tile);
     const size_t smem = fixed + (size_t)NW * n_stages * tile;
-    const void* fn = small ? (const void*)bgtq_decode_kernel<4> : (const void*)bgtq_decode_kernel<8>;
+    const BgKernel kern = kBgKernels[small ? 0 : 1][v_bits - 1];
+    const int kid = (small ? 0 : 8) + v_bits - 1;
     {
         // opt in once per device and kernel, to the full shared-memory size
         static std::mutex mu;
-        static bool done[64][2] = {};
+        static bool done[64][16] = {};
         int dev = 0;
         kvq_status s2 = kvq_check_cuda(cudaGetDevice(&dev), "bgtq_decode_attn: cudaGetDevice");
         if (s2 != KVQ_OK) return s2;
         std::lock_guard<std::mutex> lock(mu);
-        if (dev < 0 || dev >= 64 || !done[dev][small ? 0 : 1]) {
-            s2 = kvq_check_cuda(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMax),
-                                "bgtq_decode_attn smem attribute");
+        if (dev < 0 || dev >= 64 || !done[dev][kid]) {
+            s2 = kvq_check_cuda(
+                cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMax),
+                "bgtq_decode_attn smem attribute");
             if (s2 != KVQ_OK) return s2;
-            if (dev >= 0 && dev < 64) done[dev][small ? 0 : 1] = true;
+            if (dev >= 0 && dev < 64) done[dev][kid] = true;
         }
     }
     dim3 grid(S, H_kv, B);
     const cudaError_t e =
-        launch_pdl(small ? bgtq_decode_kernel<4> : bgtq_decode_kernel<8>, grid, dim3(NW * 32), smem,
+        launch_pdl(kern, grid, dim3(NW * 32), smem,
                    static_cast<cudaStream_t>(stream), static_cast<const __nv_bfloat16*>(q), H_q, H_kv, G,
                    static_cast<const uint8_t*>(cache), num_pages, block_table, max_pages_per_seq, context_lens, widths,
                    total_bits, v_bits, pi_table, pi_offsets, codebooks, scale * 1.4426950408889634f, out,

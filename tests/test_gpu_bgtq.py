@@ -109,6 +109,36 @@ def test_decode_vs_oracle(table, h_q, h_kv, ctxs, splits):
         _close(out[b].cpu().numpy(), ref[b])
 
 
+@pytest.mark.parametrize("avg_bits,v_bits,b_max,h_q", [(2, 2, 8, 8), (1, 1, 8, 8), (8, 8, 8, 16), (4, 5, 6, 16),
+                                                     (3, 4, 8, 8), (3, 6, 8, 16), (3, 7, 8, 8)])
+def test_decode_value_widths(table, avg_bits, v_bits, b_max, h_q):
+    """Every value width has its own kernel instance (groups up to 4 and of 8)."""
+    ctxs = [70, 33]
+    spec = _spec(f"bgvw{avg_bits}{v_bits}{h_q}", h_q=h_q, h_kv=2, batch=2, ctx=max(ctxs), avg_bits=avg_bits,
+                 v_bits=v_bits, b_max=b_max, permute=True)
+    layer = BgtqLayer(spec, 0, codebooks=table)
+    cache = bgtq.new_cache(layer.num_pages, 2, layer.total_bits, layer.v_bits)
+    bt = layer.block_table.cpu().numpy()
+    pis = _pis(layer)
+    for b, T in enumerate(ctxs):
+        k, v = layer.history_kv(b, device="cpu")
+        slots = np.array([bt[b, t // 16] * 16 + t % 16 for t in range(T)])
+        bgtq.append(cache, _f32(k[:T]), _f32(v[:T]), slots, layer.widths_np, layer.v_bits, layer.total_bits, pis,
+                    table)
+    layer.cache.copy_(torch.as_tensor(cache))
+    q = layer.queries()
+    cl = torch.tensor(ctxs, dtype=torch.int32, device="cuda")
+    out = torch.full((2, h_q, 128), float("nan"), device="cuda")
+    ws = layer.workspace()
+    layer.decode(q, out, ws, 0, context_lens=cl)
+    torch.cuda.synchronize()
+    assert _lib.kvq_workspace_status(ws) == 0
+    ref = bgtq.decode(q.cpu().double().numpy(), cache, bt, ctxs, layer.widths_np, layer.v_bits, layer.total_bits,
+                      pis, table, layer.scale, 2)
+    for b in range(2):
+        _close(out[b].cpu().numpy(), ref[b])
+
+
 def test_end_to_end_append_then_decode(table):
     spec = _spec("bge2e", h_q=8, h_kv=2, ctx=150)
     layer = BgtqLayer(spec, 0, codebooks=table)
