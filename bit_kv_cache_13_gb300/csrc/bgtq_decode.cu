@@ -72,11 +72,6 @@ struct __align__(16) BgDecodeSmem {
     MergeSmem<NW, MAXG> ms;
 };
 
-__device__ __forceinline__ uint32_t bfe(uint32_t x, uint32_t pos, uint32_t len) {
-    uint32_t y;
-    asm("bfe.u32 %0, %1, %2, %3;" : "=r"(y) : "r"(x), "r"(pos), "r"(len));
-    return y;
-}
 
 template <int MAXG, int VB>
 __global__ void __launch_bounds__(BgWarps<MAXG>::NW * 32, 1)
@@ -190,7 +185,8 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         bitA = sm.L.bitstart[wA] + (p0 - sm.L.start[wA]) * wA;
     }
     const int kwi = bitA >> 5, ksh = bitA & 31;
-    const uint32_t posB0 = 2 * wA, posB1 = 2 * wA + wB;
+    const uint32_t posA1 = wA, posB0 = 2 * wA, posB1 = 2 * wA + wB;
+    const uint32_t maskA = (1u << wA) - 1u, maskB = (1u << wB) - 1u;
     const float* cbA = sm.cb_k[wA - 1];
     const float* cbB = sm.cb_k[wB - 1];
     float qv[MAXG][4];
@@ -238,8 +234,8 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             const uint32_t x = __funnelshift_r(rec[kwi], rec[kwi + 1], ksh);
             const __half* nr = reinterpret_cast<const __half*>(tile + tl.off_kn + 16 * s);
             const float rA = __half2float(nr[wA - 1]), rB = __half2float(nr[wB - 1]);
-            const float v0 = cbA[bfe(x, 0, wA)] * rA, v1 = cbA[bfe(x, wA, wA)] * rA;
-            const float v2 = cbB[bfe(x, posB0, wB)] * rB, v3 = cbB[bfe(x, posB1, wB)] * rB;
+            const float v0 = cbA[x & maskA] * rA, v1 = cbA[(x >> posA1) & maskA] * rA;
+            const float v2 = cbB[(x >> posB0) & maskB] * rB, v3 = cbB[(x >> posB1) & maskB] * rB;
 #pragma unroll
             for (int jj = 0; jj < MAXG; ++jj)
                 part[jj] = fmaf(qv[jj][0], v0, fmaf(qv[jj][1], v1, fmaf(qv[jj][2], v2, qv[jj][3] * v3)));
