@@ -37,34 +37,36 @@
 namespace kvq {
 
 constexpr int BG_MAX_STAGES = 8;
-// Codebook rows 264 floats apart: width b's table starts 8(b-1) banks on, so
-// lanes of different widths reading small codes hit different banks.
-constexpr int BG_CB_STRIDE = 264;
 
 template <int MAXG>
 struct BgWarps {
     static constexpr int NW = MAXG <= 4 ? 12 : 8;
 };
 
-// values per lane after one 8-token transpose, and the transpose row length
-// (padded so that the rows of 8 consecutive lanes fall in distinct banks)
-template <int MAXG>
-struct BgTr {
-    static constexpr int VPL = MAXG / 4;
-    static constexpr int W = 8 * MAXG + 4;
+// QK works on chunks of 16 gathered positions of one width (a group's
+// positions padded to a multiple of 16): at most 64/8 + 7 = 15 chunks.
+constexpr int BG_MAX_CHUNKS = 16;
+struct BgChunk {
+    int bit0;      // first code bit of the chunk in a token's key stream
+    int8_t b;      // width
+    int8_t last;   // the last chunk of its width group
+    int16_t pos0;  // first gathered position
 };
 
 template <int NW, int MAXG>
 struct __align__(16) BgDecodeSmem {
     union {
-        float tr[NW][32][BgTr<MAXG>::W];  // per-warp transpose of partial dots
-        float o_part[NW][MAXG][D];        // per-warp o' after the loop
+        float o_part[NW][MAXG][D];  // per-warp o' after the loop
     } u;
+    uint2 bfr[BG_MAX_CHUNKS][MAXG / 4][32];  // QK B fragments per chunk, n-tile and lane
+    uint32_t cbk2[8][256];  // C_b / sqrt(n_b) per width as (fp16 hi | fp16 lo << 16)
+    BgChunk chunks[BG_MAX_CHUNKS];
+    int n_chunks;
+    float sigma[MAXG];      // power-of-two pre-scale per head
     __half pbh[NW][MAXG][PAGE];  // p^ of the warp's current page, head-major
     __half cb_vh[256];         // C_v / sqrt(128) as fp16 (PV A operand)
     float qt[MAXG][D];         // q~ in gathered order, times scale * log2(e)
     float qin[MAXG][D];
-    float cb_k[8][BG_CB_STRIDE];  // C_b / sqrt(n_b) per width b (fp32), rows bank-skewed
     float cb_v[256];           // C_v / sqrt(128)
     uint64_t bar[NW][BG_MAX_STAGES];
     int ntok[NW][BG_MAX_STAGES];
@@ -82,7 +84,6 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                    const double* __restrict__ codebooks, float scale_log2, float* __restrict__ out,
                    uint8_t* __restrict__ ws, int n_stages) {
     constexpr int NW = BgWarps<MAXG>::NW;
-    constexpr int VPL = BgTr<MAXG>::VPL;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     BgDecodeSmem<NW, MAXG>& sm = *reinterpret_cast<BgDecodeSmem<NW, MAXG>*>(smem_raw);
     const BgtqTile tl(total_bits, VB);
@@ -137,8 +138,21 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         for (int l = tid; l < D * D * 4 / 128; l += NW * 32) prefetch_l2_keep(rot + 128 * l);
     }
 
-    // ---- per-head layout, codebooks and rotated queries
-    if (tid == 0) build_layout(widths + h * (D / 2), sm.L);
+    // ---- per-head layout, chunk schedule, codebooks and rotated queries
+    if (tid == 0) {
+        build_layout(widths + h * (D / 2), sm.L);
+        int nc = 0;
+        for (int bb = 1; bb <= 8; ++bb)
+            for (int c = 0; c < (sm.L.n[bb] + 15) / 16 && nc < BG_MAX_CHUNKS; ++c) {
+                BgChunk ch;
+                ch.bit0 = sm.L.bitstart[bb] + 16 * c * bb;
+                ch.b = (int8_t)bb;
+                ch.last = (int8_t)(16 * (c + 1) >= sm.L.n[bb]);
+                ch.pos0 = (int16_t)(sm.L.start[bb] + 16 * c);
+                sm.chunks[nc++] = ch;
+            }
+        sm.n_chunks = nc;
+    }
     const __nv_bfloat16* qb = q + ((size_t)b * H_q + (size_t)h * G) * D;
     for (int idx = tid; idx < G * D; idx += NW * 32) sm.qin[idx / D][idx % D] = __bfloat162float(qb[idx]);
     __syncthreads();
@@ -146,7 +160,12 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     if (!layout_ok && tid == 0) atomicOr(err_word, ERR_BAD_WIDTHS);
     for (int idx = tid; idx < 8 * 256; idx += NW * 32) {
         const int bb = idx / 256 + 1, c = idx % 256;
-        if (c < (1 << bb) && sm.L.n[bb] > 0) sm.cb_k[bb - 1][c] = scaled_centroid(codebooks, bb, c, sm.L.n[bb]);
+        if (c < (1 << bb) && sm.L.n[bb] > 0) {
+            // the scaled centroid as an fp16 hi/lo pair (about 22 significant bits)
+            const float v = scaled_centroid(codebooks, bb, c, sm.L.n[bb]);
+            const __half hi = __float2half_rn(v), lo = __float2half_rn(v - __half2float(hi));
+            sm.cbk2[bb - 1][c] = (uint32_t)__half_as_ushort(hi) | ((uint32_t)__half_as_ushort(lo) << 16);
+        }
     }
     for (int c = tid; c < (1 << VB); c += NW * 32) {
         sm.cb_v[c] = scaled_centroid(codebooks, VB, c, D);
@@ -175,29 +194,53 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         for (int jj = 0; jj < MAXG; ++jj) sm.qt[jj][p] = jj < G ? acc[jj] * scale_log2 : 0.f;
     }
     __syncthreads();
-
-    // ---- this lane's key positions 4l .. 4l+3: blocks A (4l, 4l+1) and B
-    const int p0 = 4 * lane;
-    int wA = 1, wB = 1, bitA = 0;
-    if (layout_ok) {
-        wA = group_of(sm.L, p0);
-        wB = group_of(sm.L, p0 + 2);
-        bitA = sm.L.bitstart[wA] + (p0 - sm.L.start[wA]) * wA;
+    // per head: power-of-two pre-scale so that max |q~| sigma is in [2^14, 2^15)
+    for (int jj = warp; jj < MAXG; jj += NW) {
+        float mx = 0.f;
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k) mx = fmaxf(mx, fabsf(sm.qt[jj][32 * k + lane]));
+#pragma unroll
+        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) sm.sigma[jj] = mx > 0.f ? ldexpf(1.f, 14 - ilogbf(mx)) : 1.f;
     }
-    const int kwi = bitA >> 5, ksh = bitA & 31;
-    const uint32_t posA1 = wA, posB0 = 2 * wA, posB1 = 2 * wA + wB;
-    const uint32_t maskA = (1u << wA) - 1u, maskB = (1u << wB) - 1u;
-    const float* cbA = sm.cb_k[wA - 1];
-    const float* cbB = sm.cb_k[wB - 1];
-    float qv[MAXG][4];
+    __syncthreads();
+
+    constexpr int NT = MAXG / 4;  // n-tiles of 8 columns (4 heads x hi/lo)
+    constexpr int VPL = NT;
+    const int r = lane >> 2, t = lane & 3;
+    // ---- QK B fragments: column n = r -> head 4 nt + (r >> 1), part r & 1
+    // (hi / lo of q~ sigma); rows k = 2t, 2t+1 (b0) are the chunk positions
+    // 4t, 4t+1 and k = 2t+8, 2t+9 (b1) the positions 4t+2, 4t+3, so a lane's
+    // two RoPE blocks are adjacent in the code stream; positions past the
+    // group are zero
+    const int NC = layout_ok ? sm.n_chunks : 0;
+    for (int idx = warp; idx < NC * NT; idx += NW) {
+        const int k = idx / NT, nt = idx % NT;
+        const BgChunk ch = sm.chunks[k];
+        const int hq = 4 * nt + (r >> 1), gend = sm.L.start[ch.b] + sm.L.n[ch.b];
+        uint32_t w[2];
 #pragma unroll
-    for (int jj = 0; jj < MAXG; ++jj)
+        for (int e = 0; e < 2; ++e) {
+            float v[2];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) qv[jj][e] = sm.qt[jj][p0 + e];
+            for (int u = 0; u < 2; ++u) {
+                const int p = ch.pos0 + 4 * t + 2 * e + u;
+                v[u] = (hq < G && p < gend) ? sm.qt[hq][p] * sm.sigma[hq] : 0.f;
+            }
+            const __half h0 = __float2half_rn(v[0]), h1 = __float2half_rn(v[1]);
+            w[e] = (r & 1) ? pack_half2(v[0] - __half2float(h0), v[1] - __half2float(h1))
+                           : h2_as_u32(__halves2half2(h0, h1));
+        }
+        sm.bfr[k][nt][lane] = make_uint2(w[0], w[1]);
+    }
+    float inv_sig[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) inv_sig[nt] = 4 * nt + t < G ? 1.f / sm.sigma[4 * nt + t] : 0.f;
+    __syncthreads();
+
     // ---- this lane's value field: channels 16r .. 16r+15, the 16 VB bits
     // at bit 16 VB r of a token's value stream, in VW words from vword on
     // (shifted down by vshift = 0 or 16)
-    const int r = lane >> 2, t = lane & 3;
     constexpr int VW = (VB + 1) / 2;
     const int vword = (VB * r) >> 1, vshift = 16 * ((VB * r) & 1);
 
@@ -208,13 +251,13 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     for (int m = 0; m < 8; ++m)
 #pragma unroll
         for (int e = 0; e < 4; ++e) oacc[m][e] = 0.f;
-    float mrun[VPL], lsum[VPL];
+    // online softmax state of head 4 nt + t
+    float mrun[NT], lsum[NT];
 #pragma unroll
-    for (int e = 0; e < VPL; ++e) {
-        mrun[e] = -CUDART_INF_F;
-        lsum[e] = 0.f;
+    for (int nt = 0; nt < NT; ++nt) {
+        mrun[nt] = -CUDART_INF_F;
+        lsum[nt] = 0.f;
     }
-    float(*tr)[BgTr<MAXG>::W] = sm.u.tr[warp];
     bool timed_out = false;
 
     for (int i = 0; i < my_count; ++i) {
@@ -227,104 +270,103 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         }
         const uint8_t* tile = my_ring + (size_t)stage * tl.bytes;
         const int n_tok = layout_ok ? sm.ntok[warp][stage] : 0;
-
-        // ---- QK, 8 tokens at a time: partial dots -> transpose -> column sums
-        auto partial = [&](int s, float (&part)[MAXG]) {
-            const uint32_t* rec = reinterpret_cast<const uint32_t*>(tile + s * tl.kb);
-            const uint32_t x = __funnelshift_r(rec[kwi], rec[kwi + 1], ksh);
-            const __half* nr = reinterpret_cast<const __half*>(tile + tl.off_kn + 16 * s);
-            const float rA = __half2float(nr[wA - 1]), rB = __half2float(nr[wB - 1]);
-            const float v0 = cbA[x & maskA] * rA, v1 = cbA[(x >> posA1) & maskA] * rA;
-            const float v2 = cbB[(x >> posB0) & maskB] * rB, v3 = cbB[(x >> posB1) & maskB] * rB;
-#pragma unroll
-            for (int jj = 0; jj < MAXG; ++jj)
-                part[jj] = fmaf(qv[jj][0], v0, fmaf(qv[jj][1], v1, fmaf(qv[jj][2], v2, qv[jj][3] * v3)));
-        };
-        auto store = [&](int u, const float (&part)[MAXG]) {
-#pragma unroll
-            for (int c = 0; c < MAXG; c += 4)
-                *reinterpret_cast<float4*>(&tr[lane][u * MAXG + c]) =
-                    make_float4(part[c], part[c + 1], part[c + 2], part[c + 3]);
-        };
         const bool full = n_tok == PAGE;  // warp-uniform: every page but a sequence's last
-        float lg[2][VPL];
+
+        // ---- QK on the tensor cores, one chunk (16 positions of width b) at
+        // a time: A = C_b[code] / sqrt(n_b) as an fp16 hi/lo pair, rows =
+        // tokens r, r + 8, K = the chunk's positions (lane t: blocks t and
+        // t + 4 of the chunk); the group norm r_{s,b} scales the group's sum.
+        float lg[NT][2];
+        {
+            const uint32_t* rec0 = reinterpret_cast<const uint32_t*>(tile + r * tl.kb);
+            const uint32_t* rec8 = reinterpret_cast<const uint32_t*>(tile + (r + 8) * tl.kb);
+            const __half* nr0 = reinterpret_cast<const __half*>(tile + tl.off_kn + 16 * r);
+            const __half* nr8 = reinterpret_cast<const __half*>(tile + tl.off_kn + 16 * (r + 8));
+            float acc[NT][2], cg[NT][4];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            if (full) {
+            for (int nt = 0; nt < NT; ++nt) {
+                acc[nt][0] = acc[nt][1] = 0.f;
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    float part[MAXG];
-                    partial(8 * half + u, part);
-                    store(u, part);
+                for (int e = 0; e < 4; ++e) cg[nt][e] = 0.f;
+            }
+            for (int k = 0; k < NC; ++k) {
+                const BgChunk ch = sm.chunks[k];  // warp-uniform
+                const int bw = ch.b;
+                // this lane's blocks 2t, 2t+1 of the chunk: 4 bw contiguous bits
+                const int off = ch.bit0 + 4 * t * bw, wi = off >> 5, sh = off & 31;
+                const uint32_t x0 = __funnelshift_r(rec0[wi], rec0[wi + 1], sh);
+                const uint32_t x8 = __funnelshift_r(rec8[wi], rec8[wi + 1], sh);
+                // A registers: a0 token r block 2t, a1 token r+8 block 2t,
+                // a2 token r block 2t+1, a3 token r+8 block 2t+1
+                uint32_t ah[4], al[4];
+                const uint32_t* cb = sm.cbk2[bw - 1];
+                const uint32_t mask = (1u << bw) - 1u;
+                const uint32_t xs[4] = {x0, x8, x0 >> (2 * bw), x8 >> (2 * bw)};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t e0 = cb[xs[j] & mask], e1 = cb[(xs[j] >> bw) & mask];
+                    ah[j] = prmt(e0, e1, 0x5410);
+                    al[j] = prmt(e0, e1, 0x7632);
                 }
-            } else {
-                for (int u = 0; u < 8; ++u) {
-                    float part[MAXG];
-                    if (8 * half + u < n_tok) {
-                        partial(8 * half + u, part);
-                    } else {
 #pragma unroll
-                        for (int jj = 0; jj < MAXG; ++jj) part[jj] = 0.f;
+                for (int nt = 0; nt < NT; ++nt) {
+                    const uint2 bb = sm.bfr[k][nt][lane];
+                    mma_f16_16816(cg[nt], ah, bb.x, bb.y);
+                    mma_f16_16816(cg[nt], al, bb.x, bb.y);
+                }
+                if (ch.last) {
+                    const float rn0 = __half2float(nr0[bw - 1]), rn8 = __half2float(nr8[bw - 1]);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        acc[nt][0] = fmaf(rn0, cg[nt][0] + cg[nt][1], acc[nt][0]);
+                        acc[nt][1] = fmaf(rn8, cg[nt][2] + cg[nt][3], acc[nt][1]);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) cg[nt][e] = 0.f;
                     }
-                    store(u, part);
                 }
             }
-            __syncwarp();
-            // lane l sums column VPL*l + e over the 32 rows: token 8*half + l/4,
-            // head VPL*(l%4) + e
-            float acc[VPL];
 #pragma unroll
-            for (int e = 0; e < VPL; ++e) acc[e] = 0.f;
-#pragma unroll 8
-            for (int m = 0; m < 32; ++m) {
-                if constexpr (VPL == 1) {
-                    acc[0] += tr[m][lane];
-                } else {
-                    const float2 t2 = *reinterpret_cast<const float2*>(&tr[m][2 * lane]);
-                    acc[0] += t2.x;
-                    acc[1] += t2.y;
-                }
+            for (int nt = 0; nt < NT; ++nt) {
+                lg[nt][0] = r < n_tok ? acc[nt][0] * inv_sig[nt] : -CUDART_INF_F;
+                lg[nt][1] = r + 8 < n_tok ? acc[nt][1] * inv_sig[nt] : -CUDART_INF_F;
             }
-            __syncwarp();
-            const int s = 8 * half + (lane >> 2);
-#pragma unroll
-            for (int e = 0; e < VPL; ++e) lg[half][e] = s < n_tok ? acc[e] : -CUDART_INF_F;
         }
 
-        // ---- online softmax (base 2): this lane's heads VPL*(l%4) + e
-        float corr[VPL];
+        // ---- online softmax (base 2) of head 4 nt + t; p^ goes to pbh
+        float corr[NT];
         bool need = false;
 #pragma unroll
-        for (int e = 0; e < VPL; ++e) {
-            float pm = fmaxf(lg[0][e], lg[1][e]);
+        for (int nt = 0; nt < NT; ++nt) {
+            float pm = fmaxf(lg[nt][0], lg[nt][1]);
             pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
             pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
             pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-            corr[e] = 1.f;
-            if (pm > mrun[e]) {
-                corr[e] = ex2(mrun[e] - pm);
-                mrun[e] = pm;
+            corr[nt] = 1.f;
+            if (pm > mrun[nt]) {
+                corr[nt] = ex2(mrun[nt] - pm);
+                mrun[nt] = pm;
                 need = true;
             }
-            const float mref = mrun[e] == -CUDART_INF_F ? 0.f : mrun[e];
-            const int jj = VPL * (lane & 3) + e;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const __half ph = __float2half_rn(ex2(lg[half][e] - mref));
-                lsum[e] = fmaf(lsum[e], half == 0 ? corr[e] : 1.f, __half2float(ph));
-                sm.pbh[warp][jj][8 * half + (lane >> 2)] = ph;
+            const float mref = mrun[nt] == -CUDART_INF_F ? 0.f : mrun[nt];
+            const __half p0 = __float2half_rn(ex2(lg[nt][0] - mref)), p8 = __float2half_rn(ex2(lg[nt][1] - mref));
+            lsum[nt] = fmaf(lsum[nt], corr[nt], __half2float(p0) + __half2float(p8));
+            const int hq = 4 * nt + t;
+            if (hq < MAXG) {
+                sm.pbh[warp][hq][r] = p0;
+                sm.pbh[warp][hq][r + 8] = p8;
             }
         }
         if (__any_sync(0xffffffffu, need)) {
             // PV columns 2t, 2t + 1: heads (2t) & 3, (2t + 1) & 3 for groups up
-            // to 4 (columns 4..7 hold the low parts), heads 2t, 2t + 1 for 8
-            float cA, cB;
-            if constexpr (VPL == 1) {
-                cA = __shfl_sync(0xffffffffu, corr[0], (2 * t) & 3);
-                cB = __shfl_sync(0xffffffffu, corr[0], (2 * t + 1) & 3);
-            } else {
-                cA = __shfl_sync(0xffffffffu, corr[0], t);
-                cB = __shfl_sync(0xffffffffu, corr[1], t);
+            // to 4 (columns 4..7 hold the low parts), heads 2t, 2t + 1 for 8;
+            // head h's correction lives in lane h & 3, n-tile h >> 2
+            const int hA = 2 * t, hB = 2 * t + 1;
+            float cA = __shfl_sync(0xffffffffu, corr[0], hA & 3), cB = __shfl_sync(0xffffffffu, corr[0], hB & 3);
+            if constexpr (NT == 2) {
+                const float cA1 = __shfl_sync(0xffffffffu, corr[1], hA & 3);
+                const float cB1 = __shfl_sync(0xffffffffu, corr[1], hB & 3);
+                if (hA >= 4) cA = cA1;
+                if (hB >= 4) cB = cB1;
             }
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
@@ -413,12 +455,11 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
 
     // ---- warp partial: normalisers summed over the lanes of each head
 #pragma unroll
-    for (int e = 0; e < VPL; ++e) {
-        lsum[e] += __shfl_xor_sync(0xffffffffu, lsum[e], 4);
-        lsum[e] += __shfl_xor_sync(0xffffffffu, lsum[e], 8);
-        lsum[e] += __shfl_xor_sync(0xffffffffu, lsum[e], 16);
+    for (int nt = 0; nt < NT; ++nt) {
+        lsum[nt] += __shfl_xor_sync(0xffffffffu, lsum[nt], 4);
+        lsum[nt] += __shfl_xor_sync(0xffffffffu, lsum[nt], 8);
+        lsum[nt] += __shfl_xor_sync(0xffffffffu, lsum[nt], 16);
     }
-    __syncthreads();  // all warps are done with the transpose buffers (o_part aliases them)
     if constexpr (VPL == 1) {
         // columns 4..7 (lanes t = 2, 3) hold the low parts of heads 0..3
 #pragma unroll
@@ -442,11 +483,11 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     }
     if (lane < 4) {
 #pragma unroll
-        for (int e = 0; e < VPL; ++e) {
-            const int jj = VPL * lane + e;
+        for (int nt = 0; nt < NT; ++nt) {
+            const int jj = 4 * nt + lane;
             if (jj < G) {
-                sm.ms.m_part[warp][jj] = mrun[e];
-                sm.ms.l_part[warp][jj] = lsum[e];
+                sm.ms.m_part[warp][jj] = mrun[nt];
+                sm.ms.l_part[warp][jj] = lsum[nt];
             }
         }
     }

@@ -44,8 +44,9 @@ struct RowPrefetch {
 };
 
 // MAXG: the largest query-head group the kernel instance handles (G <= MAXG).
+// 16-byte aligned: o_final and red are read and written as float4 rows.
 template <int NW, int MAXG>
-struct MergeSmem {
+struct __align__(16) MergeSmem {
     float m_part[NW][MAXG];
     float l_part[NW][MAXG];
     float o_final[MAXG][D];
