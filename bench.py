@@ -334,7 +334,7 @@ def measure_append_prefill(spec, device, stream, reps):
     th = k.shape[0] * spec.h_kv
     tflops = th * 2 * 2 * spec.d * spec.d / (ms * 1e-3) / 1e12
     out = {"workload": f"{spec.name}: one layer, {k.shape[0]} tokens x {spec.h_kv} KV heads appended in one call",
-           "kernel": "append_int2_kernel", "ms_per_layer": round(ms, 4),
+           "kernel": "append_int2_prefill_kernel", "ms_per_layer": round(ms, 4),
            "value": round(th / (ms * 1e-3) / 1e6, 2), "unit": "M token-heads/s",
            "roofline": {"bound": "alu", "achieved": round(tflops, 3), "peak": round(FP32_PEAK_TFLOPS, 1),
                         "unit": "TFLOP/s", "frac": round(tflops / FP32_PEAK_TFLOPS, 4),

@@ -13,10 +13,45 @@
 // fixed-order fp32 fma chain over the 128 inputs (the order the format's
 // documentation promises).  Within the warp: min/max by shuffles, exact
 // threshold comparisons, and the four 2-bit codes of a byte gathered from
-// four neighbouring lanes.
+// four neighbouring lanes.  Appends of 256 tokens or more (prefill) take a
+// register-tiled kernel with R in shared memory that runs the same chains.
+#include <mutex>
+
 #include "kvq_common.cuh"
 
 namespace kvq {
+
+// Group parameters from the exact group min / max: the clip ratio c of
+// Q2(.; c, G) scales both range ends, scale = (max - min) / 3 and min go
+// to fp16 (saturating).
+__device__ __forceinline__ void int2_params(float mn, float mx, float clip, __half& sh, __half& mh) {
+    mn = __fmul_rn(clip, mn);
+    mx = __fmul_rn(clip, mx);
+    sh = f16_sat(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+    mh = f16_sat(mn);
+}
+
+// code = #{c : min + (c + 1/2) scale < x}, decided exactly
+__device__ __forceinline__ int int2_code(float x, float mnf, float scf) {
+    if (!(scf > 0.f)) return 0;
+    float hi, lo;
+    two_sum(x, -mnf, hi, lo);
+    return (int)diff_gt(hi, lo, __fmul_rn(scf, 0.5f)) + (int)diff_gt(hi, lo, __fmul_rn(scf, 1.5f)) +
+           (int)diff_gt(hi, lo, __fmul_rn(scf, 2.5f));
+}
+
+// The (scale, min) of slot s, group g: keys one word per group, values
+// pair-major halves.
+__device__ __forceinline__ void int2_store_meta(uint8_t* tile, int is_v, int s, int g, __half sh, __half mh) {
+    if (is_v) {
+        uint8_t* m = tile + vm_scale_off(s, g);
+        *reinterpret_cast<__half*>(m) = sh;
+        *reinterpret_cast<__half*>(m + VM_MINS) = mh;
+    } else {
+        const uint32_t meta = (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(mh) << 16);
+        *reinterpret_cast<uint32_t*>(tile + OFF_KM + 16 * s + 4 * g) = meta;
+    }
+}
 
 __global__ void __launch_bounds__(64)
 append_int2_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v, int n_tok,
@@ -85,21 +120,9 @@ append_int2_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
             mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         }
-        // clip ratio c (Q2(.; c, G)): the range ends scale to c*min, c*max
-        mn = __fmul_rn(clip, mn);
-        mx = __fmul_rn(clip, mx);
-        const __half sh = f16_sat(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
-        const __half mh = f16_sat(mn);
-        const float scf = __half2float(sh), mnf = __half2float(mh);
-
-        // code = #{c : mn + (c + 1/2) scale < x}, decided exactly
-        int code = 0;
-        if (scf > 0.f) {
-            float hi, lo;
-            two_sum(acc, -mnf, hi, lo);
-            code = (int)diff_gt(hi, lo, __fmul_rn(scf, 0.5f)) + (int)diff_gt(hi, lo, __fmul_rn(scf, 1.5f)) +
-                   (int)diff_gt(hi, lo, __fmul_rn(scf, 2.5f));
-        }
+        __half sh, mh;
+        int2_params(mn, mx, clip, sh, mh);
+        const int code = int2_code(acc, __half2float(mh), __half2float(sh));
 
         // byte 4*b + g holds channels 32g + 4b + c at bits 2c
         uint32_t bits = (uint32_t)code << (2 * (lane & 3));
@@ -109,15 +132,143 @@ append_int2_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
         uint8_t* tile = cache + ((size_t)page * H_kv + h) * INT2_TILE;
         uint8_t* rec = tile + (is_v ? OFF_VC : OFF_KC) + 32 * s;
         if ((lane & 3) == 0) rec[4 * (lane >> 2) + grp] = (uint8_t)bits;
-        if (lane == 0) {
-            if (is_v) {
-                uint8_t* m = tile + vm_scale_off(s, grp);
-                *reinterpret_cast<__half*>(m) = sh;
-                *reinterpret_cast<__half*>(m + VM_MINS) = mh;
-            } else {
-                const uint32_t meta = (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(mh) << 16);
-                *reinterpret_cast<uint32_t*>(tile + OFF_KM + 16 * s + 4 * grp) = meta;
+        if (lane == 0) int2_store_meta(tile, is_v, s, grp, sh, mh);
+    }
+}
+
+// Prefill-sized appends: the same chains, register-tiled.  A CTA of 256
+// threads takes one (KV head, side) and PF_TILES tiles of PF_TOK tokens;
+// R (64 KB) is staged in shared memory once, each tile's inputs are stored
+// transposed (X[i][token]).  Thread (warp w, lane l) owns channels
+// 4l .. 4l+3 -- one byte of the code record (group l / 8, byte-row l % 8)
+// -- for tokens 8w .. 8w+7 of the tile: per input index i it reads R[i][4l
+// .. 4l+3] and X[i][8w .. 8w+7] and runs 32 chains one step, each chain the
+// same fixed-order fp32 fma sequence over i = 0 .. 127 as above, so the
+// codes are the same bit for bit.  A group's 32 channels sit in 8
+// neighbouring lanes (min / max over 3 shuffles), and a warp writes whole
+// 32-byte code records.
+constexpr int PF_TOK = 64;
+constexpr int PF_TILES = 4;
+constexpr int PF_XS = PF_TOK + 4;  // padded transposed-tile row (16-byte multiple)
+
+struct __align__(16) PrefillSmem {
+    float R[D][D];
+    float X[D][PF_XS];
+    int slot[PF_TOK];
+};
+
+__global__ void __launch_bounds__(256, 2)
+append_int2_prefill_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v, int n_tok,
+                           int H_kv, const int32_t* __restrict__ slot_mapping, const float* __restrict__ mu,
+                           const float* __restrict__ Rk, const float* __restrict__ Rv, uint8_t* __restrict__ cache,
+                           int64_t num_pages, float* __restrict__ dbg_k, float* __restrict__ dbg_v,
+                           int32_t* __restrict__ err_count, float clip) {
+    griddep_launch_dependents();
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    PrefillSmem& sm = *reinterpret_cast<PrefillSmem*>(smem_raw);
+    const int h = blockIdx.y, is_v = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    {
+        // the rotation is a layer constant: staged before the dependency wait
+        const float4* R4 = reinterpret_cast<const float4*>((is_v ? Rv : Rk) + (size_t)h * D * D);
+        float4* S4 = reinterpret_cast<float4*>(&sm.R[0][0]);
+        for (int idx = tid; idx < D * D / 4; idx += 256) S4[idx] = __ldg(R4 + idx);
+    }
+    griddep_wait();  // k, v, the slot mapping or the cache may come from the previous kernel
+
+    const __nv_bfloat16* src = is_v ? v : k;
+    const int64_t n_slots = num_pages * PAGE;
+    const int g = lane >> 3, row = lane & 7;  // this lane's group and byte-row
+    float* dbg = is_v ? dbg_v : dbg_k;
+    // a tile's inputs: job (half, chunk) of this warp = tokens t0 + 32 half +
+    // lane, channels 8 chunk .. +7; loaded into registers one tile ahead
+    uint4 raw[4];
+    int slot_pf = -1;
+    auto load_tile = [&](int t0) {
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int job = warp + 8 * m, half = job >> 4, c = job & 15, t = t0 + 32 * half + lane;
+            raw[m] = t < n_tok ? __ldg(reinterpret_cast<const uint4*>(src + ((size_t)t * H_kv + h) * D + 8 * c))
+                               : make_uint4(0u, 0u, 0u, 0u);
+        }
+        slot_pf = tid < PF_TOK && t0 + tid < n_tok ? __ldg(slot_mapping + t0 + tid) : -1;
+    };
+    const int tile0 = blockIdx.x * PF_TILES * PF_TOK;
+    if (tile0 < n_tok) load_tile(tile0);
+    for (int tl = 0; tl < PF_TILES; ++tl) {
+        const int t0 = tile0 + tl * PF_TOK;
+        if (t0 >= n_tok) break;
+        __syncthreads();  // the previous tile's inputs are consumed
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int job = warp + 8 * m, half = job >> 4, c = job & 15, tt = 32 * half + lane;
+            const uint32_t w[4] = {raw[m].x, raw[m].y, raw[m].z, raw[m].w};
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                x[2 * e] = __uint_as_float(w[e] << 16);
+                x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
             }
+            if (!is_v && t0 + tt < n_tok) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = __fsub_rn(x[e], __ldg(mu + h * D + 8 * c + e));
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sm.X[8 * c + e][tt] = x[e];
+        }
+        if (tid < PF_TOK) sm.slot[tid] = slot_pf;
+        __syncthreads();
+        if (tl + 1 < PF_TILES && t0 + PF_TOK < n_tok) load_tile(t0 + PF_TOK);
+
+        float acc[4][8];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int u = 0; u < 8; ++u) acc[a][u] = 0.f;
+#pragma unroll 4
+        for (int i = 0; i < D; ++i) {
+            const float4 r4 = *reinterpret_cast<const float4*>(&sm.R[i][4 * lane]);
+            const float4 xa = *reinterpret_cast<const float4*>(&sm.X[i][8 * warp]);
+            const float4 xb = *reinterpret_cast<const float4*>(&sm.X[i][8 * warp + 4]);
+            const float rc[4] = {r4.x, r4.y, r4.z, r4.w};
+            const float xt[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int u = 0; u < 8; ++u) acc[a][u] = __fmaf_rn(xt[u], rc[a], acc[a][u]);
+        }
+
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int tt = 8 * warp + u, t = t0 + tt;
+            if (t >= n_tok) break;               // warp-uniform
+            const int slot = sm.slot[tt];        // warp-uniform
+            if (slot == -1) continue;
+            if (slot < -1 || (int64_t)slot >= n_slots) {
+                if (lane == 0 && h == 0 && is_v == 0 && err_count) atomicAdd(err_count, 1);
+                continue;
+            }
+            if (dbg)
+                *reinterpret_cast<float4*>(dbg + ((size_t)t * H_kv + h) * D + 4 * lane) =
+                    make_float4(acc[0][u], acc[1][u], acc[2][u], acc[3][u]);
+            float mn = fminf(fminf(acc[0][u], acc[1][u]), fminf(acc[2][u], acc[3][u]));
+            float mx = fmaxf(fmaxf(acc[0][u], acc[1][u]), fmaxf(acc[2][u], acc[3][u]));
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            }
+            __half sh, mh;
+            int2_params(mn, mx, clip, sh, mh);
+            const float scf = __half2float(sh), mnf = __half2float(mh);
+            uint32_t byte = 0;
+#pragma unroll
+            for (int a = 0; a < 4; ++a) byte |= (uint32_t)int2_code(acc[a][u], mnf, scf) << (2 * a);
+            const int page = slot / PAGE, s = slot % PAGE;
+            uint8_t* tile = cache + ((size_t)page * H_kv + h) * INT2_TILE;
+            // channels 32g + 4 row + a sit in byte 4 row + g, bits 2a
+            tile[(is_v ? OFF_VC : OFF_KC) + 32 * s + 4 * row + g] = (uint8_t)byte;
+            if (row == 0) int2_store_meta(tile, is_v, s, g, sh, mh);
         }
     }
 }
@@ -127,6 +278,9 @@ append_int2_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
 using namespace kvq;
 
 extern "C" size_t kvq_int2_tile_bytes(int d) { return d == D ? (size_t)INT2_TILE : 0; }
+
+// appends of at least this many tokens take the register-tiled kernel
+static constexpr int PREFILL_MIN_TOKENS = 256;
 
 static kvq_status append_int2_launch(const void* k, const void* v, int n_tok, int H_kv, int d,
                                       const int32_t* slot_mapping, const float* mu_k, const float* R_k,
@@ -145,6 +299,36 @@ static kvq_status append_int2_launch(const void* k, const void* v, int n_tok, in
     if (reinterpret_cast<uintptr_t>(cache) % 16)
         return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_append_int2: cache not 16-byte aligned");
 
+    const bool aligned = reinterpret_cast<uintptr_t>(k) % 16 == 0 && reinterpret_cast<uintptr_t>(v) % 16 == 0 &&
+                         (!dbg_rot_k || reinterpret_cast<uintptr_t>(dbg_rot_k) % 16 == 0) &&
+                         (!dbg_rot_v || reinterpret_cast<uintptr_t>(dbg_rot_v) % 16 == 0);
+    if (n_tok >= PREFILL_MIN_TOKENS && aligned) {
+        // prefill: the register-tiled kernel (same arithmetic, same codes)
+        static std::mutex mu;
+        static bool done[64] = {};
+        int dev = 0;
+        kvq_status s2 = kvq_check_cuda(cudaGetDevice(&dev), "kvq_append_int2: cudaGetDevice");
+        if (s2 != KVQ_OK) return s2;
+        {
+            std::lock_guard<std::mutex> lock(mu);
+            if (dev < 0 || dev >= 64 || !done[dev]) {
+                s2 = kvq_check_cuda(cudaFuncSetAttribute((const void*)append_int2_prefill_kernel,
+                                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                         (int)sizeof(PrefillSmem)),
+                                    "kvq_append_int2 smem attribute");
+                if (s2 != KVQ_OK) return s2;
+                if (dev >= 0 && dev < 64) done[dev] = true;
+            }
+        }
+        const int per_cta = PF_TOK * PF_TILES;
+        dim3 grid((n_tok + per_cta - 1) / per_cta, H_kv, 2);
+        return kvq_check_cuda(
+            launch_pdl(append_int2_prefill_kernel, grid, dim3(256), sizeof(PrefillSmem), static_cast<cudaStream_t>(stream),
+                       static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), n_tok, H_kv,
+                       slot_mapping, mu_k, R_k, R_v, static_cast<uint8_t*>(cache), num_pages, dbg_rot_k, dbg_rot_v,
+                       err_count, clip),
+            "kvq_append_int2 launch");
+    }
     // enough CTAs for about four waves of the 152 SMs; at most 64 tokens each
     const int want_ctas = 152 * 16;
     int chunks = (want_ctas + 4 * H_kv - 1) / (4 * H_kv);

@@ -141,6 +141,52 @@ def test_append_adversarial_bit_exact():
     assert np.array_equal(layer.cache.cpu().numpy(), cache)
 
 
+@pytest.mark.parametrize("clip", [1.0, 0.9])
+def test_prefill_append_matches_token_appends_and_oracle(clip):
+    """A 1000-token append takes the register-tiled prefill kernel: its cache
+    bytes, rotated vectors and error count equal those of the same tokens
+    appended 200 at a time (the per-token kernel) and the oracle's cache."""
+    torch.manual_seed(3)
+    h_kv, n = 2, 1000
+    spec = inputs.small_spec("pfapp", h_q=8, h_kv=h_kv, ctx=1024)
+    layer = Int2Layer(spec, 0)
+    k = (torch.randn(n, h_kv, 128) * 2 + torch.randn(1, h_kv, 128) * 3).to(torch.bfloat16)
+    v = torch.randn(n, h_kv, 128).to(torch.bfloat16)
+    k[10, 0, :32] = 1.5                                   # constant group
+    bt = layer.block_table[0].cpu()
+    slots = inputs.slot_mapping(bt, torch.arange(n)).to(torch.int32)
+    slots[17] = -1
+    slots[500] = -1
+    slots[333] = layer.num_pages * 16 + 5                 # beyond the pool: skipped and counted
+    slots[999] = -7                                       # invalid: skipped and counted
+    mu = inputs.key_centre(k).to("cuda").contiguous()
+    kd, vd, sd = k.cuda().contiguous(), v.cuda().contiguous(), slots.cuda().contiguous()
+    outs = []
+    for step in (n, 200):
+        layer.cache.fill_(0)
+        dk = torch.zeros((n, h_kv, 128), dtype=torch.float32, device="cuda")
+        dv = torch.zeros_like(dk)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for t0 in range(0, n, step):
+            t1 = min(n, t0 + step)
+            _lib.kvq_append_int2_clip(kd[t0:t1], vd[t0:t1], sd[t0:t1], mu, layer.R_k, layer.R_v, clip, layer.cache,
+                                      layer.num_pages, dk[t0:t1], dv[t0:t1], err)
+        torch.cuda.synchronize()
+        outs.append((layer.cache.cpu().numpy().copy(), _np_f32(dk), _np_f32(dv), int(err.item())))
+    (c_big, dk_big, dv_big, e_big), (c_small, dk_small, dv_small, e_small) = outs
+    assert e_big == e_small == 2
+    assert np.array_equal(c_big, c_small)
+    assert np.array_equal(dk_big, dk_small) and np.array_equal(dv_big, dv_small)
+    sl = slots.numpy().copy()
+    sl[333] = sl[999] = -1
+    cache = int2.new_cache(layer.num_pages, h_kv)
+    info = int2.append(cache, _np_f32(k), _np_f32(v), sl, _np_f32(mu), _np_f32(layer.R_k), _np_f32(layer.R_v),
+                       clip=clip)
+    assert np.array_equal(c_big, cache)
+    keep = sl >= 0
+    assert np.array_equal(dk_big[keep], info["z"][keep]) and np.array_equal(dv_big[keep], info["w"][keep])
+
+
 # --------------------------------------------------------------------------- decode
 
 def test_decode_tiny_end_to_end():
