@@ -233,8 +233,7 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     // Lane 0 issues unit u with its (already loaded) page ids and records how
     // many tokens of each page are valid (0 for a slot past the warp's pages
     // or with a bad page id); the mbarrier publishes the counts with the data.
-    auto issue_unit = [&](int u, const int (&pid)[UNIT_PAGES]) {  // lane 0 only
-        const int st = u % DEC_UNITS;
+    auto issue_unit = [&](int u, int st, const int (&pid)[UNIT_PAGES]) {  // lane 0 only; st = u % DEC_UNITS
         uint64_t* bar = &sm.bar[warp][st];
         bool ok[UNIT_PAGES];
         uint32_t tx = 0;
@@ -307,7 +306,7 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                     int pu[UNIT_PAGES];
 #pragma unroll
                     for (int e = 0; e < UNIT_PAGES; ++e) pu[e] = pids[UNIT_PAGES * u + e];
-                    issue_unit(u, pu);
+                    issue_unit(u, u, pu);
                     n_issued = u + 1;
                 }
 #pragma unroll
@@ -394,9 +393,8 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     // are zeroed here, so p = 0
     // always meets finite factors and the PV step needs no per-slot masks
     // (the QK step drops those slots' logits by selection).
-    auto wait_unit = [&](int u) -> bool {
-        const int st = u % DEC_UNITS;
-        const bool ok = mbar_wait_bounded(&sm.bar[warp][st], (u / DEC_UNITS) & 1, WAIT_LIMIT_CYCLES);
+    auto wait_unit = [&](int st, uint32_t parity) -> bool {  // slot group st = u % DEC_UNITS
+        const bool ok = mbar_wait_bounded(&sm.bar[warp][st], parity, WAIT_LIMIT_CYCLES);
         if (__any_sync(0xffffffffu, !ok)) {
             if (lane == 0) atomicOr(err_word, ERR_TIMEOUT);
             return false;
@@ -421,9 +419,9 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
 
     // ---------------- QK of page i: base-2 logits of tokens r, r + 8 for
     // head 4*nt + t (-inf past the context)
-    auto qk_page = [&](int i, float (&lg)[NT][2]) {
-        const uint8_t* tile = sm.u.ring[warp][i % DEC_STAGES];
-        const int n_tok = sm.ntok[warp][i % DEC_STAGES];
+    auto qk_page = [&](int slot, float (&lg)[NT][2]) {
+        const uint8_t* tile = sm.u.ring[warp][slot];
+        const int n_tok = sm.ntok[warp][slot];
         const uint2 kr = lds64(tile + OFF_KC + 32 * r + 8 * t);
         const uint2 kr8 = lds64(tile + OFF_KC + 32 * (r + 8) + 8 * t);
         const uint32_t P01 = prmt(kr.x, kr.y, 0x5410), P23 = prmt(kr.x, kr.y, 0x7632);
@@ -463,9 +461,9 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     };
 
     // QK of unit u and each head's maximum over its pages
-    auto qk_unit = [&](int u, float (&lg)[UNIT_PAGES][NT][2], float (&pm)[NT]) {
+    auto qk_unit = [&](int st, float (&lg)[UNIT_PAGES][NT][2], float (&pm)[NT]) {
 #pragma unroll
-        for (int e = 0; e < UNIT_PAGES; ++e) qk_page(UNIT_PAGES * u + e, lg[e]);
+        for (int e = 0; e < UNIT_PAGES; ++e) qk_page(UNIT_PAGES * st + e, lg[e]);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             float m = fmaxf(lg[0][nt][0], lg[0][nt][1]);
@@ -529,8 +527,8 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     };
 
     // ---------------- PV of page i with its weights p^
-    auto pv_page = [&](int i, const float (&pr)[NT][2]) {
-        const uint8_t* tile = sm.u.ring[warp][i % DEC_STAGES];
+    auto pv_page = [&](int slot, const float (&pr)[NT][2]) {
+        const uint8_t* tile = sm.u.ring[warp][slot];
         // P in the PV B layout: column n = r (head n), rows = tokens 2t, 2t+1 | 2t+8, 2t+9
         uint32_t pb0, pb1;
         {
@@ -595,11 +593,11 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
 
     // Hand unit u's slots back: issue the unit DEC_UNITS ahead into them and
     // load the page ids of the unit after that.
-    auto release_unit = [&](int u) {
+    auto release_unit = [&](int u, int st) {  // st = u % DEC_UNITS, also the slot group of u + DEC_UNITS
         __syncwarp();
         if (lane == 0 && u + DEC_UNITS < n_units) {
             fence_proxy_async_smem();
-            issue_unit(u + DEC_UNITS, pid_next);
+            issue_unit(u + DEC_UNITS, st, pid_next);
             n_issued = u + DEC_UNITS + 1;
             const int j = UNIT_PAGES * (u + DEC_UNITS + 1);
 #pragma unroll
@@ -611,32 +609,40 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     // Software pipeline over the warp's units: the QK of unit u + 1 does not
     // depend on the softmax or PV of unit u, and the two sit in one
     // straight-line block so their instruction streams interleave.
+    // The slot group and mbarrier parity of unit u advance with u (no
+    // division by the ring size in the loop).
     int u_fail = -1;  // the unit whose wait timed out
     float lg[UNIT_PAGES][NT][2], pm[NT];
+    int st = 0;             // u % DEC_UNITS
+    uint32_t parity = 0u;   // (u / DEC_UNITS) & 1
     if (n_units > 0) {
-        if (wait_unit(0))
+        if (wait_unit(0, 0u))
             qk_unit(0, lg, pm);
         else
             u_fail = 0;
     }
     int u = 0;
     for (; u + 1 < n_units && u_fail < 0; ++u) {
+        const int st1 = st + 1 == DEC_UNITS ? 0 : st + 1;
+        const uint32_t parity1 = st + 1 == DEC_UNITS ? parity ^ 1u : parity;
         float pr[UNIT_PAGES][NT][2];
         softmax_unit(lg, pm, pr);
-        if (!wait_unit(u + 1)) {
+        if (!wait_unit(st1, parity1)) {
             u_fail = u + 1;
             break;
         }
 #pragma unroll
-        for (int e = 0; e < UNIT_PAGES; ++e) pv_page(UNIT_PAGES * u + e, pr[e]);
-        qk_unit(u + 1, lg, pm);  // lg, pm of unit u are spent (pr holds what PV needs)
-        release_unit(u);
+        for (int e = 0; e < UNIT_PAGES; ++e) pv_page(UNIT_PAGES * st + e, pr[e]);
+        qk_unit(st1, lg, pm);  // lg, pm of unit u are spent (pr holds what PV needs)
+        release_unit(u, st);
+        st = st1;
+        parity = parity1;
     }
     if (u_fail < 0 && n_units > 0) {
         float pr[UNIT_PAGES][NT][2];
         softmax_unit(lg, pm, pr);
 #pragma unroll
-        for (int e = 0; e < UNIT_PAGES; ++e) pv_page(UNIT_PAGES * u + e, pr[e]);
+        for (int e = 0; e < UNIT_PAGES; ++e) pv_page(UNIT_PAGES * st + e, pr[e]);
     }
     if (u_fail >= 0 && lane == 0) {
         // let copies still in flight land before the shared memory is reused
