@@ -71,6 +71,7 @@ struct __align__(16) BgDecodeSmem {
     uint64_t bar[NW][BG_MAX_STAGES];
     int ntok[NW][BG_MAX_STAGES];
     BgtqLayout L;
+    int8_t wsm[D / 2];      // this head's block widths
     MergeSmem<NW, MAXG> ms;
 };
 
@@ -95,6 +96,16 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint32_t* err_word = reinterpret_cast<uint32_t*>(ws);
 
+    {
+        // prefetches into L2 only (coherent with any later write of the
+        // previous kernel): the warp's first block-table entries, the
+        // context length, the query rows and the output rotation
+        const int j = split * NW + warp + S * NW * lane;
+        if (lane <= BG_MAX_STAGES && j < max_pages) prefetch_l2(block_table + (size_t)b * max_pages + j);
+        if (tid == 0) prefetch_l2(context_lens + b);
+        const char* qc = reinterpret_cast<const char*>(q + ((size_t)b * H_q + (size_t)h * G) * D);
+        if (tid < (G * D * 2 + 127) / 128) prefetch_l2(qc + 128 * tid);
+    }
     griddep_wait();  // every input may come from the previous kernel in the stream
     int ctx = __ldg(context_lens + b);
     ctx = max(0, min(ctx, max_pages * PAGE));
@@ -139,8 +150,8 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     }
 
     // ---- per-head layout, chunk schedule, codebooks and rotated queries
+    build_layout_cta(widths + h * (D / 2), sm.L, sm.wsm);
     if (tid == 0) {
-        build_layout(widths + h * (D / 2), sm.L);
         int nc = 0;
         for (int bb = 1; bb <= 8; ++bb)
             for (int c = 0; c < (sm.L.n[bb] + 15) / 16 && nc < BG_MAX_CHUNKS; ++c) {
@@ -282,13 +293,10 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             const uint32_t* rec8 = reinterpret_cast<const uint32_t*>(tile + (r + 8) * tl.kb);
             const __half* nr0 = reinterpret_cast<const __half*>(tile + tl.off_kn + 16 * r);
             const __half* nr8 = reinterpret_cast<const __half*>(tile + tl.off_kn + 16 * (r + 8));
-            float acc[NT][2], cg[NT][4];
+            float acc[NT][2];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                acc[nt][0] = acc[nt][1] = 0.f;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) cg[nt][e] = 0.f;
-            }
+            for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = 0.f;
+#pragma unroll 2
             for (int k = 0; k < NC; ++k) {
                 const BgChunk ch = sm.chunks[k];  // warp-uniform
                 const int bw = ch.b;
@@ -308,21 +316,16 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                     ah[j] = prmt(e0, e1, 0x5410);
                     al[j] = prmt(e0, e1, 0x7632);
                 }
+                // the chunk's dot products, scaled by the group norms r_{s,b}
+                const float rn0 = __half2float(nr0[bw - 1]), rn8 = __half2float(nr8[bw - 1]);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const uint2 bb = sm.bfr[k][nt][lane];
-                    mma_f16_16816(cg[nt], ah, bb.x, bb.y);
-                    mma_f16_16816(cg[nt], al, bb.x, bb.y);
-                }
-                if (ch.last) {
-                    const float rn0 = __half2float(nr0[bw - 1]), rn8 = __half2float(nr8[bw - 1]);
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        acc[nt][0] = fmaf(rn0, cg[nt][0] + cg[nt][1], acc[nt][0]);
-                        acc[nt][1] = fmaf(rn8, cg[nt][2] + cg[nt][3], acc[nt][1]);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) cg[nt][e] = 0.f;
-                    }
+                    float c[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma_f16_16816(c, ah, bb.x, bb.y);
+                    mma_f16_16816(c, al, bb.x, bb.y);
+                    acc[nt][0] = fmaf(rn0, c[0] + c[1], acc[nt][0]);
+                    acc[nt][1] = fmaf(rn8, c[2] + c[3], acc[nt][1]);
                 }
             }
 #pragma unroll
