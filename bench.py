@@ -542,16 +542,25 @@ def run_ours(args, world, rank, local):
 
 
 def run_profile_case(args):
-    """A decode case for a full ncu capture: one Qwen3-8B-shaped layer
-    (32 q / 8 KV heads) at --profile-ctx tokens (default 32K; 131072 is one
-    layer of the benchmark step, ~100 MB of cache), three decode launches of
-    the chosen kernel."""
+    """A case for a full ncu capture: one Qwen3-8B-shaped layer (32 q / 8 KV
+    heads) at --profile-ctx tokens (default 32K; 131072 is one layer of the
+    benchmark step, ~100 MB of cache), three launches of the chosen kernel:
+    a decode, or the append of the layer's whole history in one call."""
     torch.cuda.set_device(0)
     spec = inputs.small_spec(f"prof{args.profile_ctx // 1024}k", h_q=32, h_kv=8, batch=1, ctx=args.profile_ctx,
                              permute=True, k_kind="energy_rope", v_kind="gauss", avg_bits=3, v_bits=3, b_min=1,
                              b_max=8)
     out = torch.zeros((1, spec.h_q, spec.d), dtype=torch.float32, device="cuda")
-    if args.profile_case == "decode_int2":
+    if args.profile_case == "append_prefill":
+        # one Qwen3-8B-shaped layer's --profile-ctx history appended in one call, three times
+        L = Int2Layer(spec, 0)
+        k, v = L.history_kv(0)
+        L.mu = inputs.key_centre(k).to("cuda").contiguous()
+        sl = L.slots(0, history_positions(spec)).contiguous()
+        k, v = k.contiguous(), v.contiguous()
+        for _ in range(3):
+            _lib.kvq_append_int2(k, v, sl, L.mu, L.R_k, L.R_v, L.cache, L.num_pages)
+    elif args.profile_case == "decode_int2":
         L = Int2Layer(spec, 0)
         L.prefill()
         q, ws = L.queries(), L.workspace()
@@ -577,7 +586,7 @@ def main():
     ap.add_argument("--workload", default="qwen8b", choices=["qwen8b", "llama8b"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-bgtq", action="store_true")
-    ap.add_argument("--profile-case", choices=["decode_int2", "bgtq_decode"], default=None,
+    ap.add_argument("--profile-case", choices=["decode_int2", "bgtq_decode", "append_prefill"], default=None,
                     help="run a small decode case for an ncu capture instead of the benchmark")
     ap.add_argument("--profile-ctx", type=int, default=32768, help="context length of the --profile-case layer")
     args = ap.parse_args()
