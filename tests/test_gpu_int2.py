@@ -187,6 +187,32 @@ def test_prefill_append_matches_token_appends_and_oracle(clip):
     assert np.array_equal(dk_big[keep], info["z"][keep]) and np.array_equal(dv_big[keep], info["w"][keep])
 
 
+def test_prefill_append_unaligned_inputs_take_the_token_kernel():
+    """Inputs that are not 16-byte aligned go to the per-token kernel; the
+    cache comes out the same as from aligned inputs."""
+    torch.manual_seed(5)
+    h_kv, n = 2, 600
+    spec = inputs.small_spec("pfal", h_q=8, h_kv=h_kv, ctx=640)
+    layer = Int2Layer(spec, 0)
+    k = torch.randn(n, h_kv, 128).to(torch.bfloat16).cuda()
+    v = torch.randn(n, h_kv, 128).to(torch.bfloat16).cuda()
+    slots = inputs.slot_mapping(layer.block_table[0].cpu(), torch.arange(n)).to(torch.int32).cuda()
+    mu = torch.zeros(h_kv, 128, device="cuda")
+    caches = []
+    for shift in (0, 4):  # 4 bf16 = 8 bytes: 8-byte but not 16-byte aligned
+        bk = torch.empty(n * h_kv * 128 + shift, dtype=torch.bfloat16, device="cuda")
+        bv = torch.empty_like(bk)
+        kk, vv = bk[shift:].view(n, h_kv, 128), bv[shift:].view(n, h_kv, 128)
+        kk.copy_(k)
+        vv.copy_(v)
+        assert (kk.data_ptr() % 16 == 0) == (shift == 0)
+        layer.cache.fill_(0)
+        _lib.kvq_append_int2(kk, vv, slots, mu, layer.R_k, layer.R_v, layer.cache, layer.num_pages)
+        torch.cuda.synchronize()
+        caches.append(layer.cache.cpu().numpy().copy())
+    assert np.array_equal(caches[0], caches[1])
+
+
 # --------------------------------------------------------------------------- decode
 
 def test_decode_tiny_end_to_end():
@@ -341,3 +367,9 @@ def test_qwen8b_full_context_sampled_layers():
 def test_sweep70b_gqa8_sampled():
     _sampled_check(inputs.sweep70b_spec(8, 4096), 0, [(1, 0), (6, 7)])
     _sampled_check(inputs.sweep70b_spec(1, 524288), 0, [(0, 3)], token_samples=64)
+
+
+def test_sweep70b_batch64_multiwave_sampled():
+    # 64 sequences x 8 KV heads = 512 (sequence, KV head) units at one split
+    # each: a grid of 3.4 waves of 152 CTAs
+    _sampled_check(inputs.sweep70b_spec(64, 4096), 0, [(0, 0), (37, 5), (63, 7)], token_samples=64)
