@@ -233,54 +233,59 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     // Lane 0 issues unit u with its (already loaded) page ids and records how
     // many tokens of each page are valid (0 for a slot past the warp's pages
     // or with a bad page id); the mbarrier publishes the counts with the data.
-    auto issue_unit = [&](int u, int st, const int (&pid)[UNIT_PAGES]) {  // lane 0 only; st = u % DEC_UNITS
+    auto issue_unit = [&](int u, int st, int pid) {
+        // whole warp; lane e < UNIT_PAGES issues page e of unit u (id pid),
+        // st = u % DEC_UNITS
         uint64_t* bar = &sm.bar[warp][st];
-        bool ok[UNIT_PAGES];
-        uint32_t tx = 0;
-#pragma unroll
-        for (int e = 0; e < UNIT_PAGES; ++e) {
-            const int j = UNIT_PAGES * u + e;
+        const int j = UNIT_PAGES * u + lane;
+        bool ok = false;
+        if (lane < UNIT_PAGES) {
             int n = 0;
-            ok[e] = false;
             if (j < my_count) {
-                if (pid[e] < 0 || (int64_t)pid[e] >= num_pages) {
+                if (pid < 0 || (int64_t)pid >= num_pages) {
                     atomicOr(err_word, ERR_BAD_PAGE);
                 } else {
-                    ok[e] = true;
+                    ok = true;
                     n = min(PAGE, ctx - page_of(j) * PAGE);
-                    tx += INT2_TILE;
                 }
             }
-            sm.ntok[warp][UNIT_PAGES * st + e] = n;
+            sm.ntok[warp][UNIT_PAGES * st + lane] = n;
         }
-        if (tx == 0) {
-            mbar_arrive(bar);  // complete the phase without data
-        } else {
-            mbar_arrive_expect_tx(bar, tx);
-#pragma unroll
-            for (int e = 0; e < UNIT_PAGES; ++e)
-                if (ok[e])
-                    bulk_g2s(sm.u.ring[warp][UNIT_PAGES * st + e], cache + ((size_t)pid[e] * H_kv + h) * INT2_TILE,
-                             INT2_TILE, bar);
+        const uint32_t n_ok = __popc(__ballot_sync(0xffffffffu, ok));
+        __syncwarp();  // the lanes' counts are ordered before lane 0's arrive (release)
+        if (lane == 0) {
+            if (n_ok == 0)
+                mbar_arrive(bar);  // complete the phase without data
+            else
+                mbar_arrive_expect_tx(bar, n_ok * INT2_TILE);
         }
+        __syncwarp();  // the expected bytes are set before any copy is issued
+        if (ok)
+            bulk_g2s(sm.u.ring[warp][UNIT_PAGES * st + lane], cache + ((size_t)pid * H_kv + h) * INT2_TILE,
+                     INT2_TILE, bar);
     };
-    // ---- the page ids of the first units (lane 0).  Their copies are
-    // issued after the query rotation, which runs while the ids arrive; the
-    // copies then fly during the B-fragment setup.  Lane 0 keeps the ids of
-    // the next unit to issue, loaded one release before their use.
-    int pid_next[UNIT_PAGES];
-    int n_issued = 0;  // units issued so far (lane 0)
+    // ---- the page ids of the first units (lane e < UNIT_PAGES holds page e
+    // of each).  Their copies are issued after the query rotation, which runs
+    // while the ids arrive; the copies then fly during the B-fragment setup.
+    // Lanes keep the ids of the next unit to issue, loaded one release
+    // before their use.
+    int pid_first[DEC_UNITS];
+    int pid_next = 0;
+    int n_issued = 0;  // units issued so far
 #pragma unroll
-    for (int e = 0; e < UNIT_PAGES; ++e) pid_next[e] = 0;
-    int pids[DEC_STAGES + UNIT_PAGES];
-#pragma unroll
-    for (int j = 0; j < DEC_STAGES + UNIT_PAGES; ++j) pids[j] = 0;
-    if (lane == 0) {
+    for (int u = 0; u < DEC_UNITS; ++u) pid_first[u] = 0;
+    if (lane < UNIT_PAGES) {
         // bounded by the block table's row length, not the context, so these
         // loads need not wait for context_lens
 #pragma unroll
-        for (int j = 0; j < DEC_STAGES + UNIT_PAGES; ++j)
-            if (page_of(j) < max_pages) pids[j] = __ldg(bt + page_of(j));
+        for (int u = 0; u <= DEC_UNITS; ++u) {
+            const int j = page_of(UNIT_PAGES * u + lane);
+            const int pid = j < max_pages ? __ldg(bt + j) : 0;
+            if (u < DEC_UNITS)
+                pid_first[u] = pid;
+            else
+                pid_next = pid;
+        }
     }
     {
         // the rest of this sequence's block table is read one entry at a
@@ -299,19 +304,12 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         }
         __syncthreads();
         rotate_rows<NW, MAXG>(sm.ms.o_final, Rk + (size_t)h * D * D, rr, G, scale_log2, sm.q, sm.ms);
-        if (lane == 0) {
 #pragma unroll
-            for (int u = 0; u < DEC_UNITS; ++u)
-                if (u < n_units) {
-                    int pu[UNIT_PAGES];
-#pragma unroll
-                    for (int e = 0; e < UNIT_PAGES; ++e) pu[e] = pids[UNIT_PAGES * u + e];
-                    issue_unit(u, u, pu);
-                    n_issued = u + 1;
-                }
-#pragma unroll
-            for (int e = 0; e < UNIT_PAGES; ++e) pid_next[e] = pids[DEC_STAGES + e];
-        }
+        for (int u = 0; u < DEC_UNITS; ++u)
+            if (u < n_units) {  // warp-uniform
+                issue_unit(u, u, pid_first[u]);
+                n_issued = u + 1;
+            }
         // per head: power-of-two pre-scale (max |q~| * sigma in [2^14, 2^15)) and group sums
         for (int jj = warp; jj < G; jj += NW) {
             float mx = 0.f;
@@ -352,7 +350,7 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                 const int c0 = 32 * g + 8 * t + k, c1 = c0 + 4;
                 float v0 = 0.f, v1 = 0.f;
                 if (hq < G) {
-                    const float f = ldexpf(sm.sigma[hq], -2 * k);
+                    const float f = sm.sigma[hq] * (k == 0 ? 1.f : k == 1 ? 0.25f : k == 2 ? 0.0625f : 0.015625f);
                     v0 = sm.q[hq][c0] * f;
                     v1 = sm.q[hq][c1] * f;
                 }
@@ -595,14 +593,12 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     // load the page ids of the unit after that.
     auto release_unit = [&](int u, int st) {  // st = u % DEC_UNITS, also the slot group of u + DEC_UNITS
         __syncwarp();
-        if (lane == 0 && u + DEC_UNITS < n_units) {
+        if (u + DEC_UNITS < n_units) {  // warp-uniform
             fence_proxy_async_smem();
             issue_unit(u + DEC_UNITS, st, pid_next);
             n_issued = u + DEC_UNITS + 1;
-            const int j = UNIT_PAGES * (u + DEC_UNITS + 1);
-#pragma unroll
-            for (int e = 0; e < UNIT_PAGES; ++e)
-                if (j + e < my_count) pid_next[e] = __ldg(bt + page_of(j + e));
+            const int j = UNIT_PAGES * (u + DEC_UNITS + 1) + lane;
+            if (lane < UNIT_PAGES && j < my_count) pid_next = __ldg(bt + page_of(j));
         }
     };
 
