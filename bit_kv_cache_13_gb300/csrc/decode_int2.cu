@@ -287,13 +287,6 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                 pid_next = pid;
         }
     }
-    {
-        // the rest of this sequence's block table is read one entry at a
-        // time during the loop: have L2 fetch it now
-        const char* btc = reinterpret_cast<const char*>(bt);
-        const int lines = (n_pages * 4 + 127) / 128;
-        for (int l = split * NW * 32 + tid; l < lines; l += S_pages * NW * 32) prefetch_l2_keep(btc + 128 * l);
-    }
 
     // ---- q~ = (q R_k) * scale * log2(e) for the G heads of this KV head
     {
@@ -310,6 +303,14 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                 issue_unit(u, u, pid_first[u]);
                 n_issued = u + 1;
             }
+        {
+            // the rest of this sequence's block table is read one entry at a
+            // time during the loop: have L2 fetch it now (after the rotation,
+            // which need not wait for the context length this bound needs)
+            const char* btc = reinterpret_cast<const char*>(bt);
+            const int lines = (n_pages * 4 + 127) / 128;
+            for (int l = split * NW * 32 + tid; l < lines; l += S_pages * NW * 32) prefetch_l2_keep(btc + 128 * l);
+        }
         // per head: power-of-two pre-scale (max |q~| * sigma in [2^14, 2^15)) and group sums
         for (int jj = warp; jj < G; jj += NW) {
             float mx = 0.f;
@@ -354,12 +355,9 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                     v0 = sm.q[hq][c0] * f;
                     v1 = sm.q[hq][c1] * f;
                 }
-                const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
-                if (lo_part) {
-                    bq[nt][s][e] = pack_half2(v0 - __half2float(h0), v1 - __half2float(h1));
-                } else {
-                    bq[nt][s][e] = h2_as_u32(__halves2half2(h0, h1));
-                }
+                // hi part (even columns) or the exact remainder (odd columns), one path
+                const float h0 = __half2float(__float2half_rn(v0)), h1 = __half2float(__float2half_rn(v1));
+                bq[nt][s][e] = pack_half2(lo_part ? v0 - h0 : h0, lo_part ? v1 - h1 : h1);
             }
         }
     }
