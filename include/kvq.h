@@ -91,7 +91,11 @@ size_t kvq_int2_tile_bytes(int d);
  * scale = fp16(fp32(fp32(max - min) / 3)), min = fp16(min) (saturating at
  * +-65504); code = number of thresholds min + (c + 1/2) scale (c = 0..2)
  * strictly below the value (ties to the lower level), 0 when scale == 0.
- * Tokens with equal slots race (last writer unspecified). */
+ * Tokens with equal slots race (last writer unspecified).  Appends of 256
+ * tokens or more with 16-byte aligned k, v (and exports) take a
+ * register-tiled kernel (R in shared memory, about 100 KB per CTA, opted in on
+ * first use); it runs the same chains, so the cache bytes and exports are
+ * identical to those of smaller calls. */
 kvq_status kvq_append_int2(const void* k, const void* v, int n_tok, int H_kv, int d,
                            const int32_t* slot_mapping, const float* mu_k,
                            const float* R_k, const float* R_v,
