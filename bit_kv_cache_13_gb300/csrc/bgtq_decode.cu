@@ -11,7 +11,9 @@
 // Grid (split, kv_head, seq) with one CTA per SM (12 warps for head groups
 // up to 4, 8 for groups of 8); the pages of a (sequence, KV head) are dealt
 // round-robin over all warps of its CTAs and streamed through per-warp rings
-// of bulk async copies, as in the INT2 decode.  Per page (16 tokens):
+// of bulk async copies, as in the INT2 decode, two pages per mbarrier phase
+// (one wait, one release, one softmax rescale, and one pass over the chunk
+// descriptors per pair).  Per page (16 tokens):
 //   QK  lane l owns gathered positions 4l .. 4l+3 (two RoPE blocks).  Their
 //       q~ for every head stays in registers, and their four codes are
 //       contiguous bits of a token's stream (groups are laid out in
@@ -37,6 +39,7 @@
 namespace kvq {
 
 constexpr int BG_MAX_STAGES = 8;
+constexpr int BG_UNIT = 2;  // pages per mbarrier phase (ring stages come in pairs)
 
 template <int MAXG>
 struct BgWarps {
@@ -63,7 +66,7 @@ struct __align__(16) BgDecodeSmem {
     BgChunk chunks[BG_MAX_CHUNKS];
     int n_chunks;
     float sigma[MAXG];      // power-of-two pre-scale per head
-    __half pbh[NW][MAXG][PAGE];  // p^ of the warp's current page, head-major
+    __half pbh[NW][MAXG][BG_UNIT * PAGE];  // p^ of the warp's current unit, head-major
     __half cb_vh[256];         // C_v / sqrt(128) as fp16 (PV A operand)
     float qt[MAXG][D];         // q~ in gathered order, times scale * log2(e)
     float qin[MAXG][D];
@@ -116,29 +119,67 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     const int my_count = n_pages > k0 ? (n_pages - k0 + KS - 1) / KS : 0;
     auto page_of = [&](int j) { return k0 + KS * j; };
 
+    // Pages travel in units of BG_UNIT (one mbarrier phase, one wait, one
+    // release): unit u is the warp's pages 2u, 2u + 1 in ring slots
+    // 2 st, 2 st + 1 of slot group st = u % n_grp.
+    const int n_grp = n_stages / BG_UNIT;
+    const int n_units = (my_count + BG_UNIT - 1) / BG_UNIT;
     if (lane == 0) {
-        for (int s = 0; s < n_stages; ++s) mbar_init(&sm.bar[warp][s], 1);
+        for (int s = 0; s < n_grp; ++s) mbar_init(&sm.bar[warp][s], 1);
         fence_mbar_init();
         fence_proxy_async_smem();
     }
     __syncwarp();
-    auto issue = [&](int i, int p, int pid) {  // lane 0 only
-        const int st = i % n_stages;
+    auto issue_unit = [&](int u, int st, int pid) {
+        // whole warp; lane e < BG_UNIT issues page e of unit u (id pid)
         uint64_t* bar = &sm.bar[warp][st];
-        if (pid < 0 || (int64_t)pid >= num_pages) {
-            atomicOr(err_word, ERR_BAD_PAGE);
-            sm.ntok[warp][st] = 0;
-            mbar_arrive(bar);
-        } else {
-            sm.ntok[warp][st] = min(PAGE, ctx - p * PAGE);
-            mbar_arrive_expect_tx(bar, tl.bytes);
-            bulk_g2s(my_ring + (size_t)st * tl.bytes, cache + ((size_t)pid * H_kv + h) * tl.bytes, tl.bytes, bar);
+        const int j = BG_UNIT * u + lane;
+        bool ok = false;
+        if (lane < BG_UNIT) {
+            int n = 0;
+            if (j < my_count) {
+                if (pid < 0 || (int64_t)pid >= num_pages) {
+                    atomicOr(err_word, ERR_BAD_PAGE);
+                } else {
+                    ok = true;
+                    n = min(PAGE, ctx - page_of(j) * PAGE);
+                }
+            }
+            sm.ntok[warp][BG_UNIT * st + lane] = n;
         }
+        const uint32_t n_ok = __popc(__ballot_sync(0xffffffffu, ok));
+        __syncwarp();  // the lanes' counts are ordered before lane 0's arrive (release)
+        if (lane == 0) {
+            if (n_ok == 0)
+                mbar_arrive(bar);
+            else
+                mbar_arrive_expect_tx(bar, n_ok * (uint32_t)tl.bytes);
+        }
+        __syncwarp();  // the expected bytes are set before any copy is issued
+        if (ok)
+            bulk_g2s(my_ring + (size_t)(BG_UNIT * st + lane) * tl.bytes, cache + ((size_t)pid * H_kv + h) * tl.bytes,
+                     tl.bytes, bar);
     };
-    int pid_next = 0;
-    if (lane == 0) {
-        for (int j = 0; j < n_stages && j < my_count; ++j) issue(j, page_of(j), __ldg(bt + page_of(j)));
-        if (n_stages < my_count) pid_next = __ldg(bt + page_of(n_stages));
+    int pid_next = 0, n_issued = 0;
+    {
+        int pid_first[BG_MAX_STAGES / BG_UNIT];
+#pragma unroll
+        for (int u = 0; u < BG_MAX_STAGES / BG_UNIT; ++u) pid_first[u] = 0;
+        if (lane < BG_UNIT) {
+#pragma unroll
+            for (int u = 0; u <= BG_MAX_STAGES / BG_UNIT; ++u) {
+                const int j = BG_UNIT * u + lane;
+                const int pid = u <= n_grp && j < my_count ? __ldg(bt + page_of(j)) : 0;
+                if (u < BG_MAX_STAGES / BG_UNIT) pid_first[u] = pid;
+                if (u == n_grp) pid_next = pid;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < BG_MAX_STAGES / BG_UNIT; ++u)
+            if (u < n_grp && u < n_units) {  // warp-uniform
+                issue_unit(u, u, pid_first[u]);
+                n_issued = u + 1;
+            }
     }
     {
         // the block table and the output rotation are read later: have L2 keep them
@@ -269,70 +310,82 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         mrun[nt] = -CUDART_INF_F;
         lsum[nt] = 0.f;
     }
-    bool timed_out = false;
+    int u_fail = -1;  // the unit whose wait timed out
+    int st = 0;             // u % n_grp
+    uint32_t parity = 0u;   // (u / n_grp) & 1
 
-    for (int i = 0; i < my_count; ++i) {
-        const int stage = i % n_stages;
-        const bool ok = mbar_wait_bounded(&sm.bar[warp][stage], (i / n_stages) & 1, WAIT_LIMIT_CYCLES);
+    for (int u = 0; u < n_units; ++u) {
+        const bool ok = mbar_wait_bounded(&sm.bar[warp][st], parity, WAIT_LIMIT_CYCLES);
         if (__any_sync(0xffffffffu, !ok)) {
-            timed_out = true;
+            u_fail = u;
             if (lane == 0) atomicOr(err_word, ERR_TIMEOUT);
             break;
         }
-        const uint8_t* tile = my_ring + (size_t)stage * tl.bytes;
-        const int n_tok = layout_ok ? sm.ntok[warp][stage] : 0;
-        const bool full = n_tok == PAGE;  // warp-uniform: every page but a sequence's last
+        const uint8_t* tiles[BG_UNIT];
+        int n_tok[BG_UNIT];
+#pragma unroll
+        for (int e = 0; e < BG_UNIT; ++e) {
+            tiles[e] = my_ring + (size_t)(BG_UNIT * st + e) * tl.bytes;
+            n_tok[e] = layout_ok ? sm.ntok[warp][BG_UNIT * st + e] : 0;
+        }
 
         // ---- QK on the tensor cores, one chunk (16 positions of width b) at
-        // a time: A = C_b[code] / sqrt(n_b) as an fp16 hi/lo pair, rows =
-        // tokens r, r + 8, K = the chunk's positions (lane t: blocks t and
-        // t + 4 of the chunk); the group norm r_{s,b} scales the group's sum.
-        float lg[NT][2];
+        // a time for both pages of the unit: A = C_b[code] / sqrt(n_b) as an
+        // fp16 hi/lo pair, rows = tokens r, r + 8, K = the chunk's positions
+        // (lane t: blocks 2t, 2t + 1 of the chunk); the group norm r_{s,b}
+        // scales each chunk's dot products.
+        float lg[BG_UNIT][NT][2];
         {
-            const uint32_t* rec0 = reinterpret_cast<const uint32_t*>(tile + r * tl.kb);
-            const uint32_t* rec8 = reinterpret_cast<const uint32_t*>(tile + (r + 8) * tl.kb);
-            const __half* nr0 = reinterpret_cast<const __half*>(tile + tl.off_kn + 16 * r);
-            const __half* nr8 = reinterpret_cast<const __half*>(tile + tl.off_kn + 16 * (r + 8));
-            float acc[NT][2];
+            float acc[BG_UNIT][NT][2];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = 0.f;
-#pragma unroll 2
+            for (int e = 0; e < BG_UNIT; ++e)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) acc[e][nt][0] = acc[e][nt][1] = 0.f;
             for (int k = 0; k < NC; ++k) {
                 const BgChunk ch = sm.chunks[k];  // warp-uniform
                 const int bw = ch.b;
                 // this lane's blocks 2t, 2t+1 of the chunk: 4 bw contiguous bits
                 const int off = ch.bit0 + 4 * t * bw, wi = off >> 5, sh = off & 31;
-                const uint32_t x0 = __funnelshift_r(rec0[wi], rec0[wi + 1], sh);
-                const uint32_t x8 = __funnelshift_r(rec8[wi], rec8[wi + 1], sh);
-                // A registers: a0 token r block 2t, a1 token r+8 block 2t,
-                // a2 token r block 2t+1, a3 token r+8 block 2t+1
-                uint32_t ah[4], al[4];
                 const uint32_t* cb = sm.cbk2[bw - 1];
                 const uint32_t mask = (1u << bw) - 1u;
-                const uint32_t xs[4] = {x0, x8, x0 >> (2 * bw), x8 >> (2 * bw)};
+                uint2 bb[NT];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t e0 = cb[xs[j] & mask], e1 = cb[(xs[j] >> bw) & mask];
-                    ah[j] = prmt(e0, e1, 0x5410);
-                    al[j] = prmt(e0, e1, 0x7632);
+                for (int nt = 0; nt < NT; ++nt) bb[nt] = sm.bfr[k][nt][lane];
+#pragma unroll
+                for (int e = 0; e < BG_UNIT; ++e) {
+                    const uint32_t* rec0 = reinterpret_cast<const uint32_t*>(tiles[e] + r * tl.kb);
+                    const uint32_t* rec8 = reinterpret_cast<const uint32_t*>(tiles[e] + (r + 8) * tl.kb);
+                    const uint32_t x0 = __funnelshift_r(rec0[wi], rec0[wi + 1], sh);
+                    const uint32_t x8 = __funnelshift_r(rec8[wi], rec8[wi + 1], sh);
+                    // A registers: a0 token r block 2t, a1 token r+8 block 2t,
+                    // a2 token r block 2t+1, a3 token r+8 block 2t+1
+                    uint32_t ah[4], al[4];
+                    const uint32_t xs[4] = {x0, x8, x0 >> (2 * bw), x8 >> (2 * bw)};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t e0 = cb[xs[j] & mask], e1 = cb[(xs[j] >> bw) & mask];
+                        ah[j] = prmt(e0, e1, 0x5410);
+                        al[j] = prmt(e0, e1, 0x7632);
+                    }
+                    const __half* nrm = reinterpret_cast<const __half*>(tiles[e] + tl.off_kn + 2 * (bw - 1));
+                    const float rn0 = __half2float(nrm[8 * r]), rn8 = __half2float(nrm[8 * (r + 8)]);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        float c[4] = {0.f, 0.f, 0.f, 0.f};
+                        mma_f16_16816(c, ah, bb[nt].x, bb[nt].y);
+                        mma_f16_16816(c, al, bb[nt].x, bb[nt].y);
+                        acc[e][nt][0] = fmaf(rn0, c[0] + c[1], acc[e][nt][0]);
+                        acc[e][nt][1] = fmaf(rn8, c[2] + c[3], acc[e][nt][1]);
+                    }
                 }
-                // the chunk's dot products, scaled by the group norms r_{s,b}
-                const float rn0 = __half2float(nr0[bw - 1]), rn8 = __half2float(nr8[bw - 1]);
+            }
+#pragma unroll
+            for (int e = 0; e < BG_UNIT; ++e)
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const uint2 bb = sm.bfr[k][nt][lane];
-                    float c[4] = {0.f, 0.f, 0.f, 0.f};
-                    mma_f16_16816(c, ah, bb.x, bb.y);
-                    mma_f16_16816(c, al, bb.x, bb.y);
-                    acc[nt][0] = fmaf(rn0, c[0] + c[1], acc[nt][0]);
-                    acc[nt][1] = fmaf(rn8, c[2] + c[3], acc[nt][1]);
+                    lg[e][nt][0] = r < n_tok[e] ? acc[e][nt][0] * inv_sig[nt] : -CUDART_INF_F;
+                    lg[e][nt][1] = r + 8 < n_tok[e] ? acc[e][nt][1] * inv_sig[nt] : -CUDART_INF_F;
                 }
-            }
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                lg[nt][0] = r < n_tok ? acc[nt][0] * inv_sig[nt] : -CUDART_INF_F;
-                lg[nt][1] = r + 8 < n_tok ? acc[nt][1] * inv_sig[nt] : -CUDART_INF_F;
-            }
         }
 
         // ---- online softmax (base 2) of head 4 nt + t; p^ goes to pbh
@@ -340,7 +393,7 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         bool need = false;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            float pm = fmaxf(lg[nt][0], lg[nt][1]);
+            float pm = fmaxf(fmaxf(lg[0][nt][0], lg[0][nt][1]), fmaxf(lg[1][nt][0], lg[1][nt][1]));
             pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
             pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
             pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
@@ -351,13 +404,19 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                 need = true;
             }
             const float mref = mrun[nt] == -CUDART_INF_F ? 0.f : mrun[nt];
-            const __half p0 = __float2half_rn(ex2(lg[nt][0] - mref)), p8 = __float2half_rn(ex2(lg[nt][1] - mref));
-            lsum[nt] = fmaf(lsum[nt], corr[nt], __half2float(p0) + __half2float(p8));
+            float ps = 0.f;
             const int hq = 4 * nt + t;
-            if (hq < MAXG) {
-                sm.pbh[warp][hq][r] = p0;
-                sm.pbh[warp][hq][r + 8] = p8;
+#pragma unroll
+            for (int e = 0; e < BG_UNIT; ++e) {
+                const __half p0 = __float2half_rn(ex2(lg[e][nt][0] - mref));
+                const __half p8 = __float2half_rn(ex2(lg[e][nt][1] - mref));
+                ps += __half2float(p0) + __half2float(p8);
+                if (hq < MAXG) {
+                    sm.pbh[warp][hq][PAGE * e + r] = p0;
+                    sm.pbh[warp][hq][PAGE * e + r + 8] = p8;
+                }
             }
+            lsum[nt] = fmaf(lsum[nt], corr[nt], ps);
         }
         if (__any_sync(0xffffffffu, need)) {
             // PV columns 2t, 2t + 1: heads (2t) & 3, (2t + 1) & 3 for groups up
@@ -385,19 +444,22 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         // lo for r >= 4; head r, hi then lo, for groups of 8); rows k =
         // tokens 2t, 2t+1 (b0) and 2t+8, 2t+9 (b1).  Slots past the context
         // get r_v = 0 (their p^ is 0, but a stale norm may be NaN).
-        {
+#pragma unroll
+        for (int e = 0; e < BG_UNIT; ++e) {
+            const uint8_t* tile = tiles[e];
+            const bool full = n_tok[e] == PAGE;
             const int hq = VPL == 1 ? (r & 3) : r;
             const uint32_t* vn = reinterpret_cast<const uint32_t*>(tile + tl.off_vn);
             uint32_t R0 = vn[t], R1 = vn[t + 4];
             if (!full) {
                 const uint32_t lo16 = 0x0000ffffu, hi16 = 0xffff0000u;
-                R0 &= (2 * t < n_tok ? lo16 : 0u) | (2 * t + 1 < n_tok ? hi16 : 0u);
-                R1 &= (2 * t + 8 < n_tok ? lo16 : 0u) | (2 * t + 9 < n_tok ? hi16 : 0u);
+                R0 &= (2 * t < n_tok[e] ? lo16 : 0u) | (2 * t + 1 < n_tok[e] ? hi16 : 0u);
+                R1 &= (2 * t + 8 < n_tok[e] ? lo16 : 0u) | (2 * t + 9 < n_tok[e] ? hi16 : 0u);
             }
             uint32_t P0 = 0u, P1 = 0u;
             if (hq < G) {
-                P0 = lds32(&sm.pbh[warp][hq][2 * t]);
-                P1 = lds32(&sm.pbh[warp][hq][2 * t + 8]);
+                P0 = lds32(&sm.pbh[warp][hq][PAGE * e + 2 * t]);
+                P1 = lds32(&sm.pbh[warp][hq][PAGE * e + 2 * t + 8]);
             }
             const __half2 H0 = __hmul2(u32_as_h2(P0), u32_as_h2(R0)), H1 = __hmul2(u32_as_h2(P1), u32_as_h2(R1));
             const __half2 L0 = __hfma2(u32_as_h2(P0), u32_as_h2(R0), __hneg2(H0));
@@ -445,15 +507,21 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             }
         }
 
+        // hand the unit's slots back: issue the unit n_grp ahead into them
         __syncwarp();
-        if (lane == 0 && i + n_stages < my_count) {
+        if (u + n_grp < n_units) {  // warp-uniform
             fence_proxy_async_smem();
-            issue(i + n_stages, page_of(i + n_stages), pid_next);
-            if (i + n_stages + 1 < my_count) pid_next = __ldg(bt + page_of(i + n_stages + 1));
+            issue_unit(u + n_grp, st, pid_next);
+            n_issued = u + n_grp + 1;
+            const int j = BG_UNIT * (u + n_grp + 1) + lane;
+            if (lane < BG_UNIT && j < my_count) pid_next = __ldg(bt + page_of(j));
         }
+        parity ^= st + 1 == n_grp ? 1u : 0u;
+        st = st + 1 == n_grp ? 0 : st + 1;
     }
-    if (timed_out && lane == 0)
-        for (int s = 0; s < n_stages; ++s) (void)mbar_wait_bounded(&sm.bar[warp][s], 0, 1000000LL);
+    if (u_fail >= 0 && lane == 0)
+        for (int v = u_fail; v < n_issued; ++v)
+            (void)mbar_wait_bounded(&sm.bar[warp][v % n_grp], (v / n_grp) & 1, 1000000LL);
     griddep_launch_dependents();
 
     // ---- warp partial: normalisers summed over the lanes of each head
@@ -551,6 +619,7 @@ extern "C" kvq_status bgtq_decode_attn(const void* q, int B, int H_q, int H_kv, 
                                   128);
     int n_stages = (int)((kSmemMax - fixed) / ((size_t)NW * tile));
     n_stages = n_stages > BG_MAX_STAGES ? BG_MAX_STAGES : n_stages;
+    n_stages -= n_stages % BG_UNIT;  // whole units of pages
     if (n_stages < 2)
         return kvq_set_error(KVQ_ERR_UNSUPPORTED, "bgtq_decode_attn: %d-byte tiles leave no room for two stages", tile);
     const size_t smem = fixed + (size_t)NW * n_stages * tile;
