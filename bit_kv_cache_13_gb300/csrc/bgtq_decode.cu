@@ -39,7 +39,7 @@
 namespace kvq {
 
 constexpr int BG_MAX_STAGES = 8;
-constexpr int BG_UNIT = 2;  // pages per mbarrier phase (ring stages come in pairs)
+constexpr int BG_UNIT = 3;  // pages per mbarrier phase (ring stages come in threes)
 
 template <int MAXG>
 struct BgWarps {
@@ -58,9 +58,6 @@ struct BgChunk {
 
 template <int NW, int MAXG>
 struct __align__(16) BgDecodeSmem {
-    union {
-        float o_part[NW][MAXG][D];  // per-warp o' after the loop
-    } u;
     uint2 bfr[BG_MAX_CHUNKS][MAXG / 4][32];  // QK B fragments per chunk, n-tile and lane
     uint32_t cbk2[8][256];  // C_b / sqrt(n_b) per width as (fp16 hi | fp16 lo << 16)
     BgChunk chunks[BG_MAX_CHUNKS];
@@ -91,8 +88,11 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     extern __shared__ __align__(128) uint8_t smem_raw[];
     BgDecodeSmem<NW, MAXG>& sm = *reinterpret_cast<BgDecodeSmem<NW, MAXG>*>(smem_raw);
     const BgtqTile tl(total_bits, VB);
-    uint8_t* my_ring = smem_raw + align_up(sizeof(BgDecodeSmem<NW, MAXG>), 128) +
-                       (size_t)(threadIdx.x >> 5) * n_stages * tl.bytes;
+    // the page rings follow the fixed part; after the loop the per-warp o'
+    // partials take their place (the host sizes the region for both)
+    uint8_t* ring_base = smem_raw + align_up(sizeof(BgDecodeSmem<NW, MAXG>), 128);
+    uint8_t* my_ring = ring_base + (size_t)(threadIdx.x >> 5) * n_stages * tl.bytes;
+    float(*o_part)[MAXG][D] = reinterpret_cast<float(*)[MAXG][D]>(ring_base);
 
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int S = gridDim.x, B = gridDim.z;
@@ -393,7 +393,9 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         bool need = false;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            float pm = fmaxf(fmaxf(lg[0][nt][0], lg[0][nt][1]), fmaxf(lg[1][nt][0], lg[1][nt][1]));
+            float pm = fmaxf(lg[0][nt][0], lg[0][nt][1]);
+#pragma unroll
+            for (int e = 1; e < BG_UNIT; ++e) pm = fmaxf(pm, fmaxf(lg[e][nt][0], lg[e][nt][1]));
             pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 4));
             pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
             pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
@@ -531,6 +533,7 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         lsum[nt] += __shfl_xor_sync(0xffffffffu, lsum[nt], 8);
         lsum[nt] += __shfl_xor_sync(0xffffffffu, lsum[nt], 16);
     }
+    __syncthreads();  // every warp is done with its ring (o_part takes its place)
     if constexpr (VPL == 1) {
         // columns 4..7 (lanes t = 2, 3) hold the low parts of heads 0..3
 #pragma unroll
@@ -543,12 +546,12 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         for (int m = 0; m < 8; ++m) {
             const int c0 = 16 * r + 2 * m;
             if (2 * t < G) {
-                sm.u.o_part[warp][2 * t][c0] = oacc[m][0];
-                sm.u.o_part[warp][2 * t][c0 + 1] = oacc[m][2];
+                o_part[warp][2 * t][c0] = oacc[m][0];
+                o_part[warp][2 * t][c0 + 1] = oacc[m][2];
             }
             if (2 * t + 1 < G) {
-                sm.u.o_part[warp][2 * t + 1][c0] = oacc[m][1];
-                sm.u.o_part[warp][2 * t + 1][c0 + 1] = oacc[m][3];
+                o_part[warp][2 * t + 1][c0] = oacc[m][1];
+                o_part[warp][2 * t + 1][c0 + 1] = oacc[m][3];
             }
         }
     }
@@ -563,7 +566,7 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         }
     }
     __syncthreads();
-    finish_decode<NW, MAXG>(sm.ms, sm.u.o_part, G, H_q, H_kv, B, b, h, split, S, ws, pi_table + __ldg(pi_offsets + D),
+    finish_decode<NW, MAXG>(sm.ms, o_part, G, H_q, H_kv, B, b, h, split, S, ws, pi_table + __ldg(pi_offsets + D),
                             out);
 }
 
@@ -620,9 +623,12 @@ extern "C" kvq_status bgtq_decode_attn(const void* q, int B, int H_q, int H_kv, 
     int n_stages = (int)((kSmemMax - fixed) / ((size_t)NW * tile));
     n_stages = n_stages > BG_MAX_STAGES ? BG_MAX_STAGES : n_stages;
     n_stages -= n_stages % BG_UNIT;  // whole units of pages
-    if (n_stages < 2)
-        return kvq_set_error(KVQ_ERR_UNSUPPORTED, "bgtq_decode_attn: %d-byte tiles leave no room for two stages", tile);
-    const size_t smem = fixed + (size_t)NW * n_stages * tile;
+    if (n_stages < BG_UNIT)
+        return kvq_set_error(KVQ_ERR_UNSUPPORTED, "bgtq_decode_attn: %d-byte tiles leave no room for a unit of stages", tile);
+    const size_t ring = (size_t)NW * n_stages * tile, o_bytes = (size_t)NW * (small ? 4 : 8) * D * sizeof(float);
+    const size_t smem = fixed + (ring > o_bytes ? ring : o_bytes);
+    if (smem > kSmemMax)
+        return kvq_set_error(KVQ_ERR_UNSUPPORTED, "bgtq_decode_attn: %d-byte tiles leave no room", tile);
     const BgKernel kern = kBgKernels[small ? 0 : 1][v_bits - 1];
     const int kid = (small ? 0 : 8) + v_bits - 1;
     {
