@@ -11,18 +11,18 @@
 // Grid (split, kv_head, seq) with one CTA per SM (12 warps for head groups
 // up to 4, 8 for groups of 8); the pages of a (sequence, KV head) are dealt
 // round-robin over all warps of its CTAs and streamed through per-warp rings
-// of bulk async copies, as in the INT2 decode, two pages per mbarrier phase
-// (one wait, one release, one softmax rescale, and one pass over the chunk
-// descriptors per pair).  Per page (16 tokens):
-//   QK  lane l owns gathered positions 4l .. 4l+3 (two RoPE blocks).  Their
-//       q~ for every head stays in registers, and their four codes are
-//       contiguous bits of a token's stream (groups are laid out in
-//       ascending width), cut out by one funnel shift and four bit-field
-//       extracts.  C_b[code] comes from the shared-memory codebook and is
-//       scaled by the token's group norm r_b.  The lanes' partial dots of 8
-//       tokens at a time go through a padded shared-memory transpose and are
-//       summed by column, which leaves each lane the logit of one token for
-//       one head (two heads for groups of 8).
+// of bulk async copies, as in the INT2 decode, three pages per mbarrier
+// phase (one wait, one release, one softmax rescale, and one pass over the
+// chunk descriptors and B fragments per unit).  Per page (16 tokens):
+//   QK  mma.sync m16n8k16 over chunks of 16 gathered positions of one width
+//       (a width group padded to a multiple of 16; groups are laid out in
+//       ascending width).  Rows = tokens r, r + 8; lane t holds the chunk's
+//       RoPE blocks 2t, 2t + 1, whose 4b code bits are contiguous in a
+//       token's stream and come out of one 32-bit window.  A = C_b[code] /
+//       sqrt(n_b) as an fp16 hi/lo pair from a shared-memory table; B =
+//       q~ sigma (a per-head power of two) as hi/lo columns, zero past the
+//       group; the token's group norm r_{s,b} scales each chunk's dot
+//       products in fp32.
 //   softmax  online, base 2, exact running maximum per head; p is rounded to
 //       fp16 once (p^), and the same p^ weights the values and the
 //       normaliser.

@@ -413,7 +413,7 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         return true;
     };
 
-    // ---------------- QK of page i: base-2 logits of tokens r, r + 8 for
+    // ---------------- QK of the page in ring slot `slot`: base-2 logits of tokens r, r + 8 for
     // head 4*nt + t (-inf past the context)
     auto qk_page = [&](int slot, float (&lg)[NT][2]) {
         const uint8_t* tile = sm.u.ring[warp][slot];
@@ -522,7 +522,7 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         }
     };
 
-    // ---------------- PV of page i with its weights p^
+    // ---------------- PV of the page in ring slot `slot` with its weights p^
     auto pv_page = [&](int slot, const float (&pr)[NT][2]) {
         const uint8_t* tile = sm.u.ring[warp][slot];
         // P in the PV B layout: column n = r (head n), rows = tokens 2t, 2t+1 | 2t+8, 2t+9
