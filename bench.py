@@ -314,6 +314,53 @@ def measure_bgtq(device, stream, reps):
             "l2": "256 MB buffer written before every timed launch"}
 
 
+def measure_int2_window(spec, device, stream, reps):
+    """INT2 decode of one 128K layer with a BF16 window of 4 sink + 128
+    recent tokens per sequence (kvq_decode_attn_int2_window), against the
+    plain decode of the same layer; a 256 MB L2 flush before each launch."""
+    layer = Int2Layer(spec, 0, device=device)
+    layer.prefill()
+    q = layer.queries()
+    g = torch.Generator(device=device)
+    g.manual_seed(13)
+    w = 4 + 128
+    win_k = torch.randn((spec.batch, w, spec.h_kv, spec.d), generator=g, device=device).to(torch.bfloat16)
+    win_v = torch.randn((spec.batch, w, spec.h_kv, spec.d), generator=g, device=device).to(torch.bfloat16)
+    win_lens = torch.full((spec.batch,), w, dtype=torch.int32, device=device)
+    out = torch.zeros((spec.batch, spec.h_q, spec.d), dtype=torch.float32, device=device)
+    ws = layer.workspace()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    plain = lambda: _lib.kvq_decode_attn_int2(q, layer.cache, layer.num_pages, layer.block_table, layer.context_lens,
+                                              layer.R_k, layer.R_v, layer.scale, out, ws)
+    window = lambda: _lib.kvq_decode_attn_int2_window(q, layer.cache, layer.num_pages, layer.block_table,
+                                                      layer.context_lens, layer.R_k, layer.R_v, layer.mu, win_k,
+                                                      win_v, win_lens, layer.scale, out, ws)
+    res = {}
+    for name, fn in (("plain", plain), ("window", window)):
+        for _ in range(3):
+            fn()
+        durs = []
+        for _ in range(reps):
+            flush.zero_()
+            durs.append(time_launches(stream, fn, 1))
+        res[name] = statistics.median(durs)
+    # the packed cache, the BF16 window (keys and values), q in and out
+    nbytes = (layer.packed_bytes_per_decode() + spec.batch * w * spec.h_kv * spec.d * 2 * 2
+              + spec.batch * spec.h_q * spec.d * 6)
+    peak, kind = peaks()
+    gbs = nbytes / (res["window"] * 1e-3) / 1e9
+    out_line = {"workload": f"{spec.name}: one layer, batch {spec.batch}, {spec.ctx} cached tokens + a BF16 window of "
+                            f"{w} tokens (4 sink + 128 recent) per sequence",
+                "kernel": "decode_int2_kernel<1, true>", "ms_per_decode": round(res["window"], 4),
+                "ms_plain_decode": round(res["plain"], 4), "value": round(gbs, 2), "unit": "GB/s",
+                "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peak, "unit": "GB/s",
+                             "frac": round(gbs / peak, 4), "peak_kind": kind},
+                "l2": "256 MB buffer written before every timed launch"}
+    del layer
+    torch.cuda.empty_cache()
+    return out_line
+
+
 # 128 fp32 lanes per SM x 152 SMs x 2 flop per fma at the 2070 MHz maximum SM clock
 FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 
@@ -532,6 +579,7 @@ def run_ours(args, world, rank, local):
             line["bgtq"] = measure_bgtq(device, stream, reps=max(3, min(args.steps, 10)))
         line["append_prefill"] = measure_append_prefill(spec, device, stream, reps=3)
         line["gqa8"] = measure_int2_gqa8(device, stream, reps=3)
+        line["window"] = measure_int2_window(spec, device, stream, reps=5)
     if rank == 0 and not args.no_cpu_baseline:
         gbs, el, sample = oracle_baseline(spec)
         line["cpu_baseline"] = {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",

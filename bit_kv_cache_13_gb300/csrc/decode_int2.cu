@@ -772,7 +772,10 @@ static kvq_status decode_int2_launch(const char* fn, const void* q, int B, int H
         if (reinterpret_cast<uintptr_t>(win_k) % 16 || reinterpret_cast<uintptr_t>(win_v) % 16)
             return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: win_k and win_v need 16-byte alignment", fn);
     }
-    const int S_pages = num_splits > 0 ? num_splits : kvq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
+    int S_pages = num_splits > 0 ? num_splits : kvq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
+    // the automatic choice fills one wave; with a window, its split takes
+    // one of those CTAs (a 153rd CTA would run alone in a second wave)
+    if (num_splits == 0 && win_k && S_pages > 1 && (long)(S_pages + 1) * B * H_kv > 152L) S_pages -= 1;
     const int S = S_pages + (win_k ? 1 : 0);
     if (S > MAX_SPLITS)
         return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: %d splits above %d", fn, S, MAX_SPLITS);
