@@ -341,6 +341,7 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             for (int e = 0; e < BG_UNIT; ++e)
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) acc[e][nt][0] = acc[e][nt][1] = 0.f;
+#pragma unroll 2
             for (int k = 0; k < NC; ++k) {
                 const BgChunk ch = sm.chunks[k];  // warp-uniform
                 const int bw = ch.b;
