@@ -33,6 +33,34 @@ def test_sizes(cpu_lib):
     assert ws >= 2 * 8 * 3 * 132 * 4
 
 
+@pytest.mark.parametrize("B,H_kv,pages,want", [
+    (1, 8, 8192, 19),      # 128K batch 1: 8 x 19 = 152 CTAs, one wave
+    (8, 8, 2048, 2),       # 32K batch 8: 64 (sequence, KV head) units, 128 CTAs
+    (8, 8, 8192, 2),
+    (64, 8, 256, 1),       # more units than SMs: one split each
+    (1, 1, 16, 1),         # at least 32 pages per split
+    (1, 1, 64, 2),
+    (1, 1, 100000, 152),   # bounded by the SM count, then by 256
+    (1, 2, 4096, 76),
+])
+def test_auto_splits_fill_one_wave(cpu_lib, B, H_kv, pages, want):
+    s = _lib.kvq_decode_auto_splits(B, 4 * H_kv, H_kv, pages)
+    assert s == want
+    assert s * B * H_kv <= max(152, B * H_kv)          # never a second wave of CTAs of its own
+    assert 1 <= s <= min(max(1, (pages + 31) // 32), 256)
+
+
+def test_workspace_with_auto_splits_holds_every_entry_point(cpu_lib):
+    """num_splits = 0 sizes the partials for the automatic choice of every
+    decode call, the BF16-window form (one more split) included."""
+    for B, H_kv, pages in [(1, 8, 8192), (8, 8, 2048), (3, 2, 40)]:
+        H_q = 4 * H_kv
+        auto = _lib.kvq_decode_auto_splits(B, H_q, H_kv, pages)
+        ws0 = _lib.kvq_decode_workspace_bytes(B, H_q, H_kv, pages, 0)
+        assert ws0 >= _lib.kvq_decode_workspace_bytes(B, H_q, H_kv, pages, auto + 1)
+        assert ws0 >= B * H_q * (auto + 1) * 132 * 4
+
+
 def test_allocator_matches_oracle(cpu_lib):
     rng = np.random.default_rng(0)
     for trial in range(50):
