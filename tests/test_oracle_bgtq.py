@@ -272,3 +272,176 @@ def test_energy_scores_recover_the_generators_block_energies():
     for h in range(2):
         want = inputs.block_energies(spec, 0, h)
         assert np.max(np.abs(s[h] / want - 1)) < 0.1
+
+
+# ------------------------------------------------- nearest centroid (tie rule)
+
+def _brute_nearest(y32, cb32):
+    """Nearest centroid by exact rational distances; equal distances go to
+    the lower index (the reading of the TQ-MSE scalar quantiser taken here)."""
+    from fractions import Fraction
+    cs = [Fraction(float(c)) for c in np.asarray(cb32, np.float32)]
+    out = []
+    for y in np.asarray(y32, np.float32).ravel():
+        yf = Fraction(float(y))
+        d = [abs(yf - c) for c in cs]
+        out.append(min(range(len(cs)), key=lambda k: (d[k], k)))
+    return np.asarray(out).reshape(np.shape(y32))
+
+
+@pytest.mark.parametrize("b,n", [(1, 2), (2, 8), (3, 30), (4, 64), (6, 128), (8, 2)])
+def test_nearest_codes_brute_force_random(table, b, n):
+    cb = bgtq.scaled_codebook(table, b, n)
+    rng = np.random.default_rng(100 * b + n)
+    y = (rng.standard_normal(400) * 1.3 / np.sqrt(n)).astype(np.float32)
+    assert np.array_equal(bgtq.nearest_codes(y, cb), _brute_nearest(y, cb))
+
+
+def test_nearest_codes_exact_midpoints_go_low():
+    # a codebook whose midpoints are exact in fp32: -1, 0, 1 lie exactly
+    # between two centroids and must take the lower index; the fp32
+    # neighbours on either side go to the nearer centroid
+    cb = np.array([-1.5, -0.5, 0.5, 1.5], np.float32)
+    mids = np.array([-1.0, 0.0, 1.0], np.float32)
+    assert bgtq.nearest_codes(mids, cb).tolist() == [0, 1, 2]
+    up = np.nextafter(mids, np.float32(np.inf))
+    dn = np.nextafter(mids, np.float32(-np.inf))
+    assert bgtq.nearest_codes(up, cb).tolist() == [1, 2, 3]
+    assert bgtq.nearest_codes(dn, cb).tolist() == [0, 1, 2]
+    ends = np.array([-1e30, 1e30, -1.5, 1.5], np.float32)
+    assert bgtq.nearest_codes(ends, cb).tolist() == [0, 3, 0, 3]
+    allv = np.concatenate([mids, up, dn, ends])
+    assert np.array_equal(bgtq.nearest_codes(allv, cb), _brute_nearest(allv, cb))
+
+
+def test_nearest_codes_ties_on_the_real_codebooks(table):
+    # wherever the fp64 midpoint of two adjacent scaled centroids is itself
+    # an fp32 value, y on it takes the lower index (brute force agrees); the
+    # next fp32 values above it take the upper one
+    seen = 0
+    for b in range(1, 9):
+        for n in (2, 6, 16, 40, 128):
+            cb = bgtq.scaled_codebook(table, b, n)
+            c64 = cb.astype(np.float64)
+            m = 0.5 * (c64[:-1] + c64[1:])
+            exact = m.astype(np.float32).astype(np.float64) == m
+            if not exact.any():
+                continue
+            k = np.nonzero(exact)[0]
+            y = m[k].astype(np.float32)
+            assert np.array_equal(bgtq.nearest_codes(y, cb), k)
+            assert np.array_equal(bgtq.nearest_codes(np.nextafter(y, np.float32(np.inf)), cb), k + 1)
+            assert np.array_equal(bgtq.nearest_codes(y, cb), _brute_nearest(y, cb))
+            seen += len(k)
+    assert seen >= 8   # the symmetric codebooks put an exact midpoint at 0 for every width
+
+
+# ------------------------------------ TQ-MSE with the rotation taken in fp64
+
+def _signed_permutation(n, seed):
+    rng = np.random.default_rng(seed)
+    while True:                                   # a non-symmetric one, so Pi != Pi^T
+        perm = rng.permutation(n)
+        sign = rng.choice([-1.0, 1.0], n)
+        p = np.zeros((n, n), np.float32)
+        p[np.arange(n), perm] = sign
+        if not np.array_equal(p, p.T):
+            return p, perm, sign
+
+
+@pytest.mark.parametrize("n", [2, 10, 64, 128])
+def test_tq_fp64_rotation_on_a_signed_permutation(table, n):
+    # with Pi a signed permutation every product is exact, so y = u Pi can be
+    # written out by index: y[perm[i]] = sign[i] u[i]; a transposed Pi (u Pi^T)
+    # or a dropped normalisation would not match
+    p, perm, sign = _signed_permutation(n, n)
+    rng = np.random.default_rng(7 + n)
+    x = (rng.standard_normal((50, n)) * rng.lognormal(0, 1, (50, 1))).astype(np.float32)
+    x[3] = 0.0
+    cb = bgtq.scaled_codebook(table, 3, n)
+    codes, nh, r, y = bgtq.tq_encode_fp64_rotation(x, p, cb)
+    r64 = np.sqrt(np.sum(x.astype(np.float64) ** 2, -1))
+    assert np.array_equal(r, r64.astype(np.float32))
+    u = (x / np.where(r > 0, r, 1)[:, None].astype(np.float32)).astype(np.float32)
+    want = np.zeros_like(u)
+    want[:, perm] = u * sign[None, :].astype(np.float32)
+    assert np.array_equal(y, want)
+    assert np.array_equal(codes[r > 0], _brute_nearest(want, cb)[r > 0])
+    assert codes[3].max() == 0 and float(nh[3]) == 0.0
+    assert np.array_equal(nh, r.astype(np.float16))
+
+
+def test_tq_fp64_rotation_agrees_with_the_fp32_chain(table):
+    # the two encoders differ only in how y and r are rounded: a code may
+    # differ only where y lies within a few fp32 ulps of a midpoint, and such
+    # flips must be rare
+    pis = bgtq.tq_rotation_dict(*inputs.tq_rotations(128, "pin"))
+    rng = np.random.default_rng(21)
+    flips = total = 0
+    for n, b in ((8, 4), (30, 3), (128, 3), (64, 2)):
+        x = (rng.standard_normal((600, n)) * rng.lognormal(0, 1, (600, 1))).astype(np.float32)
+        cb = bgtq.scaled_codebook(table, b, n)
+        c1, n1, r1, y1 = bgtq.tq_encode(x, pis[n], cb)
+        c2, n2, r2, y2 = bgtq.tq_encode_fp64_rotation(x, pis[n], cb)
+        assert np.max(np.abs(r1.astype(np.float64) / r2 - 1)) <= 4e-7
+        assert np.max(np.abs(y1.astype(np.float64) - y2)) <= 1e-5
+        diff = c1 != c2
+        if diff.any():
+            c64 = cb.astype(np.float64)
+            mids = 0.5 * (c64[:-1] + c64[1:])
+            lo = np.minimum(c1[diff], c2[diff])
+            gap = np.abs(y2[diff].astype(np.float64) - mids[lo])
+            ulp = np.spacing(np.abs(y2[diff])).astype(np.float64)
+            assert np.all(gap <= 8 * ulp + np.abs(y1[diff].astype(np.float64) - y2[diff]))
+            assert np.all(np.abs(c1[diff] - c2[diff]) == 1)
+        flips += int(diff.sum())
+        total += diff.size
+        assert np.sum(n1 != n2) <= 0.01 * n1.size
+    assert flips <= 1e-3 * total
+
+
+# --------------------------------------------- dense dequantisation of a head
+
+def test_dequantize_dense_equals_the_packed_cache_read_back(table):
+    # dequantize_dense (no packing) against read_token of the cache that
+    # append wrote (bit streams, norm slots, grouped layout): a gather or
+    # scatter slip in either path breaks the equality
+    pis = bgtq.tq_rotation_dict(*inputs.tq_rotations(128, "pin"))
+    rng = np.random.default_rng(41)
+    T, v_bits = 21, 3
+    s = rng.lognormal(0, 2, 64)
+    widths = bgtq.greedy_allocate(s, 1, 8, 192)
+    sd = np.sqrt(np.concatenate([s, s]) / 2)
+    k = (rng.standard_normal((T, 1, 128)) * sd).astype(np.float32)
+    v = rng.standard_normal((T, 1, 128)).astype(np.float32)
+    k[4] = 0.0
+    cache = bgtq.new_cache(2, 1, 192, v_bits)
+    slots = rng.permutation(32)[:T]
+    bgtq.append(cache, k, v, slots, widths[None], v_bits, 192, pis, table)
+    kh, vh = bgtq.dequantize_dense(k[:, 0], v[:, 0], widths, v_bits, pis, table)
+    for t in range(T):
+        page, sl = divmod(int(slots[t]), 16)
+        kt, vt = bgtq.read_token(cache, page, sl, 0, widths, v_bits, 192, pis, table)
+        # equal up to the summation order of the batched and single products
+        assert np.max(np.abs(kh[t] - kt)) <= 1e-12 * max(1.0, np.max(np.abs(kt)))
+        assert np.max(np.abs(vh[t] - vt)) <= 1e-12 * max(1.0, np.max(np.abs(vt)))
+    assert np.all(kh[4] == 0)
+
+
+def test_dequantize_dense_approaches_the_input_at_high_width(table):
+    # at 8 bits per coordinate TQ-MSE keeps ~1e-4 of the energy as error;
+    # a transposed rotation, a wrong dimension pairing or a dropped norm gives
+    # errors of order one.  Both rotation paths are checked.
+    pis = bgtq.tq_rotation_dict(*inputs.tq_rotations(128, "pin"))
+    rng = np.random.default_rng(42)
+    T = 40
+    widths = np.concatenate([np.full(20, 8), np.full(44, 7)])
+    rng.shuffle(widths)
+    k = (rng.standard_normal((T, 128)) * rng.lognormal(0, 1, (T, 1))).astype(np.float32)
+    v = (rng.standard_normal((T, 128)) * 3).astype(np.float32)
+    for exact in (True, False):
+        kh, vh = bgtq.dequantize_dense(k, v, widths, 8, pis, table, exact_chain=exact)
+        ek = np.sum((kh - k) ** 2, -1) / np.sum(k.astype(np.float64) ** 2, -1)
+        ev = np.sum((vh - v) ** 2, -1) / np.sum(v.astype(np.float64) ** 2, -1)
+        assert ek.max() <= 20 * bgtq.C_TQ * 4.0 ** -7 and ev.max() <= 20 * bgtq.C_TQ * 4.0 ** -8
+        assert ek.mean() <= bgtq.C_TQ * 4.0 ** -7
