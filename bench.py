@@ -181,12 +181,14 @@ def arena(tensors, device):
 
 class Int2Step:
     """All layers of one decode step, resident on the device; the per-step
-    inputs (q, new k / v, slots) and outputs live in one arena each."""
+    inputs (q, new k / v) and outputs live in one arena each.  A layer's step
+    is one launch of kvq_decode_step_int2: the new token is appended at
+    position ctx - 1 and the ctx tokens are attended."""
 
     def __init__(self, spec, device):
         self.spec = spec
         self.layers = []
-        self.q, self.k_new, self.v_new, self.slots, self.out, self.ws = [], [], [], [], [], []
+        self.q, self.k_new, self.v_new, self.out, self.ws = [], [], [], [], []
         for l in range(spec.n_layers):
             layer = Int2Layer(spec, l, device=device)
             layer.prefill()
@@ -195,18 +197,21 @@ class Int2Step:
             self.q.append(layer.queries())
             self.k_new.append(k)
             self.v_new.append(v)
-            self.slots.append(layer.new_slots())
             self.out.append(torch.zeros((spec.batch, spec.h_q, spec.d), dtype=torch.float32, device=device))
             self.ws.append(layer.workspace())
         L = spec.n_layers
-        self.in_arena, views = arena(self.q + self.k_new + self.v_new + self.slots, device)
-        self.q, self.k_new, self.v_new, self.slots = views[:L], views[L:2 * L], views[2 * L:3 * L], views[3 * L:]
+        self.in_arena, views = arena(self.q + self.k_new + self.v_new, device)
+        self.q, self.k_new, self.v_new = views[:L], views[L:2 * L], views[2 * L:]
         self.out_arena, self.out = arena(self.out, device)
         torch.cuda.synchronize()
 
-    def append(self, l):
+    def step(self, l):
         L = self.layers[l]
-        _lib.kvq_append_int2(self.k_new[l], self.v_new[l], self.slots[l], L.mu, L.R_k, L.R_v, L.cache, L.num_pages)
+        # each layer's rotations, block table and cache are written only by
+        # its own step, never by the launch just before (another layer's)
+        _lib.kvq_decode_step_int2(self.q[l], self.k_new[l], self.v_new[l], L.cache, L.num_pages, L.block_table,
+                                  L.context_lens, L.mu, L.R_k, L.R_v, L.scale, self.out[l], self.ws[l],
+                                  flags=_lib.KVQ_STEP_INPUTS_READY)
 
     def decode(self, l):
         L = self.layers[l]
@@ -215,8 +220,7 @@ class Int2Step:
 
     def run(self):
         for l in range(len(self.layers)):
-            self.append(l)
-            self.decode(l)
+            self.step(l)
 
     # byte accounting (algorithmic)
     def units_per_decode(self) -> int:
@@ -519,17 +523,19 @@ def run_ours(args, world, rank, local):
     value = world * bytes_step / (ms_per_step * 1e-3) / 1e9
     clocks = clk.summary()
 
-    # ---- decode kernel alone: the 36 layers' decode launches back to back
-    # between one pair of CUDA events (launches are enqueued faster than they
-    # run, so no host gap is timed); each layer's cache is cold in L2
-    dec_ms = []
+    # ---- the step kernel alone: the 36 layers' launches back to back between
+    # one pair of CUDA events (launches are enqueued faster than they run, so
+    # no host gap is timed); each layer's cache is cold in L2.  The same for
+    # the decode-only entry point, for comparison.
+    dec_ms, only_ms = [], []
     for _ in range(max(2, min(args.steps, 5))):
-        dec_ms.append(time_launches(stream, lambda: [st.decode(l) for l in range(spec.n_layers)], 1)
-                      / spec.n_layers)
+        dec_ms.append(time_launches(stream, lambda: [st.step(l) for l in range(spec.n_layers)], 1) / spec.n_layers)
+        only_ms.append(time_launches(stream, lambda: [st.decode(l) for l in range(spec.n_layers)], 1)
+                       / spec.n_layers)
     dec_avg_ms = statistics.median(dec_ms)
     peak, peak_kind = peaks()
-    achieved = st.bytes_per_decode() / (dec_avg_ms * 1e-3) / 1e9
-    traffic = profiled_traffic("decode_int2", ("decode_int2.cu", "merge.cuh", "kvq_common.cuh"),
+    achieved = (st.bytes_per_decode() + st.bytes_per_append()) / (dec_avg_ms * 1e-3) / 1e9
+    traffic = profiled_traffic("decode_int2", ("decode_int2.cu", "int2_quant.cuh", "merge.cuh", "kvq_common.cuh"),
                                st.units_per_decode())
 
     # ---- end to end through the C ABI with host buffers
@@ -542,7 +548,7 @@ def run_ours(args, world, rank, local):
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(args.steps):
-            st.in_arena.copy_(host_in, non_blocking=True)     # the step's q, new k / v and slots
+            st.in_arena.copy_(host_in, non_blocking=True)     # the step's q and new k / v
             graph.replay()
             host_out.copy_(st.out_arena, non_blocking=True)   # the step's outputs
         e1.record(stream)
@@ -561,12 +567,14 @@ def run_ours(args, world, rank, local):
         "bytes_per_step": bytes_step,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "decode_int2_kernel", "avg_launch_us": round(dec_avg_ms * 1e3, 3),
-                     "timing": "36 layer decodes back to back, one event pair, median of 5",
-                     "bytes_per_launch": st.bytes_per_decode()},
+                     "kernel": "decode_int2_kernel (step: new-token append + decode)",
+                     "avg_launch_us": round(dec_avg_ms * 1e3, 3),
+                     "timing": "36 layer steps back to back, one event pair, median of 5",
+                     "bytes_per_launch": st.bytes_per_decode() + st.bytes_per_append(),
+                     "decode_only_us": round(statistics.median(only_ms) * 1e3, 3)},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": 2 * spec.n_layers * args.steps,
+        "gpu_launches": spec.n_layers * args.steps,
         "clocks": clocks,
     }
     del graph, st

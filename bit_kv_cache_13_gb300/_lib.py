@@ -35,6 +35,8 @@ _SIGS = {
     "kvq_dequant_int2": ([P, I64, I, I, P, I, P, P, P], I),
     "bgtq_energy_scores": ([P, P, I, I, I, I, P, P, P], I),
     "kvq_decode_attn_int2_noalloc": ([P, I, I, I, I, P, I64, P, I, P, P, P, F, P, I, P], I),
+    "kvq_debug_drop_next_copy": ([], None),
+    "kvq_decode_step_int2": ([P, P, P, I, I, I, I, P, I64, P, I, P, P, P, P, F, P, P, SZ, I, I, P], I),
     "bgtq_lloyd_max_codebook": ([I, P], I),
     "bgtq_allocate": ([P, I, I, I, I64, P], I),
     "bgtq_tile_bytes": ([I, I], SZ),
@@ -157,6 +159,28 @@ def kvq_decode_attn_int2(q, cache, num_pages: int, block_table, context_lens, R_
         _dev(workspace, torch.uint8, "workspace"), workspace.numel(), int(num_splits), _stream(stream)))
 
 
+KVQ_STEP_INPUTS_READY = 1
+
+
+def kvq_decode_step_int2(q, k_new, v_new, cache, num_pages: int, block_table, context_lens, mu_k, R_k, R_v,
+                         scale: float, out, workspace, num_splits: int = 0, flags: int = 0, stream=None):
+    """One decode step in one launch: the new token k_new, v_new [B, H_kv, d]
+    bf16 is appended at position context_lens[b] - 1 of each sequence, then
+    the context_lens[b] tokens are attended.  flags = KVQ_STEP_INPUTS_READY
+    declares the rotations, key centre, block table, context lengths and
+    cache untouched by the kernel just before (read early)."""
+    B, H_q, d = q.shape
+    h_kv = k_new.shape[1]
+    _check(load().kvq_decode_step_int2(
+        _dev(q, torch.bfloat16, "q"), _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+        B, H_q, h_kv, d, _dev(cache, torch.uint8, "cache"), int(num_pages),
+        _dev(block_table, torch.int32, "block_table"), block_table.shape[1],
+        _dev(context_lens, torch.int32, "context_lens"), _dev(mu_k, torch.float32, "mu_k"),
+        _dev(R_k, torch.float32, "R_k"), _dev(R_v, torch.float32, "R_v"), float(scale),
+        _dev(out, torch.float32, "out"), _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+        int(num_splits), int(flags), _stream(stream)))
+
+
 def kvq_decode_attn_int2_window(q, cache, num_pages: int, block_table, context_lens, R_k, R_v, mu_k, win_k, win_v,
                                 win_lens, scale: float, out, workspace, num_splits: int = 0, H_kv: int | None = None,
                                 stream=None):
@@ -186,6 +210,12 @@ def kvq_decode_attn_int2_noalloc(q, cache, num_pages: int, block_table, context_
         _dev(context_lens, torch.int32, "context_lens"), _dev(R_k, torch.float32, "R_k"),
         _dev(R_v, torch.float32, "R_v"), float(scale), _dev(out, torch.float32, "out"), int(num_splits),
         _stream(stream)))
+
+
+def kvq_debug_drop_next_copy() -> None:
+    """Test hook: the next INT2 decode launch leaves one bulk copy unissued
+    so a bounded wait runs out (the call then reports KVQ_ERR_CUDA)."""
+    load().kvq_debug_drop_next_copy()
 
 
 def kvq_workspace_status(workspace, stream=None) -> int:

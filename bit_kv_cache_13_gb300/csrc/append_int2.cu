@@ -17,41 +17,9 @@
 // register-tiled kernel with R in shared memory that runs the same chains.
 #include <mutex>
 
-#include "kvq_common.cuh"
+#include "int2_quant.cuh"
 
 namespace kvq {
-
-// Group parameters from the exact group min / max: the clip ratio c of
-// Q2(.; c, G) scales both range ends, scale = (max - min) / 3 and min go
-// to fp16 (saturating).
-__device__ __forceinline__ void int2_params(float mn, float mx, float clip, __half& sh, __half& mh) {
-    mn = __fmul_rn(clip, mn);
-    mx = __fmul_rn(clip, mx);
-    sh = f16_sat(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
-    mh = f16_sat(mn);
-}
-
-// code = #{c : min + (c + 1/2) scale < x}, decided exactly
-__device__ __forceinline__ int int2_code(float x, float mnf, float scf) {
-    if (!(scf > 0.f)) return 0;
-    float hi, lo;
-    two_sum(x, -mnf, hi, lo);
-    return (int)diff_gt(hi, lo, __fmul_rn(scf, 0.5f)) + (int)diff_gt(hi, lo, __fmul_rn(scf, 1.5f)) +
-           (int)diff_gt(hi, lo, __fmul_rn(scf, 2.5f));
-}
-
-// The (scale, min) of slot s, group g: keys one word per group, values
-// pair-major halves.
-__device__ __forceinline__ void int2_store_meta(uint8_t* tile, int is_v, int s, int g, __half sh, __half mh) {
-    if (is_v) {
-        uint8_t* m = tile + vm_scale_off(s, g);
-        *reinterpret_cast<__half*>(m) = sh;
-        *reinterpret_cast<__half*>(m + VM_MINS) = mh;
-    } else {
-        const uint32_t meta = (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(mh) << 16);
-        *reinterpret_cast<uint32_t*>(tile + OFF_KM + 16 * s + 4 * g) = meta;
-    }
-}
 
 __global__ void __launch_bounds__(64)
 append_int2_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v, int n_tok,
@@ -66,13 +34,17 @@ append_int2_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
     const int lane = tid & 31;
     const int j = 32 * grp + lane;  // output channel
 
-    // the rotations are constants of the layer: loaded while the previous
-    // kernel in the stream may still be running
+    // this thread's column of the rotation: its 128-byte row segments are
+    // fetched into L2 while the previous kernel in the stream may still be
+    // running (a prefetch returns no data; L2 is the point of coherence, so
+    // a later write by that kernel still wins), and read after the wait
     const float* R = (is_v ? Rv : Rk) + (size_t)h * D * D;
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) prefetch_l2(R + (size_t)(lane + 32 * e) * D + 32 * grp);
+    griddep_wait();  // every input (rotations included) may come from the previous kernel
     float rcol[D];
 #pragma unroll
     for (int i = 0; i < D; ++i) rcol[i] = __ldg(R + i * D + j);
-    griddep_wait();  // k, v, the slot mapping or the cache may come from the previous kernel
 
     __shared__ float xs[2][2][D];
     const int t0 = blockIdx.x * tok_per_cta;
@@ -169,12 +141,14 @@ append_int2_prefill_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloa
     const int h = blockIdx.y, is_v = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     {
-        // the rotation is a layer constant: staged before the dependency wait
+        // the rotation: fetched into L2 before the dependency wait (no data
+        // returned, coherent), staged in shared memory after it
         const float4* R4 = reinterpret_cast<const float4*>((is_v ? Rv : Rk) + (size_t)h * D * D);
+        for (int l = tid; l < D * D * 4 / 128; l += 256) prefetch_l2(R4 + 8 * l);
+        griddep_wait();  // every input (rotations included) may come from the previous kernel
         float4* S4 = reinterpret_cast<float4*>(&sm.R[0][0]);
         for (int idx = tid; idx < D * D / 4; idx += 256) S4[idx] = __ldg(R4 + idx);
     }
-    griddep_wait();  // k, v, the slot mapping or the cache may come from the previous kernel
 
     const __nv_bfloat16* src = is_v ? v : k;
     const int64_t n_slots = num_pages * PAGE;

@@ -611,7 +611,8 @@ extern "C" kvq_status bgtq_decode_attn(const void* q, int B, int H_q, int H_kv, 
     const int S = num_splits > 0 ? num_splits : bgtq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
     if (S > MAX_SPLITS)
         return kvq_set_error(KVQ_ERR_INVALID_ARG, "bgtq_decode_attn: num_splits=%d above %d", S, MAX_SPLITS);
-    const size_t need = kvq_decode_workspace_bytes(B, H_q, H_kv, max_pages_per_seq, S);
+    // header, one ticket per (sequence, KV head), B * H_q * S split partials
+    const size_t need = WS_HEADER + tickets_bytes(B, H_kv) + (size_t)B * H_q * S * PART_STRIDE * sizeof(float);
     if (workspace_bytes < need)
         return kvq_set_error(KVQ_ERR_WORKSPACE, "bgtq_decode_attn: workspace %zu < %zu bytes", workspace_bytes, need);
 

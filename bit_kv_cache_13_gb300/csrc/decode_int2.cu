@@ -32,8 +32,10 @@
 // Split partials (m, l, o') go to the workspace; the last CTA of a
 // (sequence, KV head) to finish (atomic ticket, no waiting) merges them,
 // applies R_v^T and writes the output.
+#include <atomic>
 #include <mutex>
 
+#include "int2_quant.cuh"
 #include "merge.cuh"
 
 namespace kvq {
@@ -53,17 +55,22 @@ struct DecWarps {
 
 template <int NW, int MAXG>
 struct __align__(16) DecodeSmem {
-    union {
+    struct {
         uint8_t ring[NW][DEC_STAGES][INT2_TILE];  // page tiles in flight
-        float o_part[NW][MAXG][D];                // per-warp o' after the loop
     } u;
+    float o_part[NW][MAXG][D];  // per-warp o' after the loop (its own space: a warp writes it as soon as it is done)
     uint64_t bar[NW][DEC_UNITS];
     int ntok[NW][DEC_STAGES];  // valid tokens of the page in each stage (0: skipped page)
     float q[MAXG][D];          // scaled rotated queries q~ = q R_k * scale * log2(e)
     float gsum[MAXG][NGROUP];
     float sigma[MAXG];         // power-of-two pre-scale per head
+    int64_t share[2];          // this CTA's virtual pages [share[0], share[1])
+    int dead;                  // a wait of this CTA ran out: no further copies
     MergeSmem<NW, MAXG> ms;
 };
+
+static_assert(sizeof(DecodeSmem<12, 4>) <= 227 * 1024 && sizeof(DecodeSmem<8, 8>) <= 227 * 1024,
+              "decode shared memory above 227 KB");
 
 // BF16 window (the INT2 paper keeps a small BF16 window, §3.1; the
 // Block-GTQ page keeps 4 sink and 128 recent tokens, Table 6): the first
@@ -139,157 +146,413 @@ __device__ __forceinline__ void window_partials(float (*o_part)[MAXG][D], MergeS
         }
 }
 
-// WIN: the grid's last split attends the BF16 window (a separate
-// instantiation, so the plain decode carries none of it).
-template <int NT, bool WIN>
+// Work split.  The B * H_kv (sequence, KV head) units are laid end to end
+// as V = units * max_pages "virtual" pages: unit u = b * H_kv + h owns
+// [u * MP, (u + 1) * MP), of which the first ceil(ctx_b / 16) are real.
+// Page CTA c of C takes the virtual pages [c V / C, (c + 1) V / C), so every
+// CTA gets the same share (within one page) whatever B * H_kv is, and a CTA
+// whose share crosses a unit boundary works on each unit in turn (a
+// segment).  The CTAs that touch unit u are cta_of(u MP) .. cta_of(u MP +
+// MP - 1); each publishes one partial in slot u + c (unique: the shares are
+// ordered), and the one that arrives last merges them.  Needs 1 <= C <= V.
+struct PageSplit {
+    int64_t V;
+    int C, MP;
+    __device__ __forceinline__ int64_t start(int c) const { return (int64_t)c * V / C; }
+    __device__ __forceinline__ int cta_of(int64_t g) const { return (int)(((g + 1) * C - 1) / V); }
+};
+
+// What the CTAs after the page CTAs do, one per (sequence, KV head) unit.
+enum DecodeMode : int {
+    MODE_CACHE = 0,   // nothing: the cache alone
+    MODE_WINDOW = 1,  // attend the unit's BF16 window
+    MODE_STEP = 2,    // append the decode token to the cache and attend it
+};
+
+// The new token of a decode step (MODE_STEP), for KV head h of sequence b at
+// position ctx - 1: quantised exactly as the append kernels do it (the same
+// fp32 chains z = (k - mu) R_k, w = v R_v in ascending input order, the same
+// group parameters and codes), written to its cache slot, and attended here:
+// its logit q' . Q2(z) and value Q2(w) (rotated basis) form a partial
+// (m, l = 1, o' = Q2(w)) that merges with the page CTAs', which stop one
+// token short.  The CTA's first 256 threads work: thread j < 128 owns
+// rotated key channel j, thread 128 + j value channel j.  Returns false when
+// the token's page id is out of range (nothing written; the partial is empty).
+template <int NW, int MAXG>
+__device__ __forceinline__ bool step_token_partial(MergeSmem<NW, MAXG>& ms, float (*xs)[D], float (*qs)[D],
+                                                   const __nv_bfloat16* __restrict__ q,
+                                                   const __nv_bfloat16* __restrict__ k_new,
+                                                   const __nv_bfloat16* __restrict__ v_new,
+                                                   const float* __restrict__ mu, const float* __restrict__ Rk,
+                                                   const float* __restrict__ Rv, uint8_t* __restrict__ cache,
+                                                   int64_t num_pages, int pid, int slot, int H_q, int H_kv, int G,
+                                                   int b, int h, float scale_log2, float (*vout)[D]) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int side = tid >> 7, j = tid & (D - 1);  // side 0: key channel j, 1: value channel j
+    const bool worker = tid < 2 * D;
+    // inputs: the centred key and the value (fp32), the G query rows
+    if (tid < D) {
+        const size_t row = ((size_t)b * H_kv + h) * D + tid;
+        xs[0][tid] = __fsub_rn(__bfloat162float(k_new[row]), __ldg(mu + (size_t)h * D + tid));
+        xs[1][tid] = __bfloat162float(v_new[row]);
+    }
+    for (int idx = tid; idx < G * D; idx += NW * 32)
+        qs[idx / D][idx % D] = __bfloat162float(q[((size_t)b * H_q + (size_t)h * G) * D + idx]);
+    float rcol[D];
+    if (worker) {
+        const float* R = (side ? Rv : Rk) + (size_t)h * D * D + j;
+#pragma unroll
+        for (int i = 0; i < D; ++i) rcol[i] = __ldg(R + (size_t)i * D);
+    }
+    __syncthreads();
+    const bool ok = pid >= 0 && (int64_t)pid < num_pages;
+    float xhat = 0.f;
+    // q' = q R_k for the key threads (thread j holds column j of R_k), in the
+    // same pass over the column as the key's chain
+    float qp[MAXG];
+#pragma unroll
+    for (int jj = 0; jj < MAXG; ++jj) qp[jj] = 0.f;
+    if (worker) {
+        float acc = 0.f;
+        if (side == 0) {
+#pragma unroll
+            for (int i = 0; i < D; ++i) {
+                acc = __fmaf_rn(xs[0][i], rcol[i], acc);
+#pragma unroll
+                for (int jj = 0; jj < MAXG; ++jj)
+                    if (jj < G) qp[jj] = fmaf(qs[jj][i], rcol[i], qp[jj]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < D; ++i) acc = __fmaf_rn(xs[1][i], rcol[i], acc);
+        }
+        // group parameters (exact min / max over the 32 lanes of the group)
+        float mn = acc, mx = acc;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        }
+        __half sh, mh;
+        int2_params(mn, mx, 1.f, sh, mh);
+        const float scf = __half2float(sh), mnf = __half2float(mh);
+        const int code = int2_code(acc, mnf, scf);
+        const uint32_t byte = int2_gather_byte(code, lane);
+        const int grp = warp & 3;
+        if (ok) {
+            uint8_t* tile = cache + ((size_t)pid * H_kv + h) * INT2_TILE;
+            if ((lane & 3) == 0) tile[(side ? OFF_VC : OFF_KC) + 32 * slot + 4 * (lane >> 2) + grp] = (uint8_t)byte;
+            if (lane == 0) int2_store_meta(tile, side, slot, grp, sh, mh);
+        }
+        xhat = fmaf((float)code, scf, mnf);  // the level the cache now holds
+    }
+    // the key's logit for each head: sum_j q'_j xhat_j, q' = q R_k (thread j
+    // holds column j of R_k); the value stays in the rotated basis
+    float part[MAXG];
+#pragma unroll
+    for (int jj = 0; jj < MAXG; ++jj) {
+        float v = qp[jj] * xhat;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        part[jj] = v;
+    }
+    // per-warp partial dots of the four key warps, summed below
+    if (lane == 0 && warp < 4) {
+#pragma unroll
+        for (int jj = 0; jj < MAXG; ++jj) ms.fac[jj][warp] = part[jj];
+    }
+    if (worker && side == 1) {
+#pragma unroll
+        for (int jj = 0; jj < MAXG; ++jj)
+            if (jj < G) vout[jj][j] = ok ? xhat : 0.f;
+    }
+    __syncthreads();
+    if (tid < G) {
+        const float lg = (ms.fac[tid][0] + ms.fac[tid][1] + ms.fac[tid][2] + ms.fac[tid][3]) * scale_log2;
+        ms.Mh[tid] = ok ? lg : -CUDART_INF_F;
+        ms.Lh[tid] = ok ? 1.f : 0.f;
+    }
+    __syncthreads();
+    return ok;
+}
+
+// Test hook: CTA 0 leaves the bulk copy of its first page unissued (the unit
+// is still armed with its bytes), so that wait runs out after a short limit.
+constexpr int DBG_DROP_FIRST_COPY = 1;
+// The caller declares that the rotations, key centre, block table, context
+// lengths and cache are not written by the kernel just before: the first
+// segment's page ids, first copies and rows of R_k then go out before the
+// dependency wait (the query, the new token and the workspace are only read
+// or written after it).
+constexpr int FLAG_EARLY_INPUTS = 2;
+constexpr long long DBG_WAIT_LIMIT_CYCLES = 2000000LL;
+
+// Grid: n_cta page CTAs, then (MODE != MODE_CACHE) one CTA per unit for the
+// BF16 window or the new token.  In MODE_STEP, k_new / v_new are the decode
+// token's [B][H_kv][d] key and value, appended at position ctx - 1 (win_k and
+// win_v carry them).
+template <int NT, int MODE>
 __global__ void __launch_bounds__(DecWarps<NT>::NW * 32, 1)
-decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G, const uint8_t* __restrict__ cache,
-                   int64_t num_pages, const int32_t* __restrict__ block_table, int max_pages,
-                   const int32_t* __restrict__ context_lens, const float* __restrict__ Rk,
+decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv, int G,
+                   uint8_t* __restrict__ cache, int64_t num_pages, const int32_t* __restrict__ block_table,
+                   int max_pages, const int32_t* __restrict__ context_lens, const float* __restrict__ Rk,
                    const float* __restrict__ Rv, const float* __restrict__ mu,
                    const __nv_bfloat16* __restrict__ win_k, const __nv_bfloat16* __restrict__ win_v,
                    const int32_t* __restrict__ win_lens, int win_max, float scale_log2, float* __restrict__ out,
-                   uint8_t* __restrict__ ws) {
+                   uint8_t* __restrict__ ws, int n_cta, int flags) {
+    constexpr bool EXTRA = MODE != MODE_CACHE;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     constexpr int MAXG = 4 * NT;
     constexpr int NW = DecWarps<NT>::NW;
     DecodeSmem<NW, MAXG>& sm = *reinterpret_cast<DecodeSmem<NW, MAXG>*>(smem_raw);
 
-    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int S = gridDim.x, B = gridDim.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r = lane >> 2, t = lane & 3;
+    // The workspace pointers and the split are formed where they are used
+    // (from the kernel parameters), so the page loop holds no registers for
+    // them.
+    auto slot_ptr = [&](int64_t slot) {
+        float* partials = reinterpret_cast<float*>(ws + WS_HEADER + tickets_bytes(B, H_kv));
+        return partials + (size_t)slot * G * PART_STRIDE;
+    };
+    auto finish_unit = [&](int u) {
+        // publish this CTA's slot (already written), then the last CTA merges;
+        // the partials of unit u are the page CTAs' slots u + c, then (with a
+        // window or a new token) the slot of its extra CTA
+        const PageSplit sp{(int64_t)B * H_kv * max_pages, n_cta, max_pages};
+        const int units = B * H_kv;
+        const int c0 = sp.cta_of((int64_t)u * max_pages);
+        const int n = sp.cta_of((int64_t)u * max_pages + max_pages - 1) - c0 + 1;
+        const int expected = n + (EXTRA ? 1 : 0);
+        int32_t* tickets = reinterpret_cast<int32_t*>(ws + WS_HEADER);
+        if (!arrive_last(sm.ms, tickets + u, expected)) return;
+        const int b = u / H_kv, h = u % H_kv;
+        auto slot_of = [&](int s) -> const float* {
+            return s < n ? slot_ptr((int64_t)u + c0 + s) : slot_ptr((int64_t)units + n_cta + u);
+        };
+        merge_out<NW, MAXG>(sm.ms, slot_of, expected, G, out + ((size_t)b * H_q + (size_t)h * G) * D);
+        if (tid == 0) tickets[u] = 0;
+    };
 
-    uint32_t* err_word = reinterpret_cast<uint32_t*>(ws);
-
-    // The rotations are constants of the layer: this warp's rows of R_k are
-    // loaded, and R_v (read only after the loop) fetched into L2, while the
-    // previous kernel in the stream may still be running.
-    float4 rr[RowPrefetch<NW, MAXG>::N];
-    load_rows<NW>(Rk + (size_t)h * D * D, rr);
-    {
-        const char* rv = reinterpret_cast<const char*>(Rv + (size_t)h * D * D);
-        for (int l = tid; l < D * D * 4 / 128; l += NW * 32) prefetch_l2_keep(rv + 128 * l);
+    if constexpr (MODE == MODE_STEP) {
+        if (blockIdx.x >= n_cta) {
+            const int units = B * H_kv;
+            const int u = blockIdx.x - n_cta, b = u / H_kv, h = u % H_kv;
+            if (tid < D) {
+                prefetch_l2(Rk + (size_t)h * D * D + (size_t)tid * D);
+                prefetch_l2(Rv + (size_t)h * D * D + (size_t)tid * D);
+            }
+            griddep_wait();
+            griddep_launch_dependents();
+            int ctx = __ldg(context_lens + b);
+            ctx = max(0, min(ctx, max_pages * PAGE));
+            bool ok = false;
+            if (ctx > 0) {
+                const int t_new = ctx - 1;
+                const int pid = __ldg(block_table + (size_t)b * max_pages + t_new / PAGE);
+                ok = step_token_partial<NW, MAXG>(sm.ms, sm.q, sm.o_part[0], q, win_k, win_v, mu, Rk, Rv, cache,
+                                                  num_pages, pid, t_new % PAGE, H_q, H_kv, G, b, h, scale_log2,
+                                                  sm.ms.o_final);
+                if (!ok && tid == 0) atomicOr(reinterpret_cast<uint32_t*>(ws), ERR_BAD_PAGE);
+            }
+            float* slot = slot_ptr((int64_t)units + n_cta + u);
+            if (ok) {
+                // the token's value is in the R_v basis: carry it to the output basis
+                float4 rr[RowPrefetch<NW, MAXG>::N];
+                load_rows<NW>(Rv + (size_t)h * D * D, rr);
+                rotate_publish<NW, MAXG>(sm.ms, rr, G, Rv + (size_t)h * D * D, slot);
+            } else {
+                publish_slot<NW, MAXG>(sm.ms, sm.ms.o_final, G, slot, true);
+            }
+            finish_unit(u);
+            return;
+        }
     }
+    if constexpr (MODE == MODE_WINDOW) {
+        if (blockIdx.x >= n_cta) {
+            // BF16 window of unit u: attended exactly in the original basis,
+            // which is the output basis, so its partial merges as it is
+            const int units = B * H_kv;
+            const int u = blockIdx.x - n_cta, b = u / H_kv, h = u % H_kv;
+            griddep_wait();
+            griddep_launch_dependents();
+            window_partials<NW, MAXG>(sm.o_part, sm.ms, q, H_q, H_kv, G, b, h, mu, win_k, win_v, win_lens, win_max,
+                                      scale_log2);
+            __syncthreads();
+            merge_warps<NW, MAXG>(sm.ms, sm.o_part, G);
+            publish_slot<NW, MAXG>(sm.ms, sm.ms.o_final, G, slot_ptr((int64_t)units + n_cta + u), false);
+            finish_unit(u);
+            return;
+        }
+    }
+
+    const int cta = blockIdx.x;
+    int u_first;
     {
-        // The inputs the prologue reads first -- this warp's first block-table
-        // entries, the context length, the query rows -- are only prefetched
-        // into L2 here; the loads that use them follow the wait.
-        const int S_pf = WIN ? S - 1 : S, k0_pf = split * NW + warp;
-        const int j = k0_pf + S_pf * NW * lane;
+        const PageSplit sp{(int64_t)B * H_kv * max_pages, n_cta, max_pages};
+        const int64_t g0 = sp.start(cta);
+        u_first = (int)(g0 / max_pages);
+        if (tid == 0) {
+            // the share bounds live in shared memory, so the page loop below
+            // holds no registers for them
+            sm.share[0] = g0;
+            sm.share[1] = sp.start(cta + 1);
+            sm.dead = 0;
+        }
+        // the ring's mbarriers are set up once: a warp's units keep one
+        // numbering across the segments (slot group k % 3, parity (k / 3) & 1)
+        if (lane == 0) {
+            for (int s2 = 0; s2 < DEC_UNITS; ++s2) mbar_init(&sm.bar[warp][s2], 1);
+            fence_mbar_init();
+        }
+        // Prefetches into L2 only (a prefetch returns no data, and L2 is the
+        // point of coherence, so a write the previous kernel makes later
+        // still wins): the first unit's rotations, context length and query
+        // rows, and this warp's first block-table entries.
+        const int b = u_first / H_kv, h = u_first % H_kv;
+        const char* rk = reinterpret_cast<const char*>(Rk + (size_t)h * D * D);
+        const char* rv = reinterpret_cast<const char*>(Rv + (size_t)h * D * D);
+        for (int l = tid; l < D * D * 4 / 128; l += NW * 32) {
+            prefetch_l2(rk + 128 * l);
+            prefetch_l2_keep(rv + 128 * l);
+        }
+        const int pa = (int)(g0 - (int64_t)u_first * max_pages);
+        const int j = pa + warp + NW * lane;
         if (lane < DEC_STAGES + UNIT_PAGES && j < max_pages) prefetch_l2(block_table + (size_t)b * max_pages + j);
         if (tid == 0) prefetch_l2(context_lens + b);
         const char* qc = reinterpret_cast<const char*>(q + ((size_t)b * H_q + (size_t)h * G) * D);
         if (tid < (G * D * 2 + 127) / 128) prefetch_l2(qc + 128 * tid);
     }
-    griddep_wait();  // every other input may come from the previous kernel in the stream
-    if constexpr (WIN) {
-        if (split == S - 1) {
-            // the last split attends the BF16 window instead of cache pages
-            griddep_launch_dependents();
-            window_partials<NW, MAXG>(sm.u.o_part, sm.ms, q, H_q, H_kv, G, b, h, mu, win_k, win_v, win_lens, win_max,
-                                      scale_log2);
-            __syncthreads();
-            finish_decode<NW, MAXG, false>(sm.ms, sm.u.o_part, G, H_q, H_kv, B, b, h, split, S, ws, nullptr, out);
-            return;
-        }
-    }
-    const int S_pages = WIN ? S - 1 : S;  // splits that stream cache pages
-    int ctx = __ldg(context_lens + b);
-    ctx = max(0, min(ctx, max_pages * PAGE));
-    const int n_pages = (ctx + PAGE - 1) / PAGE;
-    const int32_t* bt = block_table + (size_t)b * max_pages;
-    // Page schedule: the pages of a (sequence, KV head) are dealt round-robin
-    // over all S * NW warps of its split CTAs, so warp k0 = split * NW + warp
-    // takes pages k0, k0 + KS, k0 + 2 KS, ...  Every warp gets the same
-    // number of pages to within one, and page ids come from anywhere in the
-    // sequence (the block table scatters them over the cache anyway).
-    const int KS = S_pages * NW, k0 = split * NW + warp;
-    const int my_count = n_pages > k0 ? (n_pages - k0 + KS - 1) / KS : 0;
-    auto page_of = [&](int j) { return k0 + KS * j; };
+    const bool early = flags & FLAG_EARLY_INPUTS;
+    if (!early) griddep_wait();  // every input may come from the previous kernel in the stream
+    __syncthreads();             // the share bounds are in shared memory
 
     constexpr int QPT = (MAXG * D + NW * 32 - 1) / (NW * 32);  // query values per thread
-    // the query loads go out before lane 0 waits for its page ids, so the
-    // two global round trips overlap
-    float qv[QPT];
-    {
-        const __nv_bfloat16* qb = q + ((size_t)b * H_q + (size_t)h * G) * D;
+    int kbase = 0;  // units this warp consumed in earlier segments
+
+    // One segment: the part of this CTA's share that lies in unit u.  A share
+    // spans at most two units (the host keeps C >= B * H_kv), so the body is
+    // expanded twice instead of looped: no loop-carried state competes with
+    // the page loop for registers.
+    auto segment = [&](int u, bool second) {
+        const int b = u / H_kv, h = u % H_kv;
+        const int64_t ubase = (int64_t)u * max_pages;
+        const int64_t g0 = sm.share[0], g1 = sm.share[1];
+        const bool last_seg = g1 <= ubase + max_pages;  // this CTA's share ends in unit u
+        const int pa = (int)(max(g0, ubase) - ubase), pb = (int)(min(g1, ubase + max_pages) - ubase);
+        const int32_t* bt = block_table + (size_t)b * max_pages;
+        // pages pa .. pe - 1 of the unit (pe: the share's end or the context's),
+        // dealt round-robin over the warps
+        auto page_of = [&](int j) { return pa + warp + NW * j; };
+        // The loads the prologue needs all go out together: the context length,
+        // (lanes 0..2) the page ids of the warp's first units -- bounded by the
+        // share, not the context, so they need not wait for its length -- this
+        // warp's rows of R_k and the query values.
+        int ctx = __ldg(context_lens + b);
+        int pid_first[DEC_UNITS];
+        int pid_next = 0;
+        {
+            const int cs = pb - pa, my_share = cs > warp ? (cs - warp + NW - 1) / NW : 0;
 #pragma unroll
-        for (int k = 0; k < QPT; ++k) {
-            const int idx = tid + k * NW * 32;
-            qv[k] = idx < G * D ? __bfloat162float(qb[idx]) : 0.f;
-        }
-    }
-    // Pages travel in units of UNIT_PAGES: unit u holds the warp's pages
-    // UNIT_PAGES u .. UNIT_PAGES u + UNIT_PAGES - 1 (ring slots j % DEC_STAGES) on
-    // one mbarrier phase, so a unit costs one wait and one release.
-    const int n_units = (my_count + UNIT_PAGES - 1) / UNIT_PAGES;
-    if (lane == 0) {
-        for (int s = 0; s < DEC_UNITS; ++s) mbar_init(&sm.bar[warp][s], 1);
-        fence_mbar_init();
-        fence_proxy_async_smem();
-    }
-    __syncwarp();
-    // Lane 0 issues unit u with its (already loaded) page ids and records how
-    // many tokens of each page are valid (0 for a slot past the warp's pages
-    // or with a bad page id); the mbarrier publishes the counts with the data.
-    auto issue_unit = [&](int u, int st, int pid) {
-        // whole warp; lane e < UNIT_PAGES issues page e of unit u (id pid),
-        // st = u % DEC_UNITS
-        uint64_t* bar = &sm.bar[warp][st];
-        const int j = UNIT_PAGES * u + lane;
-        bool ok = false;
-        if (lane < UNIT_PAGES) {
-            int n = 0;
-            if (j < my_count) {
-                if (pid < 0 || (int64_t)pid >= num_pages) {
-                    atomicOr(err_word, ERR_BAD_PAGE);
-                } else {
-                    ok = true;
-                    n = min(PAGE, ctx - page_of(j) * PAGE);
+            for (int k = 0; k < DEC_UNITS; ++k) pid_first[k] = 0;
+            if (lane < UNIT_PAGES) {
+#pragma unroll
+                for (int k = 0; k <= DEC_UNITS; ++k) {
+                    const int j = UNIT_PAGES * k + lane;
+                    const int pid = j < my_share ? __ldg(bt + page_of(j)) : 0;
+                    if (k < DEC_UNITS)
+                        pid_first[k] = pid;
+                    else
+                        pid_next = pid;
                 }
             }
-            sm.ntok[warp][UNIT_PAGES * st + lane] = n;
         }
-        const uint32_t n_ok = __popc(__ballot_sync(0xffffffffu, ok));
-        __syncwarp();  // the lanes' counts are ordered before lane 0's arrive (release)
-        if (lane == 0) {
-            if (n_ok == 0)
-                mbar_arrive(bar);  // complete the phase without data
-            else
-                mbar_arrive_expect_tx(bar, n_ok * INT2_TILE);
-        }
-        __syncwarp();  // the expected bytes are set before any copy is issued
-        if (ok)
-            bulk_g2s(sm.u.ring[warp][UNIT_PAGES * st + lane], cache + ((size_t)pid * H_kv + h) * INT2_TILE,
-                     INT2_TILE, bar);
-    };
-    // ---- the page ids of the first units (lane e < UNIT_PAGES holds page e
-    // of each).  Their copies are issued after the query rotation, which runs
-    // while the ids arrive; the copies then fly during the B-fragment setup.
-    // Lanes keep the ids of the next unit to issue, loaded one release
-    // before their use.
-    int pid_first[DEC_UNITS];
-    int pid_next = 0;
-    int n_issued = 0;  // units issued so far
-#pragma unroll
-    for (int u = 0; u < DEC_UNITS; ++u) pid_first[u] = 0;
-    if (lane < UNIT_PAGES) {
-        // bounded by the block table's row length, not the context, so these
-        // loads need not wait for context_lens
-#pragma unroll
-        for (int u = 0; u <= DEC_UNITS; ++u) {
-            const int j = page_of(UNIT_PAGES * u + lane);
-            const int pid = j < max_pages ? __ldg(bt + j) : 0;
-            if (u < DEC_UNITS)
-                pid_first[u] = pid;
-            else
-                pid_next = pid;
-        }
-    }
+        ctx = max(0, min(ctx, max_pages * PAGE));
+        if (MODE == MODE_STEP) ctx = max(ctx - 1, 0);  // the new token is attended by its own CTA
+        const int n_pages = (ctx + PAGE - 1) / PAGE;
+        const int pe = min(pb, n_pages);
+        // no cached page of this unit in this CTA's share (or a wait ran out
+        // earlier): the segment publishes an empty partial
+        const bool empty = pe <= pa || sm.dead;
+        if (!empty) {
+        const int count = pe - pa;
+        const int my_count = count > warp ? (count - warp + NW - 1) / NW : 0;
 
-    // ---- q~ = (q R_k) * scale * log2(e) for the G heads of this KV head
-    {
+        float4 rr[RowPrefetch<NW, MAXG>::N];
+        load_rows<NW>(Rk + (size_t)h * D * D, rr);
+        float qv[QPT];
+        auto load_q = [&]() {
+            const __nv_bfloat16* qb = q + ((size_t)b * H_q + (size_t)h * G) * D;
+#pragma unroll
+            for (int k = 0; k < QPT; ++k) {
+                const int idx = tid + k * NW * 32;
+                qv[k] = idx < G * D ? __bfloat162float(qb[idx]) : 0.f;
+            }
+        };
+        if (!early) load_q();
+        const int n_units = (my_count + UNIT_PAGES - 1) / UNIT_PAGES;
+        __syncwarp();
+        // in a second segment the ring was last read through the generic
+        // proxy: order that before the bulk copies any lane issues
+        if (second) fence_proxy_async_smem();
+        // slot group and parity of this segment's first unit
+        const int st0 = kbase % DEC_UNITS;
+        const uint32_t par0 = (kbase / DEC_UNITS) & 1;
+
+        // Lanes e < UNIT_PAGES issue page e of unit k (id pid) into slot group
+        // st and record how many tokens of it are valid (0 for a slot past the
+        // warp's pages or with a bad page id); the mbarrier publishes the
+        // counts with the data.
+        auto issue_unit = [&](int k, int st, int pid) {
+            uint64_t* bar = &sm.bar[warp][st];
+            const int j = UNIT_PAGES * k + lane;
+            bool ok = false;
+            if (lane < UNIT_PAGES) {
+                int n = 0;
+                if (j < my_count) {
+                    if (pid < 0 || (int64_t)pid >= num_pages) {
+                        atomicOr(reinterpret_cast<uint32_t*>(ws), ERR_BAD_PAGE);
+                    } else {
+                        ok = true;
+                        n = min(PAGE, ctx - page_of(j) * PAGE);
+                    }
+                }
+                sm.ntok[warp][UNIT_PAGES * st + lane] = n;
+            }
+            const uint32_t n_ok = __popc(__ballot_sync(0xffffffffu, ok));
+            __syncwarp();  // the lanes' counts are ordered before lane 0's arrive (release)
+            if (lane == 0) {
+                if (n_ok == 0)
+                    mbar_arrive(bar);  // complete the phase without data
+                else
+                    mbar_arrive_expect_tx(bar, n_ok * INT2_TILE);
+            }
+            __syncwarp();  // the expected bytes are set before any copy is issued
+            // (test hook: CTA 0 leaves its first copy unissued)
+            if (ok && !((flags & DBG_DROP_FIRST_COPY) && cta == 0 && warp == 0 && u == 0 && k == 0 && lane == 0))
+                bulk_g2s(sm.u.ring[warp][UNIT_PAGES * st + lane], cache + ((size_t)pid * H_kv + h) * INT2_TILE,
+                         INT2_TILE, bar);
+        };
+        // the first units go out as soon as their page ids are here: the copies
+        // fly while the query is rotated
+        int n_issued = 0;
+#pragma unroll
+        for (int k = 0; k < DEC_UNITS; ++k)
+            if (k < n_units) {  // warp-uniform
+                issue_unit(k, st0 + k < DEC_UNITS ? st0 + k : st0 + k - DEC_UNITS, pid_first[k]);
+                n_issued = k + 1;
+            }
+        // the rest of this share of the block table is read one entry at a
+        // time during the loop: have L2 fetch it now (every address is an
+        // entry of the share, so no line past the table is touched)
+        for (int i = pa + 32 * tid; i < pe + 31; i += 32 * NW * 32) prefetch_l2_keep(bt + min(i, pe - 1));
+        if (early) {
+            // the early inputs are out; the query may come from the previous kernel
+            griddep_wait();
+            load_q();
+        }
+
+        // ---- q~ = (q R_k) * scale * log2(e) for the G heads of this KV head
 #pragma unroll
         for (int k = 0; k < QPT; ++k) {
             const int idx = tid + k * NW * 32;
@@ -297,20 +560,6 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         }
         __syncthreads();
         rotate_rows<NW, MAXG>(sm.ms.o_final, Rk + (size_t)h * D * D, rr, G, scale_log2, sm.q, sm.ms);
-#pragma unroll
-        for (int u = 0; u < DEC_UNITS; ++u)
-            if (u < n_units) {  // warp-uniform
-                issue_unit(u, u, pid_first[u]);
-                n_issued = u + 1;
-            }
-        {
-            // the rest of this sequence's block table is read one entry at a
-            // time during the loop: have L2 fetch it now (after the rotation,
-            // which need not wait for the context length this bound needs)
-            const char* btc = reinterpret_cast<const char*>(bt);
-            const int lines = (n_pages * 4 + 127) / 128;
-            for (int l = split * NW * 32 + tid; l < lines; l += S_pages * NW * 32) prefetch_l2_keep(btc + 128 * l);
-        }
         // per head: power-of-two pre-scale (max |q~| * sigma in [2^14, 2^15)) and group sums
         for (int jj = warp; jj < G; jj += NW) {
             float mx = 0.f;
@@ -334,370 +583,390 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             }
         }
         __syncthreads();
-    }
 
-    // ---- QK B fragments: column n = r -> head 4*nt + (r >> 1), part r & 1 (hi / lo)
-    uint32_t bq[NT][8][2];
+        // ---- QK B fragments: column n = r -> head 4*nt + (r >> 1), part r & 1 (hi / lo)
+        uint32_t bq[NT][8][2];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int hq = 4 * nt + (r >> 1);
-        const bool lo_part = r & 1;
+        for (int nt = 0; nt < NT; ++nt) {
+            const int hq = 4 * nt + (r >> 1);
+            const bool lo_part = r & 1;
 #pragma unroll
-        for (int s = 0; s < 8; ++s) {
-            const int g = s >> 1, hs = s & 1;
+            for (int s = 0; s < 8; ++s) {
+                const int g = s >> 1, hs = s & 1;
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {  // b0 (k = 2hs), b1 (k = 2hs + 1)
-                const int k = 2 * hs + e;
-                const int c0 = 32 * g + 8 * t + k, c1 = c0 + 4;
-                float v0 = 0.f, v1 = 0.f;
-                if (hq < G) {
-                    const float f = sm.sigma[hq] * (k == 0 ? 1.f : k == 1 ? 0.25f : k == 2 ? 0.0625f : 0.015625f);
-                    v0 = sm.q[hq][c0] * f;
-                    v1 = sm.q[hq][c1] * f;
+                for (int e = 0; e < 2; ++e) {  // b0 (k = 2hs), b1 (k = 2hs + 1)
+                    const int k = 2 * hs + e;
+                    const int c0 = 32 * g + 8 * t + k, c1 = c0 + 4;
+                    float v0 = 0.f, v1 = 0.f;
+                    if (hq < G) {
+                        const float f = sm.sigma[hq] * (k == 0 ? 1.f : k == 1 ? 0.25f : k == 2 ? 0.0625f : 0.015625f);
+                        v0 = sm.q[hq][c0] * f;
+                        v1 = sm.q[hq][c1] * f;
+                    }
+                    // hi part (even columns) or the exact remainder (odd columns), one path
+                    const float h0 = __half2float(__float2half_rn(v0)), h1 = __half2float(__float2half_rn(v1));
+                    bq[nt][s][e] = pack_half2(lo_part ? v0 - h0 : h0, lo_part ? v1 - h1 : h1);
                 }
-                // hi part (even columns) or the exact remainder (odd columns), one path
-                const float h0 = __half2float(__float2half_rn(v0)), h1 = __half2float(__float2half_rn(v1));
-                bq[nt][s][e] = pack_half2(lo_part ? v0 - h0 : h0, lo_part ? v1 - h1 : h1);
             }
         }
-    }
-    float inv_sig[NT], gsum[NT][NGROUP];
+        float inv_sig[NT], gsum[NT][NGROUP];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int hq = 4 * nt + t;
-        inv_sig[nt] = hq < G ? 16777216.f / sm.sigma[hq] : 0.f;
+        for (int nt = 0; nt < NT; ++nt) {
+            const int hq = 4 * nt + t;
+            inv_sig[nt] = hq < G ? 16777216.f / sm.sigma[hq] : 0.f;
 #pragma unroll
-        for (int g = 0; g < NGROUP; ++g) gsum[nt][g] = hq < G ? sm.gsum[hq][g] : 0.f;
-    }
-
-    float oacc[8][4];
-#pragma unroll
-    for (int m = 0; m < 8; ++m)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) oacc[m][e] = 0.f;
-    float cmin[4] = {0.f, 0.f, 0.f, 0.f};
-    float mrun[NT], lsum[NT];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        mrun[nt] = -CUDART_INF_F;
-        lsum[nt] = 0.f;
-    }
-
-    // Wait for unit u of this warp; false on a timeout.  On a sequence's
-    // last page the slots past the context may hold stale bytes (even NaN
-    // scales), and so does a slot with no page: their value scale/min words
-    // are zeroed here, so p = 0
-    // always meets finite factors and the PV step needs no per-slot masks
-    // (the QK step drops those slots' logits by selection).
-    auto wait_unit = [&](int st, uint32_t parity) -> bool {  // slot group st = u % DEC_UNITS
-        const bool ok = mbar_wait_bounded(&sm.bar[warp][st], parity, WAIT_LIMIT_CYCLES);
-        if (__any_sync(0xffffffffu, !ok)) {
-            if (lane == 0) atomicOr(err_word, ERR_TIMEOUT);
-            return false;
+            for (int g = 0; g < NGROUP; ++g) gsum[nt][g] = hq < G ? sm.gsum[hq][g] : 0.f;
         }
-        bool short_page = false;
+
+        float oacc[8][4];
 #pragma unroll
-        for (int e = 0; e < UNIT_PAGES; ++e) short_page |= sm.ntok[warp][UNIT_PAGES * st + e] < PAGE;
-        if (short_page) {  // warp-uniform
-            // 64 meta words per page (32 scale, 32 min words of slot pairs):
-            // clear the halves of slots at or past the page's token count
-            for (int k = lane; k < UNIT_PAGES * 64; k += 32) {
-                const int e = k >> 6, w = k & 63, pair = (w & 31) >> 2;
-                const int n = sm.ntok[warp][UNIT_PAGES * st + e];
-                const uint32_t keep = (2 * pair < n ? 0x0000ffffu : 0u) | (2 * pair + 1 < n ? 0xffff0000u : 0u);
-                uint32_t* word = reinterpret_cast<uint32_t*>(sm.u.ring[warp][UNIT_PAGES * st + e] + OFF_VM) + w;
-                if (keep != 0xffffffffu) *word &= keep;
+        for (int m = 0; m < 8; ++m)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) oacc[m][e] = 0.f;
+        float cmin[4] = {0.f, 0.f, 0.f, 0.f};
+        float mrun[NT], lsum[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            mrun[nt] = -CUDART_INF_F;
+            lsum[nt] = 0.f;
+        }
+
+        // Wait for the unit in slot group st; false on a timeout.  On a
+        // sequence's last page the slots past the context may hold stale bytes
+        // (even NaN scales), and so does a slot with no page: their value
+        // scale/min words are zeroed here, so p = 0 always meets finite factors
+        // and the PV step needs no per-slot masks (the QK step drops those
+        // slots' logits by selection).
+        auto wait_unit = [&](int st, uint32_t parity) -> bool {
+            const bool ok = mbar_wait_bounded(&sm.bar[warp][st], parity,
+                                              (flags & DBG_DROP_FIRST_COPY) ? DBG_WAIT_LIMIT_CYCLES : WAIT_LIMIT_CYCLES);
+            if (__any_sync(0xffffffffu, !ok)) {
+                if (lane == 0) atomicOr(reinterpret_cast<uint32_t*>(ws), ERR_TIMEOUT);
+                return false;
             }
-            __syncwarp();
-        }
-        return true;
-    };
+            bool short_page = false;
+#pragma unroll
+            for (int e = 0; e < UNIT_PAGES; ++e) short_page |= sm.ntok[warp][UNIT_PAGES * st + e] < PAGE;
+            if (short_page) {  // warp-uniform
+                // 64 meta words per page (32 scale, 32 min words of slot pairs):
+                // clear the halves of slots at or past the page's token count
+                for (int k = lane; k < UNIT_PAGES * 64; k += 32) {
+                    const int e = k >> 6, w = k & 63, pair = (w & 31) >> 2;
+                    const int n = sm.ntok[warp][UNIT_PAGES * st + e];
+                    const uint32_t keep = (2 * pair < n ? 0x0000ffffu : 0u) | (2 * pair + 1 < n ? 0xffff0000u : 0u);
+                    uint32_t* word = reinterpret_cast<uint32_t*>(sm.u.ring[warp][UNIT_PAGES * st + e] + OFF_VM) + w;
+                    if (keep != 0xffffffffu) *word &= keep;
+                }
+                __syncwarp();
+            }
+            return true;
+        };
 
-    // ---------------- QK of the page in ring slot `slot`: base-2 logits of tokens r, r + 8 for
-    // head 4*nt + t (-inf past the context)
-    auto qk_page = [&](int slot, float (&lg)[NT][2]) {
-        const uint8_t* tile = sm.u.ring[warp][slot];
-        const int n_tok = sm.ntok[warp][slot];
-        const uint2 kr = lds64(tile + OFF_KC + 32 * r + 8 * t);
-        const uint2 kr8 = lds64(tile + OFF_KC + 32 * (r + 8) + 8 * t);
-        const uint32_t P01 = prmt(kr.x, kr.y, 0x5410), P23 = prmt(kr.x, kr.y, 0x7632);
-        const uint32_t Q01 = prmt(kr8.x, kr8.y, 0x5410), Q23 = prmt(kr8.x, kr8.y, 0x7632);
-        const uint4 mr = lds128(tile + OFF_KM + 16 * r);
-        const uint4 mr8 = lds128(tile + OFF_KM + 16 * (r + 8));
-        const uint32_t mrw[4] = {mr.x, mr.y, mr.z, mr.w}, mr8w[4] = {mr8.x, mr8.y, mr8.z, mr8.w};
-        float acc_r[NT], acc_r8[NT], mn_r[NT], mn_r8[NT];
+        // ---------------- QK of the page in ring slot `slot`: base-2 logits of tokens r, r + 8 for
+        // head 4*nt + t (-inf past the context)
+        auto qk_page = [&](int slot, float (&lg)[NT][2]) {
+            const uint8_t* tile = sm.u.ring[warp][slot];
+            const int n_tok = sm.ntok[warp][slot];
+            const uint2 kr = lds64(tile + OFF_KC + 32 * r + 8 * t);
+            const uint2 kr8 = lds64(tile + OFF_KC + 32 * (r + 8) + 8 * t);
+            const uint32_t P01 = prmt(kr.x, kr.y, 0x5410), P23 = prmt(kr.x, kr.y, 0x7632);
+            const uint32_t Q01 = prmt(kr8.x, kr8.y, 0x5410), Q23 = prmt(kr8.x, kr8.y, 0x7632);
+            const uint4 mr = lds128(tile + OFF_KM + 16 * r);
+            const uint4 mr8 = lds128(tile + OFF_KM + 16 * (r + 8));
+            const uint32_t mrw[4] = {mr.x, mr.y, mr.z, mr.w}, mr8w[4] = {mr8.x, mr8.y, mr8.z, mr8.w};
+            float acc_r[NT], acc_r8[NT], mn_r[NT], mn_r8[NT];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) acc_r[nt] = acc_r8[nt] = mn_r[nt] = mn_r8[nt] = 0.f;
+            for (int nt = 0; nt < NT; ++nt) acc_r[nt] = acc_r8[nt] = mn_r[nt] = mn_r8[nt] = 0.f;
 #pragma unroll
-        for (int g = 0; g < NGROUP; ++g) {
-            const uint32_t xr = g == 0 ? P01 : g == 1 ? (P01 >> 8) : g == 2 ? P23 : (P23 >> 8);
-            const uint32_t xr8 = g == 0 ? Q01 : g == 1 ? (Q01 >> 8) : g == 2 ? Q23 : (Q23 >> 8);
-            const float2 smr = __half22float2(u32_as_h2(mrw[g]));    // (scale, min) token r
-            const float2 smr8 = __half22float2(u32_as_h2(mr8w[g]));  // token r + 8
+            for (int g = 0; g < NGROUP; ++g) {
+                const uint32_t xr = g == 0 ? P01 : g == 1 ? (P01 >> 8) : g == 2 ? P23 : (P23 >> 8);
+                const uint32_t xr8 = g == 0 ? Q01 : g == 1 ? (Q01 >> 8) : g == 2 ? Q23 : (Q23 >> 8);
+                const float2 smr = __half22float2(u32_as_h2(mrw[g]));    // (scale, min) token r
+                const float2 smr8 = __half22float2(u32_as_h2(mr8w[g]));  // token r + 8
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int hs = 0; hs < 2; ++hs) {
+                        const uint32_t m0 = 0x00030003u << (4 * hs), m1 = 0x00030003u << (4 * hs + 2);
+                        const uint32_t a[4] = {xr & m0, xr8 & m0, xr & m1, xr8 & m1};
+                        mma_f16_16816(c, a, bq[nt][2 * g + hs][0], bq[nt][2 * g + hs][1]);
+                    }
+                    acc_r[nt] = fmaf(smr.x, c[0] + c[1], acc_r[nt]);
+                    acc_r8[nt] = fmaf(smr8.x, c[2] + c[3], acc_r8[nt]);
+                    mn_r[nt] = fmaf(smr.y, gsum[nt][g], mn_r[nt]);
+                    mn_r8[nt] = fmaf(smr8.y, gsum[nt][g], mn_r8[nt]);
+                }
+            }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                float c[4] = {0.f, 0.f, 0.f, 0.f};
+                lg[nt][0] = r < n_tok ? fmaf(acc_r[nt], inv_sig[nt], mn_r[nt]) : -CUDART_INF_F;
+                lg[nt][1] = r + 8 < n_tok ? fmaf(acc_r8[nt], inv_sig[nt], mn_r8[nt]) : -CUDART_INF_F;
+            }
+        };
+
+        // QK of a unit and each head's maximum over its pages
+        auto qk_unit = [&](int st, float (&lg)[UNIT_PAGES][NT][2], float (&pm)[NT]) {
+#pragma unroll
+            for (int e = 0; e < UNIT_PAGES; ++e) qk_page(UNIT_PAGES * st + e, lg[e]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float m = fmaxf(lg[0][nt][0], lg[0][nt][1]);
+#pragma unroll
+                for (int e = 1; e < UNIT_PAGES; ++e) m = fmaxf(m, fmaxf(lg[e][nt][0], lg[e][nt][1]));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                pm[nt] = m;
+            }
+        };
+
+        // ---------------- online softmax (base 2) for one unit, head 4*nt + t:
+        // raise the running maxima, rescale the accumulators when one grew, and
+        // return p^ (p rounded to fp16 once; the same p^ weights the codes, the
+        // group minima and the normaliser)
+        auto softmax_unit = [&](const float (&lg)[UNIT_PAGES][NT][2], const float (&pm)[NT],
+                                float (&pr)[UNIT_PAGES][NT][2]) {
+            float corr[NT];
+            bool need = false;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                corr[nt] = 1.f;
+                if (pm[nt] > mrun[nt]) {
+                    corr[nt] = ex2(mrun[nt] - pm[nt]);  // 0 when mrun = -inf
+                    mrun[nt] = pm[nt];
+                    need = true;
+                }
+                const float mref = mrun[nt] == -CUDART_INF_F ? 0.f : mrun[nt];
+#pragma unroll
+                for (int e = 0; e < UNIT_PAGES; ++e) {
+                    pr[e][nt][0] = __half2float(__float2half_rn(ex2(lg[e][nt][0] - mref)));
+                    pr[e][nt][1] = __half2float(__float2half_rn(ex2(lg[e][nt][1] - mref)));
+                }
+                float ps = pr[0][nt][0] + pr[0][nt][1];
+#pragma unroll
+                for (int e = 1; e < UNIT_PAGES; ++e) ps += pr[e][nt][0] + pr[e][nt][1];
+                lsum[nt] = fmaf(lsum[nt], corr[nt], ps);
+            }
+            if (__any_sync(0xffffffffu, need)) {
+                // PV columns 2t, 2t+1 hold heads 2t, 2t+1, whose maxima live in lanes (2t)&3, (2t+1)&3
+                const int hA = 2 * t, hB = 2 * t + 1;
+                float cA = __shfl_sync(0xffffffffu, corr[0], hA & 3), cB = __shfl_sync(0xffffffffu, corr[0], hB & 3);
+                if constexpr (NT == 2) {
+                    const float cA1 = __shfl_sync(0xffffffffu, corr[1], hA & 3);
+                    const float cB1 = __shfl_sync(0xffffffffu, corr[1], hB & 3);
+                    if (hA >= 4) cA = cA1;
+                    if (hB >= 4) cB = cB1;
+                }
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    oacc[m][0] *= cA;
+                    oacc[m][2] *= cA;
+                    oacc[m][1] *= cB;
+                    oacc[m][3] *= cB;
+                }
+                cmin[0] *= cA;
+                cmin[2] *= cA;
+                cmin[1] *= cB;
+                cmin[3] *= cB;
+            }
+        };
+
+        // ---------------- PV of the page in ring slot `slot` with its weights p^
+        auto pv_page = [&](int slot, const float (&pr)[NT][2]) {
+            const uint8_t* tile = sm.u.ring[warp][slot];
+            // P in the PV B layout: column n = r (head n), rows = tokens 2t, 2t+1 | 2t+8, 2t+9
+            uint32_t pb0, pb1;
+            {
+                const uint32_t X0 = pack_half2(pr[0][0], pr[0][1]);  // (token r, token r+8) of head t
+                const int srcA = 8 * t + (r & 3), srcB = 8 * t + 4 + (r & 3);
+                uint32_t Y0 = __shfl_sync(0xffffffffu, X0, srcA), Y1 = __shfl_sync(0xffffffffu, X0, srcB);
+                if constexpr (NT == 2) {
+                    const uint32_t X1 = pack_half2(pr[1][0], pr[1][1]);
+                    const uint32_t Z0 = __shfl_sync(0xffffffffu, X1, srcA), Z1 = __shfl_sync(0xffffffffu, X1, srcB);
+                    if (r >= 4) {
+                        Y0 = Z0;
+                        Y1 = Z1;
+                    }
+                }
+                // NT == 1: columns 4..7 repeat heads 0..3 and carry the low part of p*scale
+                if ((NT == 1 ? (r & 3) : r) >= G) Y0 = Y1 = 0u;
+                pb0 = prmt(Y0, Y1, 0x5410);  // p(2t), p(2t+1)
+                pb1 = prmt(Y0, Y1, 0x7632);  // p(2t+8), p(2t+9)
+            }
+            // value scales of tokens (2t, 2t+1) and (2t+8, 2t+9), one word per group
+            const uint4 sA = lds128(tile + OFF_VM + 16 * t);
+            const uint4 sB = lds128(tile + OFF_VM + 16 * (t + 4));
+            const uint32_t wA[4] = {sA.x, sA.y, sA.z, sA.w}, wB[4] = {sB.x, sB.y, sB.z, sB.w};
+
+            // min term: rows = groups (rows 4..15 are never read), K = tokens
+            {
+                uint32_t a[4] = {0u, 0u, 0u, 0u};
+                a[0] = lds32(tile + OFF_VM + VM_MINS + 16 * t + 4 * (r & 3));
+                a[2] = lds32(tile + OFF_VM + VM_MINS + 16 * (t + 4) + 4 * (r & 3));
+                mma_f16_16816(cmin, a, pb0, pb1);
+            }
+
+            const uint32_t v0 = lds32(tile + OFF_VC + 32 * (2 * t) + 4 * r);
+            const uint32_t v1 = lds32(tile + OFF_VC + 32 * (2 * t + 1) + 4 * r);
+            const uint32_t v8 = lds32(tile + OFF_VC + 32 * (2 * t + 8) + 4 * r);
+            const uint32_t v9 = lds32(tile + OFF_VC + 32 * (2 * t + 9) + 4 * r);
+            const uint32_t A01 = prmt(v0, v1, 0x5410), A23 = prmt(v0, v1, 0x7632);
+            const uint32_t B01 = prmt(v8, v9, 0x5410), B23 = prmt(v8, v9, 0x7632);
+            const __half2 P0 = u32_as_h2(pb0), P1 = u32_as_h2(pb1);
+#pragma unroll
+            for (int g = 0; g < NGROUP; ++g) {
+                const uint32_t xa = g == 0 ? A01 : g == 1 ? (A01 >> 8) : g == 2 ? A23 : (A23 >> 8);
+                const uint32_t xb = g == 0 ? B01 : g == 1 ? (B01 >> 8) : g == 2 ? B23 : (B23 >> 8);
+                // p^ * scale exactly as an fp16 pair: hi = rn(p^ s), lo = p^ s - hi (exact)
+                const __half2 S01 = u32_as_h2(wA[g]), S89 = u32_as_h2(wB[g]);
+                const __half2 H0 = __hmul2(P0, S01), H1 = __hmul2(P1, S89);
+                const __half2 L0 = __hfma2(P0, S01, __hneg2(H0)), L1 = __hfma2(P1, S89, __hneg2(H1));
 #pragma unroll
                 for (int hs = 0; hs < 2; ++hs) {
-                    const uint32_t m0 = 0x00030003u << (4 * hs), m1 = 0x00030003u << (4 * hs + 2);
-                    const uint32_t a[4] = {xr & m0, xr8 & m0, xr & m1, xr8 & m1};
-                    mma_f16_16816(c, a, bq[nt][2 * g + hs][0], bq[nt][2 * g + hs][1]);
+                    const uint32_t k0 = 0x00030003u << (4 * hs), k1 = 0x00030003u << (4 * hs + 2);
+                    const uint32_t a[4] = {xa & k0, xa & k1, xb & k0, xb & k1};
+                    if constexpr (NT == 1) {
+                        const bool lo = r >= 4;
+                        mma_f16_16816(oacc[2 * g + hs], a, h2_as_u32(lo ? L0 : H0), h2_as_u32(lo ? L1 : H1));
+                    } else {
+                        mma_f16_16816(oacc[2 * g + hs], a, h2_as_u32(H0), h2_as_u32(H1));
+                        mma_f16_16816(oacc[2 * g + hs], a, h2_as_u32(L0), h2_as_u32(L1));
+                    }
                 }
-                acc_r[nt] = fmaf(smr.x, c[0] + c[1], acc_r[nt]);
-                acc_r8[nt] = fmaf(smr8.x, c[2] + c[3], acc_r8[nt]);
-                mn_r[nt] = fmaf(smr.y, gsum[nt][g], mn_r[nt]);
-                mn_r8[nt] = fmaf(smr8.y, gsum[nt][g], mn_r8[nt]);
             }
-        }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            lg[nt][0] = r < n_tok ? fmaf(acc_r[nt], inv_sig[nt], mn_r[nt]) : -CUDART_INF_F;
-            lg[nt][1] = r + 8 < n_tok ? fmaf(acc_r8[nt], inv_sig[nt], mn_r8[nt]) : -CUDART_INF_F;
-        }
-    };
+        };
 
-    // QK of unit u and each head's maximum over its pages
-    auto qk_unit = [&](int st, float (&lg)[UNIT_PAGES][NT][2], float (&pm)[NT]) {
-#pragma unroll
-        for (int e = 0; e < UNIT_PAGES; ++e) qk_page(UNIT_PAGES * st + e, lg[e]);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            float m = fmaxf(lg[0][nt][0], lg[0][nt][1]);
-#pragma unroll
-            for (int e = 1; e < UNIT_PAGES; ++e) m = fmaxf(m, fmaxf(lg[e][nt][0], lg[e][nt][1]));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-            pm[nt] = m;
-        }
-    };
+        // Hand unit k's slots back: issue the unit DEC_UNITS ahead into them and
+        // load the page ids of the unit after that.
+        auto release_unit = [&](int k, int st) {  // st = k % DEC_UNITS, also the slot group of k + DEC_UNITS
+            __syncwarp();
+            if (k + DEC_UNITS < n_units) {  // warp-uniform
+                fence_proxy_async_smem();
+                issue_unit(k + DEC_UNITS, st, pid_next);
+                n_issued = k + DEC_UNITS + 1;
+                const int j = UNIT_PAGES * (k + DEC_UNITS + 1) + lane;
+                if (lane < UNIT_PAGES && j < my_count) pid_next = __ldg(bt + page_of(j));
+            }
+        };
 
-    // ---------------- online softmax (base 2) for one unit, head 4*nt + t:
-    // raise the running maxima, rescale the accumulators when one grew, and
-    // return p^ (p rounded to fp16 once; the same p^ weights the codes, the
-    // group minima and the normaliser)
-    auto softmax_unit = [&](const float (&lg)[UNIT_PAGES][NT][2], const float (&pm)[NT], float (&pr)[UNIT_PAGES][NT][2]) {
-        float corr[NT];
-        bool need = false;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            corr[nt] = 1.f;
-            if (pm[nt] > mrun[nt]) {
-                corr[nt] = ex2(mrun[nt] - pm[nt]);  // 0 when mrun = -inf
-                mrun[nt] = pm[nt];
-                need = true;
-            }
-            const float mref = mrun[nt] == -CUDART_INF_F ? 0.f : mrun[nt];
-#pragma unroll
-            for (int e = 0; e < UNIT_PAGES; ++e) {
-                pr[e][nt][0] = __half2float(__float2half_rn(ex2(lg[e][nt][0] - mref)));
-                pr[e][nt][1] = __half2float(__float2half_rn(ex2(lg[e][nt][1] - mref)));
-            }
-            float ps = pr[0][nt][0] + pr[0][nt][1];
-#pragma unroll
-            for (int e = 1; e < UNIT_PAGES; ++e) ps += pr[e][nt][0] + pr[e][nt][1];
-            lsum[nt] = fmaf(lsum[nt], corr[nt], ps);
+        // Software pipeline over the warp's units: the QK of unit k + 1 does not
+        // depend on the softmax or PV of unit k, and the two sit in one
+        // straight-line block so their instruction streams interleave.  The
+        // slot group and mbarrier parity advance with k (no division by the
+        // ring size in the loop).
+        int k_fail = -1;  // the unit whose wait timed out
+        float lg[UNIT_PAGES][NT][2], pm[NT];
+        int st = st0;           // (kbase + k) % DEC_UNITS
+        uint32_t parity = par0;  // ((kbase + k) / DEC_UNITS) & 1
+        if (n_units > 0) {
+            if (wait_unit(st, parity))
+                qk_unit(st, lg, pm);
+            else
+                k_fail = 0;
         }
-        if (__any_sync(0xffffffffu, need)) {
-            // PV columns 2t, 2t+1 hold heads 2t, 2t+1, whose maxima live in lanes (2t)&3, (2t+1)&3
-            const int hA = 2 * t, hB = 2 * t + 1;
-            float cA = __shfl_sync(0xffffffffu, corr[0], hA & 3), cB = __shfl_sync(0xffffffffu, corr[0], hB & 3);
-            if constexpr (NT == 2) {
-                const float cA1 = __shfl_sync(0xffffffffu, corr[1], hA & 3);
-                const float cB1 = __shfl_sync(0xffffffffu, corr[1], hB & 3);
-                if (hA >= 4) cA = cA1;
-                if (hB >= 4) cB = cB1;
+        int k = 0;
+        for (; k + 1 < n_units && k_fail < 0; ++k) {
+            const int st1 = st + 1 == DEC_UNITS ? 0 : st + 1;
+            const uint32_t parity1 = st + 1 == DEC_UNITS ? parity ^ 1u : parity;
+            float pr[UNIT_PAGES][NT][2];
+            softmax_unit(lg, pm, pr);
+            if (!wait_unit(st1, parity1)) {
+                k_fail = k + 1;
+                break;
             }
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                oacc[m][0] *= cA;
-                oacc[m][2] *= cA;
-                oacc[m][1] *= cB;
-                oacc[m][3] *= cB;
-            }
-            cmin[0] *= cA;
-            cmin[2] *= cA;
-            cmin[1] *= cB;
-            cmin[3] *= cB;
+            for (int e = 0; e < UNIT_PAGES; ++e) pv_page(UNIT_PAGES * st + e, pr[e]);
+            qk_unit(st1, lg, pm);  // lg, pm of unit k are spent (pr holds what PV needs)
+            release_unit(k, st);
+            st = st1;
+            parity = parity1;
         }
-    };
+        if (k_fail < 0 && n_units > 0) {
+            float pr[UNIT_PAGES][NT][2];
+            softmax_unit(lg, pm, pr);
+#pragma unroll
+            for (int e = 0; e < UNIT_PAGES; ++e) pv_page(UNIT_PAGES * st + e, pr[e]);
+        }
+        if (k_fail >= 0) {
+            if (lane == 0) {
+                sm.dead = 1;
+                // let copies still in flight land before the shared memory is reused
+                for (int v = k_fail; v < n_issued; ++v)
+                    (void)mbar_wait_bounded(&sm.bar[warp][(kbase + v) % DEC_UNITS], ((kbase + v) / DEC_UNITS) & 1,
+                                            1000000LL);
+            }
+        }
 
-    // ---------------- PV of the page in ring slot `slot` with its weights p^
-    auto pv_page = [&](int slot, const float (&pr)[NT][2]) {
-        const uint8_t* tile = sm.u.ring[warp][slot];
-        // P in the PV B layout: column n = r (head n), rows = tokens 2t, 2t+1 | 2t+8, 2t+9
-        uint32_t pb0, pb1;
+
+        // the rows of R_v this warp rotates the CTA's partial with: loaded now,
+        // so their latency passes during the merge of the warps
+        float4 rvr[RowPrefetch<NW, MAXG>::N];
+        load_rows<NW>(Rv + (size_t)h * D * D, rvr);
+        // ---------------- warp partial -> shared memory, as soon as this warp is done
         {
-            const uint32_t X0 = pack_half2(pr[0][0], pr[0][1]);  // (token r, token r+8) of head t
-            const int srcA = 8 * t + (r & 3), srcB = 8 * t + 4 + (r & 3);
-            uint32_t Y0 = __shfl_sync(0xffffffffu, X0, srcA), Y1 = __shfl_sync(0xffffffffu, X0, srcB);
-            if constexpr (NT == 2) {
-                const uint32_t X1 = pack_half2(pr[1][0], pr[1][1]);
-                const uint32_t Z0 = __shfl_sync(0xffffffffu, X1, srcA), Z1 = __shfl_sync(0xffffffffu, X1, srcB);
-                if (r >= 4) {
-                    Y0 = Z0;
-                    Y1 = Z1;
-                }
+            // min term of (group g, head 2t / 2t+1) lives in lane 4g + t
+            float cm[NGROUP][2];
+#pragma unroll
+            for (int g = 0; g < NGROUP; ++g) {
+                cm[g][0] = __shfl_sync(0xffffffffu, cmin[0], 4 * g + t);
+                cm[g][1] = __shfl_sync(0xffffffffu, cmin[1], 4 * g + t);
             }
-            // NT == 1: columns 4..7 repeat heads 0..3 and carry the low part of p*scale
-            if ((NT == 1 ? (r & 3) : r) >= G) Y0 = Y1 = 0u;
-            pb0 = prmt(Y0, Y1, 0x5410);  // p(2t), p(2t+1)
-            pb1 = prmt(Y0, Y1, 0x7632);  // p(2t+8), p(2t+9)
-        }
-        // value scales of tokens (2t, 2t+1) and (2t+8, 2t+9), one word per group
-        const uint4 sA = lds128(tile + OFF_VM + 16 * t);
-        const uint4 sB = lds128(tile + OFF_VM + 16 * (t + 4));
-        const uint32_t wA[4] = {sA.x, sA.y, sA.z, sA.w}, wB[4] = {sB.x, sB.y, sB.z, sB.w};
-
-        // min term: rows = groups (rows 4..15 are never read), K = tokens
-        {
-            uint32_t a[4] = {0u, 0u, 0u, 0u};
-            a[0] = lds32(tile + OFF_VM + VM_MINS + 16 * t + 4 * (r & 3));
-            a[2] = lds32(tile + OFF_VM + VM_MINS + 16 * (t + 4) + 4 * (r & 3));
-            mma_f16_16816(cmin, a, pb0, pb1);
-        }
-
-        const uint32_t v0 = lds32(tile + OFF_VC + 32 * (2 * t) + 4 * r);
-        const uint32_t v1 = lds32(tile + OFF_VC + 32 * (2 * t + 1) + 4 * r);
-        const uint32_t v8 = lds32(tile + OFF_VC + 32 * (2 * t + 8) + 4 * r);
-        const uint32_t v9 = lds32(tile + OFF_VC + 32 * (2 * t + 9) + 4 * r);
-        const uint32_t A01 = prmt(v0, v1, 0x5410), A23 = prmt(v0, v1, 0x7632);
-        const uint32_t B01 = prmt(v8, v9, 0x5410), B23 = prmt(v8, v9, 0x7632);
-        const __half2 P0 = u32_as_h2(pb0), P1 = u32_as_h2(pb1);
+            if constexpr (NT == 1) {
+                // columns 4..7 (lanes t = 2, 3) hold the low parts of heads 0..3
 #pragma unroll
-        for (int g = 0; g < NGROUP; ++g) {
-            const uint32_t xa = g == 0 ? A01 : g == 1 ? (A01 >> 8) : g == 2 ? A23 : (A23 >> 8);
-            const uint32_t xb = g == 0 ? B01 : g == 1 ? (B01 >> 8) : g == 2 ? B23 : (B23 >> 8);
-            // p^ * scale exactly as an fp16 pair: hi = rn(p^ s), lo = p^ s - hi (exact)
-            const __half2 S01 = u32_as_h2(wA[g]), S89 = u32_as_h2(wB[g]);
-            const __half2 H0 = __hmul2(P0, S01), H1 = __hmul2(P1, S89);
-            const __half2 L0 = __hfma2(P0, S01, __hneg2(H0)), L1 = __hfma2(P1, S89, __hneg2(H1));
+                for (int m = 0; m < 8; ++m)
 #pragma unroll
-            for (int hs = 0; hs < 2; ++hs) {
-                const uint32_t k0 = 0x00030003u << (4 * hs), k1 = 0x00030003u << (4 * hs + 2);
-                const uint32_t a[4] = {xa & k0, xa & k1, xb & k0, xb & k1};
-                if constexpr (NT == 1) {
-                    const bool lo = r >= 4;
-                    mma_f16_16816(oacc[2 * g + hs], a, h2_as_u32(lo ? L0 : H0), h2_as_u32(lo ? L1 : H1));
-                } else {
-                    mma_f16_16816(oacc[2 * g + hs], a, h2_as_u32(H0), h2_as_u32(H1));
-                    mma_f16_16816(oacc[2 * g + hs], a, h2_as_u32(L0), h2_as_u32(L1));
+                    for (int e = 0; e < 4; ++e) oacc[m][e] += __shfl_xor_sync(0xffffffffu, oacc[m][e], 2);
+            }
+            const bool writer = NT == 2 || t < 2;
+#pragma unroll
+            for (int g = 0; g < NGROUP; ++g)
+#pragma unroll
+                for (int hs = 0; hs < 2; ++hs) {
+                    const int m = 2 * g + hs;
+                    const int ch0 = 32 * g + 4 * r + 2 * hs;     // row r, k = 2hs
+                    const float f0 = ldexpf(1.f, 24 - 4 * hs);  // 2^24 / 4^(2hs)
+                    const float f1 = f0 * 0.25f;                 // row r + 8, k = 2hs + 1
+                    if (writer && 2 * t < G) {
+                        sm.o_part[warp][2 * t][ch0] = fmaf(oacc[m][0], f0, cm[g][0]);
+                        sm.o_part[warp][2 * t][ch0 + 1] = fmaf(oacc[m][2], f1, cm[g][0]);
+                    }
+                    if (writer && 2 * t + 1 < G) {
+                        sm.o_part[warp][2 * t + 1][ch0] = fmaf(oacc[m][1], f0, cm[g][1]);
+                        sm.o_part[warp][2 * t + 1][ch0 + 1] = fmaf(oacc[m][3], f1, cm[g][1]);
+                    }
+                }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float l = lsum[nt];
+                l += __shfl_xor_sync(0xffffffffu, l, 4);
+                l += __shfl_xor_sync(0xffffffffu, l, 8);
+                l += __shfl_xor_sync(0xffffffffu, l, 16);
+                const int hq = 4 * nt + t;
+                if (r == 0 && hq < G) {
+                    sm.ms.m_part[warp][hq] = mrun[nt];
+                    sm.ms.l_part[warp][hq] = l;
                 }
             }
         }
+        __syncthreads();
+        merge_warps<NW, MAXG>(sm.ms, sm.o_part, G);
+        kbase += n_units;
+        // the next kernel in the stream may be scheduled once every CTA is here
+        if (last_seg) griddep_launch_dependents();
+        // this CTA's partial, carried to the output basis (O = o' R_v^T)
+        rotate_publish<NW, MAXG>(sm.ms, rvr, G, Rv + (size_t)h * D * D, slot_ptr((int64_t)u + cta));
+        } else {
+            if (last_seg) griddep_launch_dependents();
+            griddep_wait();  // (early inputs) nothing is written before the wait
+            publish_slot<NW, MAXG>(sm.ms, sm.ms.o_final, G, slot_ptr((int64_t)u + cta), true);
+        }
+        finish_unit(u);
+        __syncthreads();  // the next segment reuses the ring and the merge scratch
     };
-
-    // Hand unit u's slots back: issue the unit DEC_UNITS ahead into them and
-    // load the page ids of the unit after that.
-    auto release_unit = [&](int u, int st) {  // st = u % DEC_UNITS, also the slot group of u + DEC_UNITS
-        __syncwarp();
-        if (u + DEC_UNITS < n_units) {  // warp-uniform
-            fence_proxy_async_smem();
-            issue_unit(u + DEC_UNITS, st, pid_next);
-            n_issued = u + DEC_UNITS + 1;
-            const int j = UNIT_PAGES * (u + DEC_UNITS + 1) + lane;
-            if (lane < UNIT_PAGES && j < my_count) pid_next = __ldg(bt + page_of(j));
-        }
-    };
-
-    // Software pipeline over the warp's units: the QK of unit u + 1 does not
-    // depend on the softmax or PV of unit u, and the two sit in one
-    // straight-line block so their instruction streams interleave.
-    // The slot group and mbarrier parity of unit u advance with u (no
-    // division by the ring size in the loop).
-    int u_fail = -1;  // the unit whose wait timed out
-    float lg[UNIT_PAGES][NT][2], pm[NT];
-    int st = 0;             // u % DEC_UNITS
-    uint32_t parity = 0u;   // (u / DEC_UNITS) & 1
-    if (n_units > 0) {
-        if (wait_unit(0, 0u))
-            qk_unit(0, lg, pm);
-        else
-            u_fail = 0;
-    }
-    int u = 0;
-    for (; u + 1 < n_units && u_fail < 0; ++u) {
-        const int st1 = st + 1 == DEC_UNITS ? 0 : st + 1;
-        const uint32_t parity1 = st + 1 == DEC_UNITS ? parity ^ 1u : parity;
-        float pr[UNIT_PAGES][NT][2];
-        softmax_unit(lg, pm, pr);
-        if (!wait_unit(st1, parity1)) {
-            u_fail = u + 1;
-            break;
-        }
-#pragma unroll
-        for (int e = 0; e < UNIT_PAGES; ++e) pv_page(UNIT_PAGES * st + e, pr[e]);
-        qk_unit(st1, lg, pm);  // lg, pm of unit u are spent (pr holds what PV needs)
-        release_unit(u, st);
-        st = st1;
-        parity = parity1;
-    }
-    if (u_fail < 0 && n_units > 0) {
-        float pr[UNIT_PAGES][NT][2];
-        softmax_unit(lg, pm, pr);
-#pragma unroll
-        for (int e = 0; e < UNIT_PAGES; ++e) pv_page(UNIT_PAGES * st + e, pr[e]);
-    }
-    if (u_fail >= 0 && lane == 0) {
-        // let copies still in flight land before the shared memory is reused
-        for (int v = u_fail; v < n_issued; ++v)
-            (void)mbar_wait_bounded(&sm.bar[warp][v % DEC_UNITS], (v / DEC_UNITS) & 1, 1000000LL);
-    }
-
-    // the next kernel in the stream may be scheduled once every CTA is here
-    griddep_launch_dependents();
-
-    // ---------------- warp partial -> shared memory
-    __syncthreads();  // all warps are done with the ring (o_part aliases it)
-    {
-        // min term of (group g, head 2t / 2t+1) lives in lane 4g + t
-        float cm[NGROUP][2];
-#pragma unroll
-        for (int g = 0; g < NGROUP; ++g) {
-            cm[g][0] = __shfl_sync(0xffffffffu, cmin[0], 4 * g + t);
-            cm[g][1] = __shfl_sync(0xffffffffu, cmin[1], 4 * g + t);
-        }
-        if constexpr (NT == 1) {
-            // columns 4..7 (lanes t = 2, 3) hold the low parts of heads 0..3
-#pragma unroll
-            for (int m = 0; m < 8; ++m)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) oacc[m][e] += __shfl_xor_sync(0xffffffffu, oacc[m][e], 2);
-        }
-        const bool writer = NT == 2 || t < 2;
-#pragma unroll
-        for (int g = 0; g < NGROUP; ++g)
-#pragma unroll
-            for (int hs = 0; hs < 2; ++hs) {
-                const int m = 2 * g + hs;
-                const int ch0 = 32 * g + 4 * r + 2 * hs;     // row r, k = 2hs
-                const float f0 = ldexpf(1.f, 24 - 4 * hs);  // 2^24 / 4^(2hs)
-                const float f1 = f0 * 0.25f;                     // row r + 8, k = 2hs + 1
-                if (writer && 2 * t < G) {
-                    sm.u.o_part[warp][2 * t][ch0] = fmaf(oacc[m][0], f0, cm[g][0]);
-                    sm.u.o_part[warp][2 * t][ch0 + 1] = fmaf(oacc[m][2], f1, cm[g][0]);
-                }
-                if (writer && 2 * t + 1 < G) {
-                    sm.u.o_part[warp][2 * t + 1][ch0] = fmaf(oacc[m][1], f0, cm[g][1]);
-                    sm.u.o_part[warp][2 * t + 1][ch0 + 1] = fmaf(oacc[m][3], f1, cm[g][1]);
-                }
-            }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            float l = lsum[nt];
-            l += __shfl_xor_sync(0xffffffffu, l, 4);
-            l += __shfl_xor_sync(0xffffffffu, l, 8);
-            l += __shfl_xor_sync(0xffffffffu, l, 16);
-            const int hq = 4 * nt + t;
-            if (r == 0 && hq < G) {
-                sm.ms.m_part[warp][hq] = mrun[nt];
-                sm.ms.l_part[warp][hq] = l;
-            }
-        }
-    }
-    __syncthreads();
-
-    finish_decode<NW, MAXG>(sm.ms, sm.u.o_part, G, H_q, H_kv, B, b, h, split, S, ws, Rv + (size_t)h * D * D, out);
+    segment(u_first, false);
+    if (sm.share[1] > (int64_t)(u_first + 1) * max_pages) segment(u_first + 1, true);
 }
 
 }  // namespace kvq
@@ -708,7 +977,7 @@ using namespace kvq;
 // set it on the first call on each device only.
 static kvq_status set_smem_once(const void* fn, int bytes, int which) {
     static std::mutex mu;
-    static bool done[64][4] = {};
+    static bool done[64][6] = {};
     int dev = 0;
     kvq_status st = kvq_check_cuda(cudaGetDevice(&dev), "kvq_decode_attn_int2: cudaGetDevice");
     if (st != KVQ_OK) return st;
@@ -720,13 +989,58 @@ static kvq_status set_smem_once(const void* fn, int bytes, int which) {
     return st;
 }
 
+// Streaming multiprocessors of the current device (looked up once per
+// device); 152 (a GB300) where no device can be queried, so the host-only
+// sizing helpers still answer on a machine without a GPU.
+int kvq_device_sm_count() {
+    static std::mutex mu;
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        (void)cudaGetLastError();
+        return 152;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            (void)cudaGetLastError();
+            n = 152;
+        }
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// Page CTAs of the INT2 decode: num_splits per (sequence, KV head) unit when
+// given, else one wave (one CTA per SM, less the window CTAs when they fit
+// beside it) with at least 32 pages of the virtual page space per CTA; never
+// fewer CTAs than units (so a CTA's share spans at most two units) and never
+// more than virtual pages (so every share holds a page).
+static int64_t int2_page_ctas(int B, int H_kv, int max_pages, int num_splits, bool win) {
+    const int64_t units = (int64_t)B * H_kv, V = units * max_pages;
+    int64_t C;
+    if (num_splits > 0) {
+        C = (int64_t)num_splits * units;
+    } else {
+        const int64_t nsm = kvq_device_sm_count();
+        C = win && 2 * units <= nsm ? nsm - units : nsm;
+        const int64_t cap = (V + 31) / 32;
+        if (C > cap) C = cap;
+        // a CTA's share must not span more than two units
+        if (C < units) C = units;
+    }
+    if (C > V) C = V;
+    return C;
+}
+
 extern "C" int kvq_decode_auto_splits(int B, int H_q, int H_kv, int max_pages_per_seq) {
     if (B <= 0 || H_kv <= 0 || H_q < H_kv || max_pages_per_seq <= 0) return 1;
-    // at most one wave of CTAs, one per SM of the 152, over the (sequence,
-    // KV head) pairs (a CTA past the wave would run alone in a second one);
-    // at least 32 pages per split (the CTAs have 8-12 warps)
+    // at most one wave of CTAs, one per SM, over the (sequence, KV head)
+    // pairs (a CTA past the wave would run alone in a second one); at least
+    // 32 pages per split (the CTAs have 8-12 warps)
     const long units = (long)B * H_kv;
-    long s = 152L / units;
+    long s = (long)kvq_device_sm_count() / units;
     long max_s = (max_pages_per_seq + 31) / 32;
     if (max_s > MAX_SPLITS) max_s = MAX_SPLITS;
     if (s > max_s) s = max_s;
@@ -734,25 +1048,53 @@ extern "C" int kvq_decode_auto_splits(int B, int H_q, int H_kv, int max_pages_pe
     return (int)s;
 }
 
-extern "C" size_t kvq_decode_workspace_bytes(int B, int H_q, int H_kv, int max_pages_per_seq, int num_splits) {
-    if (B <= 0 || H_q <= 0 || H_kv <= 0) return 0;
-    int S = num_splits;
-    if (S <= 0) {  // room for the automatic choice of every decode entry point
-        S = kvq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq) + 1;  // + 1: a BF16 window split
-        const int Sb = bgtq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
-        if (Sb > S) S = Sb;
-    }
-    return WS_HEADER + tickets_bytes(B, H_kv) + (size_t)B * H_q * S * PART_STRIDE * sizeof(float);
+// Partial slots the INT2 decode uses: one per (unit, page CTA) pair (units +
+// C - 1 at most) and, with the window, one per unit.
+static size_t int2_workspace_bytes(int B, int H_q, int H_kv, int64_t slots) {
+    const int G = (H_q + H_kv - 1) / H_kv;
+    return WS_HEADER + tickets_bytes(B, H_kv) + (size_t)slots * G * PART_STRIDE * sizeof(float);
 }
 
-// Validation and launch shared by the two INT2 decode entry points; `win_k`
-// null means no BF16 window.
-static kvq_status decode_int2_launch(const char* fn, const void* q, int B, int H_q, int H_kv, int d,
-                                     const void* cache, int64_t num_pages, const int32_t* block_table,
-                                     int max_pages_per_seq, const int32_t* context_lens, const float* R_k,
-                                     const float* R_v, const float* mu_k, const void* win_k, const void* win_v,
-                                     const int32_t* win_lens, int win_max, float scale, float* out, void* workspace,
-                                     size_t workspace_bytes, int num_splits, void* stream) {
+extern "C" size_t kvq_decode_workspace_bytes(int B, int H_q, int H_kv, int max_pages_per_seq, int num_splits) {
+    if (B <= 0 || H_q <= 0 || H_kv <= 0 || max_pages_per_seq <= 0 || num_splits < 0) return 0;
+    const int64_t units = (int64_t)B * H_kv;
+    int64_t slots;
+    if (num_splits > 0) {
+        // INT2 with and without the window, and Block-GTQ's num_splits per unit
+        slots = ((int64_t)num_splits + 2) * units;
+    } else {  // room for the automatic choice of every decode entry point
+        const int64_t plain = units + int2_page_ctas(B, H_kv, max_pages_per_seq, 0, false);
+        const int64_t win = 2 * units + int2_page_ctas(B, H_kv, max_pages_per_seq, 0, true);
+        const int64_t bg = units * bgtq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
+        slots = plain > win ? plain : win;
+        if (bg > slots) slots = bg;
+    }
+    return int2_workspace_bytes(B, H_q, H_kv, slots);
+}
+
+// Test hook: makes the next INT2 decode launch on this process drop one bulk
+// copy so that a bounded wait runs out (kvq_debug_drop_next_copy).
+static std::atomic<int> g_debug_flags{0};
+
+extern "C" void kvq_debug_drop_next_copy(void) { g_debug_flags.store(DBG_DROP_FIRST_COPY); }
+
+// A validated INT2 decode launch.
+struct Int2Plan {
+    int G = 0, C = 0, grid = 0, threads = 0, mode = MODE_CACHE;
+    size_t smem = 0, need = 0;
+};
+
+// Argument checks shared by the INT2 decode entry points (nothing is
+// enqueued).  mode MODE_WINDOW: win_k, win_v, win_lens, win_max and mu_k
+// describe the BF16 window; MODE_STEP: win_k, win_v are the new token's key
+// and value and mu_k the key centre.  workspace is checked for null and
+// alignment only when check_ws is set.
+static kvq_status decode_int2_plan(const char* fn, int mode, const void* q, int B, int H_q, int H_kv, int d,
+                                   const void* cache, int64_t num_pages, const int32_t* block_table,
+                                   int max_pages_per_seq, const int32_t* context_lens, const float* R_k,
+                                   const float* R_v, const float* mu_k, const void* win_k, const void* win_v,
+                                   const int32_t* win_lens, int win_max, float* out, const void* workspace,
+                                   bool check_ws, int num_splits, Int2Plan& plan) {
     if (d != D) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "%s: d=%d (only 128)", fn, d);
     if (B <= 0 || H_kv <= 0 || H_q <= 0 || H_q % H_kv || max_pages_per_seq <= 0 || num_pages <= 0 ||
         num_splits < 0)
@@ -761,42 +1103,66 @@ static kvq_status decode_int2_launch(const char* fn, const void* q, int B, int H
     const int G = H_q / H_kv;
     if (G > 8) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "%s: GQA group %d > 8", fn, G);
     if (B > 65535 || H_kv > 65535) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "%s: B or H_kv above 65535", fn);
-    if (!q || !cache || !block_table || !context_lens || !R_k || !R_v || !out || !workspace)
+    if ((int64_t)B * H_kv * max_pages_per_seq > (int64_t(1) << 40))
+        return kvq_set_error(KVQ_ERR_UNSUPPORTED, "%s: B * H_kv * max_pages above 2^40", fn);
+    if (num_splits > MAX_SPLITS - 2)
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: %d splits above %d", fn, num_splits, MAX_SPLITS - 2);
+    if (!q || !cache || !block_table || !context_lens || !R_k || !R_v || !out || (check_ws && !workspace))
         return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: null pointer", fn);
-    if (reinterpret_cast<uintptr_t>(cache) % 16 || reinterpret_cast<uintptr_t>(workspace) % 16 ||
-        reinterpret_cast<uintptr_t>(R_v) % 16)
-        return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: cache, R_v and workspace need 16-byte alignment", fn);
-    if (win_k) {
-        if (win_max <= 0 || !win_v || !win_lens || !mu_k)
+    if (reinterpret_cast<uintptr_t>(cache) % 16 || (check_ws && reinterpret_cast<uintptr_t>(workspace) % 16) ||
+        reinterpret_cast<uintptr_t>(R_k) % 16 || reinterpret_cast<uintptr_t>(R_v) % 16)
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: cache, R_k, R_v and workspace need 16-byte alignment", fn);
+    if (mode == MODE_WINDOW) {
+        if (!win_k || win_max <= 0 || !win_v || !win_lens || !mu_k)
             return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: window needs win_max > 0, win_v, win_lens and mu_k", fn);
         if (reinterpret_cast<uintptr_t>(win_k) % 16 || reinterpret_cast<uintptr_t>(win_v) % 16)
             return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: win_k and win_v need 16-byte alignment", fn);
     }
-    int S_pages = num_splits > 0 ? num_splits : kvq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
-    // the automatic choice fills one wave; with a window, its split takes
-    // one of those CTAs (a 153rd CTA would run alone in a second wave)
-    if (num_splits == 0 && win_k && S_pages > 1 && (long)(S_pages + 1) * B * H_kv > 152L) S_pages -= 1;
-    const int S = S_pages + (win_k ? 1 : 0);
-    if (S > MAX_SPLITS)
-        return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: %d splits above %d", fn, S, MAX_SPLITS);
-    const size_t need = kvq_decode_workspace_bytes(B, H_q, H_kv, max_pages_per_seq, S);
-    if (workspace_bytes < need)
-        return kvq_set_error(KVQ_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, workspace_bytes, need);
-    const float scale_log2 = scale * 1.4426950408889634f;
+    if (mode == MODE_STEP && (!win_k || !win_v || !mu_k))
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: null k_new, v_new or mu_k", fn);
+    const bool extra = mode != MODE_CACHE;
+    const int64_t units = (int64_t)B * H_kv;
+    const int64_t C = int2_page_ctas(B, H_kv, max_pages_per_seq, num_splits, extra);
+    // a unit's partials: the page CTAs over its pages (its share of the
+    // virtual pages spans at most ceil(C / units) + 1 of them) and the window
+    if ((C + units - 1) / units + 2 > MAX_SPLITS)
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: %lld CTAs over %lld units exceed %d partials per unit", fn,
+                             (long long)C, (long long)units, MAX_SPLITS);
+    const int64_t grid = C + (extra ? units : 0);
+    if (grid > 0x7fffffff) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "%s: grid of %lld CTAs", fn, (long long)grid);
     constexpr int NW1 = DecWarps<1>::NW, NW2 = DecWarps<2>::NW;
-    const size_t smem = G <= 4 ? sizeof(DecodeSmem<NW1, 4>) : sizeof(DecodeSmem<NW2, 8>);
-    dim3 grid(S, H_kv, B);
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    auto* kern = G <= 4 ? (win_k ? decode_int2_kernel<1, true> : decode_int2_kernel<1, false>)
-                        : (win_k ? decode_int2_kernel<2, true> : decode_int2_kernel<2, false>);
-    kvq_status sa = set_smem_once((const void*)kern, (int)smem, (G <= 4 ? 0 : 2) + (win_k ? 1 : 0));
+    plan.G = G;
+    plan.C = (int)C;
+    plan.grid = (int)grid;
+    plan.mode = mode;
+    plan.threads = (G <= 4 ? NW1 : NW2) * 32;
+    plan.smem = G <= 4 ? sizeof(DecodeSmem<NW1, 4>) : sizeof(DecodeSmem<NW2, 8>);
+    plan.need = int2_workspace_bytes(B, H_q, H_kv, units + C + (extra ? units : 0));
+    return KVQ_OK;
+}
+
+static kvq_status decode_int2_launch(const Int2Plan& plan, const void* q, int B, int H_q, int H_kv,
+                                     void* cache, int64_t num_pages, const int32_t* block_table,
+                                     int max_pages_per_seq, const int32_t* context_lens, const float* R_k,
+                                     const float* R_v, const float* mu_k, const void* win_k, const void* win_v,
+                                     const int32_t* win_lens, int win_max, float scale, float* out, void* workspace,
+                                     void* stream, int kernel_flags = 0) {
+    const float scale_log2 = scale * 1.4426950408889634f;
+    const bool small = plan.G <= 4;
+    using Kern = decltype(&decode_int2_kernel<1, MODE_CACHE>);
+    static const Kern kerns[2][3] = {
+        {decode_int2_kernel<1, MODE_CACHE>, decode_int2_kernel<1, MODE_WINDOW>, decode_int2_kernel<1, MODE_STEP>},
+        {decode_int2_kernel<2, MODE_CACHE>, decode_int2_kernel<2, MODE_WINDOW>, decode_int2_kernel<2, MODE_STEP>}};
+    const Kern kern = kerns[small ? 0 : 1][plan.mode];
+    kvq_status sa = set_smem_once((const void*)kern, (int)plan.smem, (small ? 0 : 3) + plan.mode);
     if (sa != KVQ_OK) return sa;
-    const cudaError_t e =
-        launch_pdl(kern, grid, dim3((G <= 4 ? NW1 : NW2) * 32), smem, st, static_cast<const __nv_bfloat16*>(q), H_q,
-                   H_kv, G, static_cast<const uint8_t*>(cache), num_pages, block_table, max_pages_per_seq,
-                   context_lens, R_k, R_v, mu_k, static_cast<const __nv_bfloat16*>(win_k),
-                   static_cast<const __nv_bfloat16*>(win_v), win_lens, win_max, scale_log2, out,
-                   static_cast<uint8_t*>(workspace));
+    const int flags = g_debug_flags.exchange(0) | kernel_flags;
+    const cudaError_t e = launch_pdl(
+        kern, dim3(plan.grid), dim3(plan.threads), plan.smem, static_cast<cudaStream_t>(stream),
+        static_cast<const __nv_bfloat16*>(q), B, H_q, H_kv, plan.G, static_cast<uint8_t*>(cache), num_pages,
+        block_table, max_pages_per_seq, context_lens, R_k, R_v, mu_k, static_cast<const __nv_bfloat16*>(win_k),
+        static_cast<const __nv_bfloat16*>(win_v), win_lens, win_max, scale_log2, out,
+        static_cast<uint8_t*>(workspace), plan.C, flags);
     return kvq_check_cuda(e, "decode launch");
 }
 
@@ -805,9 +1171,17 @@ extern "C" kvq_status kvq_decode_attn_int2(const void* q, int B, int H_q, int H_
                                            const int32_t* context_lens, const float* R_k, const float* R_v,
                                            float scale, float* out, void* workspace, size_t workspace_bytes,
                                            int num_splits, void* stream) {
-    return decode_int2_launch("kvq_decode_attn_int2", q, B, H_q, H_kv, d, cache, num_pages, block_table,
+    Int2Plan plan;
+    kvq_status st = decode_int2_plan("kvq_decode_attn_int2", MODE_CACHE, q, B, H_q, H_kv, d, cache, num_pages, block_table,
+                                     max_pages_per_seq, context_lens, R_k, R_v, nullptr, nullptr, nullptr, nullptr,
+                                     0, out, workspace, true, num_splits, plan);
+    if (st != KVQ_OK) return st;
+    if (workspace_bytes < plan.need)
+        return kvq_set_error(KVQ_ERR_WORKSPACE, "kvq_decode_attn_int2: workspace %zu < %zu bytes", workspace_bytes,
+                             plan.need);
+    return decode_int2_launch(plan, q, B, H_q, H_kv, const_cast<void*>(cache), num_pages, block_table,
                               max_pages_per_seq, context_lens, R_k, R_v, nullptr, nullptr, nullptr, nullptr, 0, scale,
-                              out, workspace, workspace_bytes, num_splits, stream);
+                              out, workspace, stream);
 }
 
 extern "C" kvq_status kvq_decode_attn_int2_window(const void* q, int B, int H_q, int H_kv, int d, const void* cache,
@@ -818,9 +1192,64 @@ extern "C" kvq_status kvq_decode_attn_int2_window(const void* q, int B, int H_q,
                                                   int win_max, float scale, float* out, void* workspace,
                                                   size_t workspace_bytes, int num_splits, void* stream) {
     if (!win_k) return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_decode_attn_int2_window: null win_k");
-    return decode_int2_launch("kvq_decode_attn_int2_window", q, B, H_q, H_kv, d, cache, num_pages, block_table,
+    Int2Plan plan;
+    kvq_status st = decode_int2_plan("kvq_decode_attn_int2_window", MODE_WINDOW, q, B, H_q, H_kv, d, cache, num_pages,
+                                     block_table, max_pages_per_seq, context_lens, R_k, R_v, mu_k, win_k, win_v,
+                                     win_lens, win_max, out, workspace, true, num_splits, plan);
+    if (st != KVQ_OK) return st;
+    if (workspace_bytes < plan.need)
+        return kvq_set_error(KVQ_ERR_WORKSPACE, "kvq_decode_attn_int2_window: workspace %zu < %zu bytes",
+                             workspace_bytes, plan.need);
+    return decode_int2_launch(plan, q, B, H_q, H_kv, const_cast<void*>(cache), num_pages, block_table,
                               max_pages_per_seq, context_lens, R_k, R_v, mu_k, win_k, win_v, win_lens, win_max, scale,
-                              out, workspace, workspace_bytes, num_splits, stream);
+                              out, workspace, stream);
+}
+
+extern "C" kvq_status kvq_decode_step_int2(const void* q, const void* k_new, const void* v_new, int B, int H_q,
+                                           int H_kv, int d, void* cache, int64_t num_pages,
+                                           const int32_t* block_table, int max_pages_per_seq,
+                                           const int32_t* context_lens, const float* mu_k, const float* R_k,
+                                           const float* R_v, float scale, float* out, void* workspace,
+                                           size_t workspace_bytes, int num_splits, int flags, void* stream) {
+    if (flags & ~KVQ_STEP_INPUTS_READY)
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_decode_step_int2: unknown flags %d", flags);
+    Int2Plan plan;
+    kvq_status st = decode_int2_plan("kvq_decode_step_int2", MODE_STEP, q, B, H_q, H_kv, d, cache, num_pages,
+                                     block_table, max_pages_per_seq, context_lens, R_k, R_v, mu_k, k_new, v_new,
+                                     nullptr, 0, out, workspace, true, num_splits, plan);
+    if (st != KVQ_OK) return st;
+    if (workspace_bytes < plan.need)
+        return kvq_set_error(KVQ_ERR_WORKSPACE, "kvq_decode_step_int2: workspace %zu < %zu bytes", workspace_bytes,
+                             plan.need);
+    return decode_int2_launch(plan, q, B, H_q, H_kv, cache, num_pages, block_table, max_pages_per_seq, context_lens,
+                              R_k, R_v, mu_k, k_new, v_new, nullptr, 0, scale, out, workspace, stream,
+                              (flags & KVQ_STEP_INPUTS_READY) ? FLAG_EARLY_INPUTS : 0);
+}
+
+// Checks and launch used by kvq_decode_attn_int2_noalloc (its own file): the
+// arguments are validated before `prepare` runs, which may enqueue work on
+// the scratch it returns.
+kvq_status kvq_decode_int2_checked(const char* fn, const void* q, int B, int H_q, int H_kv, int d,
+                                   const void* cache, int64_t num_pages, const int32_t* block_table,
+                                   int max_pages_per_seq, const int32_t* context_lens, const float* R_k,
+                                   const float* R_v, float scale, float* out, int num_splits, void* stream,
+                                   size_t scratch_bytes, kvq_status (*prepare)(size_t zeroed, void* stream, void** ws)) {
+    Int2Plan plan;
+    kvq_status st = decode_int2_plan(fn, MODE_CACHE, q, B, H_q, H_kv, d, cache, num_pages, block_table, max_pages_per_seq,
+                                     context_lens, R_k, R_v, nullptr, nullptr, nullptr, nullptr, 0, out, nullptr,
+                                     false, num_splits, plan);
+    if (st != KVQ_OK) return st;
+    if (plan.need > scratch_bytes)
+        return kvq_set_error(KVQ_ERR_WORKSPACE,
+                             "%s: this shape needs %zu bytes of scratch, above the fixed %zu; use "
+                             "kvq_decode_attn_int2 with a workspace, or fewer splits",
+                             fn, plan.need, scratch_bytes);
+    void* ws = nullptr;
+    st = prepare(WS_HEADER + tickets_bytes(B, H_kv), stream, &ws);
+    if (st != KVQ_OK) return st;
+    return decode_int2_launch(plan, q, B, H_q, H_kv, const_cast<void*>(cache), num_pages, block_table,
+                              max_pages_per_seq, context_lens, R_k, R_v, nullptr, nullptr, nullptr, nullptr, 0, scale,
+                              out, ws, stream);
 }
 
 extern "C" kvq_status kvq_workspace_status(void* workspace, void* stream) {

@@ -25,7 +25,8 @@ void* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of g_decode_scratch on the current device.  The name is
 // only a host-side stand-in; the address comes from cudaGetSymbolAddress,
-// looked up once per device with that device current.
+// looked up once per device with that device current (so the entry point
+// must not be used across a cudaDeviceReset, which may move the array).
 kvq_status scratch_address(void** out) {
     int dev = 0;
     kvq_status st = kvq_check_cuda(cudaGetDevice(&dev), "kvq_decode_attn_int2_noalloc: cudaGetDevice");
@@ -45,6 +46,19 @@ kvq_status scratch_address(void** out) {
     return KVQ_OK;
 }
 
+// Runs once the arguments have passed every check: the error word and the
+// split tickets at the front of the scratch must start at zero.
+kvq_status prepare_scratch(size_t zeroed, void* stream, void** ws) {
+    void* scratch = nullptr;
+    kvq_status st = scratch_address(&scratch);
+    if (st != KVQ_OK) return st;
+    st = kvq_check_cuda(cudaMemsetAsync(scratch, 0, zeroed, static_cast<cudaStream_t>(stream)),
+                        "kvq_decode_attn_int2_noalloc: clearing scratch");
+    if (st != KVQ_OK) return st;
+    *ws = scratch;
+    return KVQ_OK;
+}
+
 }  // namespace
 
 extern "C" kvq_status kvq_decode_attn_int2_noalloc(const void* q, int B, int H_q, int H_kv, int d, const void* cache,
@@ -52,24 +66,7 @@ extern "C" kvq_status kvq_decode_attn_int2_noalloc(const void* q, int B, int H_q
                                                    int max_pages_per_seq, const int32_t* context_lens,
                                                    const float* R_k, const float* R_v, float scale, float* out,
                                                    int num_splits, void* stream) {
-    if (B <= 0 || H_q <= 0 || H_kv <= 0 || max_pages_per_seq <= 0 || num_splits < 0)
-        return kvq_set_error(KVQ_ERR_INVALID_ARG, "kvq_decode_attn_int2_noalloc: B=%d H_q=%d H_kv=%d max_pages=%d",
-                             B, H_q, H_kv, max_pages_per_seq);
-    const int S = num_splits > 0 ? num_splits : kvq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
-    const size_t need = kvq_decode_workspace_bytes(B, H_q, H_kv, max_pages_per_seq, S);
-    if (need > kNoallocScratchBytes)
-        return kvq_set_error(KVQ_ERR_WORKSPACE,
-                             "kvq_decode_attn_int2_noalloc: this shape needs %zu bytes of scratch, above the fixed "
-                             "%zu; use kvq_decode_attn_int2 with a workspace, or fewer splits",
-                             need, kNoallocScratchBytes);
-    void* scratch = nullptr;
-    kvq_status st = scratch_address(&scratch);
-    if (st != KVQ_OK) return st;
-    // the error word and the split tickets must start at zero
-    const size_t zeroed = kvq::WS_HEADER + kvq::tickets_bytes(B, H_kv);
-    st = kvq_check_cuda(cudaMemsetAsync(scratch, 0, zeroed, static_cast<cudaStream_t>(stream)),
-                        "kvq_decode_attn_int2_noalloc: clearing scratch");
-    if (st != KVQ_OK) return st;
-    return kvq_decode_attn_int2(q, B, H_q, H_kv, d, cache, num_pages, block_table, max_pages_per_seq, context_lens,
-                                R_k, R_v, scale, out, scratch, kNoallocScratchBytes, S, stream);
+    return kvq_decode_int2_checked("kvq_decode_attn_int2_noalloc", q, B, H_q, H_kv, d, cache, num_pages, block_table,
+                                   max_pages_per_seq, context_lens, R_k, R_v, scale, out, num_splits, stream,
+                                   kNoallocScratchBytes, prepare_scratch);
 }

@@ -58,6 +58,18 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // Automatic split count of the Block-GTQ decode (host).
 int bgtq_decode_auto_splits(int B, int H_q, int H_kv, int max_pages_per_seq);
 
+// Streaming multiprocessors of the current device (host; 152 without one).
+int kvq_device_sm_count();
+
+// The INT2 decode with every argument validated before `prepare` is called
+// to clear (`zeroed` bytes) and return the scratch it runs in (host; used by
+// the allocation-free entry point).
+kvq_status kvq_decode_int2_checked(const char* fn, const void* q, int B, int H_q, int H_kv, int d,
+                                   const void* cache, int64_t num_pages, const int32_t* block_table,
+                                   int max_pages_per_seq, const int32_t* context_lens, const float* R_k,
+                                   const float* R_v, float scale, float* out, int num_splits, void* stream,
+                                   size_t scratch_bytes, kvq_status (*prepare)(size_t zeroed, void* stream, void** ws));
+
 namespace kvq {
 
 // ---------------------------------------------------------------- PTX

@@ -302,4 +302,206 @@ __device__ __forceinline__ void finish_decode(MergeSmem<NW, MAXG>& ms, const flo
     if (tid == 0) tickets[unit] = 0;
 }
 
+
+// ---------------------------------------------------------------------------
+// Page-granular split-K (INT2 decode).  A CTA publishes one unrotated
+// partial (m, l, o') per (sequence, KV head) unit it worked on; the last CTA
+// of a unit merges them and applies the output rotation once.
+
+// Combines the NW warps' (m, l, o') of this CTA: per head jj < G, Mh = max_w
+// m_w, Lh = sum_w l_w 2^(m_w - Mh) and o_final = sum_w 2^(m_w - Mh) o_w.
+// Every thread of the CTA calls it once the warps' (m, l, o') are in shared
+// memory (after a barrier); each thread forms the weights of its own head,
+// so one barrier, at the end, suffices.
+template <int NW, int MAXG>
+__device__ __forceinline__ void merge_warps(MergeSmem<NW, MAXG>& ms, const float (*o_part)[MAXG][D], int G) {
+    for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
+        const int jj = idx / D, c = idx % D;
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, ms.m_part[w][jj]);
+        float O = 0.f, L = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const float f = M == -CUDART_INF_F ? 0.f : ex2(ms.m_part[w][jj] - M);
+            O = fmaf(o_part[w][jj][c], f, O);
+            L = fmaf(ms.l_part[w][jj], f, L);
+        }
+        ms.o_final[jj][c] = O;
+        if (c == 0) {
+            ms.Mh[jj] = M;
+            ms.Lh[jj] = L;
+        }
+    }
+    __syncthreads();
+}
+
+// Writes G heads of (Mh, Lh, src) to a partial slot: head jj at
+// slot + jj * PART_STRIDE as (m, l, -, -, o[128]).  With empty set, writes
+// an empty partial (m = -inf, l = 0, o = 0) instead.
+template <int NW, int MAXG>
+__device__ __forceinline__ void publish_slot(const MergeSmem<NW, MAXG>& ms, const float (*src)[D], int G,
+                                             float* __restrict__ slot, bool empty) {
+    for (int idx = threadIdx.x; idx < G * (D / 4); idx += NW * 32) {
+        const int jj = idx / (D / 4), c4 = idx % (D / 4);
+        float4 v = empty ? make_float4(0.f, 0.f, 0.f, 0.f) : *reinterpret_cast<const float4*>(&src[jj][4 * c4]);
+        *reinterpret_cast<float4*>(slot + (size_t)jj * PART_STRIDE + 4 + 4 * c4) = v;
+        if (c4 == 0) {
+            slot[(size_t)jj * PART_STRIDE] = empty ? -CUDART_INF_F : ms.Mh[jj];
+            slot[(size_t)jj * PART_STRIDE + 1] = empty ? 0.f : ms.Lh[jj];
+        }
+    }
+}
+
+// Publishes under the unit's ticket: true in the one CTA that arrives last
+// (of `expected`).  The barrier before orders every thread's partial writes
+// before thread 0's release-acquire add; the barrier after orders the last
+// CTA's reads of the other partials after it.
+template <int NW, int MAXG>
+__device__ __forceinline__ bool arrive_last(MergeSmem<NW, MAXG>& ms, int32_t* ticket, int expected) {
+    __syncthreads();
+    if (threadIdx.x == 0) ms.is_last = atomic_add_acq_rel_gpu(ticket, 1) == expected - 1;
+    __syncthreads();
+    return ms.is_last;
+}
+
+// Rotates this CTA's merged partial o_final (G heads) by Rot^T -- O_i =
+// sum_j o'_j Rot[i][j], Rot row-major [D][D], 16-byte aligned -- and writes
+// it, with (Mh, Lh), to a partial slot (head jj at slot + jj * PART_STRIDE as
+// m, l, -, -, O[128]).  rr holds each rotating warp's first rows of Rot
+// (load_rows, issued early so their latency is hidden).  Each lane forms the
+// partial dots of its 4 columns with its warp's rows, and a reduce-scatter
+// over the lanes leaves each row's full dot in one lane (heads two at a time
+// so their shuffle chains overlap).  All threads call it.
+template <int NW, int MAXG>
+__device__ __forceinline__ void rotate_publish(const MergeSmem<NW, MAXG>& ms, float4 (&rr)[RowPrefetch<NW, MAXG>::N],
+                                               int G, const float* __restrict__ Rot, float* __restrict__ slot) {
+    constexpr int NR = RotSplit<NW>::NR, RPW = RotSplit<NW>::RPW, RP = RowPrefetch<NW, MAXG>::N;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (warp < NR) {
+#pragma unroll
+        for (int pass = 0; pass < RPW / RP; ++pass) {
+            if (pass > 0) {
+#pragma unroll
+                for (int ii = 0; ii < RP; ++ii)
+                    rr[ii] = ldg4(Rot + (size_t)(RPW * warp + RP * pass + ii) * D + 4 * lane);
+            }
+            for (int jj = 0; jj < G; jj += 2) {
+                const int jb = jj + 1 < MAXG ? jj + 1 : jj;
+                const float4 oa = *reinterpret_cast<const float4*>(&ms.o_final[jj][4 * lane]);
+                const float4 ob = *reinterpret_cast<const float4*>(&ms.o_final[jb][4 * lane]);
+                float va[RP], vb[RP];
+#pragma unroll
+                for (int ii = 0; ii < RP; ++ii) {
+                    va[ii] = fmaf(oa.x, rr[ii].x, fmaf(oa.y, rr[ii].y, fmaf(oa.z, rr[ii].z, oa.w * rr[ii].w)));
+                    vb[ii] = fmaf(ob.x, rr[ii].x, fmaf(ob.y, rr[ii].y, fmaf(ob.z, rr[ii].z, ob.w * rr[ii].w)));
+                }
+                if constexpr (RP == 16) {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        va[k] += __shfl_xor_sync(0xffffffffu, va[k], 16);
+                        vb[k] += __shfl_xor_sync(0xffffffffu, vb[k], 16);
+                    }
+                }
+#pragma unroll
+                for (int off = RP / 2; off >= 1; off >>= 1) {
+                    const bool upper = lane & off;
+#pragma unroll
+                    for (int k = 0; k < off; ++k) {
+                        const float sa = upper ? va[k] : va[k + off], ka = upper ? va[k + off] : va[k];
+                        const float sb = upper ? vb[k] : vb[k + off], kb = upper ? vb[k + off] : vb[k];
+                        va[k] = ka + __shfl_xor_sync(0xffffffffu, sa, off);
+                        vb[k] = kb + __shfl_xor_sync(0xffffffffu, sb, off);
+                    }
+                }
+                const int row = 4 + RPW * warp + RP * pass + (lane & (RP - 1));
+                if (RP == 32 || lane < 16) {
+                    slot[(size_t)jj * PART_STRIDE + row] = va[0];
+                    if (jj + 1 < G) slot[(size_t)(jj + 1) * PART_STRIDE + row] = vb[0];
+                }
+            }
+        }
+    }
+    if (tid < G) {
+        slot[(size_t)tid * PART_STRIDE] = ms.Mh[tid];
+        slot[(size_t)tid * PART_STRIDE + 1] = ms.Lh[tid];
+    }
+}
+
+// In the last CTA of a unit: merges its n partial slots (slot_of(s), s < n;
+// already in the output basis) per head with the log-sum-exp rule and writes
+// out[jj][c] = O_c / L (zeros when L = 0) for the G heads.  All threads call
+// it.  Each head's partials are spread over P = NW / G warps (split p, p + P,
+// ...); a warp loads up to CH of them at once and folds them in with an
+// online rescale, so a unit of up to P * CH partials costs one round trip to
+// L2; the P per-warp results of a head are then combined in shared memory.
+template <int NW, int MAXG, typename SlotFn>
+__device__ __forceinline__ void merge_out(MergeSmem<NW, MAXG>& ms, SlotFn slot_of, int n, int G,
+                                          float* __restrict__ out) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr int CH = 8;  // partials in flight per lane
+    const int P = NW / G;  // warps per head (G <= NW)
+    float* wo = &ms.red[0][0][0];  // [NW][D] per-warp merged o
+    if (warp < P * G) {
+        const int jj = warp % G, p = warp / G;
+        float M = -CUDART_INF_F, L = 0.f;
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s0 = p; s0 < n; s0 += P * CH) {
+            float2 ml[CH];
+            float4 ov[CH];
+#pragma unroll
+            for (int k = 0; k < CH; ++k) {
+                const int s = s0 + P * k;
+                if (s < n) {
+                    const float* ph = slot_of(s) + (size_t)jj * PART_STRIDE;
+                    ml[k] = __ldcg(reinterpret_cast<const float2*>(ph));
+                    ov[k] = ldcg4(ph + 4 + 4 * lane);
+                } else {
+                    ml[k] = make_float2(-CUDART_INF_F, 0.f);
+                    ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < CH; ++k) {
+                const float Mn = fmaxf(M, ml[k].x);
+                const float a = Mn == -CUDART_INF_F ? 0.f : ex2(M - Mn);
+                const float b = Mn == -CUDART_INF_F ? 0.f : ex2(ml[k].x - Mn);
+                L = fmaf(L, a, ml[k].y * b);
+                O.x = fmaf(O.x, a, ov[k].x * b);
+                O.y = fmaf(O.y, a, ov[k].y * b);
+                O.z = fmaf(O.z, a, ov[k].z * b);
+                O.w = fmaf(O.w, a, ov[k].w * b);
+                M = Mn;
+            }
+        }
+        *reinterpret_cast<float4*>(wo + (size_t)warp * D + 4 * lane) = O;
+        if (lane == 0) {
+            ms.fac[0][warp] = M;
+            ms.lsp[0][warp] = L;
+        }
+    }
+    __syncthreads();
+    // combine the P warps of each head and normalise: out = sum_p 2^(M_p - M) O_p / L
+    for (int idx = tid; idx < G * (D / 4); idx += NW * 32) {
+        const int jj = idx / (D / 4), c4 = idx % (D / 4);
+        float M = -CUDART_INF_F;
+        for (int p = 0; p < P; ++p) M = fmaxf(M, ms.fac[0][jj + G * p]);
+        float L = 0.f;
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int p = 0; p < P; ++p) {
+            const int w = jj + G * p;
+            const float f = M == -CUDART_INF_F ? 0.f : ex2(ms.fac[0][w] - M);
+            const float4 v = *reinterpret_cast<const float4*>(wo + (size_t)w * D + 4 * c4);
+            L = fmaf(ms.lsp[0][w], f, L);
+            O.x = fmaf(v.x, f, O.x);
+            O.y = fmaf(v.y, f, O.y);
+            O.z = fmaf(v.z, f, O.z);
+            O.w = fmaf(v.w, f, O.w);
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        *reinterpret_cast<float4*>(out + (size_t)jj * D + 4 * c4) =
+            make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+    }
+}
+
 }  // namespace kvq

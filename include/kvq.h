@@ -21,7 +21,10 @@
  * Conventions (all calls):
  *  - d (head dimension) must be 128; the page size is 16 tokens.
  *  - Device pointers are owned by the caller; the library allocates no
- *    memory and keeps no global state besides the thread-local error text.
+ *    memory at call time.  Its global state: the thread-local error text,
+ *    per-device caches (SM count, kernel shared-memory opt-ins), the fixed
+ *    scratch array of kvq_decode_attn_int2_noalloc and the one-shot flag of
+ *    the test hook kvq_debug_drop_next_copy.
  *  - Device work is enqueued on `stream` (a cudaStream_t; NULL = legacy
  *    default stream) and is asynchronous: faults surface at the caller's
  *    next synchronisation.  Argument errors are detected on the host before
@@ -33,10 +36,9 @@
  *  - slot_mapping[t] = page * 16 + slot; -1 skips token t.
  *  - Kernels are launched with programmatic dependent launch: a call's
  *    kernel may start while the kernel before it in the stream is still
- *    running, and waits for it before reading its inputs.  The INT2
- *    rotations R_k and R_v are the exception: they are constants of a
- *    layer and are read before that wait, so the kernel issued immediately
- *    before an INT2 call in the same stream must not write them.
+ *    running, and waits for it before reading any input (before the wait it
+ *    only asks L2 to prefetch lines, which returns no data), so every input,
+ *    rotations included, may be written by the kernel just before the call.
  */
 #ifndef KVQ_H
 #define KVQ_H
@@ -128,18 +130,22 @@ kvq_status kvq_dequant_int2(const void* cache, int64_t num_pages, int H_kv, int 
                             void* stream);
 
 /* Bytes of decode workspace for B sequences, H_q query heads, H_kv KV heads
- * and num_splits split-K partitions (num_splits = 0: room for the automatic
- * choice of every decode entry point, kvq_decode_attn_int2, its BF16-window
- * form or bgtq_decode_attn, at max_pages_per_seq pages).  The workspace holds an
- * error word, a split ticket per (sequence, KV head) and the split partials.
- * It must be zero-filled once before its first use; every call leaves its
- * tickets at zero again. */
+ * and num_splits split-K partitions per (sequence, KV head), enough for every
+ * decode entry point called with that num_splits (num_splits = 0: room for
+ * the automatic choice of each, kvq_decode_attn_int2, its BF16-window form
+ * and bgtq_decode_attn, at max_pages_per_seq pages on the current device,
+ * whose SM count sets the automatic choice).  The workspace holds an error
+ * word, a split ticket per (sequence, KV head) and the split partials.  It
+ * must be zero-filled once before its first use; every call leaves its
+ * tickets at zero again.  Returns 0 for invalid sizes. */
 size_t kvq_decode_workspace_bytes(int B, int H_q, int H_kv, int max_pages_per_seq, int num_splits);
 
-/* The split count the automatic choice (num_splits = 0) of the decode calls
- * uses: the most splits that keep B * H_kv * splits within one wave of one
- * CTA per SM (152), at least 1, at most one split per 32 pages and at most
- * 256. */
+/* The split count per (sequence, KV head) the automatic choice (num_splits =
+ * 0) of bgtq_decode_attn uses: the most splits that keep B * H_kv * splits
+ * within one wave of one CTA per SM of the current device (152 on a GB300,
+ * and where no device can be queried), at least 1, at most one split per 32
+ * pages and at most 256.  (The INT2 decode's automatic choice is described
+ * at kvq_decode_attn_int2.) */
 int kvq_decode_auto_splits(int B, int H_q, int H_kv, int max_pages_per_seq);
 
 /* Fused packed-cache decode attention over the INT2 cache.
@@ -152,9 +158,15 @@ int kvq_decode_auto_splits(int B, int H_q, int H_kv, int max_pages_per_seq);
  *   out          device fp32 [B][H_q][d]: o = softmax(q'.Q2(z)*scale) Q2(w) R_v^T
  *                (zeros for an empty context)
  *   workspace    device, >= kvq_decode_workspace_bytes(...), zeroed once
- *   num_splits   split-K partitions per sequence (0 = automatic)
- * Block-table entries outside [0, num_pages) are not read: their tokens are
- * dropped and kvq_workspace_status reports KVQ_ERR_BAD_BLOCK_TABLE. */
+ *   num_splits   CTAs per (sequence, KV head), at most 254: the B * H_kv
+ *                units are laid end to end as B * H_kv * max_pages_per_seq
+ *                pages and num_splits * B * H_kv CTAs take equal shares of
+ *                them; 0 = automatic: one CTA per SM of the device (at least
+ *                one per unit, at most one per 32 pages)
+ * Each CTA publishes an unrotated split partial per unit its share covers;
+ * the last to finish merges them and applies R_v^T once.  Block-table
+ * entries outside [0, num_pages) are not read: their tokens are dropped and
+ * kvq_workspace_status reports KVQ_ERR_BAD_BLOCK_TABLE. */
 kvq_status kvq_decode_attn_int2(const void* q, int B, int H_q, int H_kv, int d,
                                 const void* cache, int64_t num_pages,
                                 const int32_t* block_table, int max_pages_per_seq,
@@ -162,6 +174,42 @@ kvq_status kvq_decode_attn_int2(const void* q, int B, int H_q, int H_kv, int d,
                                 const float* R_k, const float* R_v, float scale,
                                 float* out, void* workspace, size_t workspace_bytes,
                                 int num_splits, void* stream);
+
+/* One decode step of one layer in a single launch: kvq_append_int2 of the
+ * new token followed by kvq_decode_attn_int2 ("Output-Aware Rotation for
+ * INT2 KV-Cache Quantization" §1 and §3.1 Eq. 4 for the append, §3 Eqs. 1-2
+ * for the attention).  For every sequence b with ctx = context_lens[b] >= 1
+ * the new token k_new[b], v_new[b] ([B][H_kv][d] bf16, original basis, key
+ * not centred) is quantised exactly as kvq_append_int2 does it and written
+ * to position ctx - 1, i.e. slot block_table[b][(ctx-1)/16] * 16 +
+ * (ctx-1) % 16; then the ctx tokens, the new one included, are attended.
+ * One extra CTA per (sequence, KV head) quantises, writes and attends the
+ * new token while the page CTAs stream the ctx - 1 cached ones, and the
+ * partials merge as in kvq_decode_attn_int2: the cache bytes written are
+ * identical to kvq_append_int2's, and the output equals that of the two
+ * calls in sequence up to the rounding order of the merge.
+ *   mu_k      device fp32 [H_kv][d], the key centre of the append
+ *   cache     written at the new tokens' slots
+ *   flags     0 or KVQ_STEP_INPUTS_READY
+ *   other arguments as kvq_decode_attn_int2; kvq_decode_workspace_bytes(...,
+ *   num_splits) covers this call.
+ * With KVQ_STEP_INPUTS_READY the caller declares that R_k, R_v, mu_k,
+ * block_table, context_lens and the cache are not written by the kernel
+ * issued immediately before this call on the stream (in a model's decode
+ * step that kernel is typically the projection that writes q, k_new and
+ * v_new; the previous layer's step touches other caches): the kernel then
+ * reads them, and starts streaming the cache, while that kernel finishes.
+ * q, k_new, v_new, out and the workspace are always accessed after it.
+ * Without the flag every input is read after it, as in every other call.
+ * A sequence with ctx = 0 appends nothing and gets zeros; a new token whose
+ * page id is outside [0, num_pages) is neither written nor attended, and
+ * kvq_workspace_status reports KVQ_ERR_BAD_BLOCK_TABLE. */
+enum { KVQ_STEP_INPUTS_READY = 1 };
+kvq_status kvq_decode_step_int2(const void* q, const void* k_new, const void* v_new, int B, int H_q, int H_kv,
+                                int d, void* cache, int64_t num_pages, const int32_t* block_table,
+                                int max_pages_per_seq, const int32_t* context_lens, const float* mu_k,
+                                const float* R_k, const float* R_v, float scale, float* out, void* workspace,
+                                size_t workspace_bytes, int num_splits, int flags, void* stream);
 
 /* Decode attention over the INT2 cache together with a BF16 window of
  * tokens kept unquantised.  "Output-Aware Rotation for INT2 KV-Cache
@@ -180,9 +228,9 @@ kvq_status kvq_decode_attn_int2(const void* q, int B, int H_q, int H_kv, int d,
  *             centred, not rotated), 16-byte aligned
  *   win_lens  device int32 [B], clamped to [0, win_max]
  *   win_max   > 0
- * The window takes one split of its own: the workspace must hold
- * num_splits + 1 partials (kvq_decode_workspace_bytes(..., num_splits + 1);
- * with num_splits = 0, kvq_decode_workspace_bytes(..., 0) already does). */
+ * The window of each (sequence, KV head) is attended by one CTA of its own,
+ * whose partial is carried into the R_v basis and merged with the cache's;
+ * kvq_decode_workspace_bytes(..., num_splits) covers it. */
 kvq_status kvq_decode_attn_int2_window(const void* q, int B, int H_q, int H_kv, int d,
                                        const void* cache, int64_t num_pages,
                                        const int32_t* block_table, int max_pages_per_seq,
@@ -215,14 +263,27 @@ kvq_status kvq_workspace_status(void* workspace, void* stream);
  *   stream capture.  Each call clears the scratch counters on `stream`.
  *   Every call shares the one array: calls whose work overlaps on the GPU
  *   (other streams, other host threads) race and give wrong results.
- *   In-kernel errors (out-of-range block-table entries) are not reported:
- *   such pages are skipped.  Allocates nothing. */
+ *   Argument errors are returned before anything is enqueued.  No in-kernel
+ *   error is reported (an out-of-range block-table entry, whose page is
+ *   skipped, or a wait that ran out, which leaves the output partial): the
+ *   scratch's error word is cleared by the next call and has no accessor.
+ *   The array's address is looked up once per device, so the entry point
+ *   must not be used across a cudaDeviceReset.  Allocates nothing. */
 kvq_status kvq_decode_attn_int2_noalloc(const void* q, int B, int H_q, int H_kv, int d,
                                         const void* cache, int64_t num_pages,
                                         const int32_t* block_table, int max_pages_per_seq,
                                         const int32_t* context_lens,
                                         const float* R_k, const float* R_v, float scale,
                                         float* out, int num_splits, void* stream);
+
+/* Test hook, not for production use: the next INT2 decode launch in this
+ * process leaves the bulk copy of its first page unissued (the page's bytes
+ * are still expected) and gives its waits a limit of about a millisecond, so
+ * that wait runs out: the kernel records the timeout, lets its other copies
+ * land, finishes without the missing page and returns, and
+ * kvq_workspace_status then reports KVQ_ERR_CUDA.  Nothing faults or hangs;
+ * the output of that call is incomplete. */
+void kvq_debug_drop_next_copy(void);
 
 /* ------------------------------------------------------------- Block-GTQ */
 

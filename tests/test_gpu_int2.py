@@ -364,12 +364,21 @@ def test_qwen8b_full_context_sampled_layers():
     _sampled_check(spec, 35, [(0, 6)])
 
 
-def test_sweep70b_gqa8_sampled():
-    _sampled_check(inputs.sweep70b_spec(8, 4096), 0, [(1, 0), (6, 7)])
-    _sampled_check(inputs.sweep70b_spec(1, 524288), 0, [(0, 3)], token_samples=64)
+# The 70B-class GQA-8 scaling grid: batch {1, 8, 32, 64} x context {4K, 32K,
+# 128K}, and batch 1 at 256K and 512K.  Each point is decoded in full on the
+# GPU (automatic split) and checked on sampled (sequence, KV head) pairs.
+SWEEP = [(B, T) for B in (1, 8, 32, 64) for T in (4096, 32768, 131072)] + [(1, 262144), (1, 524288)]
 
 
-def test_sweep70b_batch64_multiwave_sampled():
-    # 64 sequences x 8 KV heads = 512 (sequence, KV head) units at one split
-    # each: a grid of 3.4 waves of 152 CTAs
-    _sampled_check(inputs.sweep70b_spec(64, 4096), 0, [(0, 0), (37, 5), (63, 7)], token_samples=64)
+@pytest.mark.parametrize("B,T", SWEEP, ids=[f"b{B}_t{T // 1024}k" for B, T in SWEEP])
+def test_sweep70b_point_sampled(B, T):
+    rng = np.random.default_rng(B * 7 + T)
+    samples = sorted({(int(rng.integers(0, B)), int(rng.integers(0, 8))) for _ in range(2 if T <= 32768 else 1)})
+    if B > 1:
+        samples.append((B - 1, 7))                  # the last unit of the page split
+    _sampled_check(inputs.sweep70b_spec(B, T), 0, samples, token_samples=64 if T > 4096 else 128)
+
+
+def test_sweep70b_batch64_explicit_split():
+    # 64 sequences x 8 KV heads at one CTA each: a grid of 3.4 waves of 152
+    _sampled_check(inputs.sweep70b_spec(64, 4096), 0, [(0, 0), (37, 5), (63, 7)], splits=1, token_samples=64)

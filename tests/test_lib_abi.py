@@ -31,6 +31,7 @@ def test_sizes(cpu_lib):
     assert _lib.bgtq_tile_bytes(192, 3) == bgtq.tile_layout(192, 3)["tile"]
     ws = _lib.kvq_decode_workspace_bytes(2, 8, 2, 100, 3)
     assert ws >= 2 * 8 * 3 * 132 * 4
+    assert _lib.kvq_decode_workspace_bytes(0, 8, 2, 100, 3) == 0
 
 
 @pytest.mark.parametrize("B,H_kv,pages,want", [
@@ -52,13 +53,24 @@ def test_auto_splits_fill_one_wave(cpu_lib, B, H_kv, pages, want):
 
 def test_workspace_with_auto_splits_holds_every_entry_point(cpu_lib):
     """num_splits = 0 sizes the partials for the automatic choice of every
-    decode call, the BF16-window form (one more split) included."""
-    for B, H_kv, pages in [(1, 8, 8192), (8, 8, 2048), (3, 2, 40)]:
+    decode call: the INT2 decode's slots (one per unit and page CTA, at most
+    units + C - 1 with C = one CTA per SM (152 where no device is visible),
+    at least one per unit and at most one per 32 pages), the BF16-window
+    form's extra slot per unit, and Block-GTQ's per-unit splits."""
+    nsm = 152
+    for B, H_kv, pages in [(1, 8, 8192), (8, 8, 2048), (3, 2, 40), (64, 8, 256), (1, 1, 17)]:
         H_q = 4 * H_kv
-        auto = _lib.kvq_decode_auto_splits(B, H_q, H_kv, pages)
+        units = B * H_kv
+        V = units * pages
+        c_plain = min(max(min(nsm, -(-V // 32)), units), V)
+        c_win = min(max(min(nsm - units if 2 * units <= nsm else nsm, -(-V // 32)), units), V)
+        slots = max(units + c_plain, 2 * units + c_win, units * _lib.kvq_decode_auto_splits(B, H_q, H_kv, pages))
+        header = 256 + -(-units * 4 // 256) * 256
         ws0 = _lib.kvq_decode_workspace_bytes(B, H_q, H_kv, pages, 0)
-        assert ws0 >= _lib.kvq_decode_workspace_bytes(B, H_q, H_kv, pages, auto + 1)
-        assert ws0 >= B * H_q * (auto + 1) * 132 * 4
+        assert ws0 == header + slots * 4 * 132 * 4
+        # an explicit split count covers the plain and the window form
+        for S in (1, 3, 40):
+            assert _lib.kvq_decode_workspace_bytes(B, H_q, H_kv, pages, S) == header + (S + 2) * units * 4 * 132 * 4
 
 
 def test_allocator_matches_oracle(cpu_lib):

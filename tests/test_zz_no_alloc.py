@@ -50,6 +50,27 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
         assert err <= TOL * np.max(np.abs(ref)), err
 
 
+def test_noalloc_gqa8_and_the_largest_shape_that_fits():
+    """The 8-warp GQA-8 instance through the fixed scratch, and the largest
+    batch of 64 q / 8 KV heads at 4K context whose partials fit 4 MiB (one
+    more sequence is refused)."""
+    a = _layer("noalloc_g8", 64, 8, 2, 2500)
+    got, ref = _both(a, a.queries(), 0)
+    assert np.all(np.isfinite(got))
+    assert np.max(np.abs(got - ref)) <= TOL * np.max(np.abs(ref))
+    big = _layer("noalloc_big", 64, 8, 62, 4096)
+    got, ref = _both(big, big.queries(), 0)
+    assert np.all(np.isfinite(got))
+    assert np.max(np.abs(got - ref)) <= TOL * np.max(np.abs(ref))
+    q = torch.zeros((63, 64, 128), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((63, 64, 128), dtype=torch.float32, device="cuda")
+    bt = torch.zeros((63, 256), dtype=torch.int32, device="cuda")
+    cl = torch.full((63,), 4096, dtype=torch.int32, device="cuda")
+    with pytest.raises(_lib.KvqError) as e:
+        _lib.kvq_decode_attn_int2_noalloc(q, big.cache, big.num_pages, bt, cl, big.R_k, big.R_v, 0.1, out)
+    assert e.value.status == -3 and "scratch" in str(e.value)
+
+
 def test_noalloc_rejects_shapes_above_its_scratch():
     q = torch.zeros((64, 64, 128), dtype=torch.bfloat16, device="cuda")
     dummy = torch.zeros(16, dtype=torch.uint8, device="cuda")
