@@ -58,7 +58,8 @@ struct __align__(16) DecodeSmem {
     struct {
         uint8_t ring[NW][DEC_STAGES][INT2_TILE];  // page tiles in flight
     } u;
-    float o_part[NW][MAXG][D];  // per-warp o' after the loop (its own space: a warp writes it as soon as it is done)
+    float o_part[NW + 1][MAXG][D];  // per-warp o' after the loop (its own space: a warp writes it as soon as
+                                    // it is done), and the decode step's new token
     uint64_t bar[NW][DEC_UNITS];
     int ntok[NW][DEC_STAGES];  // valid tokens of the page in each stage (0: skipped page)
     float q[MAXG][D];          // scaled rotated queries q~ = q R_k * scale * log2(e)
@@ -147,7 +148,9 @@ __device__ __forceinline__ void window_partials(float (*o_part)[MAXG][D], MergeS
 }
 
 // Work split.  The B * H_kv (sequence, KV head) units are laid end to end
-// as V = units * max_pages "virtual" pages: unit u = b * H_kv + h owns
+// as V = units * vmp "virtual" pages (vmp = max_pages, plus in a decode step
+// a few pages without work that lighten the share holding the new token):
+// unit u = b * H_kv + h owns
 // [u * MP, (u + 1) * MP), of which the first ceil(ctx_b / 16) are real.
 // Page CTA c of C takes the virtual pages [c V / C, (c + 1) V / C), so every
 // CTA gets the same share (within one page) whatever B * H_kv is, and a CTA
@@ -169,111 +172,70 @@ enum DecodeMode : int {
     MODE_STEP = 2,    // append the decode token to the cache and attend it
 };
 
-// The new token of a decode step (MODE_STEP), for KV head h of sequence b at
+// The new token of a decode step (MODE_STEP), KV head h of sequence b, at
 // position ctx - 1: quantised exactly as the append kernels do it (the same
 // fp32 chains z = (k - mu) R_k, w = v R_v in ascending input order, the same
-// group parameters and codes), written to its cache slot, and attended here:
-// its logit q' . Q2(z) and value Q2(w) (rotated basis) form a partial
-// (m, l = 1, o' = Q2(w)) that merges with the page CTAs', which stop one
-// token short.  The CTA's first 256 threads work: thread j < 128 owns
-// rotated key channel j, thread 128 + j value channel j.  Returns false when
-// the token's page id is out of range (nothing written; the partial is empty).
-template <int NW, int MAXG>
-__device__ __forceinline__ bool step_token_partial(MergeSmem<NW, MAXG>& ms, float (*xs)[D], float (*qs)[D],
-                                                   const __nv_bfloat16* __restrict__ q,
-                                                   const __nv_bfloat16* __restrict__ k_new,
-                                                   const __nv_bfloat16* __restrict__ v_new,
-                                                   const float* __restrict__ mu, const float* __restrict__ Rk,
-                                                   const float* __restrict__ Rv, uint8_t* __restrict__ cache,
-                                                   int64_t num_pages, int pid, int slot, int H_q, int H_kv, int G,
-                                                   int b, int h, float scale_log2, float (*vout)[D]) {
+// group parameters and codes) and written to its cache slot.  The CTA whose
+// page share holds that position does it, between issuing its first copies
+// and rotating the query; its first 256 threads work (thread j < 128 owns
+// rotated key channel j, thread 128 + j value channel j) on inputs staged in
+// xs[0] (centred key) and xs[1] (value).  Returns the level the cache now
+// holds for the thread's channel (0 for other threads), so the token can be
+// attended from registers.
+__device__ __forceinline__ float new_token_codes(const float (*xs)[D], const float (&rcol)[D], uint8_t* __restrict__ cache,
+                                                 int H_kv, int h, int pid, int slot, bool write) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int side = tid >> 7, j = tid & (D - 1);  // side 0: key channel j, 1: value channel j
-    const bool worker = tid < 2 * D;
-    // inputs: the centred key and the value (fp32), the G query rows
-    if (tid < D) {
-        const size_t row = ((size_t)b * H_kv + h) * D + tid;
-        xs[0][tid] = __fsub_rn(__bfloat162float(k_new[row]), __ldg(mu + (size_t)h * D + tid));
-        xs[1][tid] = __bfloat162float(v_new[row]);
+    const int side = tid >> 7;
+    if (tid >= 2 * D) return 0.f;
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < D; ++i) acc = __fmaf_rn(xs[side][i], rcol[i], acc);
+    // group parameters (exact min / max over the 32 lanes of the group)
+    float mn = acc, mx = acc;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     }
-    for (int idx = tid; idx < G * D; idx += NW * 32)
-        qs[idx / D][idx % D] = __bfloat162float(q[((size_t)b * H_q + (size_t)h * G) * D + idx]);
-    float rcol[D];
-    if (worker) {
-        const float* R = (side ? Rv : Rk) + (size_t)h * D * D + j;
-#pragma unroll
-        for (int i = 0; i < D; ++i) rcol[i] = __ldg(R + (size_t)i * D);
+    __half sh, mh;
+    int2_params(mn, mx, 1.f, sh, mh);
+    const float scf = __half2float(sh), mnf = __half2float(mh);
+    const int code = int2_code(acc, mnf, scf);
+    const uint32_t byte = int2_gather_byte(code, lane);
+    const int grp = warp & 3;
+    if (write) {
+        uint8_t* tile = cache + ((size_t)pid * H_kv + h) * INT2_TILE;
+        if ((lane & 3) == 0) tile[(side ? OFF_VC : OFF_KC) + 32 * slot + 4 * (lane >> 2) + grp] = (uint8_t)byte;
+        if (lane == 0) int2_store_meta(tile, side, slot, grp, sh, mh);
     }
-    __syncthreads();
-    const bool ok = pid >= 0 && (int64_t)pid < num_pages;
-    float xhat = 0.f;
-    // q' = q R_k for the key threads (thread j holds column j of R_k), in the
-    // same pass over the column as the key's chain
-    float qp[MAXG];
-#pragma unroll
-    for (int jj = 0; jj < MAXG; ++jj) qp[jj] = 0.f;
-    if (worker) {
-        float acc = 0.f;
-        if (side == 0) {
-#pragma unroll
-            for (int i = 0; i < D; ++i) {
-                acc = __fmaf_rn(xs[0][i], rcol[i], acc);
-#pragma unroll
-                for (int jj = 0; jj < MAXG; ++jj)
-                    if (jj < G) qp[jj] = fmaf(qs[jj][i], rcol[i], qp[jj]);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < D; ++i) acc = __fmaf_rn(xs[1][i], rcol[i], acc);
-        }
-        // group parameters (exact min / max over the 32 lanes of the group)
-        float mn = acc, mx = acc;
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        }
-        __half sh, mh;
-        int2_params(mn, mx, 1.f, sh, mh);
-        const float scf = __half2float(sh), mnf = __half2float(mh);
-        const int code = int2_code(acc, mnf, scf);
-        const uint32_t byte = int2_gather_byte(code, lane);
-        const int grp = warp & 3;
-        if (ok) {
-            uint8_t* tile = cache + ((size_t)pid * H_kv + h) * INT2_TILE;
-            if ((lane & 3) == 0) tile[(side ? OFF_VC : OFF_KC) + 32 * slot + 4 * (lane >> 2) + grp] = (uint8_t)byte;
-            if (lane == 0) int2_store_meta(tile, side, slot, grp, sh, mh);
-        }
-        xhat = fmaf((float)code, scf, mnf);  // the level the cache now holds
-    }
-    // the key's logit for each head: sum_j q'_j xhat_j, q' = q R_k (thread j
-    // holds column j of R_k); the value stays in the rotated basis
-    float part[MAXG];
+    return fmaf((float)code, scf, mnf);
+}
+
+// The new token as one more row of this CTA's warp partials: logit
+// q~ . k^ per head (q~ the rotated, scaled query in qt, k^ held by threads
+// j < 128), l = 1, o' = v^ (threads 128 + j, rotated basis); an empty row when
+// the token was not written.  fac is scratch [MAXG][>= 4].  All threads call
+// it; it ends with a barrier.
+template <int NW, int MAXG>
+__device__ __forceinline__ void new_token_row(MergeSmem<NW, MAXG>& ms, float (*o_row)[D], const float (*qt)[D],
+                                              float xhat, bool ok, int G) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 #pragma unroll
     for (int jj = 0; jj < MAXG; ++jj) {
-        float v = qp[jj] * xhat;
+        float v = (tid < D && jj < G) ? qt[jj][tid] * xhat : 0.f;
 #pragma unroll
         for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        part[jj] = v;
+        if (lane == 0 && warp < 4) ms.fac[jj][warp] = v;
     }
-    // per-warp partial dots of the four key warps, summed below
-    if (lane == 0 && warp < 4) {
-#pragma unroll
-        for (int jj = 0; jj < MAXG; ++jj) ms.fac[jj][warp] = part[jj];
-    }
-    if (worker && side == 1) {
-#pragma unroll
-        for (int jj = 0; jj < MAXG; ++jj)
-            if (jj < G) vout[jj][j] = ok ? xhat : 0.f;
+    if (tid >= D && tid < 2 * D) {
+        for (int jj = 0; jj < G; ++jj) o_row[jj][tid - D] = ok ? xhat : 0.f;
     }
     __syncthreads();
     if (tid < G) {
-        const float lg = (ms.fac[tid][0] + ms.fac[tid][1] + ms.fac[tid][2] + ms.fac[tid][3]) * scale_log2;
-        ms.Mh[tid] = ok ? lg : -CUDART_INF_F;
-        ms.Lh[tid] = ok ? 1.f : 0.f;
+        ms.m_part[NW][tid] = ok ? ms.fac[tid][0] + ms.fac[tid][1] + ms.fac[tid][2] + ms.fac[tid][3] : -CUDART_INF_F;
+        ms.l_part[NW][tid] = ok ? 1.f : 0.f;
     }
     __syncthreads();
-    return ok;
 }
 
 // Test hook: CTA 0 leaves the bulk copy of its first page unissued (the unit
@@ -287,10 +249,10 @@ constexpr int DBG_DROP_FIRST_COPY = 1;
 constexpr int FLAG_EARLY_INPUTS = 2;
 constexpr long long DBG_WAIT_LIMIT_CYCLES = 2000000LL;
 
-// Grid: n_cta page CTAs, then (MODE != MODE_CACHE) one CTA per unit for the
-// BF16 window or the new token.  In MODE_STEP, k_new / v_new are the decode
-// token's [B][H_kv][d] key and value, appended at position ctx - 1 (win_k and
-// win_v carry them).
+// Grid: n_cta page CTAs, then (MODE_WINDOW) one CTA per unit for its BF16
+// window.  In MODE_STEP, k_new / v_new are the decode token's [B][H_kv][d] key
+// and value (win_k and win_v carry them), appended at position ctx - 1 by the
+// page CTA whose share holds that position.
 template <int NT, int MODE>
 __global__ void __launch_bounds__(DecWarps<NT>::NW * 32, 1)
 decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv, int G,
@@ -299,8 +261,8 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
                    const float* __restrict__ Rv, const float* __restrict__ mu,
                    const __nv_bfloat16* __restrict__ win_k, const __nv_bfloat16* __restrict__ win_v,
                    const int32_t* __restrict__ win_lens, int win_max, float scale_log2, float* __restrict__ out,
-                   uint8_t* __restrict__ ws, int n_cta, int flags) {
-    constexpr bool EXTRA = MODE != MODE_CACHE;
+                   uint8_t* __restrict__ ws, int n_cta, int vmp, int flags) {
+    constexpr bool EXTRA = MODE == MODE_WINDOW;  // one window CTA per unit after the page CTAs
     extern __shared__ __align__(128) uint8_t smem_raw[];
     constexpr int MAXG = 4 * NT;
     constexpr int NW = DecWarps<NT>::NW;
@@ -319,10 +281,10 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
         // publish this CTA's slot (already written), then the last CTA merges;
         // the partials of unit u are the page CTAs' slots u + c, then (with a
         // window or a new token) the slot of its extra CTA
-        const PageSplit sp{(int64_t)B * H_kv * max_pages, n_cta, max_pages};
+        const PageSplit sp{(int64_t)B * H_kv * vmp, n_cta, vmp};
         const int units = B * H_kv;
-        const int c0 = sp.cta_of((int64_t)u * max_pages);
-        const int n = sp.cta_of((int64_t)u * max_pages + max_pages - 1) - c0 + 1;
+        const int c0 = sp.cta_of((int64_t)u * vmp);
+        const int n = sp.cta_of((int64_t)u * vmp + vmp - 1) - c0 + 1;
         const int expected = n + (EXTRA ? 1 : 0);
         int32_t* tickets = reinterpret_cast<int32_t*>(ws + WS_HEADER);
         if (!arrive_last(sm.ms, tickets + u, expected)) return;
@@ -334,40 +296,6 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
         if (tid == 0) tickets[u] = 0;
     };
 
-    if constexpr (MODE == MODE_STEP) {
-        if (blockIdx.x >= n_cta) {
-            const int units = B * H_kv;
-            const int u = blockIdx.x - n_cta, b = u / H_kv, h = u % H_kv;
-            if (tid < D) {
-                prefetch_l2(Rk + (size_t)h * D * D + (size_t)tid * D);
-                prefetch_l2(Rv + (size_t)h * D * D + (size_t)tid * D);
-            }
-            griddep_wait();
-            griddep_launch_dependents();
-            int ctx = __ldg(context_lens + b);
-            ctx = max(0, min(ctx, max_pages * PAGE));
-            bool ok = false;
-            if (ctx > 0) {
-                const int t_new = ctx - 1;
-                const int pid = __ldg(block_table + (size_t)b * max_pages + t_new / PAGE);
-                ok = step_token_partial<NW, MAXG>(sm.ms, sm.q, sm.o_part[0], q, win_k, win_v, mu, Rk, Rv, cache,
-                                                  num_pages, pid, t_new % PAGE, H_q, H_kv, G, b, h, scale_log2,
-                                                  sm.ms.o_final);
-                if (!ok && tid == 0) atomicOr(reinterpret_cast<uint32_t*>(ws), ERR_BAD_PAGE);
-            }
-            float* slot = slot_ptr((int64_t)units + n_cta + u);
-            if (ok) {
-                // the token's value is in the R_v basis: carry it to the output basis
-                float4 rr[RowPrefetch<NW, MAXG>::N];
-                load_rows<NW>(Rv + (size_t)h * D * D, rr);
-                rotate_publish<NW, MAXG>(sm.ms, rr, G, Rv + (size_t)h * D * D, slot);
-            } else {
-                publish_slot<NW, MAXG>(sm.ms, sm.ms.o_final, G, slot, true);
-            }
-            finish_unit(u);
-            return;
-        }
-    }
     if constexpr (MODE == MODE_WINDOW) {
         if (blockIdx.x >= n_cta) {
             // BF16 window of unit u: attended exactly in the original basis,
@@ -389,9 +317,9 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
     const int cta = blockIdx.x;
     int u_first;
     {
-        const PageSplit sp{(int64_t)B * H_kv * max_pages, n_cta, max_pages};
+        const PageSplit sp{(int64_t)B * H_kv * vmp, n_cta, vmp};
         const int64_t g0 = sp.start(cta);
-        u_first = (int)(g0 / max_pages);
+        u_first = (int)(g0 / vmp);
         if (tid == 0) {
             // the share bounds live in shared memory, so the page loop below
             // holds no registers for them
@@ -416,7 +344,7 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
             prefetch_l2(rk + 128 * l);
             prefetch_l2_keep(rv + 128 * l);
         }
-        const int pa = (int)(g0 - (int64_t)u_first * max_pages);
+        const int pa = (int)(g0 - (int64_t)u_first * vmp);
         const int j = pa + warp + NW * lane;
         if (lane < DEC_STAGES + UNIT_PAGES && j < max_pages) prefetch_l2(block_table + (size_t)b * max_pages + j);
         if (tid == 0) prefetch_l2(context_lens + b);
@@ -436,10 +364,12 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
     // the page loop for registers.
     auto segment = [&](int u, bool second) {
         const int b = u / H_kv, h = u % H_kv;
-        const int64_t ubase = (int64_t)u * max_pages;
+        const int64_t ubase = (int64_t)u * vmp;
         const int64_t g0 = sm.share[0], g1 = sm.share[1];
-        const bool last_seg = g1 <= ubase + max_pages;  // this CTA's share ends in unit u
-        const int pa = (int)(max(g0, ubase) - ubase), pb = (int)(min(g1, ubase + max_pages) - ubase);
+        const bool last_seg = g1 <= ubase + vmp;  // this CTA's share ends in unit u
+        // the share's pages of unit u: [pa, pb) of its vmp virtual pages (the
+        // pages past max_pages, a decode step's balance, carry no work)
+        const int pa = (int)(max(g0, ubase) - ubase), pb = (int)(min(g1, ubase + vmp) - ubase);
         const int32_t* bt = block_table + (size_t)b * max_pages;
         // pages pa .. pe - 1 of the unit (pe: the share's end or the context's),
         // dealt round-robin over the warps
@@ -452,7 +382,7 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
         int pid_first[DEC_UNITS];
         int pid_next = 0;
         {
-            const int cs = pb - pa, my_share = cs > warp ? (cs - warp + NW - 1) / NW : 0;
+            const int cs = min(pb, max_pages) - pa, my_share = cs > warp ? (cs - warp + NW - 1) / NW : 0;
 #pragma unroll
             for (int k = 0; k < DEC_UNITS; ++k) pid_first[k] = 0;
             if (lane < UNIT_PAGES) {
@@ -468,18 +398,24 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
             }
         }
         ctx = max(0, min(ctx, max_pages * PAGE));
-        if (MODE == MODE_STEP) ctx = max(ctx - 1, 0);  // the new token is attended by its own CTA
+        // the decode step's new token sits at position ctx - 1: the pages hold
+        // the ctx - 1 tokens before it, and the CTA whose share holds its page
+        // quantises, writes and attends it
+        const int ctx_all = ctx;
+        if (MODE == MODE_STEP) ctx = max(ctx - 1, 0);
+        const int p_new = (ctx_all - 1) / PAGE;
+        const bool has_new = MODE == MODE_STEP && ctx_all > 0 && p_new >= pa && p_new < pb;
         const int n_pages = (ctx + PAGE - 1) / PAGE;
         const int pe = min(pb, n_pages);
         // no cached page of this unit in this CTA's share (or a wait ran out
-        // earlier): the segment publishes an empty partial
+        // earlier): nothing to stream
         const bool empty = pe <= pa || sm.dead;
-        if (!empty) {
-        const int count = pe - pa;
+        if (!empty || has_new) {
+        const int count = empty ? 0 : pe - pa;
         const int my_count = count > warp ? (count - warp + NW - 1) / NW : 0;
 
         float4 rr[RowPrefetch<NW, MAXG>::N];
-        load_rows<NW>(Rk + (size_t)h * D * D, rr);
+        if constexpr (MODE != MODE_STEP) load_rows<NW>(Rk + (size_t)h * D * D, rr);
         float qv[QPT];
         auto load_q = [&]() {
             const __nv_bfloat16* qb = q + ((size_t)b * H_q + (size_t)h * G) * D;
@@ -545,7 +481,34 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
         // the rest of this share of the block table is read one entry at a
         // time during the loop: have L2 fetch it now (every address is an
         // entry of the share, so no line past the table is touched)
-        for (int i = pa + 32 * tid; i < pe + 31; i += 32 * NW * 32) prefetch_l2_keep(bt + min(i, pe - 1));
+        for (int i = pa + 32 * tid; i < pa + count + 31; i += 32 * NW * 32) prefetch_l2_keep(bt + min(i, pe - 1));
+        float xhat = 0.f;  // (decode step) the new token's level in this thread's channel
+        bool new_ok = false;
+        if constexpr (MODE == MODE_STEP) {
+            if (has_new) {  // CTA-uniform
+                const int tsl = (ctx_all - 1) % PAGE;
+                float rcol[D];
+                if (tid < 2 * D) {
+                    const float* R = (tid < D ? Rk : Rv) + (size_t)h * D * D + (tid & (D - 1));
+#pragma unroll
+                    for (int i = 0; i < D; ++i) rcol[i] = __ldg(R + (size_t)i * D);
+                }
+                const int pid_new = __ldg(bt + p_new);
+                new_ok = pid_new >= 0 && (int64_t)pid_new < num_pages;
+                if (early) griddep_wait();  // the new token comes from the previous kernel
+                if (tid < D) {
+                    const size_t row = ((size_t)b * H_kv + h) * D + tid;
+                    sm.q[0][tid] = __fsub_rn(__bfloat162float(win_k[row]), __ldg(mu + (size_t)h * D + tid));
+                    sm.q[1][tid] = __bfloat162float(win_v[row]);
+                }
+                __syncthreads();
+                xhat = new_token_codes(sm.q, rcol, cache, H_kv, h, pid_new, tsl, new_ok);
+                if (!new_ok && tid == 0) atomicOr(reinterpret_cast<uint32_t*>(ws), ERR_BAD_PAGE);
+            }
+            // the rows of R_k for the query rotation (after the new token's
+            // columns, so the two never hold registers at once)
+            load_rows<NW>(Rk + (size_t)h * D * D, rr);
+        }
         if (early) {
             // the early inputs are out; the query may come from the previous kernel
             griddep_wait();
@@ -616,6 +579,10 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
             inv_sig[nt] = hq < G ? 16777216.f / sm.sigma[hq] : 0.f;
 #pragma unroll
             for (int g = 0; g < NGROUP; ++g) gsum[nt][g] = hq < G ? sm.gsum[hq][g] : 0.f;
+        }
+
+        if constexpr (MODE == MODE_STEP) {
+            if (has_new) new_token_row<NW, MAXG>(sm.ms, sm.o_part[NW], sm.q, xhat, new_ok, G);
         }
 
         float oacc[8][4];
@@ -951,7 +918,10 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
             }
         }
         __syncthreads();
-        merge_warps<NW, MAXG>(sm.ms, sm.o_part, G);
+        if (MODE == MODE_STEP && has_new)
+            merge_warps<NW, MAXG, NW + 1>(sm.ms, sm.o_part, G);
+        else
+            merge_warps<NW, MAXG>(sm.ms, sm.o_part, G);
         kbase += n_units;
         // the next kernel in the stream may be scheduled once every CTA is here
         if (last_seg) griddep_launch_dependents();
@@ -966,7 +936,7 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
         __syncthreads();  // the next segment reuses the ring and the merge scratch
     };
     segment(u_first, false);
-    if (sm.share[1] > (int64_t)(u_first + 1) * max_pages) segment(u_first + 1, true);
+    if (sm.share[1] > (int64_t)(u_first + 1) * vmp) segment(u_first + 1, true);
 }
 
 }  // namespace kvq
@@ -1034,6 +1004,13 @@ static int64_t int2_page_ctas(int B, int H_kv, int max_pages, int num_splits, bo
     return C;
 }
 
+// Virtual pages per unit of a decode step: in a decode step the CTA holding
+// a sequence's new token also quantises and attends it (a few microseconds,
+// about as long as streaming ~100 pages), so each unit gets that many
+// virtual pages without work after its last page, and the share holding a
+// full sequence's last page streams fewer real ones.
+static int step_virtual_pages(int max_pages) { return max_pages + (max_pages < 96 ? max_pages : 96); }
+
 extern "C" int kvq_decode_auto_splits(int B, int H_q, int H_kv, int max_pages_per_seq) {
     if (B <= 0 || H_kv <= 0 || H_q < H_kv || max_pages_per_seq <= 0) return 1;
     // at most one wave of CTAs, one per SM, over the (sequence, KV head)
@@ -1064,9 +1041,11 @@ extern "C" size_t kvq_decode_workspace_bytes(int B, int H_q, int H_kv, int max_p
         slots = ((int64_t)num_splits + 2) * units;
     } else {  // room for the automatic choice of every decode entry point
         const int64_t plain = units + int2_page_ctas(B, H_kv, max_pages_per_seq, 0, false);
+        const int64_t step = units + int2_page_ctas(B, H_kv, step_virtual_pages(max_pages_per_seq), 0, false);
         const int64_t win = 2 * units + int2_page_ctas(B, H_kv, max_pages_per_seq, 0, true);
         const int64_t bg = units * bgtq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
         slots = plain > win ? plain : win;
+        if (step > slots) slots = step;
         if (bg > slots) slots = bg;
     }
     return int2_workspace_bytes(B, H_q, H_kv, slots);
@@ -1080,7 +1059,7 @@ extern "C" void kvq_debug_drop_next_copy(void) { g_debug_flags.store(DBG_DROP_FI
 
 // A validated INT2 decode launch.
 struct Int2Plan {
-    int G = 0, C = 0, grid = 0, threads = 0, mode = MODE_CACHE;
+    int G = 0, C = 0, grid = 0, threads = 0, mode = MODE_CACHE, vmp = 0;
     size_t smem = 0, need = 0;
 };
 
@@ -1120,9 +1099,12 @@ static kvq_status decode_int2_plan(const char* fn, int mode, const void* q, int 
     }
     if (mode == MODE_STEP && (!win_k || !win_v || !mu_k))
         return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: null k_new, v_new or mu_k", fn);
-    const bool extra = mode != MODE_CACHE;
+    const bool extra = mode == MODE_WINDOW;  // one window CTA per unit
     const int64_t units = (int64_t)B * H_kv;
-    const int64_t C = int2_page_ctas(B, H_kv, max_pages_per_seq, num_splits, extra);
+    const int vmp = mode == MODE_STEP ? step_virtual_pages(max_pages_per_seq) : max_pages_per_seq;
+    if ((int64_t)B * H_kv * vmp > (int64_t(1) << 40))
+        return kvq_set_error(KVQ_ERR_UNSUPPORTED, "%s: B * H_kv * max_pages above 2^40", fn);
+    const int64_t C = int2_page_ctas(B, H_kv, vmp, num_splits, extra);
     // a unit's partials: the page CTAs over its pages (its share of the
     // virtual pages spans at most ceil(C / units) + 1 of them) and the window
     if ((C + units - 1) / units + 2 > MAX_SPLITS)
@@ -1135,6 +1117,7 @@ static kvq_status decode_int2_plan(const char* fn, int mode, const void* q, int 
     plan.C = (int)C;
     plan.grid = (int)grid;
     plan.mode = mode;
+    plan.vmp = vmp;
     plan.threads = (G <= 4 ? NW1 : NW2) * 32;
     plan.smem = G <= 4 ? sizeof(DecodeSmem<NW1, 4>) : sizeof(DecodeSmem<NW2, 8>);
     plan.need = int2_workspace_bytes(B, H_q, H_kv, units + C + (extra ? units : 0));
@@ -1162,7 +1145,7 @@ static kvq_status decode_int2_launch(const Int2Plan& plan, const void* q, int B,
         static_cast<const __nv_bfloat16*>(q), B, H_q, H_kv, plan.G, static_cast<uint8_t*>(cache), num_pages,
         block_table, max_pages_per_seq, context_lens, R_k, R_v, mu_k, static_cast<const __nv_bfloat16*>(win_k),
         static_cast<const __nv_bfloat16*>(win_v), win_lens, win_max, scale_log2, out,
-        static_cast<uint8_t*>(workspace), plan.C, flags);
+        static_cast<uint8_t*>(workspace), plan.C, plan.vmp, flags);
     return kvq_check_cuda(e, "decode launch");
 }
 

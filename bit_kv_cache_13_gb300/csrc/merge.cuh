@@ -47,8 +47,8 @@ struct RowPrefetch {
 // 16-byte aligned: o_final and red are read and written as float4 rows.
 template <int NW, int MAXG>
 struct __align__(16) MergeSmem {
-    float m_part[NW][MAXG];
-    float l_part[NW][MAXG];
+    float m_part[NW + 1][MAXG];  // per warp, and one more row for a lone token's partial
+    float l_part[NW + 1][MAXG];
     float o_final[MAXG][D];
     float red[RotSplit<NW>::NR][MAXG][D];  // cross-warp partial sums
     float fac[MAXG][MAX_SPLITS];           // per-split maxima, then weights 2^(m_s - M)
@@ -313,16 +313,18 @@ __device__ __forceinline__ void finish_decode(MergeSmem<NW, MAXG>& ms, const flo
 // Every thread of the CTA calls it once the warps' (m, l, o') are in shared
 // memory (after a barrier); each thread forms the weights of its own head,
 // so one barrier, at the end, suffices.
-template <int NW, int MAXG>
+// ROWS (NW or NW + 1) rows of (m, l, o') are combined.
+template <int NW, int MAXG, int ROWS = NW>
 __device__ __forceinline__ void merge_warps(MergeSmem<NW, MAXG>& ms, const float (*o_part)[MAXG][D], int G) {
+    static_assert(ROWS <= NW + 1, "merge rows");
     for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
         const int jj = idx / D, c = idx % D;
         float M = -CUDART_INF_F;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, ms.m_part[w][jj]);
+        for (int w = 0; w < ROWS; ++w) M = fmaxf(M, ms.m_part[w][jj]);
         float O = 0.f, L = 0.f;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) {
+        for (int w = 0; w < ROWS; ++w) {
             const float f = M == -CUDART_INF_F ? 0.f : ex2(ms.m_part[w][jj] - M);
             O = fmaf(o_part[w][jj][c], f, O);
             L = fmaf(ms.l_part[w][jj], f, L);

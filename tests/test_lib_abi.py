@@ -56,7 +56,8 @@ def test_workspace_with_auto_splits_holds_every_entry_point(cpu_lib):
     decode call: the INT2 decode's slots (one per unit and page CTA, at most
     units + C - 1 with C = one CTA per SM (152 where no device is visible),
     at least one per unit and at most one per 32 pages), the BF16-window
-    form's extra slot per unit, and Block-GTQ's per-unit splits."""
+    form's extra slot per unit, the decode step's (whose units carry up to 96
+    more virtual pages) and Block-GTQ's per-unit splits."""
     nsm = 152
     for B, H_kv, pages in [(1, 8, 8192), (8, 8, 2048), (3, 2, 40), (64, 8, 256), (1, 1, 17)]:
         H_q = 4 * H_kv
@@ -64,7 +65,10 @@ def test_workspace_with_auto_splits_holds_every_entry_point(cpu_lib):
         V = units * pages
         c_plain = min(max(min(nsm, -(-V // 32)), units), V)
         c_win = min(max(min(nsm - units if 2 * units <= nsm else nsm, -(-V // 32)), units), V)
-        slots = max(units + c_plain, 2 * units + c_win, units * _lib.kvq_decode_auto_splits(B, H_q, H_kv, pages))
+        vs = units * (pages + min(pages, 96))        # a decode step's virtual pages
+        c_step = min(max(min(nsm, -(-vs // 32)), units), vs)
+        slots = max(units + c_plain, 2 * units + c_win, units + c_step,
+                    units * _lib.kvq_decode_auto_splits(B, H_q, H_kv, pages))
         header = 256 + -(-units * 4 // 256) * 256
         ws0 = _lib.kvq_decode_workspace_bytes(B, H_q, H_kv, pages, 0)
         assert ws0 == header + slots * 4 * 132 * 4
