@@ -2,33 +2,33 @@
 """Benchmark: packed-KV decode attention over the rotated INT2 cache.
 
 Workload (default): Qwen3-8B-shaped decode step, 36 layers x (32 q / 8 KV
-heads, d = 128), batch 1, 128K context.  One step = for every layer, the
-quantise-on-append of the new token (kvq_append_int2) followed by fused
-packed-cache decode attention (kvq_decode_attn_int2); the 72 launches are
-replayed as one CUDA graph.  Inputs are synthetic and seeded; every cache
-is prefilled through the library's own append call before timing.
+heads, d = 128), batch 1, 128K context.  One step = for every layer, one
+launch of kvq_decode_step_int2: the quantise-on-append of the new token and
+the fused packed-cache decode attention over the 128K tokens; the 36
+launches are replayed as one CUDA graph.  Inputs are synthetic and seeded;
+every cache is prefilled through the library's own append call before
+timing.
 
 Prints one JSON line.  `value` is achieved algorithmic bandwidth (packed
 cache bytes + q/out + new-token traffic per step / device time per step,
 summed over ranks); `e2e` is the same metric through the C ABI with the
 step's inputs copied from pinned host memory and its outputs copied back
-inside the timed region; `roofline` is the decode kernel alone (CUDA events
-around each launch); `bgtq` is the Block-GTQ K3V3 decode at 128K measured
-the same way; `cpu_baseline` is the fp64 oracle on a bounded sample.
+inside the timed region; `roofline` is the step kernel alone (36 launches
+between one pair of CUDA events); `bgtq` is the Block-GTQ K3V3 decode at
+128K; `sweep70b`, `llama8b` and `tiny` are single decode launches of the
+other workloads with an L2 flush before each; `cpu_baseline` is the fp64
+oracle on a bounded sample.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
 from __future__ import annotations
 
 import os
-
-for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
-    os.environ.setdefault(_v, "1")
-
 import argparse
 import hashlib
 import json
 import math
+import platform
 import statistics
 import subprocess
 import sys
@@ -256,33 +256,57 @@ def time_launches(stream, fn, n):
     return statistics.mean(a.elapsed_time(b) for a, b in evs)
 
 
-def measure_int2_gqa8(device, stream, reps):
-    """INT2 decode on the GQA-8 sweep shape (64 q / 8 KV heads, Llama-3-70B
-    style) at batch 8 and 131072 tokens: 805 MB of cache per launch, larger
-    than L2, launches back to back."""
-    spec = inputs.sweep70b_spec(8, 131072)
+def measure_int2_decode(spec, device, stream, reps, step=False):
+    """One INT2 layer of `spec` decoded (kvq_decode_attn_int2, automatic split)
+    or, with step=True, one fused decode step (kvq_decode_step_int2): a 256
+    MB L2 flush before each timed launch, so the cache streams from HBM even
+    when it would fit L2.  Returns ms per launch, GB/s of the packed cache +
+    q/out and the fraction of the measured HBM bandwidth."""
     layer = Int2Layer(spec, 0, device=device)
     layer.prefill()
     q = layer.queries()
     out = torch.zeros((spec.batch, spec.h_q, spec.d), dtype=torch.float32, device=device)
     ws = layer.workspace()
-    call = lambda: _lib.kvq_decode_attn_int2(q, layer.cache, layer.num_pages, layer.block_table,
-                                             layer.context_lens, layer.R_k, layer.R_v, layer.scale, out, ws)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    if step:
+        k_new, v_new = layer.new_kv()
+        call = lambda: _lib.kvq_decode_step_int2(q, k_new, v_new, layer.cache, layer.num_pages, layer.block_table,
+                                                 layer.context_lens, layer.mu, layer.R_k, layer.R_v, layer.scale,
+                                                 out, ws)
+    else:
+        call = lambda: _lib.kvq_decode_attn_int2(q, layer.cache, layer.num_pages, layer.block_table,
+                                                 layer.context_lens, layer.R_k, layer.R_v, layer.scale, out, ws)
     for _ in range(3):
         call()
-    ms = statistics.median(time_launches(stream, call, 5) for _ in range(reps))
+    durs = []
+    for _ in range(reps):
+        flush.zero_()
+        durs.append(time_launches(stream, call, 1))
+    ms = statistics.median(durs)
     nbytes = layer.packed_bytes_per_decode() + spec.batch * spec.h_q * spec.d * 6
-    peak, kind = peaks()
+    peak, _ = peaks()
     gbs = nbytes / (ms * 1e-3) / 1e9
-    out_line = {"workload": "sweep70b: 64 q / 8 KV heads, batch 8, 131072 ctx, INT2 cache",
-                "kernel": "decode_int2_kernel<2>", "ms_per_decode": round(ms, 4), "value": round(gbs, 2),
-                "unit": "GB/s", "splits": _lib.kvq_decode_auto_splits(spec.batch, spec.h_q, spec.h_kv,
-                                                                      layer.block_table.shape[1]),
-                "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peak, "unit": "GB/s",
-                             "frac": round(gbs / peak, 4), "peak_kind": kind}}
     del layer
     torch.cuda.empty_cache()
-    return out_line
+    return {"batch": spec.batch, "ctx": spec.ctx, "us_per_launch": round(ms * 1e3, 2), "value": round(gbs, 2),
+            "frac": round(gbs / peak, 4), "bytes": nbytes}
+
+
+SWEEP70B = [(B, T) for B in (1, 8, 32, 64) for T in (4096, 32768, 131072)] + [(1, 262144), (1, 524288)]
+
+
+def measure_int2_sweep70b(device, stream, reps):
+    """The 70B-class GQA-8 grid (64 q / 8 KV heads, INT2 K/V): batch {1, 8,
+    32, 64} x context {4K, 32K, 128K}, plus batch 1 at 256K and 512K; one
+    decode launch per point, L2 flushed before each.  Points whose cache
+    fits L2 many times over (batch 1 at 4K, ~3 MB) are latency-bound and
+    reported, not held to the HBM roofline."""
+    peak, kind = peaks()
+    pts = [measure_int2_decode(inputs.sweep70b_spec(B, T), device, stream, reps) for B, T in SWEEP70B]
+    return {"workload": "sweep70b: 64 q / 8 KV heads, d=128, INT2 K/V groups of 32 + fp16 scale/min, "
+                        "batch x context grid", "kernel": "decode_int2_kernel<2>", "unit": "GB/s",
+            "peak": peak, "peak_kind": kind, "points": pts,
+            "l2": "256 MB buffer written before every timed launch"}
 
 
 def measure_bgtq(device, stream, reps):
@@ -365,8 +389,16 @@ def measure_int2_window(spec, device, stream, reps):
     return out_line
 
 
-# 128 fp32 lanes per SM x 152 SMs x 2 flop per fma at the 2070 MHz maximum SM clock
-FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+def fp32_peak_tflops():
+    """Derived fp32 fma peak of the device: 128 fp32 lanes per SM x SMs x 2
+    flop per fma at the maximum SM clock (MEASURED_PEAKS.json, else 2070 MHz)."""
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    mhz = 2070.0
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            mhz = float(json.load(f).get("sm_max_mhz", mhz))
+    return sms * 128 * 2 * mhz * 1e6 / 1e12, f"derived: {sms} SMs x 128 fp32 lanes x 2 flop x {mhz / 1e3:.2f} GHz"
 
 
 def measure_append_prefill(spec, device, stream, reps):
@@ -384,12 +416,12 @@ def measure_append_prefill(spec, device, stream, reps):
     ms = statistics.median(time_launches(stream, call, 1) for _ in range(reps))
     th = k.shape[0] * spec.h_kv
     tflops = th * 2 * 2 * spec.d * spec.d / (ms * 1e-3) / 1e12
+    peak_tf, peak_kind = fp32_peak_tflops()
     out = {"workload": f"{spec.name}: one layer, {k.shape[0]} tokens x {spec.h_kv} KV heads appended in one call",
            "kernel": "append_int2_prefill_kernel", "ms_per_layer": round(ms, 4),
            "value": round(th / (ms * 1e-3) / 1e6, 2), "unit": "M token-heads/s",
-           "roofline": {"bound": "alu", "achieved": round(tflops, 3), "peak": round(FP32_PEAK_TFLOPS, 1),
-                        "unit": "TFLOP/s", "frac": round(tflops / FP32_PEAK_TFLOPS, 4),
-                        "peak_kind": "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz"},
+           "roofline": {"bound": "alu", "achieved": round(tflops, 3), "peak": round(peak_tf, 1),
+                        "unit": "TFLOP/s", "frac": round(tflops / peak_tf, 4), "peak_kind": peak_kind},
            "bytes_per_token_head": {"read": 2 * 2 * spec.d, "written": 96}}
     del layer, k, v
     torch.cuda.empty_cache()
@@ -398,32 +430,55 @@ def measure_append_prefill(spec, device, stream, reps):
 
 # ------------------------------------------------------------------ CPU oracle
 
+def host_cpu():
+    """Host cores this process may use and the CPU model (as far as the OS says)."""
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        cores = os.cpu_count() or 1
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "Model", "CPU part"):
+            for line in info.splitlines():
+                if line.split(":")[0].strip() == key:
+                    model = line.split(":", 1)[1].strip()
+                    break
+            if model:
+                break
+    except OSError:
+        pass
+    return cores, f"{platform.machine()} {model}".strip()
+
+
 class OracleSample:
-    """The fp64 oracle on one (layer, KV head) of the same workload.  The
-    head's cache is built untimed; a step is the oracle's new-token append
-    plus the decode of that head's query group over the full context."""
+    """The fp64 oracle on one (layer, KV head) of the same workload, set up
+    from the seeded input generators alone (no GPU, no library).  The head's
+    cache is built untimed; a step is the oracle's new-token append plus the
+    decode of that head's query group over the full context."""
 
     def __init__(self, spec, layer_idx, h):
         from oracle import int2
         self.int2, self.spec, self.h = int2, spec, h
-        layer = Int2Layer(spec, layer_idx, device="cpu")
-        k, v = layer.history_kv(0, device="cpu")
+        d, g, T = spec.d, spec.g, spec.ctx
+        pos = history_positions(spec)
+        k = inputs.gen_keys(spec, layer_idx, 0, pos)
+        v = inputs.gen_values(spec, layer_idx, 0, pos.numel())
         self.mu = inputs.key_centre(k).numpy()[h:h + 1]
-        k_new, v_new = layer.new_kv(device="cpu")
-        self.k_new = k_new[0:1, h:h + 1].float().numpy()
-        self.v_new = v_new[0:1, h:h + 1].float().numpy()
-        g = spec.g
-        self.q = layer.queries(device="cpu").double().numpy()[0:1, h * g:(h + 1) * g]
-        T = spec.ctx
-        self.bt = layer.block_table.cpu().numpy()[0:1]
+        self.k_new = inputs.gen_keys(spec, layer_idx, 0, torch.tensor([T - 1]), tag="new")[:, h:h + 1].float().numpy()
+        self.v_new = inputs.gen_values(spec, layer_idx, 0, 1, tag="new")[:, h:h + 1].float().numpy()
+        self.q = inputs.gen_queries(spec, layer_idx).double().numpy()[0:1, h * g:(h + 1) * g]
+        bt = inputs.block_tables(spec).numpy()
+        self.bt = bt[0:1]
         self.slots = np.array([self.bt[0, t // 16] * 16 + t % 16 for t in range(T)])
-        self.rk = layer.R_k[h:h + 1].cpu().numpy()
-        self.rv = layer.R_v[h:h + 1].cpu().numpy()
-        self.cache = int2.new_cache(layer.num_pages, 1)
+        self.rk = inputs.head_rotation(d, spec.name, layer_idx, h, "Rk").astype(np.float32)[None]
+        self.rv = inputs.head_rotation(d, spec.name, layer_idx, h, "Rv").astype(np.float32)[None]
+        self.cache = int2.new_cache(int(bt.max()) + 1, 1)
         int2.append(self.cache, k[:, h:h + 1].float().numpy(), v[:, h:h + 1].float().numpy(), self.slots[:-1],
                     self.mu, self.rk, self.rv, exact_chain=False)
         self.label = f"layer {layer_idx} kv-head {h}"
-        self.nbytes = T * TOKEN_HEAD_BYTES + g * spec.d * 6 + (2 * spec.d * 2 + TOKEN_HEAD_BYTES)
+        self.nbytes = T * TOKEN_HEAD_BYTES + g * d * 6 + (2 * d * 2 + TOKEN_HEAD_BYTES)
 
     def step(self) -> float:
         t0 = time.perf_counter()
@@ -476,7 +531,8 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.median(times), 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_dict(spec, args, 1, l2="oracle on host cores"),
-        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": host_cpu()[0], "cpu": host_cpu()[1],
+                         "kind": "oracle",
                          "sample": f"per step: new-token append + decode of one (layer, KV head) at {spec.ctx} "
                                    f"tokens ({smp.label}); bytes = that head's packed cache + q/out"},
         "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -586,13 +642,31 @@ def run_ours(args, world, rank, local):
         if not args.no_bgtq:
             line["bgtq"] = measure_bgtq(device, stream, reps=max(3, min(args.steps, 10)))
         line["append_prefill"] = measure_append_prefill(spec, device, stream, reps=3)
-        line["gqa8"] = measure_int2_gqa8(device, stream, reps=3)
+        sweep = measure_int2_sweep70b(device, stream, reps=3)
+        line["sweep70b"] = sweep
+        g8 = next(p for p in sweep["points"] if p["batch"] == 8 and p["ctx"] == 131072)
+        line["gqa8"] = {"workload": "sweep70b: 64 q / 8 KV heads, batch 8, 131072 ctx, INT2 cache",
+                        "kernel": "decode_int2_kernel<2>", "ms_per_decode": round(g8["us_per_launch"] / 1e3, 4),
+                        "value": g8["value"], "unit": "GB/s",
+                        "roofline": {"bound": "hbm", "achieved": g8["value"], "peak": sweep["peak"], "unit": "GB/s",
+                                     "frac": g8["frac"], "peak_kind": sweep["peak_kind"]}}
+        ll = measure_int2_decode(inputs.SPECS["llama8b"], device, stream, reps=5)
+        line["llama8b"] = {"workload": "llama8b: 32 q / 8 KV heads, batch 8, 32768 ctx (post-RoPE keys, theta 5e5), "
+                                       "INT2 cache", "kernel": "decode_int2_kernel<1>", **ll, "unit": "GB/s",
+                           "l2": "256 MB buffer written before every timed launch"}
+        ti = measure_int2_decode(inputs.SPECS["tiny"], device, stream, reps=10, step=True)
+        line["tiny"] = {"workload": "tiny: 1 KV head, 4 q heads, batch 1, 256 cached tokens + 1 decode token, one "
+                                    "fused decode step", "kernel": "decode_int2_kernel<1> (step)", **ti,
+                        "unit": "GB/s", "bound": "latency (24 KB of cache)",
+                        "l2": "256 MB buffer written before every timed launch"}
         line["window"] = measure_int2_window(spec, device, stream, reps=5)
     if rank == 0 and not args.no_cpu_baseline:
         gbs, el, sample = oracle_baseline(spec)
-        line["cpu_baseline"] = {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        cores, cpu = host_cpu()
+        line["cpu_baseline"] = {"value": round(gbs, 6), "unit": "GB/s", "cores": cores, "cpu": cpu,
+                                "kind": "oracle",
                                 "sample": f"{sample}: new-token append + decode at {spec.ctx} tokens, "
-                                          f"{el:.1f} s of fp64 numpy on one host core"}
+                                          f"{el:.1f} s of fp64 numpy (BLAS on the process's {cores} host cores)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
