@@ -540,6 +540,31 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def measure_extras(line, spec, device, stream):
+    """The sub-measurements beside the headline step: the batched prefill
+    append, the 70B-class grid (and its batch-8 128K point as `gqa8`), the
+    Llama-8B-shaped decode, the tiny fused step and the BF16-window decode."""
+    line["append_prefill"] = measure_append_prefill(spec, device, stream, reps=3)
+    sweep = measure_int2_sweep70b(device, stream, reps=3)
+    line["sweep70b"] = sweep
+    g8 = next(p for p in sweep["points"] if p["batch"] == 8 and p["ctx"] == 131072)
+    line["gqa8"] = {"workload": "sweep70b: 64 q / 8 KV heads, batch 8, 131072 ctx, INT2 cache",
+                    "kernel": "decode_int2_kernel<2>", "ms_per_decode": round(g8["us_per_launch"] / 1e3, 4),
+                    "value": g8["value"], "unit": "GB/s",
+                    "roofline": {"bound": "hbm", "achieved": g8["value"], "peak": sweep["peak"], "unit": "GB/s",
+                                 "frac": g8["frac"], "peak_kind": sweep["peak_kind"]}}
+    ll = measure_int2_decode(inputs.SPECS["llama8b"], device, stream, reps=5)
+    line["llama8b"] = {"workload": "llama8b: 32 q / 8 KV heads, batch 8, 32768 ctx (post-RoPE keys, theta 5e5), "
+                                   "INT2 cache", "kernel": "decode_int2_kernel<1>", **ll, "unit": "GB/s",
+                       "l2": "256 MB buffer written before every timed launch"}
+    ti = measure_int2_decode(inputs.SPECS["tiny"], device, stream, reps=10, step=True)
+    line["tiny"] = {"workload": "tiny: 1 KV head, 4 q heads, batch 1, 256 cached tokens + 1 decode token, one "
+                                "fused decode step", "kernel": "decode_int2_kernel<1> (step)", **ti,
+                    "unit": "GB/s", "bound": "latency (24 KB of cache)",
+                    "l2": "256 MB buffer written before every timed launch"}
+    line["window"] = measure_int2_window(spec, device, stream, reps=5)
+
+
 def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     device = f"cuda:{local}"
@@ -565,12 +590,14 @@ def run_ours(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        torch.cuda.nvtx.range_push("step_timed")   # lets a profiler pick out the timed launches
         with torch.cuda.stream(stream):
             ev[0].record(stream)
             for i in range(args.steps):
                 graph.replay()
                 ev[i + 1].record(stream)
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
     barrier(world)
     step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
     total_ms = max_over_ranks(ev[0].elapsed_time(ev[-1]), world)
@@ -591,7 +618,7 @@ def run_ours(args, world, rank, local):
     dec_avg_ms = statistics.median(dec_ms)
     peak, peak_kind = peaks()
     achieved = (st.bytes_per_decode() + st.bytes_per_append()) / (dec_avg_ms * 1e-3) / 1e9
-    traffic = profiled_traffic("decode_int2", ("decode_int2.cu", "int2_quant.cuh", "merge.cuh", "kvq_common.cuh"),
+    traffic = profiled_traffic("step_int2", ("decode_int2.cu", "int2_quant.cuh", "merge.cuh", "kvq_common.cuh"),
                                st.units_per_decode())
 
     # ---- end to end through the C ABI with host buffers
@@ -639,27 +666,10 @@ def run_ours(args, world, rank, local):
     # stream, so nothing of it overlaps a timed launch
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
-        if not args.no_bgtq:
+        if not args.no_bgtq and not args.no_extras:
             line["bgtq"] = measure_bgtq(device, stream, reps=max(3, min(args.steps, 10)))
-        line["append_prefill"] = measure_append_prefill(spec, device, stream, reps=3)
-        sweep = measure_int2_sweep70b(device, stream, reps=3)
-        line["sweep70b"] = sweep
-        g8 = next(p for p in sweep["points"] if p["batch"] == 8 and p["ctx"] == 131072)
-        line["gqa8"] = {"workload": "sweep70b: 64 q / 8 KV heads, batch 8, 131072 ctx, INT2 cache",
-                        "kernel": "decode_int2_kernel<2>", "ms_per_decode": round(g8["us_per_launch"] / 1e3, 4),
-                        "value": g8["value"], "unit": "GB/s",
-                        "roofline": {"bound": "hbm", "achieved": g8["value"], "peak": sweep["peak"], "unit": "GB/s",
-                                     "frac": g8["frac"], "peak_kind": sweep["peak_kind"]}}
-        ll = measure_int2_decode(inputs.SPECS["llama8b"], device, stream, reps=5)
-        line["llama8b"] = {"workload": "llama8b: 32 q / 8 KV heads, batch 8, 32768 ctx (post-RoPE keys, theta 5e5), "
-                                       "INT2 cache", "kernel": "decode_int2_kernel<1>", **ll, "unit": "GB/s",
-                           "l2": "256 MB buffer written before every timed launch"}
-        ti = measure_int2_decode(inputs.SPECS["tiny"], device, stream, reps=10, step=True)
-        line["tiny"] = {"workload": "tiny: 1 KV head, 4 q heads, batch 1, 256 cached tokens + 1 decode token, one "
-                                    "fused decode step", "kernel": "decode_int2_kernel<1> (step)", **ti,
-                        "unit": "GB/s", "bound": "latency (24 KB of cache)",
-                        "l2": "256 MB buffer written before every timed launch"}
-        line["window"] = measure_int2_window(spec, device, stream, reps=5)
+        if not args.no_extras:
+            measure_extras(line, spec, device, stream)
     if rank == 0 and not args.no_cpu_baseline:
         gbs, el, sample = oracle_baseline(spec)
         cores, cpu = host_cpu()
@@ -675,7 +685,8 @@ def run_profile_case(args):
     """A case for a full ncu capture: one Qwen3-8B-shaped layer (32 q / 8 KV
     heads) at --profile-ctx tokens (default 32K; 131072 is one layer of the
     benchmark step, ~100 MB of cache), three launches of the chosen kernel:
-    a decode, or the append of the layer's whole history in one call."""
+    a decode, a fused decode step, or the append of the layer's whole
+    history in one call."""
     torch.cuda.set_device(0)
     spec = inputs.small_spec(f"prof{args.profile_ctx // 1024}k", h_q=32, h_kv=8, batch=1, ctx=args.profile_ctx,
                              permute=True, k_kind="energy_rope", v_kind="gauss", avg_bits=3, v_bits=3, b_min=1,
@@ -690,6 +701,15 @@ def run_profile_case(args):
         k, v = k.contiguous(), v.contiguous()
         for _ in range(3):
             _lib.kvq_append_int2(k, v, sl, L.mu, L.R_k, L.R_v, L.cache, L.num_pages)
+    elif args.profile_case == "step_int2":
+        # the fused decode step (new-token append + decode) with early inputs
+        L = Int2Layer(spec, 0)
+        L.prefill()
+        q, ws = L.queries(), L.workspace()
+        k_new, v_new = L.new_kv()
+        for _ in range(3):
+            _lib.kvq_decode_step_int2(q, k_new, v_new, L.cache, L.num_pages, L.block_table, L.context_lens, L.mu,
+                                      L.R_k, L.R_v, L.scale, out, ws, flags=_lib.KVQ_STEP_INPUTS_READY)
     elif args.profile_case == "decode_int2":
         L = Int2Layer(spec, 0)
         L.prefill()
@@ -716,7 +736,9 @@ def main():
     ap.add_argument("--workload", default="qwen8b", choices=["qwen8b", "llama8b"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-bgtq", action="store_true")
-    ap.add_argument("--profile-case", choices=["decode_int2", "bgtq_decode", "append_prefill"], default=None,
+    ap.add_argument("--no-extras", action="store_true", help="only the headline step (e.g. for an ncu launch list)")
+    ap.add_argument("--profile-case", choices=["decode_int2", "step_int2", "bgtq_decode", "append_prefill"],
+                    default=None,
                     help="run a small decode case for an ncu capture instead of the benchmark")
     ap.add_argument("--profile-ctx", type=int, default=32768, help="context length of the --profile-case layer")
     args = ap.parse_args()
