@@ -22,7 +22,8 @@ struct AppendSmem {
     float cb_v[256];
     float x[2][D];       // [0] gathered key, [1] value
     float u[2][D];       // normalised
-    uint32_t words[2][32];
+    uint32_t kw[32];     // the slot's key code stream
+    uint32_t vw[64];     // the slot's value codes in their pair row (the partner's bits zero)
     uint16_t knorm[8];
     uint16_t vnorm;
 };
@@ -61,7 +62,7 @@ bgtq_append_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
         st = 0;
         n = D;
         j = p;
-        bit = p * v_bits;
+        bit = 2 * p * v_bits;  // within the slot pair's row; the odd slot's code follows the even one's
     }
     const float* pi = pi_table + __ldg(pi_offsets + n);
     const int kb = bgtq_kb(total_bits), vb = 16 * v_bits;
@@ -79,7 +80,8 @@ bgtq_append_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
         }
         const __nv_bfloat16* src = (side ? v : k) + ((size_t)t * H_kv + h) * D;
         sm.x[side][p] = __bfloat162float(src[side ? p : sm.L.dim[p]]);
-        if (tid < 64) sm.words[tid >> 5][tid & 31] = 0u;
+        if (tid < 32) sm.kw[tid] = 0u;
+        if (tid >= 64 && tid < 128) sm.vw[tid - 64] = 0u;
         if (tid < 8) sm.knorm[tid] = 0;
         __syncthreads();
 
@@ -97,9 +99,11 @@ bgtq_append_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
 #pragma unroll 16
         for (int i = 0; i < n; ++i) y = __fmaf_rn(us[i], __ldg(pi + (size_t)i * n + j), y);
         const uint32_t code = r > 0.f ? (uint32_t)nearest_code(y, side ? sm.cb_v : sm.cb_k[b - 1], 1 << b) : 0u;
-        const int w = bit >> 5, sh = bit & 31;
-        atomicOr(&sm.words[side][w], code << sh);
-        if (sh + b > 32) atomicOr(&sm.words[side][w + 1], code >> (32 - sh));
+        const int cbit = bit + (side ? (slot & 1) * v_bits : 0);
+        const int w = cbit >> 5, sh = cbit & 31;
+        uint32_t* words = side ? sm.vw : sm.kw;
+        atomicOr(&words[w], code << sh);
+        if (sh + b > 32) atomicOr(&words[w + 1], code >> (32 - sh));
         if (j == 0) {
             const uint16_t nh = __half_as_ushort(f16_sat(r));
             if (side) sm.vnorm = nh; else sm.knorm[b - 1] = nh;
@@ -108,9 +112,19 @@ bgtq_append_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __r
 
         const int page = slot / PAGE, s = slot % PAGE;
         uint8_t* tile = cache + ((size_t)page * H_kv + h) * tile_bytes;
-        if (tid < kb / 4) reinterpret_cast<uint32_t*>(tile + s * kb)[tid] = sm.words[0][tid];
-        if (tid >= 64 && tid < 64 + vb / 4)
-            reinterpret_cast<uint32_t*>(tile + off_vc + s * vb)[tid - 64] = sm.words[1][tid - 64];
+        if (tid < kb / 4) reinterpret_cast<uint32_t*>(tile + s * kb)[tid] = sm.kw[tid];
+        if (tid >= 64 && tid < 64 + 2 * vb / 4) {
+            // the pair row is shared with the partner slot, which this or
+            // another CTA may write at the same time: clear and set only
+            // this slot's bits, atomically
+            const int wi = tid - 64;
+            uint32_t mine = 0u;
+            for (int q = 0; q < 32; ++q)
+                if (((32 * wi + q) % (2 * v_bits)) / v_bits == (s & 1)) mine |= 1u << q;
+            uint32_t* dst = reinterpret_cast<uint32_t*>(tile + off_vc + (s >> 1) * 2 * vb) + wi;
+            atomicAnd(dst, ~mine);
+            atomicOr(dst, sm.vw[wi] & mine);
+        }
         if (tid >= 128 && tid < 136) reinterpret_cast<uint16_t*>(tile + off_kn + 16 * s)[tid - 128] = sm.knorm[tid - 128];
         if (tid == 136) reinterpret_cast<uint16_t*>(tile + off_vn)[s] = sm.vnorm;
         __syncthreads();

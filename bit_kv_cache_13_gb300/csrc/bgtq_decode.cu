@@ -11,27 +11,40 @@
 // Grid (split, kv_head, seq) with one CTA per SM (12 warps for head groups
 // up to 4, 8 for groups of 8); the pages of a (sequence, KV head) are dealt
 // round-robin over all warps of its CTAs and streamed through per-warp rings
-// of bulk async copies, as in the INT2 decode, three pages per mbarrier
-// phase (one wait, one release, one softmax rescale, and one pass over the
-// chunk descriptors and B fragments per unit).  Per page (16 tokens):
-//   QK  mma.sync m16n8k16 over chunks of 16 gathered positions of one width
-//       (a width group padded to a multiple of 16; groups are laid out in
-//       ascending width).  Rows = tokens r, r + 8; lane t holds the chunk's
-//       RoPE blocks 2t, 2t + 1, whose 4b code bits are contiguous in a
-//       token's stream and come out of one 32-bit window.  A = C_b[code] /
-//       sqrt(n_b) as an fp16 hi/lo pair from a shared-memory table; B =
-//       q~ sigma (a per-head power of two) as hi/lo columns, zero past the
-//       group; the token's group norm r_{s,b} scales each chunk's dot
-//       products in fp32.
+// of bulk async copies, three pages per mbarrier phase.
+//
+// Both products run on mma.sync m16n8k16, and their A operands come from
+// lookup tables indexed by TWO codes at once, so one shared-memory load
+// yields a whole A register (two fp16 elements):
+//   QK  K = 16 gathered positions of one width (a chunk; a width group is
+//       padded to a multiple of 16 with zero B rows).  Lane t holds the
+//       chunk's positions 4t..4t+3, whose 4b code bits are contiguous in a
+//       token's stream: positions (4t, 4t+1) are one 2b-bit table index,
+//       (4t+2, 4t+3) the next.  For widths up to 5 the key table maps the
+//       index to the two scaled centroids as an fp16 hi pair and an fp16 lo
+//       pair (about 22 significant bits, one 64-bit load); wider codes use
+//       one 32-bit (hi | lo) entry per code.  Rows r and r + 8 of an MMA
+//       are the hi and lo parts of one token, so an A quad is two table
+//       entries: one MMA covers tokens 0..7, one tokens 8..15.  B = q~ sigma
+//       (a per-head power of two) as hi/lo columns.  The MMA accumulators
+//       run over a whole width group, and the token's group norm r_{s,b}
+//       scales the sum once per group in fp32.
 //   softmax  online, base 2, exact running maximum per head; p is rounded to
 //       fp16 once (p^), and the same p^ weights the values and the
 //       normaliser.
-//   PV  mma.sync m16n8k16 with rows = channels, K = the 16 tokens.  Lane
-//       (r, t) owns channels 16r .. 16r+15 (one contiguous 16 v_bits-bit
-//       field of each token's value stream): the MMA row pair (r, r + 8) of
-//       chunk m is channels 16r + 2m, 16r + 2m + 1.  A = C_v[code] / sqrt(128)
-//       as fp16 from a shared-memory table; B = p^ r_v as an exact fp16
-//       hi/lo pair (HMUL2, then HFMA2 for the remainder) in the N columns.
+//   PV  rows = channels, K = the 16 tokens of a page.  The value codes of
+//       slots 2j and 2j + 1 sit side by side per channel (the tile format),
+//       so a (channel, token pair) is one 2 v_bits-bit index into a table of
+//       fp16 pairs C_v[c0] / sqrt(128) | C_v[c1] / sqrt(128) << 16: exactly
+//       an A register.  Lane (r, t) owns channels 16r .. 16r+15 of token
+//       pairs t and t + 4 (v_bits words each).  B = p^ r_v as an exact fp16
+//       hi/lo pair in the N columns.
+// The tables live in a static shared-memory area aligned to 8 KB; each
+// table is replicated across the banks (entry e, copy c at e * copies + c,
+// a lane reads copy lane % copies), so a warp's random lookups mostly hit
+// distinct banks, and since each table is aligned to its size a lookup
+// address is (index << shift) | copy offset: one shift and one LOP3.
+#include <cmath>
 #include <mutex>
 
 #include "bgtq_common.cuh"
@@ -56,25 +69,270 @@ struct BgChunk {
     int16_t pos0;  // first gathered position
 };
 
+// ---- lookup tables (byte offsets in the 8 KB-aligned table area)
+constexpr int KP_MAX = 5;  // key widths with pair tables
+constexpr int VP_MAX = 5;  // value widths with pair tables
+// log2 of the copies of each pair table: 16 copies make a half-warp's 64-bit
+// lookups (banks 2c, 2c+1) conflict-free, 32 a warp's 32-bit ones
+__host__ __device__ constexpr int kp_lg_copies(int b) { return b <= 3 ? 4 : (b == 4 ? 2 : 0); }
+__host__ __device__ constexpr int vp_lg_copies(int b) { return b <= 3 ? 5 : (b == 4 ? 3 : 1); }
+// key pair table of width b: 4^b entries x copies x 8 bytes, aligned to its size
+__host__ __device__ constexpr int kp_off(int b) {
+    return b == 3 ? 0 : b == 4 ? 8192 : b == 5 ? 16384 : b == 2 ? 32768 : 34816;
+}
+constexpr int V_OFF = 24576;   // value table: pairs (4^v x copies x 4 B) or fp16 per code
+constexpr int KS_OFF = 35328;  // single-code key tables of widths 6..8: (hi | lo << 16) per code
+__host__ __device__ constexpr int ks_off(int b) { return KS_OFF + (b == 6 ? 0 : b == 7 ? 256 : 768); }
+constexpr int LUT_BYTES = KS_OFF + 1792;
+constexpr int LUT_ALIGN = 8192;
+static_assert((1 << (2 * 1)) * 16 * 8 == 512 && kp_off(1) % 512 == 0 && kp_off(1) + 512 <= KS_OFF, "key table 1");
+static_assert((1 << (2 * 2)) * 16 * 8 == 2048 && kp_off(2) % 2048 == 0 && kp_off(2) + 2048 <= kp_off(1), "key table 2");
+static_assert((1 << (2 * 3)) * 16 * 8 == 8192 && (1 << (2 * 4)) * 4 * 8 == 8192 && (1 << (2 * 5)) * 8 == 8192,
+              "key tables 3..5");
+static_assert((1 << (2 * 3)) * 32 * 4 == 8192 && (1 << (2 * 4)) * 8 * 4 == 8192 && (1 << (2 * 5)) * 2 * 4 == 8192,
+              "value tables");
+static_assert(V_OFF % 8192 == 0 && V_OFF + 8192 <= kp_off(2), "value table place");
+
+// scaled centroids of every width (width b at 2^b - 2) and of the values
+constexpr int CBS_V = 510;
+
+// 1 / sqrt(n) for even n = 2i (v[0] unused), computed on the host in fp64
+// (correctly rounded, as on the device) and passed with the launch: the
+// kernel needs one per width group, and fp64 arithmetic is slow here.
+struct RsqrtTab {
+    double v[D / 2 + 1];
+};
+
 template <int NW, int MAXG>
 struct __align__(16) BgDecodeSmem {
     uint2 bfr[BG_MAX_CHUNKS][MAXG / 4][32];  // QK B fragments per chunk, n-tile and lane
-    uint32_t cbk2[8][256];  // C_b / sqrt(n_b) per width as (fp16 hi | fp16 lo << 16)
+    float cbs[CBS_V + 256];                  // fp32(C_b / sqrt(n_b)) per width, then fp32(C_v / sqrt(128))
+    double rsn[9];                           // 1 / sqrt(n): [0] values (n = 128), [b] the width-b group
     BgChunk chunks[BG_MAX_CHUNKS];
     int n_chunks;
     float sigma[MAXG];      // power-of-two pre-scale per head
     __half pbh[NW][MAXG][BG_UNIT * PAGE];  // p^ of the warp's current unit, head-major
-    __half cb_vh[256];         // C_v / sqrt(128) as fp16 (PV A operand)
     float qt[MAXG][D];         // q~ in gathered order, times scale * log2(e)
     float qin[MAXG][D];
-    float cb_v[256];           // C_v / sqrt(128)
     uint64_t bar[NW][BG_MAX_STAGES];
     int ntok[NW][BG_MAX_STAGES];
     BgtqLayout L;
+    int kbase[9], nch[9];   // first chunk and chunk count of each width
+    int64_t pioff[D / 2 + 1];  // offset of Pi_n (n = 2i) in the rotation table
+    float qpart[NW * 32 / D - 1][MAXG][D];  // partial q~ sums of the other thread groups
     int8_t wsm[D / 2];      // this head's block widths
     MergeSmem<NW, MAXG> ms;
 };
 
+template <int N>
+__device__ __forceinline__ uint32_t shift_left(uint32_t x) {
+    if constexpr (N >= 0)
+        return x << N;
+    else
+        return x >> (-N);
+}
+
+__device__ __forceinline__ uint32_t pack_hi_lo(float v, bool lo) {
+    const __half h = __float2half_rn(v);
+    return lo ? (uint32_t)__half_as_ushort(__float2half_rn(v - __half2float(h))) : (uint32_t)__half_as_ushort(h);
+}
+
+// Fill the tables of this head (every thread of the CTA; the scaled
+// centroids are in cbs, and a barrier follows).  The key tables only with
+// valid widths (keys: the present widths); the value table always, so that
+// nothing reads uninitialised shared memory.
+template <int VB>
+__device__ __forceinline__ void build_tables(uint8_t* lut, const float* cbs, const BgtqLayout& L, int nthreads,
+                                             bool keys) {
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int b = 1; b <= KP_MAX; ++b) {
+        if (!keys || L.n[b] == 0) continue;
+        const int lg = kp_lg_copies(b), cnt = (1 << (2 * b)) << lg;
+        const float* cb = cbs + (1 << b) - 2;
+        uint2* tab = reinterpret_cast<uint2*>(lut + kp_off(b));
+        for (int idx = tid; idx < cnt; idx += nthreads) {
+            const int e = idx >> lg, c0 = e & ((1 << b) - 1), c1 = e >> b;
+            const float v0 = cb[c0], v1 = cb[c1];
+            tab[idx] = make_uint2(pack_hi_lo(v0, false) | (pack_hi_lo(v1, false) << 16),
+                                  pack_hi_lo(v0, true) | (pack_hi_lo(v1, true) << 16));
+        }
+    }
+#pragma unroll
+    for (int b = KP_MAX + 1; b <= 8; ++b) {
+        if (!keys || L.n[b] == 0) continue;
+        const float* cb = cbs + (1 << b) - 2;
+        uint32_t* tab = reinterpret_cast<uint32_t*>(lut + ks_off(b));
+        for (int c = tid; c < (1 << b); c += nthreads) tab[c] = pack_hi_lo(cb[c], false) | (pack_hi_lo(cb[c], true) << 16);
+    }
+    const float* cv = cbs + CBS_V;
+    if constexpr (VB <= VP_MAX) {
+        constexpr int lg = vp_lg_copies(VB), cnt = (1 << (2 * VB)) << lg;
+        uint32_t* tab = reinterpret_cast<uint32_t*>(lut + V_OFF);
+        for (int idx = tid; idx < cnt; idx += nthreads) {
+            const int e = idx >> lg, c0 = e & ((1 << VB) - 1), c1 = e >> VB;
+            tab[idx] = (uint32_t)__half_as_ushort(__float2half_rn(cv[c0])) |
+                       ((uint32_t)__half_as_ushort(__float2half_rn(cv[c1])) << 16);
+        }
+    } else {
+        __half* tab = reinterpret_cast<__half*>(lut + V_OFF);
+        for (int c = tid; c < (1 << VB); c += nthreads) tab[c] = __float2half_rn(cv[c]);
+    }
+}
+
+// QK of one chunk (16 positions of width B) for the unit's pages: the MMA
+// accumulators cg run over the chunk's width group.  xw: per page, the
+// lane's 4B code bits of tokens r and r + 8 (from bit 0).
+template <int B, int NT>
+__device__ __forceinline__ void qk_chunk(const uint32_t (&xw)[BG_UNIT][2], int lane, const uint2 (&bb)[NT],
+                                         float (&cg)[2][BG_UNIT][NT][4], const uint8_t* __restrict__ lut) {
+#pragma unroll
+    for (int e = 0; e < BG_UNIT; ++e) {
+        const uint32_t x0 = xw[e][0], x8 = xw[e][1];  // the lane's 4B code bits of tokens r, r + 8
+        // Two MMAs per page: rows r / r + 8 of the first are token r's hi /
+        // lo centroid parts, of the second token r + 8's, so each A quad is
+        // two table entries (hi pair, lo pair) of one token: positions
+        // (4t, 4t+1) give a0, a1 and positions (4t+2, 4t+3) give a2, a3.
+        uint32_t aA[4], aB[4];
+        if constexpr (B <= KP_MAX) {
+            constexpr int S = 3 + kp_lg_copies(B);
+            constexpr uint32_t MK = ((1u << (2 * B)) - 1u) << S;
+            const uint32_t cp = ((uint32_t)lane << 3) & ((1u << S) - 1u);
+            const uint8_t* tab = lut + kp_off(B);
+            const uint2 e0 = *reinterpret_cast<const uint2*>(tab + (((x0 << S) & MK) | cp));
+            const uint2 e2 = *reinterpret_cast<const uint2*>(tab + ((shift_left<S - 2 * B>(x0) & MK) | cp));
+            const uint2 e1 = *reinterpret_cast<const uint2*>(tab + (((x8 << S) & MK) | cp));
+            const uint2 e3 = *reinterpret_cast<const uint2*>(tab + ((shift_left<S - 2 * B>(x8) & MK) | cp));
+            aA[0] = e0.x; aA[1] = e0.y; aA[2] = e2.x; aA[3] = e2.y;
+            aB[0] = e1.x; aB[1] = e1.y; aB[2] = e3.x; aB[3] = e3.y;
+        } else {
+            constexpr uint32_t M = (1u << B) - 1u;
+            const uint32_t* tab = reinterpret_cast<const uint32_t*>(lut + ks_off(B));
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {  // position pair j of the lane: codes at bits 2jB, (2j+1)B
+                const uint32_t c0 = tab[(x0 >> (2 * j * B)) & M], c1 = tab[(x0 >> ((2 * j + 1) * B)) & M];
+                const uint32_t d0 = tab[(x8 >> (2 * j * B)) & M], d1 = tab[(x8 >> ((2 * j + 1) * B)) & M];
+                aA[2 * j] = prmt(c0, c1, 0x5410);
+                aA[2 * j + 1] = prmt(c0, c1, 0x7632);
+                aB[2 * j] = prmt(d0, d1, 0x5410);
+                aB[2 * j + 1] = prmt(d0, d1, 0x7632);
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {  // tokens r and r + 8 in separate chains
+            mma_f16_16816(cg[0][e][nt], aA, bb[nt].x, bb[nt].y);
+            mma_f16_16816(cg[1][e][nt], aB, bb[nt].x, bb[nt].y);
+        }
+    }
+}
+
+// QK of the unit's pages over every chunk of width B (all in registers but
+// the B fragments), then the group norm r_{s,B} of each token scales the
+// group's dot products once, in fp32.
+template <int B, int NT, int NW, int MAXG>
+__device__ __forceinline__ void qk_width(const uint8_t* const (&tiles)[BG_UNIT], const BgtqTile& tl, int lane,
+                                         const BgDecodeSmem<NW, MAXG>& sm, float (&acc)[BG_UNIT][NT][2],
+                                         const uint8_t* __restrict__ lut) {
+    const int nch = sm.nch[B];
+    if (nch == 0) return;  // warp-uniform
+    const int r = lane >> 2, t = lane & 3, k0 = sm.kbase[B];
+    float cg[2][BG_UNIT][NT][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int e = 0; e < BG_UNIT; ++e)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) cg[i][e][nt][0] = cg[i][e][nt][1] = cg[i][e][nt][2] = cg[i][e][nt][3] = 0.f;
+    int off = sm.L.bitstart[B] + 4 * t * B;  // the lane's first code bit in a token's stream
+#pragma unroll 1
+    for (int c = 0; c < nch; ++c, off += 16 * B) {
+        uint2 bb[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) bb[nt] = sm.bfr[k0 + c][nt][lane];
+        const int wofs = (off >> 5) * 4, sh = off & 31;
+        uint32_t xw[BG_UNIT][2];
+#pragma unroll
+        for (int e = 0; e < BG_UNIT; ++e)
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const uint32_t* w = reinterpret_cast<const uint32_t*>(tiles[e] + (r + 8 * i) * tl.kb + wofs);
+                xw[e][i] = __funnelshift_r(w[0], w[1], sh);
+            }
+        qk_chunk<B, NT>(xw, lane, bb, cg, lut);
+    }
+#pragma unroll
+    for (int e = 0; e < BG_UNIT; ++e) {
+        const __half* nrm = reinterpret_cast<const __half*>(tiles[e] + tl.off_kn + 2 * (B - 1));
+        const float rn0 = __half2float(nrm[8 * r]), rn8 = __half2float(nrm[8 * (r + 8)]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            // rows r (hi) and r + 8 (lo) of each MMA, columns q~ hi and lo
+            const float s0 = (cg[0][e][nt][0] + cg[0][e][nt][1]) + (cg[0][e][nt][2] + cg[0][e][nt][3]);
+            const float s8 = (cg[1][e][nt][0] + cg[1][e][nt][1]) + (cg[1][e][nt][2] + cg[1][e][nt][3]);
+            acc[e][nt][0] = fmaf(rn0, s0, acc[e][nt][0]);
+            acc[e][nt][1] = fmaf(rn8, s8, acc[e][nt][1]);
+        }
+    }
+}
+
+// The table entry (an A register) of channel 16r + I of the lane's field f
+// (the v_bits words of one token pair).
+template <int VB, int I>
+__device__ __forceinline__ uint32_t v_entry(const uint32_t (&f)[VB], uint32_t cp, const uint8_t* __restrict__ lut) {
+    constexpr int BIT = 2 * VB * I, W = BIT >> 5, SH = BIT & 31;
+    constexpr bool STRADDLE = SH + 2 * VB > 32;
+    if constexpr (VB <= VP_MAX) {
+        constexpr int SV = 2 + vp_lg_copies(VB);
+        constexpr uint32_t MV = ((1u << (2 * VB)) - 1u) << SV;
+        uint32_t x;
+        if constexpr (STRADDLE)
+            x = __funnelshift_r(f[W], f[W + 1], SH - SV);  // SH > 32 - 2 VB >= SV here
+        else
+            x = shift_left<SV - SH>(f[W]);
+        return *reinterpret_cast<const uint32_t*>(lut + V_OFF + ((x & MV) | cp));
+    } else {
+        constexpr uint32_t M = (1u << VB) - 1u;
+        uint32_t x;
+        if constexpr (STRADDLE)
+            x = __funnelshift_r(f[W], f[W + 1], SH);
+        else
+            x = f[W] >> SH;
+        const unsigned short* tab = reinterpret_cast<const unsigned short*>(lut + V_OFF);
+        return (uint32_t)tab[x & M] | ((uint32_t)tab[(x >> VB) & M] << 16);
+    }
+}
+
+// PV of one page: oacc[m] += A(channels 16r + 2m, 16r + 2m + 1 x the 16
+// tokens) B(p^ r_v hi, lo).
+template <int VB, int NT>
+__device__ __forceinline__ void pv_page(const uint8_t* tile, int off_vc, int lane, uint32_t bh0, uint32_t bh1,
+                                        uint32_t bl0, uint32_t bl1, float (&oacc)[8][4],
+                                        const uint8_t* __restrict__ lut) {
+    const int r = lane >> 2, t = lane & 3;
+    const uint32_t* p0 = reinterpret_cast<const uint32_t*>(tile + off_vc + 32 * VB * t + 4 * VB * r);
+    const uint32_t* p1 = reinterpret_cast<const uint32_t*>(tile + off_vc + 32 * VB * (t + 4) + 4 * VB * r);
+    uint32_t f0[VB], f1[VB];
+#pragma unroll
+    for (int w = 0; w < VB; ++w) {
+        f0[w] = p0[w];
+        f1[w] = p1[w];
+    }
+    uint32_t cp = 0u;
+    if constexpr (VB <= VP_MAX) cp = ((uint32_t)lane << 2) & ((1u << (2 + vp_lg_copies(VB))) - 1u);
+    // a0 = (channel 16r + 2m, tokens 2t, 2t+1), a1 = (16r + 2m + 1, same),
+    // a2 = (16r + 2m, tokens 2t+8, 2t+9), a3 = (16r + 2m + 1, same)
+#define KVQ_PV_M(m)                                                                                   \
+    {                                                                                                 \
+        const uint32_t a[4] = {v_entry<VB, 2 * (m)>(f0, cp, lut), v_entry<VB, 2 * (m) + 1>(f0, cp, lut), \
+                               v_entry<VB, 2 * (m)>(f1, cp, lut), v_entry<VB, 2 * (m) + 1>(f1, cp, lut)}; \
+        mma_f16_16816(oacc[m], a, bh0, bh1);                                                          \
+        if constexpr (NT == 2) mma_f16_16816(oacc[m], a, bl0, bl1);                                   \
+    }
+    KVQ_PV_M(0) KVQ_PV_M(1) KVQ_PV_M(2) KVQ_PV_M(3) KVQ_PV_M(4) KVQ_PV_M(5) KVQ_PV_M(6) KVQ_PV_M(7)
+#undef KVQ_PV_M
+}
+
+// ---- kernel body follows
 
 template <int MAXG, int VB>
 __global__ void __launch_bounds__(BgWarps<MAXG>::NW * 32, 1)
@@ -83,9 +341,11 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                    const int32_t* __restrict__ context_lens, const int8_t* __restrict__ widths, int total_bits,
                    int v_bits, const float* __restrict__ pi_table, const int64_t* __restrict__ pi_offsets,
                    const double* __restrict__ codebooks, float scale_log2, float* __restrict__ out,
-                   uint8_t* __restrict__ ws, int n_stages) {
+                   uint8_t* __restrict__ ws, int n_stages, const RsqrtTab rs) {
     constexpr int NW = BgWarps<MAXG>::NW;
+    constexpr int NT = MAXG / 4;  // n-tiles of 8 columns (4 heads x hi/lo)
     extern __shared__ __align__(128) uint8_t smem_raw[];
+    __shared__ __align__(LUT_ALIGN) uint8_t lut[LUT_BYTES];
     BgDecodeSmem<NW, MAXG>& sm = *reinterpret_cast<BgDecodeSmem<NW, MAXG>*>(smem_raw);
     const BgtqTile tl(total_bits, VB);
     // the page rings follow the fixed part; after the loop the per-warp o'
@@ -110,18 +370,57 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         if (tid < (G * D * 2 + 127) / 128) prefetch_l2(qc + 128 * tid);
     }
     griddep_wait();  // every input may come from the previous kernel in the stream
-    int ctx = __ldg(context_lens + b);
-    ctx = max(0, min(ctx, max_pages * PAGE));
-    const int n_pages = (ctx + PAGE - 1) / PAGE;
+    // ---- every small input is requested in one round trip, before any page
+    // copy (under the page stream a read waits microseconds behind the
+    // copies): the context length, the warp's first block-table entries
+    // (bounded by the table row, checked against the length later), the
+    // widths, the rotation offsets, the query rows and every codebook entry
+    // a width could use.
+    constexpr int NTHR = NW * 32;
     const int32_t* bt = block_table + (size_t)b * max_pages;
     // pages dealt round-robin over all S * NW warps of the (sequence, KV head)
     const int KS = S * NW, k0 = split * NW + warp;
-    const int my_count = n_pages > k0 ? (n_pages - k0 + KS - 1) / KS : 0;
     auto page_of = [&](int j) { return k0 + KS * j; };
+    const int ctx_in = __ldg(context_lens + b);
+    int pid_pre[BG_MAX_STAGES / BG_UNIT + 1];
+#pragma unroll
+    for (int u = 0; u <= BG_MAX_STAGES / BG_UNIT; ++u) {
+        const int pg = page_of(BG_UNIT * u + lane);
+        pid_pre[u] = lane < BG_UNIT && u <= n_stages / BG_UNIT && pg < max_pages ? __ldg(bt + pg) : 0;
+    }
+    if (tid < D / 2) sm.wsm[tid] = __ldg(widths + h * (D / 2) + tid);
+    if (tid <= D / 2) sm.pioff[tid] = __ldg(pi_offsets + 2 * tid);  // Pi_n for even n = 2 tid
+    {
+        const uint4* q4 = reinterpret_cast<const uint4*>(q + ((size_t)b * H_q + (size_t)h * G) * D);
+        const int nq4 = G * D / 8, i4 = tid - D / 2;
+        if (i4 >= 0 && i4 < nq4) {  // 8 bf16 per thread
+            const uint4 w = __ldg(q4 + i4);
+            const __nv_bfloat16* e8 = reinterpret_cast<const __nv_bfloat16*>(&w);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) sm.qin[(8 * i4 + k) / D][(8 * i4 + k) % D] = __bfloat162float(e8[k]);
+        }
+    }
+    // codebook entries: thread slot j < CBS_V + 2^VB holds entry j in a register
+    // until the group sizes are known (width b code c at 2^b - 2 + c)
+    double craw[(CBS_V + 256 + NTHR - 1) / NTHR];
+#pragma unroll
+    for (int u = 0; u < (CBS_V + 256 + NTHR - 1) / NTHR; ++u) {
+        const int idx = tid + u * NTHR;
+        craw[u] = 0.0;
+        if (idx < CBS_V) {
+            const int bb = 31 - __clz(idx + 2), c = idx + 2 - (1 << bb);
+            craw[u] = __ldg(codebooks + (bb - 1) * 256 + c);
+        } else if (idx < CBS_V + (1 << VB)) {
+            craw[u] = __ldg(codebooks + (VB - 1) * 256 + idx - CBS_V);
+        }
+    }
+    const int ctx = max(0, min(ctx_in, max_pages * PAGE));
+    const int n_pages = (ctx + PAGE - 1) / PAGE;
+    const int my_count = n_pages > k0 ? (n_pages - k0 + KS - 1) / KS : 0;
 
     // Pages travel in units of BG_UNIT (one mbarrier phase, one wait, one
-    // release): unit u is the warp's pages 2u, 2u + 1 in ring slots
-    // 2 st, 2 st + 1 of slot group st = u % n_grp.
+    // release): unit u is the warp's pages BG_UNIT u .. + BG_UNIT - 1 in the
+    // ring slots of slot group u % n_grp.
     const int n_grp = n_stages / BG_UNIT;
     const int n_units = (my_count + BG_UNIT - 1) / BG_UNIT;
     if (lane == 0) {
@@ -161,80 +460,101 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                      tl.bytes, bar);
     };
     int pid_next = 0, n_issued = 0;
-    {
-        int pid_first[BG_MAX_STAGES / BG_UNIT];
 #pragma unroll
-        for (int u = 0; u < BG_MAX_STAGES / BG_UNIT; ++u) pid_first[u] = 0;
-        if (lane < BG_UNIT) {
-#pragma unroll
-            for (int u = 0; u <= BG_MAX_STAGES / BG_UNIT; ++u) {
-                const int j = BG_UNIT * u + lane;
-                const int pid = u <= n_grp && j < my_count ? __ldg(bt + page_of(j)) : 0;
-                if (u < BG_MAX_STAGES / BG_UNIT) pid_first[u] = pid;
-                if (u == n_grp) pid_next = pid;
-            }
+    for (int u = 0; u <= BG_MAX_STAGES / BG_UNIT; ++u) {
+        if (u < n_grp && u < n_units) {  // warp-uniform
+            issue_unit(u, u, pid_pre[u]);
+            n_issued = u + 1;
         }
-#pragma unroll
-        for (int u = 0; u < BG_MAX_STAGES / BG_UNIT; ++u)
-            if (u < n_grp && u < n_units) {  // warp-uniform
-                issue_unit(u, u, pid_first[u]);
-                n_issued = u + 1;
-            }
+        if (u == n_grp) pid_next = pid_pre[u];
     }
     {
-        // the block table and the output rotation are read later: have L2 keep them
+        // the block table is read later: have L2 keep it
         const char* btc = reinterpret_cast<const char*>(bt);
         const int lines = (n_pages * 4 + 127) / 128;
         for (int l = split * NW * 32 + tid; l < lines; l += S * NW * 32) prefetch_l2_keep(btc + 128 * l);
-        const char* rot = reinterpret_cast<const char*>(pi_table + __ldg(pi_offsets + D));
-        for (int l = tid; l < D * D * 4 / 128; l += NW * 32) prefetch_l2_keep(rot + 128 * l);
     }
 
-    // ---- per-head layout, chunk schedule, codebooks and rotated queries
-    build_layout_cta(widths + h * (D / 2), sm.L, sm.wsm);
-    if (tid == 0) {
-        int nc = 0;
-        for (int bb = 1; bb <= 8; ++bb)
-            for (int c = 0; c < (sm.L.n[bb] + 15) / 16 && nc < BG_MAX_CHUNKS; ++c) {
-                BgChunk ch;
-                ch.bit0 = sm.L.bitstart[bb] + 16 * c * bb;
-                ch.b = (int8_t)bb;
-                ch.last = (int8_t)(16 * (c + 1) >= sm.L.n[bb]);
-                ch.pos0 = (int16_t)(sm.L.start[bb] + 16 * c);
-                sm.chunks[nc++] = ch;
-            }
-        sm.n_chunks = nc;
-    }
-    const __nv_bfloat16* qb = q + ((size_t)b * H_q + (size_t)h * G) * D;
-    for (int idx = tid; idx < G * D; idx += NW * 32) sm.qin[idx / D][idx % D] = __bfloat162float(qb[idx]);
+    // ---- per-head layout, chunk schedule, tables and rotated queries
     __syncthreads();
-    const bool layout_ok = sm.L.ok && sm.L.total_bits <= 2 * total_bits;
-    if (!layout_ok && tid == 0) atomicOr(err_word, ERR_BAD_WIDTHS);
-    for (int idx = tid; idx < 8 * 256; idx += NW * 32) {
-        const int bb = idx / 256 + 1, c = idx % 256;
-        if (c < (1 << bb) && sm.L.n[bb] > 0) {
-            // the scaled centroid as an fp16 hi/lo pair (about 22 significant bits)
-            const float v = scaled_centroid(codebooks, bb, c, sm.L.n[bb]);
-            const __half hi = __float2half_rn(v), lo = __float2half_rn(v - __half2float(hi));
-            sm.cbk2[bb - 1][c] = (uint32_t)__half_as_ushort(hi) | ((uint32_t)__half_as_ushort(lo) << 16);
+    {
+        // the output rotation is read at the end: have L2 keep it
+        const char* rot = reinterpret_cast<const char*>(pi_table + sm.pioff[D / 2]);
+        for (int l = tid; l < D * D * 4 / 128; l += NTHR) prefetch_l2_keep(rot + 128 * l);
+    }
+    if (warp == 0) {
+        // the layout by ballots: groups by ascending width, blocks ascending
+        // in a group, block i as (dim i, dim i + 64); then the chunk list and
+        // 1 / sqrt(n) per group (fp64, once)
+        const int w0 = sm.wsm[lane], w1 = sm.wsm[lane + 32];
+        const bool ok = __all_sync(0xffffffffu, w0 >= 1 && w0 <= 8 && w1 >= 1 && w1 <= 8);
+        const uint32_t lt = (1u << lane) - 1u;
+        int pos = 0, bit = 0, nc = 0;
+#pragma unroll
+        for (int bb = 1; bb <= 8; ++bb) {
+            const uint32_t m0 = __ballot_sync(0xffffffffu, w0 == bb), m1 = __ballot_sync(0xffffffffu, w1 == bb);
+            const int cnt = __popc(m0) + __popc(m1);
+            if (w0 == bb) {
+                const int rk = __popc(m0 & lt);
+                sm.L.dim[pos + 2 * rk] = (int16_t)lane;
+                sm.L.dim[pos + 2 * rk + 1] = (int16_t)(lane + D / 2);
+            }
+            if (w1 == bb) {
+                const int rk = __popc(m0) + __popc(m1 & lt);
+                sm.L.dim[pos + 2 * rk] = (int16_t)(lane + 32);
+                sm.L.dim[pos + 2 * rk + 1] = (int16_t)(lane + 32 + D / 2);
+            }
+            const int n = 2 * cnt, nch = (n + 15) / 16;
+            if (lane == 0) {
+                sm.L.start[bb] = (int16_t)pos;
+                sm.L.bitstart[bb] = (int16_t)bit;
+                sm.L.n[bb] = (int16_t)n;
+                sm.kbase[bb] = nc;
+                sm.nch[bb] = nch;
+            }
+            if (lane < nch && nc + lane < BG_MAX_CHUNKS) {
+                BgChunk ch;
+                ch.bit0 = bit + 16 * lane * bb;
+                ch.b = (int8_t)bb;
+                ch.last = (int8_t)(lane + 1 == nch);
+                ch.pos0 = (int16_t)(pos + 16 * lane);
+                sm.chunks[nc + lane] = ch;
+            }
+            if (lane == bb) sm.rsn[bb] = rs.v[n / 2];
+            pos += n;
+            bit += bb * n;
+            nc += nch;
+        }
+        if (lane == 0) {
+            sm.L.start[0] = sm.L.n[0] = sm.L.bitstart[0] = 0;
+            sm.L.total_bits = bit;
+            sm.L.ok = ok && pos == D && nc <= BG_MAX_CHUNKS;
+            sm.n_chunks = nc;
+            sm.rsn[0] = rs.v[D / 2];
         }
     }
-    for (int c = tid; c < (1 << VB); c += NW * 32) {
-        sm.cb_v[c] = scaled_centroid(codebooks, VB, c, D);
-        sm.cb_vh[c] = __float2half_rn(sm.cb_v[c]);
-    }
-    if (tid < D) {
-        // q~ at gathered position p = tid: sum_i q[dim(st + i)] Pi_n[i][p - st]
-        const int p = tid;
+    __syncthreads();
+    // the table area must sit on its alignment for the OR-formed addresses
+    const bool lut_ok = (smem_u32(lut) & (LUT_ALIGN - 1)) == 0;
+    const bool widths_ok = sm.L.ok && sm.L.total_bits <= 2 * total_bits;
+    const bool layout_ok = widths_ok && lut_ok;
+    if (tid == 0 && !widths_ok) atomicOr(err_word, ERR_BAD_WIDTHS);
+    if (tid == 0 && !lut_ok) atomicOr(err_word, ERR_LUT_ALIGN);
+    // q~ at gathered position p: sum_i q[dim(st + i)] Pi_n[i][p - st], the i
+    // split over NPART thread groups (their loads go out together)
+    constexpr int NPART = NTHR / D;
+    {
+        const int p = tid % D, part = tid / D;
         float acc[MAXG];
 #pragma unroll
         for (int jj = 0; jj < MAXG; ++jj) acc[jj] = 0.f;
         if (layout_ok) {
-            const int bb = group_of(sm.L, p);
+            int bb = 1;
+            while (bb < 8 && !(p >= sm.L.start[bb] && p < sm.L.start[bb] + sm.L.n[bb])) ++bb;
             const int st = sm.L.start[bb], n = sm.L.n[bb], j = p - st;
-            const float* pi = pi_table + __ldg(pi_offsets + n);
-#pragma unroll 16
-            for (int i = 0; i < n; ++i) {
+            const float* pi = pi_table + sm.pioff[n / 2];
+#pragma unroll 8
+            for (int i = part; i < n; i += NPART) {
                 const float pv = __ldg(pi + (size_t)i * n + j);
                 const int dm = sm.L.dim[st + i];
 #pragma unroll
@@ -242,9 +562,32 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
                     if (jj < G) acc[jj] = fmaf(sm.qin[jj][dm], pv, acc[jj]);
             }
         }
+        if (part > 0) {
 #pragma unroll
-        for (int jj = 0; jj < MAXG; ++jj) sm.qt[jj][p] = jj < G ? acc[jj] * scale_log2 : 0.f;
+            for (int jj = 0; jj < MAXG; ++jj) sm.qpart[part - 1][jj][p] = acc[jj];
+        }
+        // scaled centroids fp32(C_b[c] / sqrt(n_b)) from the registers
+#pragma unroll
+        for (int u = 0; u < (CBS_V + 256 + NTHR - 1) / NTHR; ++u) {
+            const int idx = tid + u * NTHR;
+            if (idx < CBS_V) {
+                const int bb = 31 - __clz(idx + 2);
+                sm.cbs[idx] = __double2float_rn(craw[u] * sm.rsn[bb]);
+            } else if (idx < CBS_V + (1 << VB)) {
+                sm.cbs[idx] = __double2float_rn(craw[u] * sm.rsn[0]);
+            }
+        }
+        __syncthreads();
+        if (part == 0) {
+#pragma unroll
+            for (int k = 0; k < NPART - 1; ++k)
+#pragma unroll
+                for (int jj = 0; jj < MAXG; ++jj) acc[jj] += sm.qpart[k][jj][p];
+#pragma unroll
+            for (int jj = 0; jj < MAXG; ++jj) sm.qt[jj][p] = jj < G ? acc[jj] * scale_log2 : 0.f;
+        }
     }
+    build_tables<VB>(lut, sm.cbs, sm.L, NTHR, layout_ok);
     __syncthreads();
     // per head: power-of-two pre-scale so that max |q~| sigma is in [2^14, 2^15)
     for (int jj = warp; jj < MAXG; jj += NW) {
@@ -257,13 +600,11 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     }
     __syncthreads();
 
-    constexpr int NT = MAXG / 4;  // n-tiles of 8 columns (4 heads x hi/lo)
-    constexpr int VPL = NT;
     const int r = lane >> 2, t = lane & 3;
     // ---- QK B fragments: column n = r -> head 4 nt + (r >> 1), part r & 1
     // (hi / lo of q~ sigma); rows k = 2t, 2t+1 (b0) are the chunk positions
     // 4t, 4t+1 and k = 2t+8, 2t+9 (b1) the positions 4t+2, 4t+3, so a lane's
-    // two RoPE blocks are adjacent in the code stream; positions past the
+    // two position pairs are adjacent in the code stream; positions past the
     // group are zero
     const int NC = layout_ok ? sm.n_chunks : 0;
     for (int idx = warp; idx < NC * NT; idx += NW) {
@@ -288,13 +629,7 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     float inv_sig[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) inv_sig[nt] = 4 * nt + t < G ? 1.f / sm.sigma[4 * nt + t] : 0.f;
-    __syncthreads();
-
-    // ---- this lane's value field: channels 16r .. 16r+15, the 16 VB bits
-    // at bit 16 VB r of a token's value stream, in VW words from vword on
-    // (shifted down by vshift = 0 or 16)
-    constexpr int VW = (VB + 1) / 2;
-    const int vword = (VB * r) >> 1, vshift = 16 * ((VB * r) & 1);
+    __syncthreads();  // the tables and B fragments are complete
 
     // PV accumulators: chunk m, C fragment (row r, r + 8 = channels 16r + 2m,
     // 16r + 2m + 1; columns 2t, 2t + 1)
@@ -329,11 +664,7 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             n_tok[e] = layout_ok ? sm.ntok[warp][BG_UNIT * st + e] : 0;
         }
 
-        // ---- QK on the tensor cores, one chunk (16 positions of width b) at
-        // a time for both pages of the unit: A = C_b[code] / sqrt(n_b) as an
-        // fp16 hi/lo pair, rows = tokens r, r + 8, K = the chunk's positions
-        // (lane t: blocks 2t, 2t + 1 of the chunk); the group norm r_{s,b}
-        // scales each chunk's dot products.
+        // ---- QK on the tensor cores, width by width for the unit's pages
         float lg[BG_UNIT][NT][2];
         {
             float acc[BG_UNIT][NT][2];
@@ -341,44 +672,15 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             for (int e = 0; e < BG_UNIT; ++e)
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) acc[e][nt][0] = acc[e][nt][1] = 0.f;
-#pragma unroll 2
-            for (int k = 0; k < NC; ++k) {
-                const BgChunk ch = sm.chunks[k];  // warp-uniform
-                const int bw = ch.b;
-                // this lane's blocks 2t, 2t+1 of the chunk: 4 bw contiguous bits
-                const int off = ch.bit0 + 4 * t * bw, wi = off >> 5, sh = off & 31;
-                const uint32_t* cb = sm.cbk2[bw - 1];
-                const uint32_t mask = (1u << bw) - 1u;
-                uint2 bb[NT];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) bb[nt] = sm.bfr[k][nt][lane];
-#pragma unroll
-                for (int e = 0; e < BG_UNIT; ++e) {
-                    const uint32_t* rec0 = reinterpret_cast<const uint32_t*>(tiles[e] + r * tl.kb);
-                    const uint32_t* rec8 = reinterpret_cast<const uint32_t*>(tiles[e] + (r + 8) * tl.kb);
-                    const uint32_t x0 = __funnelshift_r(rec0[wi], rec0[wi + 1], sh);
-                    const uint32_t x8 = __funnelshift_r(rec8[wi], rec8[wi + 1], sh);
-                    // A registers: a0 token r block 2t, a1 token r+8 block 2t,
-                    // a2 token r block 2t+1, a3 token r+8 block 2t+1
-                    uint32_t ah[4], al[4];
-                    const uint32_t xs[4] = {x0, x8, x0 >> (2 * bw), x8 >> (2 * bw)};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint32_t e0 = cb[xs[j] & mask], e1 = cb[(xs[j] >> bw) & mask];
-                        ah[j] = prmt(e0, e1, 0x5410);
-                        al[j] = prmt(e0, e1, 0x7632);
-                    }
-                    const __half* nrm = reinterpret_cast<const __half*>(tiles[e] + tl.off_kn + 2 * (bw - 1));
-                    const float rn0 = __half2float(nrm[8 * r]), rn8 = __half2float(nrm[8 * (r + 8)]);
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        float c[4] = {0.f, 0.f, 0.f, 0.f};
-                        mma_f16_16816(c, ah, bb[nt].x, bb[nt].y);
-                        mma_f16_16816(c, al, bb[nt].x, bb[nt].y);
-                        acc[e][nt][0] = fmaf(rn0, c[0] + c[1], acc[e][nt][0]);
-                        acc[e][nt][1] = fmaf(rn8, c[2] + c[3], acc[e][nt][1]);
-                    }
-                }
+            if (NC > 0) {  // warp-uniform
+                qk_width<1, NT>(tiles, tl, lane, sm, acc, lut);
+                qk_width<2, NT>(tiles, tl, lane, sm, acc, lut);
+                qk_width<3, NT>(tiles, tl, lane, sm, acc, lut);
+                qk_width<4, NT>(tiles, tl, lane, sm, acc, lut);
+                qk_width<5, NT>(tiles, tl, lane, sm, acc, lut);
+                qk_width<6, NT>(tiles, tl, lane, sm, acc, lut);
+                qk_width<7, NT>(tiles, tl, lane, sm, acc, lut);
+                qk_width<8, NT>(tiles, tl, lane, sm, acc, lut);
             }
 #pragma unroll
             for (int e = 0; e < BG_UNIT; ++e)
@@ -451,7 +753,7 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         for (int e = 0; e < BG_UNIT; ++e) {
             const uint8_t* tile = tiles[e];
             const bool full = n_tok[e] == PAGE;
-            const int hq = VPL == 1 ? (r & 3) : r;
+            const int hq = NT == 1 ? (r & 3) : r;
             const uint32_t* vn = reinterpret_cast<const uint32_t*>(tile + tl.off_vn);
             uint32_t R0 = vn[t], R1 = vn[t + 4];
             if (!full) {
@@ -468,46 +770,13 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             const __half2 L0 = __hfma2(u32_as_h2(P0), u32_as_h2(R0), __hneg2(H0));
             const __half2 L1 = __hfma2(u32_as_h2(P1), u32_as_h2(R1), __hneg2(H1));
             uint32_t bh0 = h2_as_u32(H0), bh1 = h2_as_u32(H1), bl0 = h2_as_u32(L0), bl1 = h2_as_u32(L1);
-            if constexpr (VPL == 1) {
+            if constexpr (NT == 1) {
                 if (r >= 4) {
                     bh0 = bl0;
                     bh1 = bl1;
                 }
             }
-
-            // this lane's value fields of tokens 2t, 2t+1, 2t+8, 2t+9, aligned
-            uint32_t f[4][VW];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int s_tok = 2 * t + (k & 1) + 8 * (k >> 1);
-                const uint32_t* vr = reinterpret_cast<const uint32_t*>(tile + tl.off_vc + s_tok * tl.vb) + vword;
-                uint32_t w[VW];
-#pragma unroll
-                for (int q2 = 0; q2 < VW; ++q2) w[q2] = vr[q2];
-#pragma unroll
-                for (int q2 = 0; q2 < VW; ++q2) f[k][q2] = __funnelshift_r(w[q2], q2 + 1 < VW ? w[q2 + 1] : 0u, vshift);
-            }
-            // code of channel 16r + i in field k
-            auto code = [&](int k, int i) -> uint32_t {
-                const int bit = VB * i, wi = bit >> 5, sh = bit & 31;
-                uint32_t x = f[k][wi] >> sh;
-                if (sh + VB > 32) x |= f[k][wi + 1] << (32 - sh);
-                return x & ((1u << VB) - 1u);
-            };
-            const unsigned short* cbv = reinterpret_cast<const unsigned short*>(sm.cb_vh);
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                uint32_t hv[4][2];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    hv[k][0] = cbv[code(k, 2 * m)];
-                    hv[k][1] = cbv[code(k, 2 * m + 1)];
-                }
-                const uint32_t a[4] = {hv[0][0] | (hv[1][0] << 16), hv[0][1] | (hv[1][1] << 16),
-                                       hv[2][0] | (hv[3][0] << 16), hv[2][1] | (hv[3][1] << 16)};
-                mma_f16_16816(oacc[m], a, bh0, bh1);
-                if constexpr (VPL == 2) mma_f16_16816(oacc[m], a, bl0, bl1);
-            }
+            pv_page<VB, NT>(tile, tl.off_vc, lane, bh0, bh1, bl0, bl1, oacc, lut);
         }
 
         // hand the unit's slots back: issue the unit n_grp ahead into them
@@ -535,14 +804,14 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         lsum[nt] += __shfl_xor_sync(0xffffffffu, lsum[nt], 16);
     }
     __syncthreads();  // every warp is done with its ring (o_part takes its place)
-    if constexpr (VPL == 1) {
+    if constexpr (NT == 1) {
         // columns 4..7 (lanes t = 2, 3) hold the low parts of heads 0..3
 #pragma unroll
         for (int m = 0; m < 8; ++m)
 #pragma unroll
             for (int e = 0; e < 4; ++e) oacc[m][e] += __shfl_xor_sync(0xffffffffu, oacc[m][e], 2);
     }
-    if (VPL == 2 || t < 2) {
+    if (NT == 2 || t < 2) {
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
             const int c0 = 16 * r + 2 * m;
@@ -583,6 +852,37 @@ const BgKernel kBgKernels[2][8] = {
      bgtq_decode_kernel<4, 5>, bgtq_decode_kernel<4, 6>, bgtq_decode_kernel<4, 7>, bgtq_decode_kernel<4, 8>},
     {bgtq_decode_kernel<8, 1>, bgtq_decode_kernel<8, 2>, bgtq_decode_kernel<8, 3>, bgtq_decode_kernel<8, 4>,
      bgtq_decode_kernel<8, 5>, bgtq_decode_kernel<8, 6>, bgtq_decode_kernel<8, 7>, bgtq_decode_kernel<8, 8>}};
+
+// Dynamic shared memory a kernel may take next to its static tables, opted
+// in once per device and kernel.
+kvq_status bgtq_dynamic_smem_limit(BgKernel kern, int kid, size_t* limit) {
+    static std::mutex mu;
+    static size_t lim[64][16] = {};
+    int dev = 0;
+    kvq_status s = kvq_check_cuda(cudaGetDevice(&dev), "bgtq_decode_attn: cudaGetDevice");
+    if (s != KVQ_OK) return s;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && lim[dev][kid]) {
+        *limit = lim[dev][kid];
+        return KVQ_OK;
+    }
+    int optin = 0;
+    s = kvq_check_cuda(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev),
+                       "bgtq_decode_attn: shared-memory limit");
+    if (s != KVQ_OK) return s;
+    cudaFuncAttributes fa;
+    s = kvq_check_cuda(cudaFuncGetAttributes(&fa, (const void*)kern), "bgtq_decode_attn: kernel attributes");
+    if (s != KVQ_OK) return s;
+    if ((size_t)optin <= fa.sharedSizeBytes)
+        return kvq_set_error(KVQ_ERR_UNSUPPORTED, "bgtq_decode_attn: no shared memory left next to the tables");
+    const size_t dyn = (size_t)optin - fa.sharedSizeBytes;
+    s = kvq_check_cuda(cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn),
+                       "bgtq_decode_attn smem attribute");
+    if (s != KVQ_OK) return s;
+    if (dev >= 0 && dev < 64) lim[dev][kid] = dyn;
+    *limit = dyn;
+    return KVQ_OK;
+}
 }  // namespace
 
 // one CTA per SM, as the INT2 decode (kvq_decode_auto_splits)
@@ -606,8 +906,9 @@ extern "C" kvq_status bgtq_decode_attn(const void* q, int B, int H_q, int H_kv, 
     if (!q || !cache || !block_table || !context_lens || !widths || !pi_table || !pi_offsets || !codebooks || !out ||
         !workspace)
         return kvq_set_error(KVQ_ERR_INVALID_ARG, "bgtq_decode_attn: null pointer");
-    if (reinterpret_cast<uintptr_t>(cache) % 16 || reinterpret_cast<uintptr_t>(workspace) % 16)
-        return kvq_set_error(KVQ_ERR_INVALID_ARG, "bgtq_decode_attn: cache and workspace need 16-byte alignment");
+    if (reinterpret_cast<uintptr_t>(cache) % 16 || reinterpret_cast<uintptr_t>(workspace) % 16 ||
+        reinterpret_cast<uintptr_t>(q) % 16)
+        return kvq_set_error(KVQ_ERR_INVALID_ARG, "bgtq_decode_attn: q, cache and workspace need 16-byte alignment");
     const int S = num_splits > 0 ? num_splits : bgtq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
     if (S > MAX_SPLITS)
         return kvq_set_error(KVQ_ERR_INVALID_ARG, "bgtq_decode_attn: num_splits=%d above %d", S, MAX_SPLITS);
@@ -617,44 +918,34 @@ extern "C" kvq_status bgtq_decode_attn(const void* q, int B, int H_q, int H_kv, 
         return kvq_set_error(KVQ_ERR_WORKSPACE, "bgtq_decode_attn: workspace %zu < %zu bytes", workspace_bytes, need);
 
     const int tile = (int)bgtq_tile_bytes(total_bits, v_bits);
-    constexpr size_t kSmemMax = 227 * 1024;
     const bool small = G <= 4;
+    const BgKernel kern = kBgKernels[small ? 0 : 1][v_bits - 1];
+    size_t dyn_max = 0;
+    st = bgtq_dynamic_smem_limit(kern, (small ? 0 : 8) + v_bits - 1, &dyn_max);
+    if (st != KVQ_OK) return st;
     const int NW = small ? BgWarps<4>::NW : BgWarps<8>::NW;
     const size_t fixed = align_up(small ? sizeof(BgDecodeSmem<BgWarps<4>::NW, 4>) : sizeof(BgDecodeSmem<BgWarps<8>::NW, 8>),
                                   128);
-    int n_stages = (int)((kSmemMax - fixed) / ((size_t)NW * tile));
+    int n_stages = dyn_max > fixed ? (int)((dyn_max - fixed) / ((size_t)NW * tile)) : 0;
     n_stages = n_stages > BG_MAX_STAGES ? BG_MAX_STAGES : n_stages;
     n_stages -= n_stages % BG_UNIT;  // whole units of pages
     if (n_stages < BG_UNIT)
         return kvq_set_error(KVQ_ERR_UNSUPPORTED, "bgtq_decode_attn: %d-byte tiles leave no room for a unit of stages", tile);
     const size_t ring = (size_t)NW * n_stages * tile, o_bytes = (size_t)NW * (small ? 4 : 8) * D * sizeof(float);
     const size_t smem = fixed + (ring > o_bytes ? ring : o_bytes);
-    if (smem > kSmemMax)
+    if (smem > dyn_max)
         return kvq_set_error(KVQ_ERR_UNSUPPORTED, "bgtq_decode_attn: %d-byte tiles leave no room", tile);
-    const BgKernel kern = kBgKernels[small ? 0 : 1][v_bits - 1];
-    const int kid = (small ? 0 : 8) + v_bits - 1;
-    {
-        // opt in once per device and kernel, to the full shared-memory size
-        static std::mutex mu;
-        static bool done[64][16] = {};
-        int dev = 0;
-        kvq_status s2 = kvq_check_cuda(cudaGetDevice(&dev), "bgtq_decode_attn: cudaGetDevice");
-        if (s2 != KVQ_OK) return s2;
-        std::lock_guard<std::mutex> lock(mu);
-        if (dev < 0 || dev >= 64 || !done[dev][kid]) {
-            s2 = kvq_check_cuda(
-                cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMax),
-                "bgtq_decode_attn smem attribute");
-            if (s2 != KVQ_OK) return s2;
-            if (dev >= 0 && dev < 64) done[dev][kid] = true;
-        }
-    }
+    static const RsqrtTab rs = [] {
+        RsqrtTab t{};
+        for (int i = 1; i <= D / 2; ++i) t.v[i] = 1.0 / std::sqrt((double)(2 * i));
+        return t;
+    }();
     dim3 grid(S, H_kv, B);
     const cudaError_t e =
         launch_pdl(kern, grid, dim3(NW * 32), smem,
                    static_cast<cudaStream_t>(stream), static_cast<const __nv_bfloat16*>(q), H_q, H_kv, G,
                    static_cast<const uint8_t*>(cache), num_pages, block_table, max_pages_per_seq, context_lens, widths,
                    total_bits, v_bits, pi_table, pi_offsets, codebooks, scale * 1.4426950408889634f, out,
-                   static_cast<uint8_t*>(workspace), n_stages);
+                   static_cast<uint8_t*>(workspace), n_stages, rs);
     return kvq_check_cuda(e, "bgtq_decode_attn launch");
 }

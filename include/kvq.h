@@ -328,7 +328,11 @@ kvq_status bgtq_allocate(const double* scores, int n_blocks, int b_min, int b_ma
  *                       1..8, each group's coordinates in order
  *   [16*KB, +256)       K norms, 8 fp16 per slot (entry b-1 = width-b group,
  *                       0 if that group is empty)
- *   [.., +16*VB)        V codes, VB = 16*v_bits bytes per slot
+ *   [.., +16*VB)        V codes, VB = 16*v_bits: slot pair j (slots 2j,
+ *                       2j+1) owns 2*VB bytes, an LSB-first stream of 128
+ *                       channel entries of 2*v_bits bits, each the slot-2j
+ *                       code then the slot-2j+1 code (one channel of two
+ *                       tokens is one field: the decode's table index)
  *   [.., +32)           V norm, fp16 per slot
  * Returns 0 for unsupported arguments. */
 size_t bgtq_tile_bytes(int total_bits, int v_bits);
@@ -341,6 +345,9 @@ size_t bgtq_tile_bytes(int total_bits, int v_bits);
  *               every even n <= d, Pi_n at pi_table + pi_offsets[n]
  *   pi_offsets  device int64 [d + 1] (-1 for odd n)
  *   codebooks   device fp64 [8][256]: row b-1 = bgtq_lloyd_max_codebook(b)
+ * A slot's value codes share their pair row with the partner slot; the call
+ * replaces only its own bits (atomically), so partners may be written in the
+ * same call or in different ones.
  *   err_count   nullable device int32: incremented once per token whose slot
  *               lies outside [0, num_pages*16) (other than -1), and at least
  *               once when a head's widths are outside 1..8 or over budget;
@@ -359,7 +366,12 @@ kvq_status bgtq_append(const void* k, const void* v, int n_tok, int H_kv, int d,
 
 /* Fused packed-cache decode attention over the Block-GTQ cache; arguments as
  * kvq_decode_attn_int2 plus the format parameters of bgtq_append.  Logits
- * are <q, k^>*scale with k^ the decoded post-RoPE key; out = softmax . V^. */
+ * are <q, k^>*scale with k^ the decoded post-RoPE key; out = softmax . V^.
+ * q, cache and workspace must be 16-byte aligned (KVQ_ERR_INVALID_ARG
+ * otherwise).  The scaled centroids the decode multiplies by are
+ * fp32(C_b[c] * (1/sqrt(n))) with the reciprocal in fp64: equal to the
+ * append's fp32(C_b[c] / sqrt(n)) but for a rare last-bit difference, which
+ * only moves a logit by an fp32 rounding. */
 kvq_status bgtq_decode_attn(const void* q, int B, int H_q, int H_kv, int d,
                             const void* cache, int64_t num_pages,
                             const int32_t* block_table, int max_pages_per_seq,

@@ -36,9 +36,15 @@ VB = 16 * v_bits):
                          order, b bits each, value LSB first
   [16*KB, +16*16)        K norms: 8 fp16 per slot, entry b-1 = width-b group
                          (0 when the group is empty)
-  [.., +16*VB)           V codes: 128 codes of v_bits, LSB-first
+  [.., +16*VB)           V codes by slot pair: pair j = slots (2j, 2j+1)
+                         holds 2*VB bytes, an LSB-first stream of 128
+                         entries in channel order, each the slot-2j code
+                         then the slot-2j+1 code (v_bits bits each)
   [.., +16*2)            V norm fp16 per slot
 KB = 4 * ceil(2 * total_bits / 32) with total_bits the per-head width budget.
+The pages fix what is stored (code streams plus norms), not the byte order;
+the value codes of two slots sit side by side so that a reader can take
+one channel of two tokens as one 2*v_bits-bit field.
 """
 from __future__ import annotations
 
@@ -305,6 +311,28 @@ def tile_layout(total_bits: int, v_bits: int) -> dict:
     return off
 
 
+def v_pair_offset(total_bits: int, v_bits: int, slot: int) -> int:
+    """Byte offset, in a tile, of the value-code pair row holding `slot`."""
+    lay = tile_layout(total_bits, v_bits)
+    return lay["v_codes"] + (slot // 2) * 2 * lay["vb"]
+
+
+def read_v_codes(tile, slot: int, total_bits: int, v_bits: int) -> np.ndarray:
+    """The 128 value codes of one slot of a tile."""
+    o = v_pair_offset(total_bits, v_bits, slot)
+    pair = unpack_bits(tile[o:o + 2 * v_code_bytes(v_bits)], [v_bits] * (2 * D)).reshape(D, 2)
+    return pair[:, slot % 2]
+
+
+def write_v_codes(tile, slot: int, codes, total_bits: int, v_bits: int):
+    """Store one slot's 128 value codes, keeping its pair partner's."""
+    o = v_pair_offset(total_bits, v_bits, slot)
+    n = 2 * v_code_bytes(v_bits)
+    pair = unpack_bits(tile[o:o + n], [v_bits] * (2 * D)).reshape(D, 2)
+    pair[:, slot % 2] = codes
+    tile[o:o + n] = pack_bits(pair.reshape(-1), [v_bits] * (2 * D), n)
+
+
 def new_cache(num_pages, h_kv, total_bits, v_bits):
     return np.zeros((num_pages, h_kv, tile_layout(total_bits, v_bits)["tile"]), np.uint8)
 
@@ -334,7 +362,7 @@ def append(cache, k, v, slot_mapping, widths, v_bits, total_bits, pis, table):
     v = np.asarray(v, np.float32)
     n, h_kv, _ = k.shape
     lay = tile_layout(total_bits, v_bits)
-    kb, vb = lay["kb"], lay["vb"]
+    kb = lay["kb"]
     cbv = scaled_codebook(table, v_bits, D)
     for t in range(n):
         slot = int(slot_mapping[t])
@@ -347,8 +375,7 @@ def append(cache, k, v, slot_mapping, widths, v_bits, total_bits, pis, table):
             o = lay["k_norms"] + 16 * s
             cache[page, h, o:o + 16] = norms.view(np.uint8)
             codes, nh, _, _ = tq_encode(v[t, h], pis[D], cbv)
-            o = lay["v_codes"] + vb * s
-            cache[page, h, o:o + vb] = pack_bits(codes, [v_bits] * D, vb)
+            write_v_codes(cache[page, h], s, codes, total_bits, v_bits)
             o = lay["v_norms"] + 2 * s
             cache[page, h, o:o + 2] = np.asarray([nh], np.float16).view(np.uint8)
 
@@ -356,7 +383,7 @@ def append(cache, k, v, slot_mapping, widths, v_bits, total_bits, pis, table):
 def read_token(cache, page, slot, h, widths, v_bits, total_bits, pis, table):
     """Dequantised (k^, v^) [d] fp64 of one cached token, original basis."""
     lay = tile_layout(total_bits, v_bits)
-    kb, vb = lay["kb"], lay["vb"]
+    kb = lay["kb"]
     tile = cache[page, h]
     kh = np.zeros(D)
     groups = [(b, bl) for b, bl in width_groups(widths) if bl]
@@ -372,8 +399,7 @@ def read_token(cache, page, slot, h, widths, v_bits, total_bits, pis, table):
         xb = tq_decode(vals[pos:pos + n], norms[b - 1], pis[n], scaled_codebook(table, b, n))
         scatter(xb, bl, kh)
         pos += n
-    o = lay["v_codes"] + vb * slot
-    vcodes = unpack_bits(tile[o:o + vb], [v_bits] * D)
+    vcodes = read_v_codes(tile, slot, total_bits, v_bits)
     o = lay["v_norms"] + 2 * slot
     vn = tile[o:o + 2].view(np.float16)[0]
     vh = tq_decode(vcodes, vn, pis[D], scaled_codebook(table, v_bits, D))

@@ -64,6 +64,26 @@ def test_append_bit_exact(table, avg_bits, v_bits, b_max):
     assert np.array_equal(layer.cache.cpu().numpy(), cache)
 
 
+def test_append_rewrites_one_slot_of_a_pair(table):
+    """Value codes of slots 2j, 2j + 1 share a pair row: writing one slot
+    again (here with other vectors, some in the same call as their partner)
+    replaces its codes and keeps the partner's."""
+    spec = _spec("bgpair", ctx=40)
+    layer = BgtqLayer(spec, 0, codebooks=table)
+    k, v = layer.history_kv(0, device="cpu")
+    slots = inputs.slot_mapping(layer.block_table[0].cpu(), history_positions(spec))
+    cache = _append_both(layer, table, k, v, slots)
+    g = torch.Generator().manual_seed(5)
+    pick = torch.tensor([3, 4, 9, 20, 21, 30])
+    k2 = (torch.randn(len(pick), *k.shape[1:], generator=g) * 2).to(k.dtype)
+    v2 = torch.randn(len(pick), *v.shape[1:], generator=g).to(v.dtype)
+    layer.append(k2.cuda(), v2.cuda(), slots[pick].cuda().contiguous())
+    torch.cuda.synchronize()
+    bgtq.append(cache, _f32(k2), _f32(v2), slots[pick].numpy(), layer.widths_np, layer.v_bits, layer.total_bits,
+                _pis(layer), table)
+    assert np.array_equal(layer.cache.cpu().numpy(), cache)
+
+
 def test_library_codebooks_give_the_same_cache(table):
     spec = _spec("bglib", ctx=24)
     a = BgtqLayer(spec, 0)                         # library Lloyd-Max codebooks
@@ -209,9 +229,11 @@ def test_full_size_k3v3_sampled(table):
         gpu = layer.cache[:, h].cpu().numpy()
         for t in idx:
             page, s = divmod(int(slots[t]), 16)
-            for off, n in ((lay["kb"] * s, lay["kb"]), (lay["k_norms"] + 16 * s, 16),
-                           (lay["v_codes"] + lay["vb"] * s, lay["vb"]), (lay["v_norms"] + 2 * s, 2)):
+            for off, n in ((lay["kb"] * s, lay["kb"]), (lay["k_norms"] + 16 * s, 16), (lay["v_norms"] + 2 * s, 2)):
                 assert np.array_equal(gpu[page, off:off + n], small[page, 0, off:off + n]), (h, t)
+            # value codes share a pair row with the partner slot: compare this slot's
+            assert np.array_equal(bgtq.read_v_codes(gpu[page], s, layer.total_bits, layer.v_bits),
+                                  bgtq.read_v_codes(small[page, 0], s, layer.total_bits, layer.v_bits)), (h, t)
         kh, vh = bgtq.dequantize_dense(kf, vf, layer.widths_np[h], layer.v_bits, pis, table, exact_chain=False)
         g = spec.g
         ref = attention.gqa_decode(q[0, h * g:(h + 1) * g].cpu().double().numpy(), kh[:, None], vh[:, None],

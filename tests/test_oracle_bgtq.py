@@ -445,3 +445,29 @@ def test_dequantize_dense_approaches_the_input_at_high_width(table):
         ev = np.sum((vh - v) ** 2, -1) / np.sum(v.astype(np.float64) ** 2, -1)
         assert ek.max() <= 20 * bgtq.C_TQ * 4.0 ** -7 and ev.max() <= 20 * bgtq.C_TQ * 4.0 ** -8
         assert ek.mean() <= bgtq.C_TQ * 4.0 ** -7
+
+
+def test_value_codes_sit_in_slot_pairs():
+    # the pair row of slots (2j, 2j+1) interleaves their codes channel by
+    # channel; writing one slot keeps the partner's codes
+    v_bits, total_bits = 3, 192
+    lay = bgtq.tile_layout(total_bits, v_bits)
+    tile = np.zeros(lay["tile"], np.uint8)
+    rng = np.random.default_rng(11)
+    even = rng.integers(0, 8, 128)
+    odd = rng.integers(0, 8, 128)
+    bgtq.write_v_codes(tile, 6, even, total_bits, v_bits)
+    bgtq.write_v_codes(tile, 7, odd, total_bits, v_bits)
+    o = lay["v_codes"] + 3 * 2 * lay["vb"]
+    row = tile[o:o + 2 * lay["vb"]]
+    # bit 6c + k of the row is bit k of slot 6's code of channel c (k < 3),
+    # bit 6c + 3 + k that of slot 7
+    bits = np.unpackbits(row, bitorder="little")
+    for c in (0, 1, 5, 127):
+        assert sum(int(bits[6 * c + k]) << k for k in range(3)) == even[c]
+        assert sum(int(bits[6 * c + 3 + k]) << k for k in range(3)) == odd[c]
+    # only that row is touched, and rewriting a slot leaves its partner alone
+    assert not tile[:o].any() and not tile[o + 2 * lay["vb"]:].any()
+    bgtq.write_v_codes(tile, 6, np.zeros(128, np.int64), total_bits, v_bits)
+    assert np.array_equal(bgtq.read_v_codes(tile, 7, total_bits, v_bits), odd)
+    assert not bgtq.read_v_codes(tile, 6, total_bits, v_bits).any()
