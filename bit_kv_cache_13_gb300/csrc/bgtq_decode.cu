@@ -39,12 +39,14 @@
 //       an A register.  Lane (r, t) owns channels 16r .. 16r+15 of token
 //       pairs t and t + 4 (v_bits words each).  B = p^ r_v as an exact fp16
 //       hi/lo pair in the N columns.
-// The tables live in a static shared-memory area aligned to 8 KB; each
-// table is replicated across the banks (entry e, copy c at e * copies + c,
-// a lane reads copy lane % copies), so a warp's random lookups mostly hit
-// distinct banks, and since each table is aligned to its size a lookup
-// address is (index << shift) | copy offset: one shift and one LOP3.
+// The tables live in a static shared-memory area; each table is replicated
+// across the banks (entry e, copy c at e * copies + c, a lane reads copy
+// lane % copies), so a warp's random lookups mostly hit distinct banks, and
+// since each table sits at an offset aligned to its size, an entry's offset
+// is index | (table offset | copy offset): one LOP3 on the index, which the
+// code window already holds at the right bit position.
 #include <cmath>
+#include <type_traits>
 #include <mutex>
 
 #include "bgtq_common.cuh"
@@ -69,7 +71,8 @@ struct BgChunk {
     int16_t pos0;  // first gathered position
 };
 
-// ---- lookup tables (byte offsets in the 8 KB-aligned table area)
+// ---- lookup tables (byte offsets in the table area; each pair table is
+// aligned, within the area, to its size)
 constexpr int KP_MAX = 5;  // key widths with pair tables
 constexpr int VP_MAX = 5;  // value widths with pair tables
 // log2 of the copies of each pair table: 16 copies make a half-warp's 64-bit
@@ -84,7 +87,6 @@ constexpr int V_OFF = 24576;   // value table: pairs (4^v x copies x 4 B) or fp1
 constexpr int KS_OFF = 35328;  // single-code key tables of widths 6..8: (hi | lo << 16) per code
 __host__ __device__ constexpr int ks_off(int b) { return KS_OFF + (b == 6 ? 0 : b == 7 ? 256 : 768); }
 constexpr int LUT_BYTES = KS_OFF + 1792;
-constexpr int LUT_ALIGN = 8192;
 static_assert((1 << (2 * 1)) * 16 * 8 == 512 && kp_off(1) % 512 == 0 && kp_off(1) + 512 <= KS_OFF, "key table 1");
 static_assert((1 << (2 * 2)) * 16 * 8 == 2048 && kp_off(2) % 2048 == 0 && kp_off(2) + 2048 <= kp_off(1), "key table 2");
 static_assert((1 << (2 * 3)) * 16 * 8 == 8192 && (1 << (2 * 4)) * 4 * 8 == 8192 && (1 << (2 * 5)) * 8 == 8192,
@@ -180,36 +182,50 @@ __device__ __forceinline__ void build_tables(uint8_t* lut, const float* cbs, con
     }
 }
 
+// D = A B (+ 0): the first MMA of an accumulator needs no zeroed registers.
+__device__ __forceinline__ void mma_f16_16816_first(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};"
+        : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// Bits the lane's code window is shifted left by before the lookups: the
+// first position pair then sits where the table index goes.
+template <int B>
+__host__ __device__ constexpr int qk_pre_shift() { return B <= KP_MAX ? 3 + kp_lg_copies(B) : 0; }
+
 // QK of one chunk (16 positions of width B) for the unit's pages: the MMA
-// accumulators cg run over the chunk's width group.  xw: per page, the
-// lane's 4B code bits of tokens r and r + 8 (from bit 0).
-template <int B, int NT>
-__device__ __forceinline__ void qk_chunk(const uint32_t (&xw)[BG_UNIT][2], int lane, const uint2 (&bb)[NT],
+// accumulators cg run over the chunk's width group (FIRST: the group's first
+// chunk starts them).  xw: per page, the lane's 4B code bits of tokens r and
+// r + 8, shifted left by qk_pre_shift<B>() (garbage below).  tsel: the byte
+// offset of the lane's copy of the width's table in the table area (the
+// table is aligned to its size, so an entry's offset is index | tsel).
+template <int B, int NT, bool FIRST>
+__device__ __forceinline__ void qk_chunk(const uint32_t (&xw)[BG_UNIT][2], uint32_t tsel, const uint2 (&bb)[NT],
                                          float (&cg)[2][BG_UNIT][NT][4], const uint8_t* __restrict__ lut) {
 #pragma unroll
     for (int e = 0; e < BG_UNIT; ++e) {
-        const uint32_t x0 = xw[e][0], x8 = xw[e][1];  // the lane's 4B code bits of tokens r, r + 8
+        const uint32_t x0 = xw[e][0], x8 = xw[e][1];
         // Two MMAs per page: rows r / r + 8 of the first are token r's hi /
         // lo centroid parts, of the second token r + 8's, so each A quad is
         // two table entries (hi pair, lo pair) of one token: positions
         // (4t, 4t+1) give a0, a1 and positions (4t+2, 4t+3) give a2, a3.
         uint32_t aA[4], aB[4];
         if constexpr (B <= KP_MAX) {
-            constexpr int S = 3 + kp_lg_copies(B);
+            constexpr int S = qk_pre_shift<B>();
             constexpr uint32_t MK = ((1u << (2 * B)) - 1u) << S;
-            const uint32_t cp = ((uint32_t)lane << 3) & ((1u << S) - 1u);
-            const uint8_t* tab = lut + kp_off(B);
-            const uint2 e0 = *reinterpret_cast<const uint2*>(tab + (((x0 << S) & MK) | cp));
-            const uint2 e2 = *reinterpret_cast<const uint2*>(tab + ((shift_left<S - 2 * B>(x0) & MK) | cp));
-            const uint2 e1 = *reinterpret_cast<const uint2*>(tab + (((x8 << S) & MK) | cp));
-            const uint2 e3 = *reinterpret_cast<const uint2*>(tab + ((shift_left<S - 2 * B>(x8) & MK) | cp));
+            const uint2 e0 = *reinterpret_cast<const uint2*>(lut + ((x0 & MK) | tsel));
+            const uint2 e2 = *reinterpret_cast<const uint2*>(lut + (((x0 >> (2 * B)) & MK) | tsel));
+            const uint2 e1 = *reinterpret_cast<const uint2*>(lut + ((x8 & MK) | tsel));
+            const uint2 e3 = *reinterpret_cast<const uint2*>(lut + (((x8 >> (2 * B)) & MK) | tsel));
             aA[0] = e0.x; aA[1] = e0.y; aA[2] = e2.x; aA[3] = e2.y;
             aB[0] = e1.x; aB[1] = e1.y; aB[2] = e3.x; aB[3] = e3.y;
         } else {
             constexpr uint32_t M = (1u << B) - 1u;
-            const uint32_t* tab = reinterpret_cast<const uint32_t*>(lut + ks_off(B));
 #pragma unroll
             for (int j = 0; j < 2; ++j) {  // position pair j of the lane: codes at bits 2jB, (2j+1)B
+                const uint32_t* tab = reinterpret_cast<const uint32_t*>(lut + tsel);
                 const uint32_t c0 = tab[(x0 >> (2 * j * B)) & M], c1 = tab[(x0 >> ((2 * j + 1) * B)) & M];
                 const uint32_t d0 = tab[(x8 >> (2 * j * B)) & M], d1 = tab[(x8 >> ((2 * j + 1) * B)) & M];
                 aA[2 * j] = prmt(c0, c1, 0x5410);
@@ -220,8 +236,13 @@ __device__ __forceinline__ void qk_chunk(const uint32_t (&xw)[BG_UNIT][2], int l
         }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {  // tokens r and r + 8 in separate chains
-            mma_f16_16816(cg[0][e][nt], aA, bb[nt].x, bb[nt].y);
-            mma_f16_16816(cg[1][e][nt], aB, bb[nt].x, bb[nt].y);
+            if constexpr (FIRST) {
+                mma_f16_16816_first(cg[0][e][nt], aA, bb[nt].x, bb[nt].y);
+                mma_f16_16816_first(cg[1][e][nt], aB, bb[nt].x, bb[nt].y);
+            } else {
+                mma_f16_16816(cg[0][e][nt], aA, bb[nt].x, bb[nt].y);
+                mma_f16_16816(cg[1][e][nt], aB, bb[nt].x, bb[nt].y);
+            }
         }
     }
 }
@@ -236,16 +257,19 @@ __device__ __forceinline__ void qk_width(const uint8_t* const (&tiles)[BG_UNIT],
     const int nch = sm.nch[B];
     if (nch == 0) return;  // warp-uniform
     const int r = lane >> 2, t = lane & 3, k0 = sm.kbase[B];
+    constexpr int S = qk_pre_shift<B>();
+    uint32_t tsel;
+    if constexpr (B <= KP_MAX)
+        tsel = kp_off(B) | (((uint32_t)lane << 3) & ((1u << S) - 1u));  // the lane's copy
+    else
+        tsel = ks_off(B);
     float cg[2][BG_UNIT][NT][4];
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int e = 0; e < BG_UNIT; ++e)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) cg[i][e][nt][0] = cg[i][e][nt][1] = cg[i][e][nt][2] = cg[i][e][nt][3] = 0.f;
-    int off = sm.L.bitstart[B] + 4 * t * B;  // the lane's first code bit in a token's stream
-#pragma unroll 1
-    for (int c = 0; c < nch; ++c, off += 16 * B) {
+    // the window starts S bits before the lane's first code bit (for the
+    // stream's first bit that is inside the word before it: the previous
+    // token's record, or the shared memory below the ring; those bits are
+    // masked off)
+    int off = sm.L.bitstart[B] + 4 * t * B - S;
+    auto chunk = [&](int c, auto first) {
         uint2 bb[NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) bb[nt] = sm.bfr[k0 + c][nt][lane];
@@ -258,8 +282,12 @@ __device__ __forceinline__ void qk_width(const uint8_t* const (&tiles)[BG_UNIT],
                 const uint32_t* w = reinterpret_cast<const uint32_t*>(tiles[e] + (r + 8 * i) * tl.kb + wofs);
                 xw[e][i] = __funnelshift_r(w[0], w[1], sh);
             }
-        qk_chunk<B, NT>(xw, lane, bb, cg, lut);
-    }
+        qk_chunk<B, NT, decltype(first)::value>(xw, tsel, bb, cg, lut);
+        off += 16 * B;
+    };
+    chunk(0, std::true_type{});
+#pragma unroll 1
+    for (int c = 1; c < nch; ++c) chunk(c, std::false_type{});
 #pragma unroll
     for (int e = 0; e < BG_UNIT; ++e) {
         const __half* nrm = reinterpret_cast<const __half*>(tiles[e] + tl.off_kn + 2 * (B - 1));
@@ -276,9 +304,10 @@ __device__ __forceinline__ void qk_width(const uint8_t* const (&tiles)[BG_UNIT],
 }
 
 // The table entry (an A register) of channel 16r + I of the lane's field f
-// (the v_bits words of one token pair).
+// (the v_bits words of one token pair); vsel: the byte offset of the lane's
+// copy of the value table in the table area.
 template <int VB, int I>
-__device__ __forceinline__ uint32_t v_entry(const uint32_t (&f)[VB], uint32_t cp, const uint8_t* __restrict__ lut) {
+__device__ __forceinline__ uint32_t v_entry(const uint32_t (&f)[VB], uint32_t vsel, const uint8_t* __restrict__ lut) {
     constexpr int BIT = 2 * VB * I, W = BIT >> 5, SH = BIT & 31;
     constexpr bool STRADDLE = SH + 2 * VB > 32;
     if constexpr (VB <= VP_MAX) {
@@ -289,7 +318,7 @@ __device__ __forceinline__ uint32_t v_entry(const uint32_t (&f)[VB], uint32_t cp
             x = __funnelshift_r(f[W], f[W + 1], SH - SV);  // SH > 32 - 2 VB >= SV here
         else
             x = shift_left<SV - SH>(f[W]);
-        return *reinterpret_cast<const uint32_t*>(lut + V_OFF + ((x & MV) | cp));
+        return *reinterpret_cast<const uint32_t*>(lut + ((x & MV) | vsel));
     } else {
         constexpr uint32_t M = (1u << VB) - 1u;
         uint32_t x;
@@ -297,7 +326,7 @@ __device__ __forceinline__ uint32_t v_entry(const uint32_t (&f)[VB], uint32_t cp
             x = __funnelshift_r(f[W], f[W + 1], SH);
         else
             x = f[W] >> SH;
-        const unsigned short* tab = reinterpret_cast<const unsigned short*>(lut + V_OFF);
+        const unsigned short* tab = reinterpret_cast<const unsigned short*>(lut + vsel);
         return (uint32_t)tab[x & M] | ((uint32_t)tab[(x >> VB) & M] << 16);
     }
 }
@@ -317,14 +346,15 @@ __device__ __forceinline__ void pv_page(const uint8_t* tile, int off_vc, int lan
         f0[w] = p0[w];
         f1[w] = p1[w];
     }
-    uint32_t cp = 0u;
-    if constexpr (VB <= VP_MAX) cp = ((uint32_t)lane << 2) & ((1u << (2 + vp_lg_copies(VB))) - 1u);
+    // the lane's copy of the value table (the table is aligned to its size)
+    uint32_t vsel = V_OFF;
+    if constexpr (VB <= VP_MAX) vsel |= ((uint32_t)lane << 2) & ((1u << (2 + vp_lg_copies(VB))) - 1u);
     // a0 = (channel 16r + 2m, tokens 2t, 2t+1), a1 = (16r + 2m + 1, same),
     // a2 = (16r + 2m, tokens 2t+8, 2t+9), a3 = (16r + 2m + 1, same)
 #define KVQ_PV_M(m)                                                                                   \
     {                                                                                                 \
-        const uint32_t a[4] = {v_entry<VB, 2 * (m)>(f0, cp, lut), v_entry<VB, 2 * (m) + 1>(f0, cp, lut), \
-                               v_entry<VB, 2 * (m)>(f1, cp, lut), v_entry<VB, 2 * (m) + 1>(f1, cp, lut)}; \
+        const uint32_t a[4] = {v_entry<VB, 2 * (m)>(f0, vsel, lut), v_entry<VB, 2 * (m) + 1>(f0, vsel, lut),   \
+                               v_entry<VB, 2 * (m)>(f1, vsel, lut), v_entry<VB, 2 * (m) + 1>(f1, vsel, lut)}; \
         mma_f16_16816(oacc[m], a, bh0, bh1);                                                          \
         if constexpr (NT == 2) mma_f16_16816(oacc[m], a, bl0, bl1);                                   \
     }
@@ -345,7 +375,7 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     constexpr int NW = BgWarps<MAXG>::NW;
     constexpr int NT = MAXG / 4;  // n-tiles of 8 columns (4 heads x hi/lo)
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    __shared__ __align__(LUT_ALIGN) uint8_t lut[LUT_BYTES];
+    __shared__ __align__(16) uint8_t lut[LUT_BYTES];
     BgDecodeSmem<NW, MAXG>& sm = *reinterpret_cast<BgDecodeSmem<NW, MAXG>*>(smem_raw);
     const BgtqTile tl(total_bits, VB);
     // the page rings follow the fixed part; after the loop the per-warp o'
@@ -459,15 +489,16 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             bulk_g2s(my_ring + (size_t)(BG_UNIT * st + lane) * tl.bytes, cache + ((size_t)pid * H_kv + h) * tl.bytes,
                      tl.bytes, bar);
     };
+    // the first slot group's copies now; the others once the setup's own
+    // reads are out (below)
     int pid_next = 0, n_issued = 0;
-#pragma unroll
-    for (int u = 0; u <= BG_MAX_STAGES / BG_UNIT; ++u) {
-        if (u < n_grp && u < n_units) {  // warp-uniform
-            issue_unit(u, u, pid_pre[u]);
-            n_issued = u + 1;
-        }
-        if (u == n_grp) pid_next = pid_pre[u];
+    if (n_units > 0) {  // warp-uniform
+        issue_unit(0, 0, pid_pre[0]);
+        n_issued = 1;
     }
+#pragma unroll
+    for (int u = 0; u <= BG_MAX_STAGES / BG_UNIT; ++u)
+        if (u == n_grp) pid_next = pid_pre[u];
     {
         // the block table is read later: have L2 keep it
         const char* btc = reinterpret_cast<const char*>(bt);
@@ -535,11 +566,8 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
     }
     __syncthreads();
     // the table area must sit on its alignment for the OR-formed addresses
-    const bool lut_ok = (smem_u32(lut) & (LUT_ALIGN - 1)) == 0;
-    const bool widths_ok = sm.L.ok && sm.L.total_bits <= 2 * total_bits;
-    const bool layout_ok = widths_ok && lut_ok;
-    if (tid == 0 && !widths_ok) atomicOr(err_word, ERR_BAD_WIDTHS);
-    if (tid == 0 && !lut_ok) atomicOr(err_word, ERR_LUT_ALIGN);
+    const bool layout_ok = sm.L.ok && sm.L.total_bits <= 2 * total_bits;
+    if (tid == 0 && !layout_ok) atomicOr(err_word, ERR_BAD_WIDTHS);
     // q~ at gathered position p: sum_i q[dim(st + i)] Pi_n[i][p - st], the i
     // split over NPART thread groups (their loads go out together)
     constexpr int NPART = NTHR / D;
@@ -548,19 +576,43 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         float acc[MAXG];
 #pragma unroll
         for (int jj = 0; jj < MAXG; ++jj) acc[jj] = 0.f;
-        if (layout_ok) {
-            int bb = 1;
-            while (bb < 8 && !(p >= sm.L.start[bb] && p < sm.L.start[bb] + sm.L.n[bb])) ++bb;
-            const int st = sm.L.start[bb], n = sm.L.n[bb], j = p - st;
-            const float* pi = pi_table + sm.pioff[n / 2];
-#pragma unroll 8
-            for (int i = part; i < n; i += NPART) {
-                const float pv = __ldg(pi + (size_t)i * n + j);
+        int bb = 1;
+        while (bb < 8 && !(p >= sm.L.start[bb] && p < sm.L.start[bb] + sm.L.n[bb])) ++bb;
+        const int st = sm.L.start[bb], n = layout_ok ? sm.L.n[bb] : 0, j = p - st;
+        const float* pi = pi_table + sm.pioff[n / 2];
+        // the first QROT_REG terms' rotation entries are requested before
+        // the later page copies go out, so they do not queue behind them
+        constexpr int QROT_REG = 16;
+        float pvr[QROT_REG];
+#pragma unroll
+        for (int k = 0; k < QROT_REG; ++k) {
+            const int i = part + NPART * k;
+            pvr[k] = i < n ? __ldg(pi + (size_t)i * n + j) : 0.f;
+        }
+        // the page copies of the remaining slot groups
+#pragma unroll
+        for (int u = 1; u < BG_MAX_STAGES / BG_UNIT; ++u)
+            if (u < n_grp && u < n_units) {  // warp-uniform
+                issue_unit(u, u, pid_pre[u]);
+                n_issued = u + 1;
+            }
+#pragma unroll
+        for (int k = 0; k < QROT_REG; ++k) {
+            const int i = part + NPART * k;
+            if (i < n) {
                 const int dm = sm.L.dim[st + i];
 #pragma unroll
                 for (int jj = 0; jj < MAXG; ++jj)
-                    if (jj < G) acc[jj] = fmaf(sm.qin[jj][dm], pv, acc[jj]);
+                    if (jj < G) acc[jj] = fmaf(sm.qin[jj][dm], pvr[k], acc[jj]);
             }
+        }
+#pragma unroll 8
+        for (int i = part + NPART * QROT_REG; i < n; i += NPART) {  // groups of more than 48 (or 32) positions
+            const float pv = __ldg(pi + (size_t)i * n + j);
+            const int dm = sm.L.dim[st + i];
+#pragma unroll
+            for (int jj = 0; jj < MAXG; ++jj)
+                if (jj < G) acc[jj] = fmaf(sm.qin[jj][dm], pv, acc[jj]);
         }
         if (part > 0) {
 #pragma unroll

@@ -1250,7 +1250,6 @@ extern "C" kvq_status kvq_workspace_status(void* workspace, void* stream) {
         if (s != KVQ_OK) return s;
     }
     if (word & ERR_TIMEOUT) return kvq_set_error(KVQ_ERR_CUDA, "decode: an in-kernel wait timed out");
-    if (word & ERR_LUT_ALIGN) return kvq_set_error(KVQ_ERR_CUDA, "decode: lookup-table area misaligned");
     if (word & ERR_BAD_WIDTHS) return kvq_set_error(KVQ_ERR_INVALID_ARG, "decode: widths outside 1..8 or over budget");
     if (word & ERR_BAD_PAGE) return kvq_set_error(KVQ_ERR_BAD_BLOCK_TABLE, "decode: block table entry out of range");
     return KVQ_OK;

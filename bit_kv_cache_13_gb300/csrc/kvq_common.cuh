@@ -28,7 +28,6 @@ __host__ __device__ constexpr int vm_scale_off(int s, int g) { return OFF_VM + 1
 constexpr int WS_HEADER = 256;
 constexpr int PART_STRIDE = 132;  // floats per (seq, q head, split): m, l, pad, pad, o[128]
 constexpr uint32_t ERR_BAD_PAGE = 1u, ERR_TIMEOUT = 2u, ERR_BAD_WIDTHS = 4u;
-constexpr uint32_t ERR_LUT_ALIGN = 8u;  // a shared-memory table area off its alignment (never expected)
 
 // give an mbarrier wait about two seconds at ~2 GHz before declaring failure
 constexpr long long WAIT_LIMIT_CYCLES = 4000000000LL;
