@@ -6,11 +6,13 @@
 // the output is rotated back once (o = o' R_v^T).  The kernel reads only the
 // packed codes and fp16 (scale, min) pairs.
 //
-// Grid (split, kv_head, seq) with one large CTA per SM (12 warps for head
-// groups up to 4, 8 for groups of 8).  Each warp streams pages through its
-// own 9-slot ring of 1536-byte tiles filled by bulk async copies
-// (cp.async.bulk + mbarrier).  The pages of a (sequence, KV head) are dealt
-// round-robin over all warps of its split CTAs.  Per page (16 tokens):
+// One large CTA per SM (12 warps for head groups up to 4, 8 for groups of
+// 8).  The batch's (sequence, KV head) units are laid end to end as virtual
+// pages and every CTA takes an equal contiguous share (at most two units),
+// so all SMs stream whatever B * H_kv is; within a share the pages are dealt
+// round-robin over the CTA's warps.  Each warp streams pages through its own
+// 9-slot ring of 1536-byte tiles filled by bulk async copies
+// (cp.async.bulk + mbarrier).  Per page (16 tokens):
 //
 //   QK  logit(s, j) = sum_g [ scale_{s,g} <q'_{j,g}, c_{s,g}> + min_{s,g} S_{j,g} ]
 //       The 2-bit codes c are fed to mma.sync m16n8k16 as exact fp16
@@ -29,9 +31,12 @@
 //   release, one softmax rescale per unit); the QK of unit u + 1 and the
 //   softmax/PV of unit u are software-pipelined.
 //
-// Split partials (m, l, o') go to the workspace; the last CTA of a
-// (sequence, KV head) to finish (atomic ticket, no waiting) merges them,
-// applies R_v^T and writes the output.
+// Each CTA merges its warps, rotates the merged partial by R_v^T (linear,
+// so this equals one rotation of the final output) and publishes it per
+// unit; the last CTA of a (sequence, KV head) to finish (atomic ticket, no
+// waiting) merges the unit's partials and writes the output.  In the decode
+// step the CTA holding a sequence's new token also quantises and writes it,
+// and attends it from registers.
 #include <atomic>
 #include <mutex>
 
