@@ -356,7 +356,7 @@ def measure_int2_window(spec, device, stream, reps):
     q = layer.queries()
     g = torch.Generator(device=device)
     g.manual_seed(13)
-    w = 4 + 128
+    w = inputs.WINDOW_SINK + inputs.WINDOW_RECENT
     win_k = torch.randn((spec.batch, w, spec.h_kv, spec.d), generator=g, device=device).to(torch.bfloat16)
     win_v = torch.randn((spec.batch, w, spec.h_kv, spec.d), generator=g, device=device).to(torch.bfloat16)
     win_lens = torch.full((spec.batch,), w, dtype=torch.int32, device=device)

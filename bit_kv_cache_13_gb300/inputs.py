@@ -147,6 +147,10 @@ SPECS = {
 }
 
 
+# BF16 window of the window workload: sink and recent tokens per sequence
+WINDOW_SINK, WINDOW_RECENT = 4, 128
+
+
 def sweep70b_spec(batch: int, ctx: int) -> Spec:
     return Spec(f"sweep70b_b{batch}_t{ctx}", 1, 64, 8, batch, ctx,
                 "outlier_offset", "outlier20", permute_pages=True)
