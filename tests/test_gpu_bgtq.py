@@ -102,6 +102,8 @@ def test_library_codebooks_give_the_same_cache(table):
     (16, 2, [17, 260, 33], 3),
     (32, 4, [129, 64], 0),
     (16, 2, [50], 40),
+    (8, 2, [0, 37, 16], 0),   # an empty sequence, an odd tail (half a slot pair), a whole page
+    (64, 8, [33, 0], 2),      # GQA 8 over 8 KV heads with an empty second sequence
 ])
 def test_decode_vs_oracle(table, h_q, h_kv, ctxs, splits):
     B = len(ctxs)
