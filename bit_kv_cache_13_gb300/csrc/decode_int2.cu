@@ -6,13 +6,13 @@
 // the output is rotated back once (o = o' R_v^T).  The kernel reads only the
 // packed codes and fp16 (scale, min) pairs.
 //
-// One large CTA per SM (12 warps for head groups up to 4, 8 for groups of
-// 8).  The batch's (sequence, KV head) units are laid end to end as virtual
+// One large CTA per SM of 12 warps.  The batch's (sequence, KV head) units are laid end to end as virtual
 // pages and every CTA takes an equal contiguous share (at most two units),
 // so all SMs stream whatever B * H_kv is; within a share the pages are dealt
 // round-robin over the CTA's warps.  Each warp streams pages through its own
-// 9-slot ring of 1536-byte tiles filled by bulk async copies
-// (cp.async.bulk + mbarrier).  Per page (16 tokens):
+// ring of 1536-byte tiles (9 slots for head groups up to 4, 6 for groups of
+// 8) filled by bulk async copies (cp.async.bulk + mbarrier).  Per page (16
+// tokens):
 //
 //   QK  logit(s, j) = sum_g [ scale_{s,g} <q'_{j,g}, c_{s,g}> + min_{s,g} S_{j,g} ]
 //       The 2-bit codes c are fed to mma.sync m16n8k16 as exact fp16
@@ -45,37 +45,44 @@
 
 namespace kvq {
 
-constexpr int DEC_STAGES = 9;  // page slots per warp
 constexpr int UNIT_PAGES = 3;  // pages per mbarrier phase (one wait, one release)
-constexpr int DEC_UNITS = DEC_STAGES / UNIT_PAGES;
-static_assert(DEC_STAGES % UNIT_PAGES == 0, "a unit is a whole number of page slots");
 
-// Warps per CTA.  Each of the SM's four schedulers owns a quarter of its
-// 64K registers: three warps of 168 registers fit one (head groups up to 4),
-// while groups of 8 need more registers per thread and run two per scheduler.
+// Page slots per warp: 9 (three units in flight) for head groups up to 4;
+// 6 for groups of 8, whose twelve warps would not fit 227 KB with nine.
+template <int MAXG>
+struct DecRing {
+    static constexpr int STAGES = MAXG <= 4 ? 9 : 6;
+    static constexpr int UNITS = STAGES / UNIT_PAGES;
+    static_assert(STAGES % UNIT_PAGES == 0, "a unit is a whole number of page slots");
+};
+
+// Warps per CTA: twelve, three per scheduler at 168 registers (a quarter of
+// the SM's 64K registers each).  Groups of 8 keep their QK B fragments in
+// shared memory (for 4 heads they stay in registers) to fit that budget.
 template <int NT>
 struct DecWarps {
-    static constexpr int NW = NT == 1 ? 12 : 8;
+    static constexpr int NW = 12;
 };
 
 template <int NW, int MAXG>
 struct __align__(16) DecodeSmem {
     struct {
-        uint8_t ring[NW][DEC_STAGES][INT2_TILE];  // page tiles in flight
+        uint8_t ring[NW][DecRing<MAXG>::STAGES][INT2_TILE];  // page tiles in flight
     } u;
     float o_part[NW + 1][MAXG][D];  // per-warp o' after the loop (its own space: a warp writes it as soon as
                                     // it is done), and the decode step's new token
-    uint64_t bar[NW][DEC_UNITS];
-    int ntok[NW][DEC_STAGES];  // valid tokens of the page in each stage (0: skipped page)
+    uint64_t bar[NW][DecRing<MAXG>::UNITS];
+    int ntok[NW][DecRing<MAXG>::STAGES];  // valid tokens of the page in each stage (0: skipped page)
     float q[MAXG][D];          // scaled rotated queries q~ = q R_k * scale * log2(e)
     float gsum[MAXG][NGROUP];
     float sigma[MAXG];         // power-of-two pre-scale per head
     int64_t share[2];          // this CTA's virtual pages [share[0], share[1])
     int dead;                  // a wait of this CTA ran out: no further copies
+    uint2 bq[MAXG == 8 ? 2 : 1][8][32];  // groups of 8: QK B fragments (n-tile, k-slice, lane)
     MergeSmem<NW, MAXG> ms;
 };
 
-static_assert(sizeof(DecodeSmem<12, 4>) <= 227 * 1024 && sizeof(DecodeSmem<8, 8>) <= 227 * 1024,
+static_assert(sizeof(DecodeSmem<12, 4>) <= 227 * 1024 && sizeof(DecodeSmem<12, 8>) <= 227 * 1024,
               "decode shared memory above 227 KB");
 
 // BF16 window (the INT2 paper keeps a small BF16 window, §3.1; the
@@ -267,6 +274,8 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
                    const __nv_bfloat16* __restrict__ win_k, const __nv_bfloat16* __restrict__ win_v,
                    const int32_t* __restrict__ win_lens, int win_max, float scale_log2, float* __restrict__ out,
                    uint8_t* __restrict__ ws, int n_cta, int vmp, int flags) {
+    constexpr int DEC_STAGES = DecRing<4 * NT>::STAGES;  // page slots per warp
+    constexpr int DEC_UNITS = DecRing<4 * NT>::UNITS;    // units in flight per warp
     constexpr bool EXTRA = MODE == MODE_WINDOW;  // one window CTA per unit after the page CTAs
     extern __shared__ __align__(128) uint8_t smem_raw[];
     constexpr int MAXG = 4 * NT;
@@ -553,7 +562,7 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
         __syncthreads();
 
         // ---- QK B fragments: column n = r -> head 4*nt + (r >> 1), part r & 1 (hi / lo)
-        uint32_t bq[NT][8][2];
+        uint32_t bq[8][2];  // NT == 1: the fragments in registers (NT == 2: sm.bq)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int hq = 4 * nt + (r >> 1);
@@ -573,10 +582,19 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
                     }
                     // hi part (even columns) or the exact remainder (odd columns), one path
                     const float h0 = __half2float(__float2half_rn(v0)), h1 = __half2float(__float2half_rn(v1));
-                    bq[nt][s][e] = pack_half2(lo_part ? v0 - h0 : h0, lo_part ? v1 - h1 : h1);
+                    const uint32_t w = pack_half2(lo_part ? v0 - h0 : h0, lo_part ? v1 - h1 : h1);
+                    if constexpr (NT == 1) {
+                        bq[s][e] = w;
+                    } else if (warp == 0) {  // the same for every warp: one writes them
+                        if (e == 0)
+                            sm.bq[nt][s][lane].x = w;
+                        else
+                            sm.bq[nt][s][lane].y = w;
+                    }
                 }
             }
         }
+        if constexpr (NT == 2) __syncthreads();  // the shared B fragments are complete
         float inv_sig[NT], gsum[NT][NGROUP];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -662,7 +680,12 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
                     for (int hs = 0; hs < 2; ++hs) {
                         const uint32_t m0 = 0x00030003u << (4 * hs), m1 = 0x00030003u << (4 * hs + 2);
                         const uint32_t a[4] = {xr & m0, xr8 & m0, xr & m1, xr8 & m1};
-                        mma_f16_16816(c, a, bq[nt][2 * g + hs][0], bq[nt][2 * g + hs][1]);
+                        if constexpr (NT == 1) {
+                            mma_f16_16816(c, a, bq[2 * g + hs][0], bq[2 * g + hs][1]);
+                        } else {
+                            const uint2 bb = sm.bq[nt][2 * g + hs][lane];
+                            mma_f16_16816(c, a, bb.x, bb.y);
+                        }
                     }
                     acc_r[nt] = fmaf(smr.x, c[0] + c[1], acc_r[nt]);
                     acc_r8[nt] = fmaf(smr8.x, c[2] + c[3], acc_r8[nt]);
