@@ -35,8 +35,9 @@ def _decode(layer, q, ws, splits=0):
     return out
 
 
-def test_wait_that_runs_out_is_reported_and_the_context_stays_usable():
-    layer = _layer("tmo", h_q=8, h_kv=2, batch=2, ctx=700)
+@pytest.mark.parametrize("h_q", [8, 16])  # GQA 4 (9-slot rings) and GQA 8 (6-slot rings)
+def test_wait_that_runs_out_is_reported_and_the_context_stays_usable(h_q):
+    layer = _layer(f"tmo{h_q}", h_q=h_q, h_kv=2, batch=2, ctx=700)
     q = layer.queries()
     ws = layer.workspace()
     good = _decode(layer, q, ws)
