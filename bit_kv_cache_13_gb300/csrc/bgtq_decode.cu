@@ -579,7 +579,7 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
         int bb = 1;
         while (bb < 8 && !(p >= sm.L.start[bb] && p < sm.L.start[bb] + sm.L.n[bb])) ++bb;
         const int st = sm.L.start[bb], n = layout_ok ? sm.L.n[bb] : 0, j = p - st;
-        const float* pi = pi_table + sm.pioff[n / 2];
+        const float* pi = pi_table + (n > 0 ? sm.pioff[n / 2] : 0);  // (n = 0: nothing is read)
         // the first QROT_REG terms' rotation entries are requested before
         // the later page copies go out, so they do not queue behind them
         constexpr int QROT_REG = 16;
