@@ -42,44 +42,6 @@ __device__ __forceinline__ void build_layout(const int8_t* __restrict__ w, BgtqL
     L.ok = ok && pos == D;
 }
 
-// The same layout built by a whole CTA (at least 64 threads) from a
-// shared-memory copy of the widths: thread b counts width b, thread i < 64
-// places block i at its rank among the blocks of its width.  Three barriers
-// inside; every thread of the CTA must call it.
-__device__ __forceinline__ void build_layout_cta(const int8_t* __restrict__ w, BgtqLayout& L, int8_t* wsm) {
-    const int tid = threadIdx.x;
-    if (tid < D / 2) wsm[tid] = w[tid];
-    __syncthreads();
-    if (tid >= 1 && tid <= 8) {  // thread b counts the blocks of width b
-        int c = 0;
-        for (int i = 0; i < D / 2; ++i) c += wsm[i] == tid;
-        L.n[tid] = (int16_t)(2 * c);
-    }
-    __syncthreads();
-    if (tid == 0) {
-        int pos = 0, bit = 0, ok = 1;
-        for (int i = 0; i < D / 2; ++i) ok &= (wsm[i] >= 1 && wsm[i] <= 8);
-        for (int b = 1; b <= 8; ++b) {
-            L.start[b] = (int16_t)pos;
-            L.bitstart[b] = (int16_t)bit;
-            pos += L.n[b];
-            bit += b * L.n[b];
-        }
-        L.total_bits = bit;
-        L.ok = ok && pos == D;
-    }
-    __syncthreads();
-    if (tid < D / 2) {
-        const int b = wsm[tid];
-        if (b >= 1 && b <= 8) {
-            int rank = 0;
-            for (int j = 0; j < tid; ++j) rank += wsm[j] == b;
-            L.dim[L.start[b] + 2 * rank] = (int16_t)tid;
-            L.dim[L.start[b] + 2 * rank + 1] = (int16_t)(tid + D / 2);
-        }
-    }
-}
-
 __host__ __device__ inline int bgtq_kb(int total_bits) { return 4 * ((2 * total_bits + 31) / 32); }
 
 // Scaled codebook fp32(C_b[c] / sqrt(n)), computed in fp64 then rounded once.

@@ -65,9 +65,7 @@ struct BgWarps {
 // positions padded to a multiple of 16): at most 64/8 + 7 = 15 chunks.
 constexpr int BG_MAX_CHUNKS = 16;
 struct BgChunk {
-    int bit0;      // first code bit of the chunk in a token's key stream
-    int8_t b;      // width
-    int8_t last;   // the last chunk of its width group
+    int16_t b;     // width
     int16_t pos0;  // first gathered position
 };
 
@@ -545,9 +543,7 @@ bgtq_decode_kernel(const __nv_bfloat16* __restrict__ q, int H_q, int H_kv, int G
             }
             if (lane < nch && nc + lane < BG_MAX_CHUNKS) {
                 BgChunk ch;
-                ch.bit0 = bit + 16 * lane * bb;
-                ch.b = (int8_t)bb;
-                ch.last = (int8_t)(lane + 1 == nch);
+                ch.b = (int16_t)bb;
                 ch.pos0 = (int16_t)(pos + 16 * lane);
                 sm.chunks[nc + lane] = ch;
             }
