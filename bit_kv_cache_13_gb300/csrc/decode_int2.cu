@@ -291,6 +291,13 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
         float* partials = reinterpret_cast<float*>(ws + WS_HEADER + tickets_bytes(B, H_kv));
         return partials + (size_t)slot * G * PART_STRIDE;
     };
+    // Unit u's partials are this CTA's alone (one page CTA, no extra CTA):
+    // then no slot, ticket or merge is needed.
+    auto sole_partial = [&](int u) {
+        if (EXTRA) return false;
+        const PageSplit sp{(int64_t)B * H_kv * vmp, n_cta, vmp};
+        return sp.cta_of((int64_t)u * vmp) == sp.cta_of((int64_t)u * vmp + vmp - 1);
+    };
     auto finish_unit = [&](int u) {
         // publish this CTA's slot (already written), then the last CTA merges;
         // the partials of unit u are the page CTAs' slots u + c, then (with a
@@ -953,14 +960,24 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
         kbase += n_units;
         // the next kernel in the stream may be scheduled once every CTA is here
         if (last_seg) griddep_launch_dependents();
-        // this CTA's partial, carried to the output basis (O = o' R_v^T)
-        rotate_publish<NW, MAXG>(sm.ms, rvr, G, Rv + (size_t)h * D * D, slot_ptr((int64_t)u + cta));
+        // this CTA's partial, carried to the output basis (O = o' R_v^T); a
+        // unit whose only partial this is gets its output written directly
+        if (sole_partial(u))
+            rotate_publish<NW, MAXG, true>(sm.ms, rvr, G, Rv + (size_t)h * D * D,
+                                           out + ((size_t)b * H_q + (size_t)h * G) * D);
+        else
+            rotate_publish<NW, MAXG>(sm.ms, rvr, G, Rv + (size_t)h * D * D, slot_ptr((int64_t)u + cta));
         } else {
             if (last_seg) griddep_launch_dependents();
             griddep_wait();  // (early inputs) nothing is written before the wait
-            publish_slot<NW, MAXG>(sm.ms, sm.ms.o_final, G, slot_ptr((int64_t)u + cta), true);
+            if (sole_partial(u)) {  // no pages and no other partial: the output is zero
+                float* o = out + ((size_t)b * H_q + (size_t)h * G) * D;
+                for (int i = tid; i < G * D; i += NW * 32) o[i] = 0.f;
+            } else {
+                publish_slot<NW, MAXG>(sm.ms, sm.ms.o_final, G, slot_ptr((int64_t)u + cta), true);
+            }
         }
-        finish_unit(u);
+        if (!sole_partial(u)) finish_unit(u);
         __syncthreads();  // the next segment reuses the ring and the merge scratch
     };
     segment(u_first, false);
@@ -1036,8 +1053,10 @@ static int64_t int2_page_ctas(int B, int H_kv, int max_pages, int num_splits, bo
 // a sequence's new token also quantises and attends it (a few microseconds,
 // about as long as streaming ~100 pages), so each unit gets that many
 // virtual pages without work after its last page, and the share holding a
-// full sequence's last page streams fewer real ones.
-static int step_virtual_pages(int max_pages) { return max_pages + (max_pages < 96 ? max_pages : 96); }
+// full sequence's last page streams fewer real ones.  Below 96 pages a
+// unit is one CTA's work anyway, and the extra pages would only add a
+// second CTA (and a split-K merge) to it.
+static int step_virtual_pages(int max_pages) { return max_pages + (max_pages < 96 ? 0 : 96); }
 
 extern "C" int kvq_decode_auto_splits(int B, int H_q, int H_kv, int max_pages_per_seq) {
     if (B <= 0 || H_kv <= 0 || H_q < H_kv || max_pages_per_seq <= 0) return 1;

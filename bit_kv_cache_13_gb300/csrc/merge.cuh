@@ -370,12 +370,15 @@ __device__ __forceinline__ bool arrive_last(MergeSmem<NW, MAXG>& ms, int32_t* ti
 // Rotates this CTA's merged partial o_final (G heads) by Rot^T -- O_i =
 // sum_j o'_j Rot[i][j], Rot row-major [D][D], 16-byte aligned -- and writes
 // it, with (Mh, Lh), to a partial slot (head jj at slot + jj * PART_STRIDE as
-// m, l, -, -, O[128]).  rr holds each rotating warp's first rows of Rot
-// (load_rows, issued early so their latency is hidden).  Each lane forms the
-// partial dots of its 4 columns with its warp's rows, and a reduce-scatter
-// over the lanes leaves each row's full dot in one lane (heads two at a time
-// so their shuffle chains overlap).  All threads call it.
-template <int NW, int MAXG>
+// m, l, -, -, O[128]).  With DIRECT, the partial is the unit's only one: the
+// output out[jj][i] = O_i / Lh (0 when Lh = 0) is written instead, the value
+// the merge of that single partial would give.  rr holds each rotating
+// warp's first rows of Rot (load_rows, issued early so their latency is
+// hidden).  Each lane forms the partial dots of its 4 columns with its warp's
+// rows, and a reduce-scatter over the lanes leaves each row's full dot in
+// one lane (heads two at a time so their shuffle chains overlap).  All
+// threads call it.
+template <int NW, int MAXG, bool DIRECT = false>
 __device__ __forceinline__ void rotate_publish(const MergeSmem<NW, MAXG>& ms, float4 (&rr)[RowPrefetch<NW, MAXG>::N],
                                                int G, const float* __restrict__ Rot, float* __restrict__ slot) {
     constexpr int NR = RotSplit<NW>::NR, RPW = RotSplit<NW>::RPW, RP = RowPrefetch<NW, MAXG>::N;
@@ -416,15 +419,21 @@ __device__ __forceinline__ void rotate_publish(const MergeSmem<NW, MAXG>& ms, fl
                         vb[k] = kb + __shfl_xor_sync(0xffffffffu, sb, off);
                     }
                 }
-                const int row = 4 + RPW * warp + RP * pass + (lane & (RP - 1));
+                const int row = RPW * warp + RP * pass + (lane & (RP - 1));
                 if (RP == 32 || lane < 16) {
-                    slot[(size_t)jj * PART_STRIDE + row] = va[0];
-                    if (jj + 1 < G) slot[(size_t)(jj + 1) * PART_STRIDE + row] = vb[0];
+                    if constexpr (DIRECT) {  // slot is the heads' output rows [G][D]
+                        const float la = ms.Lh[jj], lb = ms.Lh[jb];
+                        slot[(size_t)jj * D + row] = va[0] * (la > 0.f ? 1.f / la : 0.f);
+                        if (jj + 1 < G) slot[(size_t)(jj + 1) * D + row] = vb[0] * (lb > 0.f ? 1.f / lb : 0.f);
+                    } else {
+                        slot[(size_t)jj * PART_STRIDE + 4 + row] = va[0];
+                        if (jj + 1 < G) slot[(size_t)(jj + 1) * PART_STRIDE + 4 + row] = vb[0];
+                    }
                 }
             }
         }
     }
-    if (tid < G) {
+    if (!DIRECT && tid < G) {
         slot[(size_t)tid * PART_STRIDE] = ms.Mh[tid];
         slot[(size_t)tid * PART_STRIDE + 1] = ms.Lh[tid];
     }

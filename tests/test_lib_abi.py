@@ -65,7 +65,7 @@ def test_workspace_with_auto_splits_holds_every_entry_point(cpu_lib):
         V = units * pages
         c_plain = min(max(min(nsm, -(-V // 32)), units), V)
         c_win = min(max(min(nsm - units if 2 * units <= nsm else nsm, -(-V // 32)), units), V)
-        vs = units * (pages + min(pages, 96))        # a decode step's virtual pages
+        vs = units * (pages + (0 if pages < 96 else 96))  # a decode step's virtual pages
         c_step = min(max(min(nsm, -(-vs // 32)), units), vs)
         slots = max(units + c_plain, 2 * units + c_win, units + c_step,
                     units * _lib.kvq_decode_auto_splits(B, H_q, H_kv, pages))
