@@ -107,6 +107,31 @@ def test_window_zero_lengths_match_plain_decode():
     assert err <= 1e-5 * plain.abs().max().item()
 
 
+def test_sole_partial_output_equals_its_merge_bit_for_bit():
+    # one split per unit: the plain decode's CTA is each unit's only partial
+    # and writes the output directly; the window form adds an (empty) window
+    # partial, so the same page partial goes through the slot, ticket and
+    # merge.  Merging one partial with an empty one is exact, so the two
+    # outputs must be identical.
+    spec = inputs.small_spec("solepart", h_q=16, h_kv=4, batch=3, ctx=700, permute=True)
+    layer = Int2Layer(spec, 0)
+    layer.prefill()
+    q = layer.queries()
+    ws = layer.workspace(2)
+    plain = torch.full((3, 16, 128), float("nan"), device="cuda")
+    _lib.kvq_decode_attn_int2(q, layer.cache, layer.num_pages, layer.block_table, layer.context_lens, layer.R_k,
+                              layer.R_v, layer.scale, plain, ws, 1)
+    kw = torch.randn(3, 4, 4, 128, device="cuda").to(torch.bfloat16)
+    win = torch.full((3, 16, 128), float("nan"), device="cuda")
+    _lib.kvq_decode_attn_int2_window(q, layer.cache, layer.num_pages, layer.block_table, layer.context_lens,
+                                     layer.R_k, layer.R_v, layer.mu, kw, kw,
+                                     torch.zeros(3, dtype=torch.int32, device="cuda"), layer.scale, win, ws, 1)
+    torch.cuda.synchronize()
+    assert _lib.kvq_workspace_status(ws) == 0
+    assert torch.isfinite(plain).all()
+    assert torch.equal(plain, win)
+
+
 def test_window_argument_checks():
     spec = inputs.small_spec("winarg", h_q=4, h_kv=1, batch=1, ctx=40)
     layer = Int2Layer(spec, 0)
