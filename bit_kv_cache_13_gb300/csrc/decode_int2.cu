@@ -291,13 +291,11 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
         float* partials = reinterpret_cast<float*>(ws + WS_HEADER + tickets_bytes(B, H_kv));
         return partials + (size_t)slot * G * PART_STRIDE;
     };
-    // Unit u's partials are this CTA's alone (one page CTA, no extra CTA):
-    // then no slot, ticket or merge is needed.
-    auto sole_partial = [&](int u) {
-        if (EXTRA) return false;
-        const PageSplit sp{(int64_t)B * H_kv * vmp, n_cta, vmp};
-        return sp.cta_of((int64_t)u * vmp) == sp.cta_of((int64_t)u * vmp + vmp - 1);
-    };
+    // Each unit's partials are one CTA's alone (one page CTA per unit, no
+    // extra CTA): then no slot, ticket or merge is needed.  The shares are
+    // equal, so a unit has a single CTA exactly when there are as many CTAs
+    // as units (with more CTAs every share is shorter than a unit).
+    const bool sole = !EXTRA && n_cta == B * H_kv;
     auto finish_unit = [&](int u) {
         // publish this CTA's slot (already written), then the last CTA merges;
         // the partials of unit u are the page CTAs' slots u + c, then (with a
@@ -962,22 +960,19 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
         if (last_seg) griddep_launch_dependents();
         // this CTA's partial, carried to the output basis (O = o' R_v^T); a
         // unit whose only partial this is gets its output written directly
-        if (sole_partial(u))
-            rotate_publish<NW, MAXG, true>(sm.ms, rvr, G, Rv + (size_t)h * D * D,
-                                           out + ((size_t)b * H_q + (size_t)h * G) * D);
-        else
-            rotate_publish<NW, MAXG>(sm.ms, rvr, G, Rv + (size_t)h * D * D, slot_ptr((int64_t)u + cta));
+        rotate_publish<NW, MAXG>(sm.ms, rvr, G, Rv + (size_t)h * D * D,
+                                 sole ? out + ((size_t)b * H_q + (size_t)h * G) * D : slot_ptr((int64_t)u + cta), sole);
         } else {
             if (last_seg) griddep_launch_dependents();
             griddep_wait();  // (early inputs) nothing is written before the wait
-            if (sole_partial(u)) {  // no pages and no other partial: the output is zero
+            if (sole) {  // no pages and no other partial: the output is zero
                 float* o = out + ((size_t)b * H_q + (size_t)h * G) * D;
                 for (int i = tid; i < G * D; i += NW * 32) o[i] = 0.f;
             } else {
                 publish_slot<NW, MAXG>(sm.ms, sm.ms.o_final, G, slot_ptr((int64_t)u + cta), true);
             }
         }
-        if (!sole_partial(u)) finish_unit(u);
+        if (!sole) finish_unit(u);
         __syncthreads();  // the next segment reuses the ring and the merge scratch
     };
     segment(u_first, false);

@@ -370,17 +370,20 @@ __device__ __forceinline__ bool arrive_last(MergeSmem<NW, MAXG>& ms, int32_t* ti
 // Rotates this CTA's merged partial o_final (G heads) by Rot^T -- O_i =
 // sum_j o'_j Rot[i][j], Rot row-major [D][D], 16-byte aligned -- and writes
 // it, with (Mh, Lh), to a partial slot (head jj at slot + jj * PART_STRIDE as
-// m, l, -, -, O[128]).  With DIRECT, the partial is the unit's only one: the
-// output out[jj][i] = O_i / Lh (0 when Lh = 0) is written instead, the value
-// the merge of that single partial would give.  rr holds each rotating
+// m, l, -, -, O[128]).  With direct set, the partial is the unit's only
+// one, and slot is the heads' output rows [G][D]: out[jj][i] = O_i / Lh (0
+// when Lh = 0) is written instead, the value the merge of that single
+// partial gives (the merge path multiplies by exactly 1).  rr holds each rotating
 // warp's first rows of Rot (load_rows, issued early so their latency is
 // hidden).  Each lane forms the partial dots of its 4 columns with its warp's
 // rows, and a reduce-scatter over the lanes leaves each row's full dot in
 // one lane (heads two at a time so their shuffle chains overlap).  All
 // threads call it.
-template <int NW, int MAXG, bool DIRECT = false>
+template <int NW, int MAXG>
 __device__ __forceinline__ void rotate_publish(const MergeSmem<NW, MAXG>& ms, float4 (&rr)[RowPrefetch<NW, MAXG>::N],
-                                               int G, const float* __restrict__ Rot, float* __restrict__ slot) {
+                                               int G, const float* __restrict__ Rot, float* __restrict__ slot,
+                                               bool direct = false) {
+    const int stride = direct ? D : PART_STRIDE, first = direct ? 0 : 4;
     constexpr int NR = RotSplit<NW>::NR, RPW = RotSplit<NW>::RPW, RP = RowPrefetch<NW, MAXG>::N;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (warp < NR) {
@@ -421,19 +424,16 @@ __device__ __forceinline__ void rotate_publish(const MergeSmem<NW, MAXG>& ms, fl
                 }
                 const int row = RPW * warp + RP * pass + (lane & (RP - 1));
                 if (RP == 32 || lane < 16) {
-                    if constexpr (DIRECT) {  // slot is the heads' output rows [G][D]
-                        const float la = ms.Lh[jj], lb = ms.Lh[jb];
-                        slot[(size_t)jj * D + row] = va[0] * (la > 0.f ? 1.f / la : 0.f);
-                        if (jj + 1 < G) slot[(size_t)(jj + 1) * D + row] = vb[0] * (lb > 0.f ? 1.f / lb : 0.f);
-                    } else {
-                        slot[(size_t)jj * PART_STRIDE + 4 + row] = va[0];
-                        if (jj + 1 < G) slot[(size_t)(jj + 1) * PART_STRIDE + 4 + row] = vb[0];
-                    }
+                    const float la = ms.Lh[jj], lb = ms.Lh[jb];
+                    const float fa = direct ? (la > 0.f ? 1.f / la : 0.f) : 1.f;
+                    const float fb = direct ? (lb > 0.f ? 1.f / lb : 0.f) : 1.f;
+                    slot[(size_t)jj * stride + first + row] = va[0] * fa;
+                    if (jj + 1 < G) slot[(size_t)(jj + 1) * stride + first + row] = vb[0] * fb;
                 }
             }
         }
     }
-    if (!DIRECT && tid < G) {
+    if (!direct && tid < G) {
         slot[(size_t)tid * PART_STRIDE] = ms.Mh[tid];
         slot[(size_t)tid * PART_STRIDE + 1] = ms.Lh[tid];
     }
