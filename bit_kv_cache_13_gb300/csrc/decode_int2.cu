@@ -294,8 +294,10 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
     // Each unit's partials are one CTA's alone (one page CTA per unit, no
     // extra CTA): then no slot, ticket or merge is needed.  The shares are
     // equal, so a unit has a single CTA exactly when there are as many CTAs
-    // as units (with more CTAs every share is shorter than a unit).
-    const bool sole = !EXTRA && n_cta == B * H_kv;
+    // as units (with more CTAs every share is shorter than a unit).  Groups
+    // of 8 keep the merge path: with the direct one compiled in, their
+    // batch-32 128K decode ran 4.7 % slower (register allocation).
+    const bool sole = NT == 1 && !EXTRA && n_cta == B * H_kv;
     auto finish_unit = [&](int u) {
         // publish this CTA's slot (already written), then the last CTA merges;
         // the partials of unit u are the page CTAs' slots u + c, then (with a
