@@ -118,32 +118,78 @@ __device__ __forceinline__ void window_partials(float (*o_part)[MAXG][D], MergeS
 #pragma unroll
         for (int e = 0; e < 4; ++e) o_w[jj][e] = 0.f;
     }
-    for (int t = warp; t < wl; t += NW) {
-        const size_t row = (((size_t)b * win_max + t) * H_kv + h) * D + 4 * lane;
-        const uint2 kr = __ldg(reinterpret_cast<const uint2*>(win_k + row));
-        const uint2 vr = __ldg(reinterpret_cast<const uint2*>(win_v + row));
-        const float2 k01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kr.x));
-        const float2 k23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kr.y));
-        const float2 v01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vr.x));
-        const float2 v23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vr.y));
-        const float kc[4] = {__fsub_rn(k01.x, mc[0]), __fsub_rn(k01.y, mc[1]), __fsub_rn(k23.x, mc[2]),
-                             __fsub_rn(k23.y, mc[3])};
-        const float vc[4] = {v01.x, v01.y, v23.x, v23.y};
+    // The warp's tokens t = warp, warp + NW, ... in chunks of WC: a chunk's
+    // WC x MAXG dot products are independent, so their shuffle reductions
+    // overlap (every head is computed; heads past G have q = 0), and the
+    // chunk joins the running softmax with one maximum update.  The next
+    // chunk's rows are requested before this one is computed.  Rows past
+    // the window are clamped to its last row (a valid address) and masked.
+    constexpr int WC = MAXG == 8 ? 2 : 4;  // (registers: groups of 8 hold twice the heads)
+    auto load_chunk = [&](int t0, uint2 (&kr)[WC], uint2 (&vr)[WC]) {
+#pragma unroll
+        for (int i = 0; i < WC; ++i) {
+            const size_t row = (((size_t)b * win_max + min(t0 + i * NW, wl - 1)) * H_kv + h) * D + 4 * lane;
+            kr[i] = __ldg(reinterpret_cast<const uint2*>(win_k + row));
+            vr[i] = __ldg(reinterpret_cast<const uint2*>(win_v + row));
+        }
+    };
+    uint2 kn[WC], vn[WC];
+    if (warp < wl) load_chunk(warp, kn, vn);
+#pragma unroll 1
+    for (int t0 = warp; t0 < wl; t0 += WC * NW) {
+        uint2 kr[WC], vr[WC];
+#pragma unroll
+        for (int i = 0; i < WC; ++i) {
+            kr[i] = kn[i];
+            vr[i] = vn[i];
+        }
+        if (t0 + WC * NW < wl) load_chunk(t0 + WC * NW, kn, vn);
+        float lg[WC][MAXG];
+#pragma unroll
+        for (int i = 0; i < WC; ++i) {
+            const float2 k01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kr[i].x));
+            const float2 k23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kr[i].y));
+            const float kc[4] = {__fsub_rn(k01.x, mc[0]), __fsub_rn(k01.y, mc[1]), __fsub_rn(k23.x, mc[2]),
+                                 __fsub_rn(k23.y, mc[3])};
+#pragma unroll
+            for (int jj = 0; jj < MAXG; ++jj) {
+                float dot = qv[jj][0] * kc[0];
+#pragma unroll
+                for (int e = 1; e < 4; ++e) dot = fmaf(qv[jj][e], kc[e], dot);
+                lg[i][jj] = dot;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+#pragma unroll
+            for (int i = 0; i < WC; ++i)
+#pragma unroll
+                for (int jj = 0; jj < MAXG; ++jj) lg[i][jj] += __shfl_xor_sync(0xffffffffu, lg[i][jj], o);
 #pragma unroll
         for (int jj = 0; jj < MAXG; ++jj) {
-            if (jj >= G) continue;
-            float dot = qv[jj][0] * kc[0];
+            // token t0 is in the window, so the chunk's maximum is finite
+            float mn = m_w[jj];
 #pragma unroll
-            for (int e = 1; e < 4; ++e) dot = fmaf(qv[jj][e], kc[e], dot);
-#pragma unroll
-            for (int o = 16; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-            const float lg = dot * scale_log2;
-            const float mn = fmaxf(m_w[jj], lg);
+            for (int i = 0; i < WC; ++i) {
+                lg[i][jj] = t0 + i * NW < wl ? lg[i][jj] * scale_log2 : -CUDART_INF_F;
+                mn = fmaxf(mn, lg[i][jj]);
+            }
             const float corr = ex2(m_w[jj] - mn);  // 0 while nothing was seen
-            const float p = ex2(lg - mn);
-            l_w[jj] = fmaf(l_w[jj], corr, p);
+            float ps = 0.f, ov[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o_w[jj][e] = fmaf(o_w[jj][e], corr, p * vc[e]);
+            for (int i = 0; i < WC; ++i) {
+                const float p = ex2(lg[i][jj] - mn);  // 0 for a masked row
+                const float2 v01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vr[i].x));
+                const float2 v23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vr[i].y));
+                ps += p;
+                ov[0] = fmaf(p, v01.x, ov[0]);
+                ov[1] = fmaf(p, v01.y, ov[1]);
+                ov[2] = fmaf(p, v23.x, ov[2]);
+                ov[3] = fmaf(p, v23.y, ov[3]);
+            }
+            l_w[jj] = fmaf(l_w[jj], corr, ps);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o_w[jj][e] = fmaf(o_w[jj][e], corr, ov[e]);
             m_w[jj] = mn;
         }
     }
@@ -161,7 +207,8 @@ __device__ __forceinline__ void window_partials(float (*o_part)[MAXG][D], MergeS
 
 // Work split.  The B * H_kv (sequence, KV head) units are laid end to end
 // as V = units * vmp "virtual" pages (vmp = max_pages, plus in a decode step
-// a few pages without work that lighten the share holding the new token):
+// or a window decode a few pages without work after the real ones, which
+// lighten the share holding the new token or attending the window):
 // unit u = b * H_kv + h owns
 // [u * MP, (u + 1) * MP), of which the first ceil(ctx_b / 16) are real.
 // Page CTA c of C takes the virtual pages [c V / C, (c + 1) V / C), so every
@@ -177,10 +224,10 @@ struct PageSplit {
     __device__ __forceinline__ int cta_of(int64_t g) const { return (int)(((g + 1) * C - 1) / V); }
 };
 
-// What the CTAs after the page CTAs do, one per (sequence, KV head) unit.
+// What a decode attends besides the cached pages of a (sequence, KV head) unit.
 enum DecodeMode : int {
     MODE_CACHE = 0,   // nothing: the cache alone
-    MODE_WINDOW = 1,  // attend the unit's BF16 window
+    MODE_WINDOW = 1,  // the unit's BF16 window
     MODE_STEP = 2,    // append the decode token to the cache and attend it
 };
 
@@ -261,8 +308,9 @@ constexpr int DBG_DROP_FIRST_COPY = 1;
 constexpr int FLAG_EARLY_INPUTS = 2;
 constexpr long long DBG_WAIT_LIMIT_CYCLES = 2000000LL;
 
-// Grid: n_cta page CTAs, then (MODE_WINDOW) one CTA per unit for its BF16
-// window.  In MODE_STEP, k_new / v_new are the decode token's [B][H_kv][d] key
+// Grid: n_cta page CTAs.  In MODE_WINDOW the CTA whose share holds a unit's
+// last virtual page also attends that unit's BF16 window, after its pages,
+// and publishes it as one more partial of the unit.  In MODE_STEP, k_new / v_new are the decode token's [B][H_kv][d] key
 // and value (win_k and win_v carry them), appended at position ctx - 1 by the
 // page CTA whose share holds that position.
 template <int NT, int MODE>
@@ -276,7 +324,7 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
                    uint8_t* __restrict__ ws, int n_cta, int vmp, int flags) {
     constexpr int DEC_STAGES = DecRing<4 * NT>::STAGES;  // page slots per warp
     constexpr int DEC_UNITS = DecRing<4 * NT>::UNITS;    // units in flight per warp
-    constexpr bool EXTRA = MODE == MODE_WINDOW;  // one window CTA per unit after the page CTAs
+    constexpr bool WIN = MODE == MODE_WINDOW;  // each unit has a window partial besides the page CTAs' ones
     extern __shared__ __align__(128) uint8_t smem_raw[];
     constexpr int MAXG = 4 * NT;
     constexpr int NW = DecWarps<NT>::NW;
@@ -292,21 +340,21 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
         return partials + (size_t)slot * G * PART_STRIDE;
     };
     // Each unit's partials are one CTA's alone (one page CTA per unit, no
-    // extra CTA): then no slot, ticket or merge is needed.  The shares are
+    // window): then no slot, ticket or merge is needed.  The shares are
     // equal, so a unit has a single CTA exactly when there are as many CTAs
     // as units (with more CTAs every share is shorter than a unit).  Groups
     // of 8 keep the merge path: with the direct one compiled in, their
     // batch-32 128K decode ran 4.7 % slower (register allocation).
-    const bool sole = NT == 1 && !EXTRA && n_cta == B * H_kv;
+    const bool sole = NT == 1 && !WIN && n_cta == B * H_kv;
     auto finish_unit = [&](int u) {
         // publish this CTA's slot (already written), then the last CTA merges;
         // the partials of unit u are the page CTAs' slots u + c, then (with a
-        // window or a new token) the slot of its extra CTA
+        // window) the window's slot units + n_cta + u
         const PageSplit sp{(int64_t)B * H_kv * vmp, n_cta, vmp};
         const int units = B * H_kv;
         const int c0 = sp.cta_of((int64_t)u * vmp);
         const int n = sp.cta_of((int64_t)u * vmp + vmp - 1) - c0 + 1;
-        const int expected = n + (EXTRA ? 1 : 0);
+        const int expected = n + (WIN ? 1 : 0);
         int32_t* tickets = reinterpret_cast<int32_t*>(ws + WS_HEADER);
         if (!arrive_last(sm.ms, tickets + u, expected)) return;
         const int b = u / H_kv, h = u % H_kv;
@@ -316,24 +364,6 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
         merge_out<NW, MAXG>(sm.ms, slot_of, expected, G, out + ((size_t)b * H_q + (size_t)h * G) * D);
         if (tid == 0) tickets[u] = 0;
     };
-
-    if constexpr (MODE == MODE_WINDOW) {
-        if (blockIdx.x >= n_cta) {
-            // BF16 window of unit u: attended exactly in the original basis,
-            // which is the output basis, so its partial merges as it is
-            const int units = B * H_kv;
-            const int u = blockIdx.x - n_cta, b = u / H_kv, h = u % H_kv;
-            griddep_wait();
-            griddep_launch_dependents();
-            window_partials<NW, MAXG>(sm.o_part, sm.ms, q, H_q, H_kv, G, b, h, mu, win_k, win_v, win_lens, win_max,
-                                      scale_log2);
-            __syncthreads();
-            merge_warps<NW, MAXG>(sm.ms, sm.o_part, G);
-            publish_slot<NW, MAXG>(sm.ms, sm.ms.o_final, G, slot_ptr((int64_t)units + n_cta + u), false);
-            finish_unit(u);
-            return;
-        }
-    }
 
     const int cta = blockIdx.x;
     int u_first;
@@ -487,8 +517,8 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
             __syncwarp();  // the expected bytes are set before any copy is issued
             // (test hook: CTA 0 leaves its first copy unissued)
             if (ok && !((flags & DBG_DROP_FIRST_COPY) && cta == 0 && warp == 0 && u == 0 && k == 0 && lane == 0))
-                bulk_g2s(sm.u.ring[warp][UNIT_PAGES * st + lane], cache + ((size_t)pid * H_kv + h) * INT2_TILE,
-                         INT2_TILE, bar);
+                bulk_g2s_hint(sm.u.ring[warp][UNIT_PAGES * st + lane], cache + ((size_t)pid * H_kv + h) * INT2_TILE,
+                              INT2_TILE, bar, l2_policy_evict_first());
         };
         // the first units go out as soon as their page ids are here: the copies
         // fly while the query is rotated
@@ -975,6 +1005,20 @@ decode_int2_kernel(const __nv_bfloat16* __restrict__ q, int B, int H_q, int H_kv
             }
         }
         if (!sole) finish_unit(u);
+        if constexpr (MODE == MODE_WINDOW) {
+            if (pb == vmp) {  // CTA-uniform: this share holds the unit's last virtual page
+                // The unit's BF16 window, attended exactly in the original
+                // basis (the output basis), is one more partial of the unit:
+                // published (even after a timed-out wait, so that the unit's
+                // ticket completes) in slot units + n_cta + u.
+                window_partials<NW, MAXG>(sm.o_part, sm.ms, q, H_q, H_kv, G, b, h, mu, win_k, win_v, win_lens,
+                                          win_max, scale_log2);
+                __syncthreads();
+                merge_warps<NW, MAXG>(sm.ms, sm.o_part, G);
+                publish_slot<NW, MAXG>(sm.ms, sm.ms.o_final, G, slot_ptr((int64_t)B * H_kv + n_cta + u), false);
+                finish_unit(u);
+            }
+        }
         __syncthreads();  // the next segment reuses the ring and the merge scratch
     };
     segment(u_first, false);
@@ -1025,18 +1069,18 @@ int kvq_device_sm_count() {
 }
 
 // Page CTAs of the INT2 decode: num_splits per (sequence, KV head) unit when
-// given, else one wave (one CTA per SM, less the window CTAs when they fit
-// beside it) with at least 32 pages of the virtual page space per CTA; never
-// fewer CTAs than units (so a CTA's share spans at most two units) and never
-// more than virtual pages (so every share holds a page).
-static int64_t int2_page_ctas(int B, int H_kv, int max_pages, int num_splits, bool win) {
+// given, else one wave (one CTA per SM) with at least 32 pages of the
+// virtual page space per CTA; never fewer CTAs than units (so a CTA's share
+// spans at most two units) and never more than virtual pages (so every share
+// holds a page).  The count grows with the virtual pages per unit.
+static int64_t int2_page_ctas(int B, int H_kv, int max_pages, int num_splits) {
     const int64_t units = (int64_t)B * H_kv, V = units * max_pages;
     int64_t C;
     if (num_splits > 0) {
         C = (int64_t)num_splits * units;
     } else {
         const int64_t nsm = kvq_device_sm_count();
-        C = win && 2 * units <= nsm ? nsm - units : nsm;
+        C = nsm;
         const int64_t cap = (V + 31) / 32;
         if (C > cap) C = cap;
         // a CTA's share must not span more than two units
@@ -1054,6 +1098,20 @@ static int64_t int2_page_ctas(int B, int H_kv, int max_pages, int num_splits, bo
 // unit is one CTA's work anyway, and the extra pages would only add a
 // second CTA (and a split-K merge) to it.
 static int step_virtual_pages(int max_pages) { return max_pages + (max_pages < 96 ? 0 : 96); }
+
+// Virtual pages per unit of a window decode: the CTA holding a unit's last
+// virtual page attends its BF16 window after its pages, so each unit gets
+// one page without work per window row (win_max, at most WIN_MAX_PAGES)
+// after its last page.  The window's rows are read while the other CTAs
+// still stream the cache, each request queued behind their copies, which
+// makes a row cost about as much time as a page (measured: 33, 66, 132 and
+// 264 such pages for a 132-row window at 128K gave the window 4.9, 4.1,
+// 2.8 and 3.7 us over the plain decode).  Below 96 pages, as in the decode
+// step, a unit is one CTA's work anyway.
+constexpr int WIN_MAX_PAGES = 256;
+static int window_virtual_pages(int max_pages, int win_max) {
+    return max_pages + (max_pages < 96 ? 0 : win_max < WIN_MAX_PAGES ? win_max : WIN_MAX_PAGES);
+}
 
 extern "C" int kvq_decode_auto_splits(int B, int H_q, int H_kv, int max_pages_per_seq) {
     if (B <= 0 || H_kv <= 0 || H_q < H_kv || max_pages_per_seq <= 0) return 1;
@@ -1077,16 +1135,19 @@ static size_t int2_workspace_bytes(int B, int H_q, int H_kv, int64_t slots) {
 }
 
 extern "C" size_t kvq_decode_workspace_bytes(int B, int H_q, int H_kv, int max_pages_per_seq, int num_splits) {
-    if (B <= 0 || H_q <= 0 || H_kv <= 0 || max_pages_per_seq <= 0 || num_splits < 0) return 0;
+    if (B <= 0 || H_q <= 0 || H_kv <= 0 || max_pages_per_seq <= 0 || max_pages_per_seq > (1 << 28) ||
+        num_splits < 0)
+        return 0;
     const int64_t units = (int64_t)B * H_kv;
     int64_t slots;
     if (num_splits > 0) {
         // INT2 with and without the window, and Block-GTQ's num_splits per unit
         slots = ((int64_t)num_splits + 2) * units;
     } else {  // room for the automatic choice of every decode entry point
-        const int64_t plain = units + int2_page_ctas(B, H_kv, max_pages_per_seq, 0, false);
-        const int64_t step = units + int2_page_ctas(B, H_kv, step_virtual_pages(max_pages_per_seq), 0, false);
-        const int64_t win = 2 * units + int2_page_ctas(B, H_kv, max_pages_per_seq, 0, true);
+        const int64_t plain = units + int2_page_ctas(B, H_kv, max_pages_per_seq, 0);
+        const int64_t step = units + int2_page_ctas(B, H_kv, step_virtual_pages(max_pages_per_seq), 0);
+        // the window's pages without work are at most WIN_MAX_PAGES per unit
+        const int64_t win = 2 * units + int2_page_ctas(B, H_kv, window_virtual_pages(max_pages_per_seq, 1 << 30), 0);
         const int64_t bg = units * bgtq_decode_auto_splits(B, H_q, H_kv, max_pages_per_seq);
         slots = plain > win ? plain : win;
         if (step > slots) slots = step;
@@ -1128,6 +1189,10 @@ static kvq_status decode_int2_plan(const char* fn, int mode, const void* q, int 
     if (B > 65535 || H_kv > 65535) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "%s: B or H_kv above 65535", fn);
     if ((int64_t)B * H_kv * max_pages_per_seq > (int64_t(1) << 40))
         return kvq_set_error(KVQ_ERR_UNSUPPORTED, "%s: B * H_kv * max_pages above 2^40", fn);
+    // (an int32 context spans at most 2^27 pages; the bound keeps the virtual
+    // pages per unit, max_pages plus a few hundred, within int)
+    if (max_pages_per_seq > (1 << 28))
+        return kvq_set_error(KVQ_ERR_UNSUPPORTED, "%s: max_pages_per_seq %d above 2^28", fn, max_pages_per_seq);
     if (num_splits > MAX_SPLITS - 2)
         return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: %d splits above %d", fn, num_splits, MAX_SPLITS - 2);
     if (!q || !cache || !block_table || !context_lens || !R_k || !R_v || !out || (check_ws && !workspace))
@@ -1143,28 +1208,29 @@ static kvq_status decode_int2_plan(const char* fn, int mode, const void* q, int 
     }
     if (mode == MODE_STEP && (!win_k || !win_v || !mu_k))
         return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: null k_new, v_new or mu_k", fn);
-    const bool extra = mode == MODE_WINDOW;  // one window CTA per unit
+    const bool win = mode == MODE_WINDOW;  // one window partial per unit
     const int64_t units = (int64_t)B * H_kv;
-    const int vmp = mode == MODE_STEP ? step_virtual_pages(max_pages_per_seq) : max_pages_per_seq;
+    const int vmp = mode == MODE_STEP     ? step_virtual_pages(max_pages_per_seq)
+                    : mode == MODE_WINDOW ? window_virtual_pages(max_pages_per_seq, win_max)
+                                          : max_pages_per_seq;
     if ((int64_t)B * H_kv * vmp > (int64_t(1) << 40))
         return kvq_set_error(KVQ_ERR_UNSUPPORTED, "%s: B * H_kv * max_pages above 2^40", fn);
-    const int64_t C = int2_page_ctas(B, H_kv, vmp, num_splits, extra);
+    const int64_t C = int2_page_ctas(B, H_kv, vmp, num_splits);
     // a unit's partials: the page CTAs over its pages (its share of the
     // virtual pages spans at most ceil(C / units) + 1 of them) and the window
     if ((C + units - 1) / units + 2 > MAX_SPLITS)
         return kvq_set_error(KVQ_ERR_INVALID_ARG, "%s: %lld CTAs over %lld units exceed %d partials per unit", fn,
                              (long long)C, (long long)units, MAX_SPLITS);
-    const int64_t grid = C + (extra ? units : 0);
-    if (grid > 0x7fffffff) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "%s: grid of %lld CTAs", fn, (long long)grid);
+    if (C > 0x7fffffff) return kvq_set_error(KVQ_ERR_UNSUPPORTED, "%s: grid of %lld CTAs", fn, (long long)C);
     constexpr int NW1 = DecWarps<1>::NW, NW2 = DecWarps<2>::NW;
     plan.G = G;
     plan.C = (int)C;
-    plan.grid = (int)grid;
+    plan.grid = (int)C;
     plan.mode = mode;
     plan.vmp = vmp;
     plan.threads = (G <= 4 ? NW1 : NW2) * 32;
     plan.smem = G <= 4 ? sizeof(DecodeSmem<NW1, 4>) : sizeof(DecodeSmem<NW2, 8>);
-    plan.need = int2_workspace_bytes(B, H_q, H_kv, units + C + (extra ? units : 0));
+    plan.need = int2_workspace_bytes(B, H_q, H_kv, units + C + (win ? units : 0));
     return KVQ_OK;
 }
 

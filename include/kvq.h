@@ -137,7 +137,8 @@ kvq_status kvq_dequant_int2(const void* cache, int64_t num_pages, int H_kv, int 
  * whose SM count sets the automatic choice).  The workspace holds an error
  * word, a split ticket per (sequence, KV head) and the split partials.  It
  * must be zero-filled once before its first use; every call leaves its
- * tickets at zero again.  Returns 0 for invalid sizes. */
+ * tickets at zero again.  Returns 0 for invalid sizes (max_pages_per_seq
+ * above 2^28 among them). */
 size_t kvq_decode_workspace_bytes(int B, int H_q, int H_kv, int max_pages_per_seq, int num_splits);
 
 /* The split count per (sequence, KV head) the automatic choice (num_splits =
@@ -183,11 +184,13 @@ kvq_status kvq_decode_attn_int2(const void* q, int B, int H_q, int H_kv, int d,
  * not centred) is quantised exactly as kvq_append_int2 does it and written
  * to position ctx - 1, i.e. slot block_table[b][(ctx-1)/16] * 16 +
  * (ctx-1) % 16; then the ctx tokens, the new one included, are attended.
- * One extra CTA per (sequence, KV head) quantises, writes and attends the
- * new token while the page CTAs stream the ctx - 1 cached ones, and the
- * partials merge as in kvq_decode_attn_int2: the cache bytes written are
- * identical to kvq_append_int2's, and the output equals that of the two
- * calls in sequence up to the rounding order of the merge.
+ * The page CTA whose share holds the new token's page quantises, writes and
+ * attends it besides its cached pages (each unit's share of the page space
+ * carries 96 pages without work after its last one, from 96 pages up, to
+ * balance that), and the partials merge as in kvq_decode_attn_int2: the
+ * cache bytes written are identical to kvq_append_int2's, and the output
+ * equals that of the two calls in sequence up to the rounding order of the
+ * merge.
  *   mu_k      device fp32 [H_kv][d], the key centre of the append
  *   cache     written at the new tokens' slots
  *   flags     0 or KVQ_STEP_INPUTS_READY
@@ -228,9 +231,12 @@ kvq_status kvq_decode_step_int2(const void* q, const void* k_new, const void* v_
  *             centred, not rotated), 16-byte aligned
  *   win_lens  device int32 [B], clamped to [0, win_max]
  *   win_max   > 0
- * The window of each (sequence, KV head) is attended by one CTA of its own,
- * whose partial is carried into the R_v basis and merged with the cache's;
- * kvq_decode_workspace_bytes(..., num_splits) covers it. */
+ * The window of each (sequence, KV head) is attended, after its cached pages,
+ * by the page CTA whose share ends that unit (from 96 pages up each unit's
+ * share of the page space carries win_max pages without work, at most
+ * 256, after its last one, to balance that); the window's partial,
+ * already in the output basis, is merged with the cache's as one more
+ * split.  kvq_decode_workspace_bytes(..., num_splits) covers it. */
 kvq_status kvq_decode_attn_int2_window(const void* q, int B, int H_q, int H_kv, int d,
                                        const void* cache, int64_t num_pages,
                                        const int32_t* block_table, int max_pages_per_seq,

@@ -47,6 +47,7 @@ def _decode(lib, q=A, B=1, H_q=4, H_kv=1, d=128, cache=A, num_pages=10, bt=A, ma
     (dict(splits=-1), INVALID, "splits=-1"),
     (dict(H_q=16, H_kv=1), UNSUPPORTED, "group 16"),
     (dict(B=70000), UNSUPPORTED, "65535"),
+    (dict(max_pages=(1 << 28) + 1), UNSUPPORTED, "above 2^28"),
     (dict(q=None), INVALID, "null pointer"),
     (dict(out=None), INVALID, "null pointer"),
     (dict(cache=MIS), INVALID, "alignment"),

@@ -32,6 +32,11 @@ def _bf16_round(a):
     (8, 2, [0, 50], [5, 1], 8, 0),                # window only; a one-token window
     (4, 1, [17], [128], 128, 2),                  # window longer than the cached part
     (16, 4, [2049, 33, 160], [1, 132, 200], 200, 7),  # ragged, a full window
+    # from 96 pages up a unit's share carries window pages without work: the
+    # automatic split (shares crossing unit ends, the window attended by the
+    # CTA holding a unit's last virtual page) and one CTA per unit
+    (32, 8, [3000, 1600], [132, 60], 132, 0),
+    (32, 8, [2000], [132], 132, 1),
 ])
 def test_window_decode_matches_oracle(h_q, h_kv, ctxs, wins, win_max, splits):
     B = len(ctxs)
@@ -146,3 +151,50 @@ def test_window_argument_checks():
         _lib.kvq_decode_attn_int2_window(q, layer.cache, layer.num_pages, layer.block_table, layer.context_lens,
                                          layer.R_k, layer.R_v, layer.mu, kw, kw, lens, layer.scale, out, small, 2)
     assert e.value.status == -3
+
+
+def test_qwen8b_window_full_size_sampled():
+    """The timed window workload: one Qwen3-8B-shaped layer at 128K (the
+    decode token appended) and a window of 4 sink + 128 recent tokens per
+    sequence, decoded in full with the automatic split; the first and the
+    last KV head (whose shares hold the ends of the page space) are checked
+    against the oracle."""
+    spec = inputs.SPECS["qwen8b"]
+    layer = Int2Layer(spec, 0)
+    layer.prefill()
+    k_new, v_new = layer.new_kv()
+    _lib.kvq_append_int2(k_new, v_new, layer.new_slots(), layer.mu, layer.R_k, layer.R_v, layer.cache,
+                         layer.num_pages)
+    q = layer.queries()
+    w = inputs.WINDOW_SINK + inputs.WINDOW_RECENT
+    rng = np.random.default_rng(132)
+    mu = _np_f32(layer.mu)
+    kw = _bf16_round((rng.standard_normal((spec.batch, w, spec.h_kv, 128)) * 2 + mu * 0.5).astype(np.float32))
+    vw = _bf16_round(rng.standard_normal((spec.batch, w, spec.h_kv, 128)).astype(np.float32))
+    lens = np.full(spec.batch, w, dtype=np.int32)
+    out = torch.full((spec.batch, spec.h_q, 128), float("nan"), device="cuda")
+    ws = layer.workspace()
+    _lib.kvq_decode_attn_int2_window(q, layer.cache, layer.num_pages, layer.block_table, layer.context_lens,
+                                     layer.R_k, layer.R_v, layer.mu,
+                                     torch.as_tensor(kw, dtype=torch.bfloat16, device="cuda"),
+                                     torch.as_tensor(vw, dtype=torch.bfloat16, device="cuda"),
+                                     torch.as_tensor(lens, device="cuda"), layer.scale, out, ws)
+    torch.cuda.synchronize()
+    assert _lib.kvq_workspace_status(ws) == 0
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    bt = layer.block_table.cpu().numpy()
+    T, g = spec.ctx, spec.g
+    for b, h in [(0, 0), (spec.batch - 1, spec.h_kv - 1)]:
+        k, v = layer.history_kv(b)
+        kf = _np_f32(torch.cat([k, k_new[b:b + 1]])[:, h:h + 1])
+        vf = _np_f32(torch.cat([v, v_new[b:b + 1]])[:, h:h + 1])
+        slots = np.array([bt[b, t // 16] * 16 + t % 16 for t in range(T)])
+        rk, rv = _np_f32(layer.R_k[h:h + 1]), _np_f32(layer.R_v[h:h + 1])
+        full = int2.new_cache(layer.num_pages, 1)
+        int2.append(full, kf, vf, slots, mu[h:h + 1], rk, rv, exact_chain=False)
+        ref = int2.decode(q[b:b + 1, h * g:(h + 1) * g].cpu().double().numpy(), full, bt[b:b + 1], [T],
+                          mu[h:h + 1], rk, rv, layer.scale, 1,
+                          window=(kw[b:b + 1, :, h:h + 1], vw[b:b + 1, :, h:h + 1], lens[b:b + 1]))
+        err = np.max(np.abs(got[b, h * g:(h + 1) * g] - ref[0]))
+        assert err <= TOL * np.max(np.abs(ref[0])), (b, h, err, np.max(np.abs(ref[0])))

@@ -56,7 +56,8 @@ def test_workspace_with_auto_splits_holds_every_entry_point(cpu_lib):
     decode call: the INT2 decode's slots (one per unit and page CTA, at most
     units + C - 1 with C = one CTA per SM (152 where no device is visible),
     at least one per unit and at most one per 32 pages), the BF16-window
-    form's extra slot per unit, the decode step's (whose units carry up to 96
+    form's (whose units carry up to 256 more virtual pages, and one more
+    slot each for the window), the decode step's (whose units carry up to 96
     more virtual pages) and Block-GTQ's per-unit splits."""
     nsm = 152
     for B, H_kv, pages in [(1, 8, 8192), (8, 8, 2048), (3, 2, 40), (64, 8, 256), (1, 1, 17)]:
@@ -64,7 +65,8 @@ def test_workspace_with_auto_splits_holds_every_entry_point(cpu_lib):
         units = B * H_kv
         V = units * pages
         c_plain = min(max(min(nsm, -(-V // 32)), units), V)
-        c_win = min(max(min(nsm - units if 2 * units <= nsm else nsm, -(-V // 32)), units), V)
+        vw = units * (pages + (0 if pages < 96 else 256))  # the window's virtual pages, at most
+        c_win = min(max(min(nsm, -(-vw // 32)), units), vw)
         vs = units * (pages + (0 if pages < 96 else 96))  # a decode step's virtual pages
         c_step = min(max(min(nsm, -(-vs // 32)), units), vs)
         slots = max(units + c_plain, 2 * units + c_win, units + c_step,
