@@ -691,7 +691,8 @@ def run_profile_case(args):
     heads) at --profile-ctx tokens (default 32K; 131072 is one layer of the
     benchmark step, ~100 MB of cache), three launches of the chosen kernel:
     a decode, a fused decode step, or the append of the layer's whole
-    history in one call."""
+    history in one call.  decode_int2_gqa8 decodes the Llama-3-70B-shaped
+    layer (64 q / 8 KV heads) at --profile-batch sequences instead."""
     torch.cuda.set_device(0)
     spec = inputs.small_spec(f"prof{args.profile_ctx // 1024}k", h_q=32, h_kv=8, batch=1, ctx=args.profile_ctx,
                              permute=True, k_kind="energy_rope", v_kind="gauss", avg_bits=3, v_bits=3, b_min=1,
@@ -715,7 +716,10 @@ def run_profile_case(args):
         for _ in range(3):
             _lib.kvq_decode_step_int2(q, k_new, v_new, L.cache, L.num_pages, L.block_table, L.context_lens, L.mu,
                                       L.R_k, L.R_v, L.scale, out, ws, flags=_lib.KVQ_STEP_INPUTS_READY)
-    elif args.profile_case == "decode_int2":
+    elif args.profile_case in ("decode_int2", "decode_int2_gqa8"):
+        if args.profile_case == "decode_int2_gqa8":
+            spec = inputs.sweep70b_spec(args.profile_batch, args.profile_ctx)
+            out = torch.zeros((spec.batch, spec.h_q, spec.d), dtype=torch.float32, device="cuda")
         L = Int2Layer(spec, 0)
         L.prefill()
         q, ws = L.queries(), L.workspace()
@@ -742,10 +746,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-bgtq", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="only the headline step (e.g. for an ncu launch list)")
-    ap.add_argument("--profile-case", choices=["decode_int2", "step_int2", "bgtq_decode", "append_prefill"],
+    ap.add_argument("--profile-case", choices=["decode_int2", "decode_int2_gqa8", "step_int2", "bgtq_decode",
+                                               "append_prefill"],
                     default=None,
                     help="run a small decode case for an ncu capture instead of the benchmark")
     ap.add_argument("--profile-ctx", type=int, default=32768, help="context length of the --profile-case layer")
+    ap.add_argument("--profile-batch", type=int, default=8, help="sequences of the decode_int2_gqa8 case")
     args = ap.parse_args()
     if args.profile_case:
         run_profile_case(args)
