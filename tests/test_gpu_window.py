@@ -37,6 +37,7 @@ def _bf16_round(a):
     # CTA holding a unit's last virtual page) and one CTA per unit
     (32, 8, [3000, 1600], [132, 60], 132, 0),
     (32, 8, [2000], [132], 132, 1),
+    (8, 2, [2000, 1700], [700, 333], 700, 0),    # window past the 256-page balance cap
 ])
 def test_window_decode_matches_oracle(h_q, h_kv, ctxs, wins, win_max, splits):
     B = len(ctxs)
