@@ -148,7 +148,7 @@ def test_window_argument_checks():
     lens = torch.ones(1, dtype=torch.int32, device="cuda")
     small = torch.zeros(_lib.kvq_decode_workspace_bytes(1, 4, 1, layer.block_table.shape[1], 1), dtype=torch.uint8,
                         device="cuda")
-    with pytest.raises(_lib.KvqError) as e:    # 1 unit + 2 page CTAs + the window CTA need 4 slots, 3 are there
+    with pytest.raises(_lib.KvqError) as e:    # 1 unit + 2 page CTAs + the window partial need 4 slots, 3 are there
         _lib.kvq_decode_attn_int2_window(q, layer.cache, layer.num_pages, layer.block_table, layer.context_lens,
                                          layer.R_k, layer.R_v, layer.mu, kw, kw, lens, layer.scale, out, small, 2)
     assert e.value.status == -3
