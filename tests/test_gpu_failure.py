@@ -57,6 +57,44 @@ def test_wait_that_runs_out_is_reported_and_the_context_stays_usable(h_q):
     assert torch.equal(again, good)
 
 
+@pytest.mark.parametrize("splits", [0, 1])  # with one CTA per unit, CTA 0 (whose copy is dropped) holds the window
+def test_window_decode_wait_that_runs_out_still_completes_the_tickets(splits):
+    # The CTA whose share ends a unit also attends the unit's BF16 window;
+    # after one of its waits runs out it still publishes the window partial,
+    # so every unit's ticket completes, is reset, and the next call is exact.
+    layer = _layer(f"tmow{splits}", h_q=8, h_kv=2, batch=2, ctx=700)
+    q = layer.queries()
+    mu = torch.zeros(2, 128, device="cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    kw = torch.randn((2, 16, 2, 128), generator=g, device="cuda").to(torch.bfloat16)
+    vw = torch.randn((2, 16, 2, 128), generator=g, device="cuda").to(torch.bfloat16)
+    lens = torch.tensor([16, 9], dtype=torch.int32, device="cuda")
+    nbytes = _lib.kvq_decode_workspace_bytes(2, 8, 2, layer.block_table.shape[1], splits + 1 if splits else 0)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+
+    def win():
+        out = torch.full((2, 8, 128), float("nan"), device="cuda")
+        _lib.kvq_decode_attn_int2_window(q, layer.cache, layer.num_pages, layer.block_table, layer.context_lens,
+                                         layer.R_k, layer.R_v, mu, kw, vw, lens, layer.scale, out, ws, splits)
+        return out
+
+    good = win()
+    torch.cuda.synchronize()
+    assert _lib.kvq_workspace_status(ws) == 0
+    _lib.kvq_debug_drop_next_copy()
+    bad = win()
+    torch.cuda.synchronize()
+    assert _lib.kvq_workspace_status(ws) == -4
+    assert int(ws[256:256 + 4 * 4].view(torch.int32).abs().sum()) == 0   # tickets reset all the same
+    assert torch.isfinite(bad).all()
+    assert not torch.equal(bad, good)
+    again = win()
+    torch.cuda.synchronize()
+    assert _lib.kvq_workspace_status(ws) == 0
+    assert torch.equal(again, good)
+
+
 def test_rotations_written_just_before_append_and_decode():
     spec = inputs.small_spec("rwb", h_q=8, h_kv=2, batch=1, ctx=400, permute=True)
     ref = Int2Layer(spec, 0)
