@@ -557,7 +557,10 @@ def measure_extras(line, spec, device, stream):
                     "kernel": "decode_int2_kernel<2>", "ms_per_decode": round(g8["us_per_launch"] / 1e3, 4),
                     "value": g8["value"], "unit": "GB/s",
                     "roofline": {"bound": "hbm", "achieved": g8["value"], "peak": sweep["peak"], "unit": "GB/s",
-                                 "frac": g8["frac"], "peak_kind": sweep["peak_kind"]}}
+                                 "frac": g8["frac"], "peak_kind": sweep["peak_kind"],
+                                 "traffic": profiled_traffic("decode_int2_gqa8", ("decode_int2.cu", "int2_quant.cuh",
+                                                                                   "merge.cuh", "kvq_common.cuh"),
+                                                             8 * 131072 * 8)}}
     ll = measure_int2_decode(inputs.SPECS["llama8b"], device, stream, reps=5)
     line["llama8b"] = {"workload": "llama8b: 32 q / 8 KV heads, batch 8, 32768 ctx (post-RoPE keys, theta 5e5), "
                                    "INT2 cache", "kernel": "decode_int2_kernel<1>", **ll, "unit": "GB/s",
